@@ -1,0 +1,392 @@
+"""Benchmark of the DARTree draft-tree build + verify round on one GB300.
+
+One step = dartree_build_tree followed by dartree_verify (S1-S10) over one batch
+of seeded synthetic inputs already resident in HBM. The default workload is the
+Qwen3-4B-shaped single-request round (C=1, L=16, V=151936, H=2560, K=64, W=12,
+B=64, bf16); the C=64 stress batch (H=4096, K=512) is measured in the same run
+and reported under "c64". Prints one JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from dartree_inputs import breadth_first_slot_depth, make_config, make_inputs, make_target_per_node  # noqa: E402
+
+MAIN_CFG = "cfg1_qwen3_4b_c1"
+STRESS_CFG = "cfg4_c64_stress"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# --------------------------------------------------------------------------- algorithmic work (per round)
+
+def algorithmic(cfg, accepted_mean: float) -> dict:
+    """Bytes and flops the method must touch once per round (roofline numerator)."""
+    eb = 2 if cfg.dtype == "bf16" else 4
+    C, L, V, H, K, W = cfg.C, cfg.L, cfg.V, cfg.H, cfg.K, cfg.W
+    P = [1]
+    for _ in range(L - 1):
+        P.append(min(W, P[-1] * K))
+    topk_bytes = C * L * V * eb
+    expand_bytes = (H * H * eb                # W_q once (it fits in L2)
+                    + C * L * K * H * eb      # candidate embedding rows
+                    + C * L * H * eb)         # block hidden rows
+    rows_walked = (accepted_mean + 1) if cfg.rows == "node" else L
+    verify_bytes = C * rows_walked * V * eb
+    flops = 2 * C * H * H * sum(P) + 2 * C * K * H * sum(P)
+    return dict(topk=topk_bytes, expand=expand_bytes, verify=verify_bytes, flops=flops,
+                total=topk_bytes + expand_bytes + verify_bytes)
+
+
+# --------------------------------------------------------------------------- inputs
+
+def device_inputs(cfg, torch):
+    inp = make_inputs(cfg)
+
+    def t(a):
+        a = np.ascontiguousarray(a)
+        if cfg.dtype == "bf16":
+            return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+        return torch.from_numpy(a).cuda()
+
+    x = dict(E=t(inp["E"]), Wq=t(inp["Wq"]), base=t(inp["base"]), hidden=t(inp["hidden"]),
+             anchor=torch.from_numpy(inp["anchor"]).cuda())
+    if cfg.rows == "position":
+        x["target"] = t(inp["target"])
+    else:
+        x["target"] = t(make_target_per_node(cfg, inp, breadth_first_slot_depth(cfg)))
+    return inp, x
+
+
+# --------------------------------------------------------------------------- clocks
+
+class Clocks:
+    def __init__(self):
+        self.p = None
+        self.path = os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "-i", os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0],
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx = float(parts[1])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[3:7]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- GPU measurement
+
+def time_steps(torch, fn, steps, warmup, flush):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        if flush is not None:
+            flush.add_(1)
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    return np.array(times)  # ms
+
+
+def graphed(torch, fn, use_graph=True):
+    """fn captured in a CUDA graph (so host overhead does not show in device timings)."""
+    fn()
+    torch.cuda.synchronize()
+    if not use_graph:
+        return fn
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    graphed.keep.append(g)
+    return g.replay
+
+
+graphed.keep = []
+
+
+def measure(cfg, steps, warmup, torch, dd, graphs=True):
+    inp, x = device_inputs(cfg, torch)
+    rows = dd.ROWS_PER_POSITION if cfg.rows == "position" else dd.ROWS_PER_NODE
+    rnd = dd.Round(x["E"], x["Wq"], cfg.C, cfg.L, cfg.K, cfg.W, cfg.B, cfg.beta, rows)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def step():
+        rnd.run(x["base"], x["hidden"], x["anchor"], x["target"])
+
+    step()
+    torch.cuda.synchronize()
+    if dd.read_status(rnd.ws) != 0:
+        raise RuntimeError(f"device status {dd.read_status(rnd.ws)}")
+    run = graphed(torch, step, graphs)
+    clocks = Clocks()
+    clocks.start()
+    t_round = time_steps(torch, run, steps, warmup, flush)
+    clk = clocks.stop()
+    acc = rnd.out["accepted_len"].float().mean().item()
+
+    # per-step breakdown through the individual entry points (same inputs, same stream)
+    V = x["E"].shape[0]
+    base2 = x["base"].view(cfg.C * cfg.L, V)
+    t_topk = time_steps(torch, graphed(torch, lambda: dd.topk(base2, cfg.K, ws=rnd.ws), graphs), steps, warmup,
+                        flush)
+    t_verify = time_steps(torch, graphed(torch, lambda: dd.verify(rnd.tree, x["target"], rows, cfg.L, ws=rnd.ws),
+                                         graphs), steps, warmup, flush)
+    return dict(inp=inp, x=x, rnd=rnd, t_round=t_round, t_topk=t_topk, t_verify=t_verify, clocks=clk,
+                accepted_mean=acc, rows=rows)
+
+
+def measure_e2e(cfg, m, steps, torch, dd):
+    """Same round through the public API with host buffers: H2D of the step's inputs
+    from pinned memory, the round, D2H of the verification result, all timed."""
+    x, rnd = m["x"], m["rnd"]
+    h = {k: x[k].cpu().pin_memory() for k in ("base", "hidden", "anchor", "target")}
+    d = {k: torch.empty_like(x[k]) for k in h}
+    outs = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in rnd.out.items()}
+    h2d = sum(v.numel() * v.element_size() for v in h.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+
+    def step():
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        o = rnd.run(d["base"], d["hidden"], d["anchor"], d["target"])
+        for k in outs:
+            outs[k].copy_(o[k], non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    e.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return ms, h2d, d2h
+
+
+def launches_per_round(cfg) -> int:
+    # topk 1 + root 1 + 3 per depth + prune 1 + mask 1 + verify 2 (per-position) or 1 (per-node)
+    return 1 + 1 + 3 * cfg.L + 2 + (2 if cfg.rows == "position" else 1)
+
+
+def roofline(cfg, m, hbm_peak):
+    alg = algorithmic(cfg, m["accepted_mean"])
+    parts = {"topk": (alg["topk"], float(np.median(m["t_topk"]))),
+             "verify": (alg["verify"], float(np.median(m["t_verify"])))}
+    t_round = float(np.median(m["t_round"]))
+    rest = max(t_round - parts["topk"][1] - parts["verify"][1], 1e-6)
+    parts["expand+prune+mask"] = (alg["expand"], rest)
+    dom = max(parts, key=lambda k: parts[k][1])
+    b, ms = parts[dom]
+    achieved = b / (ms * 1e-3) / 1e9
+    return dom, {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak, "unit": "GB/s",
+                 "frac": round(achieved / hbm_peak, 4), "traffic": None, "kernel": dom,
+                 "bytes_per_launch": int(b), "ms_per_launch": round(ms, 4)}, alg, parts
+
+
+# --------------------------------------------------------------------------- CPU oracle leg
+
+def cpu_baseline(cfg, budget_s=10.0):
+    import oracle
+    inp = make_inputs(cfg)
+    t0 = time.time()
+    n = 0
+    while True:
+        o = oracle.build(inp)
+        if cfg.rows == "position":
+            oracle.verify(o, inp["target"], cfg.dtype, cfg.rows, cfg.L)
+        n += 1
+        if time.time() - t0 > budget_s:
+            break
+    dt = time.time() - t0
+    return {"value": round(n / dt, 4), "unit": "rounds/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"{n} full oracle round(s) of {cfg.name} (build+verify, float64 numpy), {dt:.1f} s"}
+
+
+def cpu_baseline_stress(cfg, budget_requests=1):
+    """Oracle on a bounded sample of the C=64 batch (one request), scaled to rounds/s."""
+    import oracle
+    inp = make_inputs(cfg, requests=list(range(budget_requests)))
+    t0 = time.time()
+    oracle.build(inp)
+    dt = time.time() - t0
+    per_round = dt * cfg.C / budget_requests
+    return {"value": round(1.0 / per_round, 6), "unit": "rounds/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"oracle build of {budget_requests} of {cfg.C} requests ({dt:.1f} s), scaled to the batch"}
+
+
+# --------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-stress", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    cfg = make_config(MAIN_CFG)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        vals = []
+        for _ in range(args.warmup):
+            pass
+        t0 = time.time()
+        import oracle
+        inp = make_inputs(cfg)
+        for _ in range(args.steps):
+            s = time.time()
+            o = oracle.build(inp)
+            oracle.verify(o, inp["target"], cfg.dtype, cfg.rows, cfg.L)
+            vals.append(time.time() - s)
+        ms = float(np.mean(vals)) * 1e3
+        v = 1e3 / ms
+        print(json.dumps({
+            "impl": "reference", "metric": "draft-tree rounds/sec (build+verify)", "value": round(v, 4),
+            "unit": "rounds/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "C": cfg.C, "L": cfg.L, "V": cfg.V, "H": cfg.H, "K": cfg.K,
+                       "W": cfg.W, "B": cfg.B, "beta": cfg.beta},
+            "cpu_baseline": {"value": round(v, 4), "unit": "rounds/s", "cores": len(os.sched_getaffinity(0)),
+                             "kind": "oracle", "sample": f"{args.steps} full rounds of {cfg.name}"},
+            "e2e": {"value": round(v, 4), "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(time.time() - t0, 1)}))
+        return
+
+    import torch
+    import diffusion_drafter_draft_gb300 as dd
+    from diffusion_drafter_draft_gb300 import _build
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    _build.build()
+    dd.lib()
+    hbm_peak, tf_peak, peak_kind = _peaks()
+
+    m = measure(cfg, args.steps, max(3, args.warmup), torch, dd, graphs=not args.no_graph)
+    ms_local = float(np.sum(m["t_round"]))
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_local], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_local = float(tt.item())
+    ms = ms_local / args.steps
+    value = world * 1e3 / ms
+    dom, roof, alg, parts = roofline(cfg, m, hbm_peak)
+    e2e_ms, h2d, d2h = measure_e2e(cfg, m, min(args.steps, 20), torch, dd)
+    line = {
+        "metric": "draft-tree rounds/sec (build+verify)", "value": round(value, 3), "unit": "rounds/s",
+        "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5),
+        "us_per_round_p50": round(float(np.median(m["t_round"])) * 1e3, 2),
+        "us_per_round_p90": round(float(np.percentile(m["t_round"], 90)) * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "C": cfg.C, "L": cfg.L, "V": cfg.V, "H": cfg.H, "K": cfg.K, "W": cfg.W,
+                   "B": cfg.B, "beta": cfg.beta, "l2": "flushed between timed steps (2x L2 write)",
+                   "cuda_graph": not args.no_graph, "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": dict(roof, peak_kind=peak_kind),
+        "breakdown_ms": {k: round(v[1], 4) for k, v in parts.items()},
+        "accepted_mean": m["accepted_mean"],
+        "gpu_launches": launches_per_round(cfg) * args.steps,
+        "e2e": {"value": round(1e3 / e2e_ms, 3), "unit": "rounds/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "clocks": m["clocks"],
+    }
+    del m
+    torch.cuda.empty_cache()
+    if not args.no_stress:
+        scfg = make_config(STRESS_CFG)
+        sm = measure(scfg, max(5, min(args.steps, 20)), 3, torch, dd, graphs=not args.no_graph)
+        sdom, sroof, salg, sparts = roofline(scfg, sm, hbm_peak)
+        sms = float(np.median(sm["t_round"]))
+        line["c64"] = {"workload": scfg.name, "value": round(1e3 / sms, 3), "unit": "rounds/s",
+                       "request_rounds_per_s": round(scfg.C * 1e3 / sms, 1), "us_per_round_p50": round(sms * 1e3, 1),
+                       "roofline": dict(sroof, peak_kind=peak_kind),
+                       "round_hbm_frac": round(salg["total"] / (sms * 1e-3) / 1e9 / hbm_peak, 4),
+                       "round_tensor_frac": round(salg["flops"] / (sms * 1e-3) / 1e12 / tf_peak, 4),
+                       "breakdown_ms": {k: round(v[1], 4) for k, v in sparts.items()},
+                       "accepted_mean": sm["accepted_mean"], "clocks": sm["clocks"]}
+        del sm
+        torch.cuda.empty_cache()
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(cfg)
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

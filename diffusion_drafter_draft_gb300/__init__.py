@@ -1,0 +1,352 @@
+"""Python binding of libdartree.so, the sm_103a DARTree draft-tree build and verify step.
+
+Argument marshalling only: every step runs in the library's CUDA kernels. Tensors
+are torch CUDA tensors (PyTorch supplies device memory and the current stream);
+they are passed to the C ABI as raw device pointers. There is no CPU fallback:
+if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "DartreeError", "lib", "library_path", "F32", "BF16", "ROWS_PER_POSITION", "ROWS_PER_NODE",
+    "workspace_bytes", "new_workspace", "topk", "expand", "prune", "tree_mask", "build_tree",
+    "verify", "read_status", "clear_status", "Round", "EXPORTS",
+]
+
+F32, BF16 = 0, 1
+ROWS_PER_POSITION, ROWS_PER_NODE = 0, 1
+OK, EINVAL, EDTYPE, EWORKSPACE, ECUDA, ETIMEOUT, EINTERNAL, EUNSUPPORTED = 0, -1, -2, -3, -4, -5, -6, -7
+
+EXPORTS = ("dartree_head_init", "dartree_workspace_bytes", "dartree_topk", "dartree_expand", "dartree_prune",
+           "dartree_tree_mask", "dartree_build_tree", "dartree_verify", "dartree_read_status",
+           "dartree_clear_status", "dartree_status_string")
+
+
+class DartreeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {code} ({status_string(code)})")
+
+
+class Head(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_void_p), ("Wq", ctypes.c_void_p), ("V", ctypes.c_int), ("H", ctypes.c_int),
+                ("dtype", ctypes.c_int)]
+
+
+class Params(ctypes.Structure):
+    _fields_ = [("C", ctypes.c_int), ("L", ctypes.c_int), ("K", ctypes.c_int), ("W", ctypes.c_int),
+                ("B", ctypes.c_int), ("beta", ctypes.c_float)]
+
+
+class Candidates(ctypes.Structure):
+    _fields_ = [("tok", ctypes.c_void_p), ("logit", ctypes.c_void_p)]
+
+
+class Supertree(ctypes.Structure):
+    _fields_ = [("tok", ctypes.c_void_p), ("par", ctypes.c_void_p), ("score", ctypes.c_void_p),
+                ("n", ctypes.c_void_p)]
+
+
+class Tree(ctypes.Structure):
+    _fields_ = [("tok", ctypes.c_void_p), ("par", ctypes.c_void_p), ("depth", ctypes.c_void_p),
+                ("score", ctypes.c_void_p), ("n_nodes", ctypes.c_void_p), ("mask", ctypes.c_void_p),
+                ("pos", ctypes.c_void_p)]
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdartree.so")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with diffusion_drafter_draft_gb300._build.build()")
+    L = ctypes.CDLL(path)
+    vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    P = ctypes.POINTER
+    sig = {
+        "dartree_head_init": (i, [P(Head), vp, vp, i, i, i]),
+        "dartree_workspace_bytes": (sz, [P(Params), i, i, i]),
+        "dartree_topk": (i, [vp, i, i, i, i, vp, vp, vp, sz, vp]),
+        "dartree_expand": (i, [P(Head), P(Params), vp, vp, P(Candidates), P(Supertree), vp, sz, vp]),
+        "dartree_prune": (i, [P(Params), P(Supertree), vp, P(Tree), vp]),
+        "dartree_tree_mask": (i, [P(Params), P(Tree), vp]),
+        "dartree_build_tree": (i, [P(Head), P(Params), vp, vp, vp, P(Tree), P(Supertree), P(Candidates), vp, sz,
+                                   vp]),
+        "dartree_verify": (i, [P(Params), P(Tree), vp, i, i, i, vp, vp, vp, vp, sz, vp]),
+        "dartree_read_status": (i, [vp, P(ctypes.c_int32), vp]),
+        "dartree_clear_status": (i, [vp, vp]),
+        "dartree_status_string": (ctypes.c_char_p, [i]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype, f.argtypes = res, args
+    _LIB = L
+    return L
+
+
+def status_string(code: int) -> str:
+    try:
+        return lib().dartree_status_string(code).decode()
+    except Exception:  # library missing while formatting an error
+        return "?"
+
+
+def _call(name: str, *args) -> None:
+    rc = getattr(lib(), name)(*args)
+    if rc != OK:
+        raise DartreeError(rc, name)
+
+
+# --------------------------------------------------------------------------- tensors
+
+_DT = {torch.float32: F32, torch.bfloat16: BF16}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DT:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    return _DT[t.dtype]
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, shape=None) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _params(C, L, K, W, B, beta) -> Params:
+    return Params(int(C), int(L), int(K), int(W), int(B), float(beta))
+
+
+def workspace_bytes(C, L, K, W, B, beta, V, H, dtype_code) -> int:
+    n = lib().dartree_workspace_bytes(ctypes.byref(_params(C, L, K, W, B, beta)), int(V), int(H), int(dtype_code))
+    if n == 0:
+        raise DartreeError(EINVAL, "dartree_workspace_bytes")
+    return int(n)
+
+
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    ws = torch.zeros(int(nbytes), dtype=torch.uint8, device=device or "cuda")
+    if ws.data_ptr() % 256:
+        raise RuntimeError("workspace is not 256-byte aligned")
+    return ws
+
+
+def read_status(ws: torch.Tensor, stream=None) -> int:
+    v = ctypes.c_int32(0)
+    _call("dartree_read_status", ctypes.c_void_p(ws.data_ptr()), ctypes.byref(v), _stream(stream))
+    return int(v.value)
+
+
+def clear_status(ws: torch.Tensor, stream=None) -> None:
+    _call("dartree_clear_status", ctypes.c_void_p(ws.data_ptr()), _stream(stream))
+
+
+def _head(E: torch.Tensor, Wq: torch.Tensor) -> Head:
+    V, H = E.shape
+    _need(E, "E")
+    _need(Wq, "Wq", E.dtype, (H, H))
+    h = Head()
+    _call("dartree_head_init", ctypes.byref(h), ctypes.c_void_p(E.data_ptr()), ctypes.c_void_p(Wq.data_ptr()),
+          int(V), int(H), _dtype_code(E))
+    return h
+
+
+# --------------------------------------------------------------------------- steps
+
+def topk(logits: torch.Tensor, K: int, ws: torch.Tensor | None = None, stream=None):
+    """S1: top-K of every row of logits [rows, V] -> (tok int32 [rows, K], val float32 [rows, K])."""
+    rows, V = logits.shape
+    _need(logits, "logits")
+    dev = logits.device
+    tok = torch.empty((rows, K), dtype=torch.int32, device=dev)
+    val = torch.empty((rows, K), dtype=torch.float32, device=dev)
+    ws = ws if ws is not None else new_workspace(256, dev)
+    _call("dartree_topk", ctypes.c_void_p(logits.data_ptr()), int(rows), int(V), int(K), _dtype_code(logits),
+          ctypes.c_void_p(tok.data_ptr()), ctypes.c_void_p(val.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
+          ws.numel(), _stream(stream))
+    return tok, val
+
+
+def _alloc_supertree(C, L, W, dev):
+    return dict(tok=torch.empty((C, L, W), dtype=torch.int32, device=dev),
+                par=torch.empty((C, L, W), dtype=torch.int32, device=dev),
+                score=torch.empty((C, L, W), dtype=torch.float32, device=dev),
+                n=torch.empty((C, L), dtype=torch.int32, device=dev))
+
+
+def _st_struct(st) -> Supertree:
+    return Supertree(st["tok"].data_ptr(), st["par"].data_ptr(), st["score"].data_ptr(), st["n"].data_ptr())
+
+
+def _alloc_tree(C, B, dev, with_mask=True):
+    S = B + 1
+    t = dict(tok=torch.empty((C, S), dtype=torch.int32, device=dev),
+             par=torch.empty((C, S), dtype=torch.int32, device=dev),
+             depth=torch.empty((C, S), dtype=torch.int32, device=dev),
+             score=torch.empty((C, S), dtype=torch.float32, device=dev),
+             n_nodes=torch.empty((C,), dtype=torch.int32, device=dev))
+    if with_mask:
+        t["mask"] = torch.empty((C, S, S), dtype=torch.uint8, device=dev)
+        t["pos"] = torch.empty((C, S), dtype=torch.int32, device=dev)
+    return t
+
+
+def _tree_struct(t) -> Tree:
+    g = lambda k: t[k].data_ptr() if k in t and t[k] is not None else None  # noqa: E731
+    return Tree(g("tok"), g("par"), g("depth"), g("score"), g("n_nodes"), g("mask"), g("pos"))
+
+
+def expand(E, Wq, hidden, anchor, cand_tok, cand_val, W, beta, ws=None, stream=None):
+    """S2-S7 from a candidate table -> supertree dict (tok, par, score, n)."""
+    C, L, H = hidden.shape
+    K = cand_tok.shape[-1]
+    head = _head(E, Wq)
+    _need(hidden, "hidden", E.dtype, (C, L, H))
+    _need(anchor, "anchor", torch.int32, (C,))
+    _need(cand_tok, "cand_tok", torch.int32, (C, L, K))
+    _need(cand_val, "cand_val", torch.float32, (C, L, K))
+    p = _params(C, L, K, W, 1, beta)
+    ws = ws if ws is not None else new_workspace(workspace_bytes(C, L, K, W, 1, beta, E.shape[0], H, head.dtype),
+                                                 hidden.device)
+    st = _alloc_supertree(C, L, W, hidden.device)
+    cand = Candidates(cand_tok.data_ptr(), cand_val.data_ptr())
+    sts = _st_struct(st)
+    _call("dartree_expand", ctypes.byref(head), ctypes.byref(p), ctypes.c_void_p(hidden.data_ptr()),
+          ctypes.c_void_p(anchor.data_ptr()), ctypes.byref(cand), ctypes.byref(sts), ctypes.c_void_p(ws.data_ptr()),
+          ws.numel(), _stream(stream))
+    return st
+
+
+def prune(st, anchor, B, stream=None):
+    """S8: deferred pruning of a supertree -> tree dict (tok, par, depth, score, n_nodes)."""
+    C, L, W = st["tok"].shape
+    for k in ("tok", "par", "n"):
+        _need(st[k], k, torch.int32)
+    _need(st["score"], "score", torch.float32)
+    _need(anchor, "anchor", torch.int32, (C,))
+    t = _alloc_tree(C, B, anchor.device, with_mask=False)
+    p = _params(C, L, 1, W, B, 0.0)
+    ts, sts = _tree_struct(t), _st_struct(st)
+    _call("dartree_prune", ctypes.byref(p), ctypes.byref(sts), ctypes.c_void_p(anchor.data_ptr()), ctypes.byref(ts),
+          _stream(stream))
+    return t
+
+
+def tree_mask(tree, L, stream=None):
+    """S9: adds mask and pos to a tree dict (in place) and returns it."""
+    C, S = tree["par"].shape
+    for k in ("par", "depth", "n_nodes"):
+        _need(tree[k], k, torch.int32)
+    tree["mask"] = torch.empty((C, S, S), dtype=torch.uint8, device=tree["par"].device)
+    tree["pos"] = torch.empty((C, S), dtype=torch.int32, device=tree["par"].device)
+    p = _params(C, L, 1, 1, S - 1, 0.0)
+    ts = _tree_struct(tree)
+    _call("dartree_tree_mask", ctypes.byref(p), ctypes.byref(ts), _stream(stream))
+    return tree
+
+
+def verify(tree, target, rows: int, L: int, ws=None, stream=None):
+    """S10: greedy longest accepted prefix -> dict(accepted_len, path, bonus)."""
+    C, S = tree["tok"].shape
+    V = target.shape[-1]
+    _need(target, "target", None, (C, L, V) if rows == ROWS_PER_POSITION else (C, S, V))
+    dev = target.device
+    out = dict(accepted_len=torch.empty((C,), dtype=torch.int32, device=dev),
+               path=torch.empty((C, L), dtype=torch.int32, device=dev),
+               bonus=torch.empty((C,), dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = new_workspace(256 + 8 * C * max(L, S), dev)
+    p = _params(C, L, 1, 1, S - 1, 0.0)
+    ts = _tree_struct(tree)
+    _call("dartree_verify", ctypes.byref(p), ctypes.byref(ts), ctypes.c_void_p(target.data_ptr()), int(rows), int(V),
+          _dtype_code(target), ctypes.c_void_p(out["accepted_len"].data_ptr()), ctypes.c_void_p(out["path"].data_ptr()),
+          ctypes.c_void_p(out["bonus"].data_ptr()), ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
+    return out
+
+
+def build_tree(E, Wq, base, hidden, anchor, K, W, B, beta, ws=None, keep_intermediates=False, stream=None):
+    """S1-S9: one tree build -> tree dict (+ 'cand_tok', 'cand_val', 'st' when keep_intermediates)."""
+    C, L, V = base.shape
+    H = E.shape[1]
+    head = _head(E, Wq)
+    _need(base, "base", E.dtype, (C, L, V))
+    _need(hidden, "hidden", E.dtype, (C, L, H))
+    _need(anchor, "anchor", torch.int32, (C,))
+    dev = base.device
+    p = _params(C, L, K, W, B, beta)
+    ws = ws if ws is not None else new_workspace(workspace_bytes(C, L, K, W, B, beta, V, H, head.dtype), dev)
+    t = _alloc_tree(C, B, dev)
+    ts = _tree_struct(t)
+    st_p = cand_p = None
+    if keep_intermediates:
+        st = _alloc_supertree(C, L, W, dev)
+        t["st"] = st
+        t["cand_tok"] = torch.empty((C, L, K), dtype=torch.int32, device=dev)
+        t["cand_val"] = torch.empty((C, L, K), dtype=torch.float32, device=dev)
+        st_p = ctypes.byref(_st_struct(st))
+        cand_p = ctypes.byref(Candidates(t["cand_tok"].data_ptr(), t["cand_val"].data_ptr()))
+    _call("dartree_build_tree", ctypes.byref(head), ctypes.byref(p), ctypes.c_void_p(base.data_ptr()),
+          ctypes.c_void_p(hidden.data_ptr()), ctypes.c_void_p(anchor.data_ptr()), ctypes.byref(ts), st_p, cand_p,
+          ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
+    return t
+
+
+class Round:
+    """One draft round (build + verify) with every buffer allocated once.
+
+    run() enqueues dartree_build_tree and dartree_verify on the current stream and
+    allocates nothing, so it can be timed, repeated or captured in a CUDA graph.
+    """
+
+    def __init__(self, E, Wq, C, L, K, W, B, beta, rows, device=None):
+        self.E, self.Wq = E, Wq
+        self.V, self.H = E.shape
+        self.C, self.L, self.K, self.W, self.B, self.beta, self.rows = C, L, K, W, B, beta, rows
+        dev = device or E.device
+        self.head = _head(E, Wq)
+        self.p = _params(C, L, K, W, B, beta)
+        self.ws = new_workspace(workspace_bytes(C, L, K, W, B, beta, self.V, self.H, self.head.dtype), dev)
+        self.tree = _alloc_tree(C, B, dev)
+        self._ts = _tree_struct(self.tree)
+        self.out = dict(accepted_len=torch.empty((C,), dtype=torch.int32, device=dev),
+                        path=torch.empty((C, L), dtype=torch.int32, device=dev),
+                        bonus=torch.empty((C,), dtype=torch.int32, device=dev))
+        self.dtype_code = self.head.dtype
+
+    def run(self, base, hidden, anchor, target, stream=None):
+        s = _stream(stream)
+        _call("dartree_build_tree", ctypes.byref(self.head), ctypes.byref(self.p), ctypes.c_void_p(base.data_ptr()),
+              ctypes.c_void_p(hidden.data_ptr()), ctypes.c_void_p(anchor.data_ptr()), ctypes.byref(self._ts), None,
+              None, ctypes.c_void_p(self.ws.data_ptr()), self.ws.numel(), s)
+        _call("dartree_verify", ctypes.byref(self.p), ctypes.byref(self._ts), ctypes.c_void_p(target.data_ptr()),
+              int(self.rows), int(self.V), int(self.dtype_code), ctypes.c_void_p(self.out["accepted_len"].data_ptr()),
+              ctypes.c_void_p(self.out["path"].data_ptr()), ctypes.c_void_p(self.out["bonus"].data_ptr()),
+              ctypes.c_void_p(self.ws.data_ptr()), self.ws.numel(), s)
+        return self.out

@@ -1,0 +1,247 @@
+// C ABI of the DARTree draft-tree build and verify step: argument checks,
+// workspace carving and kernel launches on the caller's stream.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "dartree.h"
+#include "kernels.h"
+
+namespace {
+
+using namespace dartree;
+
+constexpr size_t kAlign = 256;
+
+size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+    size_t status, cand_tok, cand_val, h[2], s[2], U, z, st_tok, st_par, st_s, st_n, keys, total;
+};
+
+Layout layout_of(const dartree_params& p, int H, int dtype) {
+    const size_t C = size_t(p.C), L = size_t(p.L), K = size_t(p.K), W = size_t(p.W), B = size_t(p.B);
+    const size_t elem = dtype == DARTREE_BF16 ? 2 : 4;
+    Layout l{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o += up(bytes); return at; };
+    l.status = take(4);
+    l.cand_tok = take(C * L * K * 4);
+    l.cand_val = take(C * L * K * 4);
+    l.h[0] = take(C * W * size_t(H) * elem);
+    l.h[1] = take(C * W * size_t(H) * elem);
+    l.s[0] = take(C * W * 4);
+    l.s[1] = take(C * W * 4);
+    l.U = take(C * W * size_t(H) * 4);
+    l.z = take(C * W * K * 4);
+    l.st_tok = take(C * L * W * 4);
+    l.st_par = take(C * L * W * 4);
+    l.st_s = take(C * L * W * 4);
+    l.st_n = take(C * L * 4);
+    l.keys = take((C * L > C * (B + 1) ? C * L : C * (B + 1)) * 8);
+    l.total = o;
+    return l;
+}
+
+bool dtype_ok(int dt) { return dt == DARTREE_F32 || dt == DARTREE_BF16; }
+
+int check_params(const dartree_params* p, int V, int H, int dtype) {
+    if (!p) return DARTREE_EINVAL;
+    if (!dtype_ok(dtype)) return DARTREE_EDTYPE;
+    if (p->C < 0 || p->L < 1 || p->K < 1 || p->W < 1 || p->B < 1 || V < 1 || H < 8) return DARTREE_EINVAL;
+    if (H % 8 != 0) return DARTREE_EINVAL;
+    if (!(p->beta <= 0.0f)) return DARTREE_EINVAL;  // also rejects NaN
+    if (p->K > V) return DARTREE_EINVAL;
+    if (p->B > p->L * p->W) return DARTREE_EINVAL;
+    if (p->L > DARTREE_MAX_L || p->K > DARTREE_MAX_K || p->W > DARTREE_MAX_W || p->B + 1 > DARTREE_MAX_SLOTS ||
+        p->W * p->K > DARTREE_MAX_CHILDREN)
+        return DARTREE_EUNSUPPORTED;
+    return DARTREE_OK;
+}
+
+int check_ws(const void* ws, size_t have, size_t need) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0 || have < need) return DARTREE_EWORKSPACE;
+    return DARTREE_OK;
+}
+
+template <typename P>
+P* at(void* ws, size_t off) { return reinterpret_cast<P*>(static_cast<uint8_t*>(ws) + off); }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+const char* dartree_status_string(int s) {
+    switch (s) {
+        case DARTREE_OK: return "ok";
+        case DARTREE_EINVAL: return "invalid argument";
+        case DARTREE_EDTYPE: return "unknown dtype or row mode";
+        case DARTREE_EWORKSPACE: return "workspace null, misaligned or too small";
+        case DARTREE_ECUDA: return "CUDA call or launch failed";
+        case DARTREE_ETIMEOUT: return "a bounded device-side wait ran out";
+        case DARTREE_EINTERNAL: return "device-side consistency check failed";
+        case DARTREE_EUNSUPPORTED: return "sizes beyond the library limits";
+        default: return "unknown status";
+    }
+}
+
+int dartree_head_init(dartree_head* head, const void* E, const void* Wq, int V, int H, int dtype) {
+    if (!head || !E || !Wq || V < 1 || H < 8 || H % 8 != 0) return DARTREE_EINVAL;
+    if (!dtype_ok(dtype)) return DARTREE_EDTYPE;
+    head->E = E;
+    head->Wq = Wq;
+    head->V = V;
+    head->H = H;
+    head->dtype = dtype;
+    return DARTREE_OK;
+}
+
+size_t dartree_workspace_bytes(const dartree_params* p, int V, int H, int dtype) {
+    if (check_params(p, V, H, dtype) != DARTREE_OK) return 0;
+    return layout_of(*p, H, dtype).total;
+}
+
+int dartree_read_status(const void* ws, int32_t* status, void* stream) {
+    if (!ws || !status) return DARTREE_EINVAL;
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, as_stream(stream)) != cudaSuccess)
+        return DARTREE_ECUDA;
+    if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return DARTREE_ECUDA;
+    *status = v;
+    return DARTREE_OK;
+}
+
+int dartree_clear_status(void* ws, void* stream) {
+    if (!ws) return DARTREE_EINVAL;
+    return cudaMemsetAsync(ws, 0, sizeof(int32_t), as_stream(stream)) == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
+}
+
+int dartree_topk(const void* logits, int rows, int V, int K, int dtype, int32_t* tok, float* val, void* ws,
+                 size_t ws_bytes, void* stream) {
+    if (!dtype_ok(dtype)) return DARTREE_EDTYPE;
+    if (rows < 0 || V < 1 || K < 1 || K > V) return DARTREE_EINVAL;
+    if (K > DARTREE_MAX_K) return DARTREE_EUNSUPPORTED;
+    if (rows > 0 && (!logits || !tok || !val)) return DARTREE_EINVAL;
+    if (int e = check_ws(ws, ws_bytes, kAlign)) return e;
+    return launch_topk(logits, rows, V, K, dtype, tok, val, at<int>(ws, 0), as_stream(stream));
+}
+
+static int expand_impl(const dartree_head* head, const dartree_params* p, const void* hidden, const int32_t* anchor,
+                       const int32_t* cand_tok, const float* cand_val, const dartree_supertree* st, void* ws,
+                       const Layout& l, cudaStream_t stream) {
+    ExpandArgs a{};
+    a.E = head->E;
+    a.Wq = head->Wq;
+    a.V = head->V;
+    a.H = head->H;
+    a.dtype = head->dtype;
+    a.C = p->C;
+    a.L = p->L;
+    a.K = p->K;
+    a.W = p->W;
+    a.beta = p->beta;
+    a.hidden = hidden;
+    a.anchor = anchor;
+    a.cand_tok = cand_tok;
+    a.cand_val = cand_val;
+    a.st_tok = st->tok;
+    a.st_par = st->par;
+    a.st_s = st->score;
+    a.st_n = st->n;
+    a.hbuf[0] = at<void>(ws, l.h[0]);
+    a.hbuf[1] = at<void>(ws, l.h[1]);
+    a.sbuf[0] = at<float>(ws, l.s[0]);
+    a.sbuf[1] = at<float>(ws, l.s[1]);
+    a.U = at<float>(ws, l.U);
+    a.z = at<float>(ws, l.z);
+    a.status = at<int>(ws, l.status);
+    return launch_expand(a, stream);
+}
+
+static bool st_ok(const dartree_supertree* st) { return st && st->tok && st->par && st->score && st->n; }
+
+int dartree_expand(const dartree_head* head, const dartree_params* p, const void* block_hidden, const int32_t* anchor,
+                   const dartree_candidates* cand, dartree_supertree* st, void* ws, size_t ws_bytes, void* stream) {
+    if (!head) return DARTREE_EINVAL;
+    if (int e = check_params(p, head->V, head->H, head->dtype)) return e;
+    if (p->C == 0) return DARTREE_OK;
+    if (!head->E || !head->Wq || !block_hidden || !anchor || !cand || !cand->tok || !cand->logit || !st_ok(st))
+        return DARTREE_EINVAL;
+    const Layout l = layout_of(*p, head->H, head->dtype);
+    if (int e = check_ws(ws, ws_bytes, l.total)) return e;
+    return expand_impl(head, p, block_hidden, anchor, cand->tok, cand->logit, st, ws, l, as_stream(stream));
+}
+
+int dartree_prune(const dartree_params* p, const dartree_supertree* st, const int32_t* anchor, dartree_tree* tree,
+                  void* stream) {
+    if (!p || p->C < 0 || p->L < 1 || p->W < 1 || p->B < 1 || p->B > p->L * p->W) return DARTREE_EINVAL;
+    if (p->L > DARTREE_MAX_L || p->W > DARTREE_MAX_W || p->B + 1 > DARTREE_MAX_SLOTS) return DARTREE_EUNSUPPORTED;
+    if (p->C == 0) return DARTREE_OK;
+    if (!st_ok(st) || !anchor || !tree || !tree->tok || !tree->par || !tree->depth || !tree->score || !tree->n_nodes)
+        return DARTREE_EINVAL;
+    return launch_prune(p->C, p->L, p->W, p->B, st->tok, st->par, st->score, st->n, anchor, tree->tok, tree->par,
+                        tree->depth, tree->score, tree->n_nodes, nullptr, as_stream(stream));
+}
+
+int dartree_tree_mask(const dartree_params* p, dartree_tree* tree, void* stream) {
+    if (!p || p->C < 0 || p->L < 1 || p->B < 1) return DARTREE_EINVAL;
+    if (p->L > DARTREE_MAX_L || p->B + 1 > DARTREE_MAX_SLOTS) return DARTREE_EUNSUPPORTED;
+    if (p->C == 0) return DARTREE_OK;
+    if (!tree || !tree->par || !tree->depth || !tree->n_nodes || !tree->mask || !tree->pos) return DARTREE_EINVAL;
+    return launch_mask(p->C, p->L, p->B, tree->par, tree->depth, tree->n_nodes, tree->mask, tree->pos,
+                       as_stream(stream));
+}
+
+int dartree_build_tree(const dartree_head* head, const dartree_params* p, const void* base_logits,
+                       const void* block_hidden, const int32_t* anchor, dartree_tree* tree, dartree_supertree* st,
+                       dartree_candidates* cand, void* ws, size_t ws_bytes, void* stream) {
+    if (!head) return DARTREE_EINVAL;
+    if (int e = check_params(p, head->V, head->H, head->dtype)) return e;
+    if (p->C == 0) return DARTREE_OK;
+    if (!head->E || !head->Wq || !base_logits || !block_hidden || !anchor || !tree || !tree->tok || !tree->par ||
+        !tree->depth || !tree->score || !tree->n_nodes)
+        return DARTREE_EINVAL;
+    if ((tree->mask == nullptr) != (tree->pos == nullptr)) return DARTREE_EINVAL;
+    if (st && !st_ok(st)) return DARTREE_EINVAL;
+    if (cand && (!cand->tok || !cand->logit)) return DARTREE_EINVAL;
+    const Layout l = layout_of(*p, head->H, head->dtype);
+    if (int e = check_ws(ws, ws_bytes, l.total)) return e;
+    cudaStream_t s = as_stream(stream);
+    int32_t* ct = cand ? cand->tok : at<int32_t>(ws, l.cand_tok);
+    float* cv = cand ? cand->logit : at<float>(ws, l.cand_val);
+    dartree_supertree wst{at<int32_t>(ws, l.st_tok), at<int32_t>(ws, l.st_par), at<float>(ws, l.st_s),
+                          at<int32_t>(ws, l.st_n)};
+    const dartree_supertree* sp = st ? st : &wst;
+    int* status = at<int>(ws, l.status);
+    if (int e = launch_topk(base_logits, p->C * p->L, head->V, p->K, head->dtype, ct, cv, status, s)) return e;
+    if (int e = expand_impl(head, p, block_hidden, anchor, ct, cv, sp, ws, l, s)) return e;
+    if (int e = launch_prune(p->C, p->L, p->W, p->B, sp->tok, sp->par, sp->score, sp->n, anchor, tree->tok, tree->par,
+                             tree->depth, tree->score, tree->n_nodes, status, s))
+        return e;
+    if (tree->mask)
+        return launch_mask(p->C, p->L, p->B, tree->par, tree->depth, tree->n_nodes, tree->mask, tree->pos, s);
+    return DARTREE_OK;
+}
+
+int dartree_verify(const dartree_params* p, const dartree_tree* tree, const void* target, int rows, int V, int dtype,
+                   int32_t* accepted_len, int32_t* path, int32_t* bonus, void* ws, size_t ws_bytes, void* stream) {
+    if (!p || p->C < 0 || p->L < 1 || p->B < 1 || V < 1) return DARTREE_EINVAL;
+    if (!dtype_ok(dtype) || (rows != DARTREE_ROWS_PER_POSITION && rows != DARTREE_ROWS_PER_NODE))
+        return DARTREE_EDTYPE;
+    if (p->L > DARTREE_MAX_L || p->B + 1 > DARTREE_MAX_SLOTS) return DARTREE_EUNSUPPORTED;
+    if (p->C == 0) return DARTREE_OK;
+    if (!tree || !tree->tok || !tree->par || !tree->depth || !tree->n_nodes || !target || !accepted_len || !path ||
+        !bonus)
+        return DARTREE_EINVAL;
+    const size_t keys_bytes = size_t(p->C) * (p->L > p->B + 1 ? p->L : p->B + 1) * 8;
+    if (int e = check_ws(ws, ws_bytes, kAlign + keys_bytes)) return e;
+    // row keys sit right after the status word (scratch of the build is dead by then)
+    const size_t keys_off = kAlign;
+    return launch_verify(p->C, p->L, p->B, tree->tok, tree->par, tree->depth, tree->n_nodes, target, rows, V, dtype,
+                         at<unsigned long long>(ws, keys_off), accepted_len, path, bonus, at<int>(ws, 0),
+                         as_stream(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,295 @@
+// S2-S7: depth-wise tree expansion with the stand-in correction head
+// (DARTree blog post, 3.1 "Basic flow": depth-wise expansion, scoring function,
+// per-depth pruning; the ainews.surl.tw article: all active branches are
+// processed in batches, one tree depth at a time).
+//
+// Per depth d = 1..L, over all C requests at once:
+//   proj     U[m, :] = W_q h_m              (all C*P parents in one matrix product)
+//   contract z[r, p, c] = L^base[r, d-1, c] + <U[r*P+p], E[cand_c]> / sqrt(H)
+//   select   log q = z - logsumexp_c z; s = s_p + log q + beta;
+//            keep the top-W children by (s desc, flat index p*K+c asc);
+//            h_child = RMSNorm(h_p + E[tok] + H_d[d-1]) stored in the input type.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dartree {
+
+// --------------------------------------------------------------------------- root
+
+template <typename T>
+__global__ void root_init_kernel(const T* __restrict__ E, const int32_t* __restrict__ anchor, int H,
+                                 T* __restrict__ h0, float* __restrict__ s0) {
+    const int r = blockIdx.x;
+    const T* e = E + size_t(anchor[r]) * H;
+    for (int j = threadIdx.x; j < H; j += blockDim.x) h0[size_t(r) * H + j] = e[j];
+    if (threadIdx.x == 0) s0[r] = 0.f;
+}
+
+// --------------------------------------------------------------------------- projection (CUDA cores)
+
+constexpr int PJ_TM = 32, PJ_TN = 64, PJ_TK = 32, PJ_NT = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(PJ_NT) proj_simple_kernel(const T* __restrict__ h, const T* __restrict__ Wq,
+                                                            float* __restrict__ U, int M, int H) {
+    __shared__ float hs[PJ_TK][PJ_TM + 1];
+    __shared__ float ws[PJ_TK][PJ_TN + 1];
+    const int m0 = blockIdx.y * PJ_TM, n0 = blockIdx.x * PJ_TN;
+    const int tm = threadIdx.x / 16, tn = threadIdx.x % 16;  // 2 rows x 4 cols per thread
+    float acc[2][4] = {};
+    for (int k0 = 0; k0 < H; k0 += PJ_TK) {
+        for (int i = threadIdx.x; i < PJ_TM * PJ_TK; i += PJ_NT) {
+            const int mm = i / PJ_TK, kk = i % PJ_TK;
+            const int m = m0 + mm, k = k0 + kk;
+            hs[kk][mm] = (m < M && k < H) ? to_float(h[size_t(m) * H + k]) : 0.f;
+        }
+        for (int i = threadIdx.x; i < PJ_TN * PJ_TK; i += PJ_NT) {
+            const int nn = i / PJ_TK, kk = i % PJ_TK;
+            const int n = n0 + nn, k = k0 + kk;
+            ws[kk][nn] = (n < H && k < H) ? to_float(Wq[size_t(n) * H + k]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < PJ_TK; ++kk) {
+            const float a0 = hs[kk][tm * 2], a1 = hs[kk][tm * 2 + 1];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float b = ws[kk][tn + 16 * q];
+                acc[0][q] = fmaf(a0, b, acc[0][q]);
+                acc[1][q] = fmaf(a1, b, acc[1][q]);
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+        const int m = m0 + tm * 2 + a;
+        if (m >= M) continue;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int n = n0 + tn + 16 * q;
+            if (n < H) U[size_t(m) * H + n] = acc[a][q];
+        }
+    }
+}
+
+// --------------------------------------------------------------------------- candidate contraction (CUDA cores)
+
+constexpr int CT_NT = 256, CT_CPW = 4, CT_PT = 16;  // candidates per warp, parents per pass
+
+template <typename T>
+__device__ __forceinline__ void load4(const T* p, float (&v)[4]);
+template <>
+__device__ __forceinline__ void load4<float>(const float* p, float (&v)[4]) {
+    const float4 x = *reinterpret_cast<const float4*>(p);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+}
+template <>
+__device__ __forceinline__ void load4<bf16_t>(const bf16_t* p, float (&v)[4]) {
+    const uint2 x = *reinterpret_cast<const uint2*>(p);
+    v[0] = bf16_bits_to_float(x.x & 0xffffu); v[1] = bf16_bits_to_float(x.x >> 16);
+    v[2] = bf16_bits_to_float(x.y & 0xffffu); v[3] = bf16_bits_to_float(x.y >> 16);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(CT_NT) contract_simple_kernel(const float* __restrict__ U, const T* __restrict__ E,
+                                                                const int32_t* __restrict__ cand_tok,
+                                                                const float* __restrict__ cand_val,
+                                                                float* __restrict__ z, int P, int K, int H, int L,
+                                                                int d, float inv_sqrt_h) {
+    const int r = blockIdx.y;
+    const size_t crow = (size_t(r) * L + (d - 1)) * K;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int cbase = (blockIdx.x * (CT_NT / 32) + wid) * CT_CPW;
+    if (cbase >= K) return;
+    const T* erow[CT_CPW];
+#pragma unroll
+    for (int q = 0; q < CT_CPW; ++q) {
+        const int c = min(cbase + q, K - 1);
+        erow[q] = E + size_t(cand_tok[crow + c]) * H;
+    }
+    for (int p0 = 0; p0 < P; p0 += CT_PT) {
+        float acc[CT_PT][CT_CPW];
+#pragma unroll
+        for (int p = 0; p < CT_PT; ++p)
+#pragma unroll
+            for (int q = 0; q < CT_CPW; ++q) acc[p][q] = 0.f;
+        for (int j = lane * 4; j < H; j += 128) {
+            float e[CT_CPW][4];
+#pragma unroll
+            for (int q = 0; q < CT_CPW; ++q) load4<T>(erow[q] + j, e[q]);
+#pragma unroll
+            for (int p = 0; p < CT_PT; ++p) {
+                if (p0 + p < P) {
+                    float u[4];
+                    load4<float>(U + (size_t(r) * P + p0 + p) * H + j, u);
+#pragma unroll
+                    for (int q = 0; q < CT_CPW; ++q)
+                        acc[p][q] = fmaf(u[0], e[q][0], fmaf(u[1], e[q][1], fmaf(u[2], e[q][2], fmaf(u[3], e[q][3], acc[p][q]))));
+                }
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < CT_PT; ++p) {
+            if (p0 + p >= P) break;
+#pragma unroll
+            for (int q = 0; q < CT_CPW; ++q) {
+                const float s = warp_sum(acc[p][q]);
+                const int c = cbase + q;
+                if (lane == 0 && c < K)
+                    z[(size_t(r) * P + p0 + p) * K + c] = cand_val[crow + c] + s * inv_sqrt_h;
+            }
+        }
+    }
+}
+
+// --------------------------------------------------------------------------- select: softmax, score, top-W, state
+
+constexpr int SL_NT = 512;
+
+template <typename T>
+__global__ void __launch_bounds__(SL_NT) select_kernel(
+    const float* __restrict__ z, const float* __restrict__ s_cur, const T* __restrict__ h_cur,
+    const int32_t* __restrict__ cand_tok,  // [C, L, K] base of the table
+    const T* __restrict__ E, const T* __restrict__ hidden, int P, int K, int W, int H, int L, int d, float beta,
+    int32_t* __restrict__ st_tok, int32_t* __restrict__ st_par, float* __restrict__ st_s, int32_t* __restrict__ st_n,
+    T* __restrict__ h_next, float* __restrict__ s_next, int update_state, int* status) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int r = blockIdx.x;
+    const int n = P * K;
+    const int n_keep = min(W, n);
+    int kpad = 1;
+    while (kpad < n_keep) kpad <<= 1;
+    uint64_t* keys = reinterpret_cast<uint64_t*>(smem);                 // n
+    uint64_t* sel = keys + n;                                            // kpad
+    float* lse = reinterpret_cast<float*>(sel + kpad);                   // P
+    uint32_t* hist = reinterpret_cast<uint32_t*>(lse + P);               // 256
+    uint32_t* bcast = hist + 256;                                        // 8
+    int* kept_par = reinterpret_cast<int*>(bcast + 8);                   // W
+    int* kept_tok = kept_par + W;                                        // W
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const float* zr = z + size_t(r) * P * K;
+    const int32_t* ct = cand_tok + (size_t(r) * L + (d - 1)) * K;
+
+    for (int p = wid; p < P; p += SL_NT / 32) {
+        float m = -INFINITY;
+        for (int c = lane; c < K; c += 32) m = fmaxf(m, zr[size_t(p) * K + c]);
+        m = warp_max(m);
+        float s = 0.f;
+        for (int c = lane; c < K; c += 32) s += expf(zr[size_t(p) * K + c] - m);
+        s = warp_sum(s);
+        if (lane == 0) lse[p] = m + logf(s);
+    }
+    if (threadIdx.x == 0) bcast[4] = 0;
+    __syncthreads();
+    for (int f = threadIdx.x; f < n; f += SL_NT) {
+        const int p = f / K;
+        float s = (s_cur[size_t(r) * P + p] + (zr[f] - lse[p])) + beta;
+        s += 0.f;
+        keys[f] = (uint64_t(ord_f32(s)) << 32) | (0xffffffffu - uint32_t(f));
+    }
+    __syncthreads();
+    uint64_t prefix = 0, mask = 0;
+    const bool ok = block_select_top<SL_NT>(keys, n, n_keep, hist, bcast, prefix, mask);
+    for (int f = threadIdx.x; f < n; f += SL_NT) {
+        if (ok && selected(keys[f], prefix, mask)) {
+            const uint32_t q = atomicAdd(&bcast[4], 1u);
+            if (q < uint32_t(n_keep)) sel[q] = keys[f];
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && (!ok || bcast[4] != uint32_t(n_keep))) set_status(status, DARTREE_EINTERNAL);
+    for (int i = threadIdx.x; i < kpad; i += SL_NT)
+        if (i >= n_keep || !ok || i >= int(bcast[4])) sel[i] = 0;
+    __syncthreads();
+    bitonic_sort_desc<SL_NT>(sel, kpad);
+
+    const size_t sto = (size_t(r) * L + (d - 1)) * W;
+    for (int k = threadIdx.x; k < W; k += SL_NT) {
+        if (k < n_keep) {
+            const uint64_t key = sel[k];
+            const uint32_t f = 0xffffffffu - uint32_t(key);
+            const int p = int(f) / K, c = int(f) % K;
+            const float s = f32_from_ord(uint32_t(key >> 32));
+            const int tk = (f < uint32_t(n)) ? ct[c] : 0;
+            st_tok[sto + k] = tk;
+            st_par[sto + k] = p;
+            st_s[sto + k] = s;
+            s_next[size_t(r) * n_keep + k] = s;
+            kept_par[k] = p;
+            kept_tok[k] = tk;
+        } else {
+            st_tok[sto + k] = -1;
+            st_par[sto + k] = -1;
+            st_s[sto + k] = 0.f;
+        }
+    }
+    if (threadIdx.x == 0) st_n[size_t(r) * L + (d - 1)] = n_keep;
+    if (!update_state) return;
+    __syncthreads();
+    const T* hd = hidden + (size_t(r) * L + (d - 1)) * H;
+    for (int k = wid; k < n_keep; k += SL_NT / 32) {
+        const T* hp = h_cur + (size_t(r) * P + kept_par[k]) * H;
+        const T* e = E + size_t(kept_tok[k]) * H;
+        float ss = 0.f;
+        for (int j = lane; j < H; j += 32) {
+            const float x = (to_float(hp[j]) + to_float(e[j])) + to_float(hd[j]);
+            ss = fmaf(x, x, ss);
+        }
+        ss = warp_sum(ss);
+        const float rs = sqrtf(ss / float(H) + 1e-6f);
+        T* out = h_next + (size_t(r) * n_keep + k) * H;
+        for (int j = lane; j < H; j += 32) {
+            const float x = (to_float(hp[j]) + to_float(e[j])) + to_float(hd[j]);
+            out[j] = from_float<T>(x / rs);
+        }
+    }
+}
+
+static size_t select_smem(int P, int K, int W) {
+    const int n = P * K;
+    const int n_keep = n < W ? n : W;
+    int kpad = 1;
+    while (kpad < n_keep) kpad <<= 1;
+    return size_t(n) * 8 + size_t(kpad) * 8 + size_t(P) * 4 + 256 * 4 + 8 * 4 + 2 * size_t(W) * 4 + 16;
+}
+
+// --------------------------------------------------------------------------- host loop
+
+template <typename T>
+static int launch_expand_t(const ExpandArgs& a, cudaStream_t st) {
+    const T* E = static_cast<const T*>(a.E);
+    const T* Wq = static_cast<const T*>(a.Wq);
+    const T* hid = static_cast<const T*>(a.hidden);
+    T* hb[2] = {static_cast<T*>(a.hbuf[0]), static_cast<T*>(a.hbuf[1])};
+    root_init_kernel<T><<<a.C, 256, 0, st>>>(E, a.anchor, a.H, hb[0], a.sbuf[0]);
+    const size_t smax = select_smem(a.W, a.K, a.W);
+    if (cudaFuncSetAttribute(select_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smax)) != cudaSuccess)
+        return DARTREE_ECUDA;
+    const float inv_sqrt_h = 1.0f / sqrtf(float(a.H));
+    int cur = 0, P = 1;
+    for (int d = 1; d <= a.L; ++d) {
+        const int M = a.C * P;
+        dim3 pg((a.H + PJ_TN - 1) / PJ_TN, (M + PJ_TM - 1) / PJ_TM);
+        proj_simple_kernel<T><<<pg, PJ_NT, 0, st>>>(hb[cur], Wq, a.U, M, a.H);
+        dim3 cg((a.K + (CT_NT / 32) * CT_CPW - 1) / ((CT_NT / 32) * CT_CPW), a.C);
+        contract_simple_kernel<T><<<cg, CT_NT, 0, st>>>(a.U, E, a.cand_tok, a.cand_val, a.z, P, a.K, a.H, a.L, d,
+                                                        inv_sqrt_h);
+        const int n_keep = P * a.K < a.W ? P * a.K : a.W;
+        select_kernel<T><<<a.C, SL_NT, select_smem(P, a.K, a.W), st>>>(
+            a.z, a.sbuf[cur], hb[cur], a.cand_tok, E, hid, P, a.K, a.W, a.H, a.L, d, a.beta, a.st_tok, a.st_par,
+            a.st_s, a.st_n, hb[1 - cur], a.sbuf[1 - cur], d < a.L ? 1 : 0, a.status);
+        cur = 1 - cur;
+        P = n_keep;
+    }
+    return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
+}
+
+int launch_expand(const ExpandArgs& a, cudaStream_t stream) {
+    if (a.dtype == DARTREE_BF16) return launch_expand_t<bf16_t>(a, stream);
+    return launch_expand_t<float>(a, stream);
+}
+
+}  // namespace dartree

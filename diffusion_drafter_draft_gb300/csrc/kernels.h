@@ -1,0 +1,54 @@
+// Host-side launchers of the DARTree kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dartree {
+
+int num_sms();
+
+// S1: top-K of `rows` rows of V values.
+int launch_topk(const void* x, int rows, int V, int K, int dtype, int32_t* tok, float* val, int* status,
+                cudaStream_t stream);
+
+struct ExpandArgs {
+    const void* E;
+    const void* Wq;
+    int V, H, dtype;
+    int C, L, K, W;
+    float beta;
+    const void* hidden;       // [C, L, H]
+    const int32_t* anchor;    // [C]
+    const int32_t* cand_tok;  // [C, L, K]
+    const float* cand_val;    // [C, L, K]
+    int32_t* st_tok;          // [C, L, W]
+    int32_t* st_par;          // [C, L, W]
+    float* st_s;              // [C, L, W]
+    int32_t* st_n;            // [C, L]
+    void* hbuf[2];            // [C, W, H] storage type, ping-pong
+    float* sbuf[2];           // [C, W]
+    float* U;                 // [C*W, H]
+    float* z;                 // [C, W, K]
+    int* status;
+};
+
+// S2-S7 over all depths.
+int launch_expand(const ExpandArgs& a, cudaStream_t stream);
+
+// S8: deferred prune.
+int launch_prune(int C, int L, int W, int B, const int32_t* st_tok, const int32_t* st_par, const float* st_s,
+                 const int32_t* st_n, const int32_t* anchor, int32_t* tok, int32_t* par, int32_t* depth,
+                 float* score, int32_t* n_nodes, int* status, cudaStream_t stream);
+
+// S9: mask and position ids.
+int launch_mask(int C, int L, int B, const int32_t* par, const int32_t* depth, const int32_t* n_nodes,
+                uint8_t* mask, int32_t* pos, cudaStream_t stream);
+
+// S10: verification.
+int launch_verify(int C, int L, int B, const int32_t* tok, const int32_t* par, const int32_t* depth,
+                  const int32_t* n_nodes, const void* target, int rows_mode, int V, int dtype,
+                  unsigned long long* keys, int32_t* accepted, int32_t* path, int32_t* bonus, int* status,
+                  cudaStream_t stream);
+
+}  // namespace dartree

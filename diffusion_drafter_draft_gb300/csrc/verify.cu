@@ -1,0 +1,220 @@
+// S10: greedy longest accepted prefix (DARTree blog post, 3.2: all draft tokens
+// are verified in one target pass with the tree-attention mask and the longest
+// valid prefix is kept).
+//
+// Walk: from the root, t = argmax of the current slot's target row (lowest token
+// id among equal maxima, i.e. the largest key (value, ~token)); move to the child
+// carrying t while one exists.
+//  - per-position rows [C, L, V]: the row of a slot depends only on its depth,
+//    so all C*L row maxima are computed in parallel first, then one warp per
+//    request walks the tree;
+//  - per-node rows [C, B+1, V]: only the rows on the accepted path are read; one
+//    thread-block cluster per request computes each row's maximum (partials
+//    exchanged through distributed shared memory) and takes the next step.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dartree {
+
+template <typename T>
+__device__ __forceinline__ uint64_t seg_max_key(const T* __restrict__ row, int lo, int hi, bool vec_ok) {
+    constexpr int VEC = ValueKey<T>::VEC;
+    uint64_t best = 0;
+    int i = lo;
+    if (vec_ok) {
+        const int a = min(hi, int((lo + VEC - 1) / VEC * VEC));
+        for (int q = lo + threadIdx.x; q < a; q += blockDim.x) {
+            const uint64_t k = (uint64_t(ValueKey<T>::ord(row[q])) << 32) | (0xffffffffu - uint32_t(q));
+            best = k > best ? k : best;
+        }
+        const int nv = (hi - a) / VEC;
+        const uint4* v4 = reinterpret_cast<const uint4*>(row + a);
+        for (int q = threadIdx.x; q < nv; q += blockDim.x) {
+            const uint4 v = __ldg(v4 + q);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            const int b = a + q * VEC;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                uint32_t o;
+                if constexpr (VEC == 8) o = ord_bf16((w[e >> 1] >> ((e & 1) * 16)) & 0xffffu);
+                else o = ord_f32(__uint_as_float(w[e]));
+                const uint64_t k = (uint64_t(o) << 32) | (0xffffffffu - uint32_t(b + e));
+                best = k > best ? k : best;
+            }
+        }
+        i = a + nv * VEC;
+    }
+    for (int q = i + threadIdx.x; q < hi; q += blockDim.x) {
+        const uint64_t k = (uint64_t(ValueKey<T>::ord(row[q])) << 32) | (0xffffffffu - uint32_t(q));
+        best = k > best ? k : best;
+    }
+    return best;
+}
+
+// ----------------------------------------------------------------------------- per-position rows
+
+constexpr int RM_NT = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(RM_NT) rowmax_kernel(const T* __restrict__ x, int V, int seg,
+                                                       unsigned long long* __restrict__ keys) {
+    const int row = blockIdx.y;
+    const int lo = blockIdx.x * seg, hi = min(V, lo + seg);
+    const T* r = x + size_t(row) * V;
+    const bool vec_ok = (reinterpret_cast<uintptr_t>(r) % 16) == 0;
+    uint64_t k = seg_max_key<T>(r, lo, hi, vec_ok);
+    k = warp_max_u64(k);
+    __shared__ uint64_t red[RM_NT / 32];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = k;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        uint64_t v = threadIdx.x < RM_NT / 32 ? red[threadIdx.x] : 0;
+        v = warp_max_u64(v);
+        if (threadIdx.x == 0) atomicMax(keys + row, (unsigned long long)v);
+    }
+}
+
+__global__ void walk_position_kernel(int L, int B, const int32_t* __restrict__ tok, const int32_t* __restrict__ par,
+                                     const int32_t* __restrict__ depth, const int32_t* __restrict__ n_nodes,
+                                     const unsigned long long* __restrict__ keys, int32_t* __restrict__ accepted,
+                                     int32_t* __restrict__ path, int32_t* __restrict__ bonus) {
+    const int r = blockIdx.x;
+    const int lane = threadIdx.x;
+    const int S = B + 1;
+    const int n = min(S, n_nodes[r]);
+    const int32_t* tk = tok + size_t(r) * S;
+    const int32_t* pr = par + size_t(r) * S;
+    const int32_t* dp = depth + size_t(r) * S;
+    int cur = 0, acc = 0, bon = -1;
+    for (int step = 0; step <= L; ++step) {
+        const int d = dp[cur];
+        if (d < 0 || d >= L) break;
+        const int t = int(0xffffffffu - uint32_t(keys[size_t(r) * L + d]));
+        int found = -1;
+        for (int j0 = 1; j0 < n && found < 0; j0 += 32) {
+            const int j = j0 + lane;
+            const bool hit = j < n && pr[j] == cur && tk[j] == t;
+            const uint32_t b = __ballot_sync(0xffffffffu, hit);
+            if (b) found = j0 + __ffs(b) - 1;
+        }
+        if (found < 0) { bon = t; break; }
+        if (lane == 0 && acc < L) path[size_t(r) * L + acc] = found;
+        ++acc;
+        cur = found;
+    }
+    for (int q = acc + lane; q < L; q += 32) path[size_t(r) * L + q] = -1;
+    if (lane == 0) { accepted[r] = acc; bonus[r] = bon; }
+}
+
+// ----------------------------------------------------------------------------- per-node rows
+
+constexpr int WK_NT = 512;
+
+template <typename T>
+__global__ void __launch_bounds__(WK_NT) walk_node_kernel(int L, int B, int V, int seg, const T* __restrict__ target,
+                                                          const int32_t* __restrict__ tok,
+                                                          const int32_t* __restrict__ par,
+                                                          const int32_t* __restrict__ n_nodes,
+                                                          int32_t* __restrict__ accepted, int32_t* __restrict__ path,
+                                                          int32_t* __restrict__ bonus) {
+    __shared__ uint64_t part[2][8];
+    __shared__ uint64_t red[WK_NT / 32];
+    __shared__ int found_s;
+    const uint32_t S = cluster_nctarank(), cr = cluster_ctarank();
+    const int r = blockIdx.x / S;
+    const int SL = B + 1;
+    const int n = min(SL, n_nodes[r]);
+    const int32_t* tk = tok + size_t(r) * SL;
+    const int32_t* pr = par + size_t(r) * SL;
+    const int lo = int(cr) * seg, hi = min(V, lo + seg);
+    int cur = 0, acc = 0, bon = -1;
+    for (int step = 0; step <= L; ++step) {
+        const T* row = target + (size_t(r) * SL + cur) * V;
+        const bool vec_ok = (reinterpret_cast<uintptr_t>(row) % 16) == 0;
+        uint64_t k = warp_max_u64(seg_max_key<T>(row, lo, hi, vec_ok));
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = k;
+        if (threadIdx.x == 0) found_s = 0x7fffffff;
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            uint64_t v = threadIdx.x < WK_NT / 32 ? red[threadIdx.x] : 0;
+            v = warp_max_u64(v);
+            if (threadIdx.x < S) st_dsmem_u64(dsmem_addr(&part[step & 1][cr], threadIdx.x), v);
+        }
+        cluster_sync();
+        uint64_t best = 0;
+        for (uint32_t q = 0; q < S; ++q) best = part[step & 1][q] > best ? part[step & 1][q] : best;
+        const int t = int(0xffffffffu - uint32_t(best));
+        for (int j = 1 + threadIdx.x; j < n; j += WK_NT)
+            if (pr[j] == cur && tk[j] == t) atomicMin(&found_s, j);
+        __syncthreads();
+        const int f = found_s;
+        __syncthreads();
+        if (f == 0x7fffffff) { bon = t; break; }
+        if (cr == 0 && threadIdx.x == 0 && acc < L) path[size_t(r) * L + acc] = f;
+        ++acc;
+        cur = f;
+        if (acc > L) break;
+    }
+    if (cr == 0) {
+        for (int q = acc + threadIdx.x; q < L; q += WK_NT) path[size_t(r) * L + q] = -1;
+        if (threadIdx.x == 0) { accepted[r] = acc; bonus[r] = bon; }
+    }
+}
+
+// ----------------------------------------------------------------------------- host
+
+template <typename T>
+static int launch_verify_t(int C, int L, int B, const int32_t* tok, const int32_t* par, const int32_t* depth,
+                           const int32_t* n_nodes, const void* target, int rows_mode, int V,
+                           unsigned long long* keys, int32_t* accepted, int32_t* path, int32_t* bonus,
+                           cudaStream_t stream) {
+    const T* tg = static_cast<const T*>(target);
+    if (rows_mode == DARTREE_ROWS_PER_POSITION) {
+        const int rows = C * L;
+        if (cudaMemsetAsync(keys, 0, size_t(rows) * sizeof(unsigned long long), stream) != cudaSuccess)
+            return DARTREE_ECUDA;
+        int splits = (2 * num_sms() + rows - 1) / rows;
+        const int min_seg = 4096;
+        if (splits > (V + min_seg - 1) / min_seg) splits = (V + min_seg - 1) / min_seg;
+        if (splits < 1) splits = 1;
+        int seg = (V + splits - 1) / splits;
+        seg = (seg + 7) / 8 * 8;
+        splits = (V + seg - 1) / seg;
+        rowmax_kernel<T><<<dim3(splits, rows), RM_NT, 0, stream>>>(tg, V, seg, keys);
+        walk_position_kernel<<<C, 32, 0, stream>>>(L, B, tok, par, depth, n_nodes, keys, accepted, path, bonus);
+        return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
+    }
+    const int S = 8;
+    int seg = (V + S - 1) / S;
+    seg = (seg + 7) / 8 * 8;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(unsigned(C) * S);
+    cfg.blockDim = dim3(WK_NT);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, walk_node_kernel<T>, L, B, V, seg, tg, tok, par, n_nodes, accepted,
+                                       path, bonus);
+    return e == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
+}
+
+int launch_verify(int C, int L, int B, const int32_t* tok, const int32_t* par, const int32_t* depth,
+                  const int32_t* n_nodes, const void* target, int rows_mode, int V, int dtype,
+                  unsigned long long* keys, int32_t* accepted, int32_t* path, int32_t* bonus, int* status,
+                  cudaStream_t stream) {
+    (void)status;
+    if (C == 0) return DARTREE_OK;
+    if (dtype == DARTREE_BF16)
+        return launch_verify_t<bf16_t>(C, L, B, tok, par, depth, n_nodes, target, rows_mode, V, keys, accepted,
+                                       path, bonus, stream);
+    return launch_verify_t<float>(C, L, B, tok, par, depth, n_nodes, target, rows_mode, V, keys, accepted, path,
+                                  bonus, stream);
+}
+
+}  // namespace dartree

@@ -1,0 +1,204 @@
+/*
+ * dartree.h — C ABI of the DARTree draft-tree build and verify step on sm_103a.
+ *
+ * Method: DARTree: Speculative Diffusion Decoding with Autoregressive Draft Trees,
+ * as described on the marsggbo.github.io blog post (section 3.1 "Basic flow",
+ * section 3.2) and the ainews.surl.tw article "DARTree Builds Trees in Batches
+ * Before Pruning". One speculative round is:
+ *   S1  top-K candidates of every block position's base logits        (3.1, candidate generation)
+ *   S2  root state h = E[anchor], score 0
+ *   S3-S7 for d = 1..L: correction head on all parents of depth d-1 in one
+ *       batch, s = s_parent + log q + beta, keep the top-W children      (3.1, depth-wise expansion,
+ *       (the kept nodes of all depths form the supertree)                   scoring function, per-depth pruning)
+ *   S8  deferred pruning: global top-B of the supertree                (3.1, deferred pruning, Lemma 1)
+ *   S9  tree-attention mask and position ids                           (3.2)
+ *   S10 greedy longest accepted prefix against the target's logits     (3.2)
+ *
+ * The pages do not define the correction head; this library implements the
+ * stand-in head  u_p = W_q h_p,  z[p,c] = L^base[d-1,c] + <u_p, E[c]>/sqrt(H),
+ * q = softmax over the K candidates of position d-1,
+ * h_child = RMSNorm(h_p + E[tok] + H_d[d-1]) (eps 1e-6, unit weight), stored in
+ * the input storage type.
+ *
+ * Conventions for every entry point:
+ *  - Tensor pointers are DEVICE pointers owned by the caller, row-major and
+ *    contiguous. The library allocates no memory: scratch lives in a caller
+ *    allocated workspace of dartree_workspace_bytes() bytes (device memory,
+ *    256-byte aligned).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    All work is enqueued asynchronously on it; outputs are valid after the
+ *    caller synchronises the stream. No call synchronises, except
+ *    dartree_read_status.
+ *  - Argument errors are detected on the host before anything is enqueued and
+ *    returned as a negative dartree_status; nothing is written then. Launch
+ *    failures return DARTREE_ECUDA. Errors detected on the device (a bounded
+ *    wait that ran out, a buffer overflow) are recorded in a status word at the
+ *    start of the workspace (first error wins) and read with
+ *    dartree_read_status.
+ *  - Floating point inputs are finite. Equal values are ordered as stated per
+ *    step; -0.0 and +0.0 compare equal.
+ *  - Calls that share a workspace must not overlap on the device.
+ */
+#ifndef DARTREE_H
+#define DARTREE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DARTREE_API __attribute__((visibility("default")))
+#else
+#define DARTREE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DARTREE_OK = 0,
+    DARTREE_EINVAL = -1,       /* bad size, null pointer or beta > 0 */
+    DARTREE_EDTYPE = -2,       /* unknown dtype or row mode */
+    DARTREE_EWORKSPACE = -3,   /* workspace null, misaligned or too small */
+    DARTREE_ECUDA = -4,        /* a CUDA runtime call or launch failed */
+    DARTREE_ETIMEOUT = -5,     /* device: a bounded wait ran out */
+    DARTREE_EINTERNAL = -6,    /* device: an internal consistency check failed */
+    DARTREE_EUNSUPPORTED = -7  /* sizes beyond the limits below */
+} dartree_status;
+
+typedef enum { DARTREE_F32 = 0, DARTREE_BF16 = 1 } dartree_dtype;
+
+/* Layout of the target logits handed to dartree_verify. */
+typedef enum {
+    DARTREE_ROWS_PER_POSITION = 0, /* [C, L, V]: the slot at depth delta is checked with row delta */
+    DARTREE_ROWS_PER_NODE = 1      /* [C, B+1, V]: slot j is checked with row j (row 0 = root) */
+} dartree_rows;
+
+/* Limits (DARTREE_EUNSUPPORTED beyond them). */
+#define DARTREE_MAX_K 1024
+#define DARTREE_MAX_W 256
+#define DARTREE_MAX_L 64
+#define DARTREE_MAX_SLOTS 1024   /* B + 1 */
+#define DARTREE_MAX_CHILDREN 8192 /* W * K children scored per depth and request */
+
+/* Stand-in correction head (shared model weights). */
+typedef struct {
+    const void* E;   /* [V, H] token embeddings, dtype */
+    const void* Wq;  /* [H, H] projection, row-major, u = Wq h */
+    int V;
+    int H;           /* multiple of 8 */
+    int dtype;       /* dartree_dtype of E, Wq, base logits and block hidden states */
+} dartree_head;
+
+/* Shape of one round. */
+typedef struct {
+    int C;       /* requests in the batch */
+    int L;       /* block length = maximum depth, 1..DARTREE_MAX_L */
+    int K;       /* candidates per position, 1..min(V, DARTREE_MAX_K) */
+    int W;       /* nodes kept per depth, 1..DARTREE_MAX_W, W*K <= DARTREE_MAX_CHILDREN */
+    int B;       /* node budget (root excluded), 1..min(L*W, DARTREE_MAX_SLOTS-1) */
+    float beta;  /* depth term, <= 0 (Lemma 1 needs beta <= 0) */
+} dartree_params;
+
+/* Candidate table of S1: per (request, position) the K best tokens ordered by
+ * (logit desc, token id asc), and their logits as float. */
+typedef struct {
+    int32_t* tok;   /* [C, L, K] */
+    float* logit;   /* [C, L, K] */
+} dartree_candidates;
+
+/* Supertree of S7: the kept nodes of every depth d (index d-1), in rank order
+ * (score desc, flat index p*K+c asc). par is the parent's rank at depth d-1
+ * (0 = the root for d = 1). Unused entries: tok = par = -1, score = 0. */
+typedef struct {
+    int32_t* tok;   /* [C, L, W] */
+    int32_t* par;   /* [C, L, W] */
+    float* score;   /* [C, L, W] s_beta of the node */
+    int32_t* n;     /* [C, L] kept nodes per depth: min(W, n_{d-1} * K), n_0 = 1 */
+} dartree_supertree;
+
+/* Verification tree of S8/S9, B+1 slots per request. Slot 0 is the root
+ * (tok = anchor, par = -1, depth 0, score 0). Slots 1..n_nodes-1 hold the
+ * chosen nodes depth-major, by rank within a depth; par holds slot ids
+ * (par < own slot). Unused slots: tok = par = depth = pos = -1, score = 0,
+ * mask row and column 0. n_nodes = 1 + min(B, supertree size). */
+typedef struct {
+    int32_t* tok;      /* [C, B+1] */
+    int32_t* par;      /* [C, B+1] */
+    int32_t* depth;    /* [C, B+1] */
+    float* score;      /* [C, B+1] */
+    int32_t* n_nodes;  /* [C] */
+    uint8_t* mask;     /* [C, B+1, B+1] mask[i][j] = 1 iff slot j is an ancestor of slot i or i itself */
+    int32_t* pos;      /* [C, B+1] position id = depth */
+} dartree_tree;
+
+/* Checks and stores the head description. E and Wq must stay valid while the
+ * head is used. Returns DARTREE_OK or a negative status. */
+DARTREE_API int dartree_head_init(dartree_head* head, const void* E, const void* Wq, int V, int H, int dtype);
+
+/* Workspace bytes needed by every call below for this shape (0 on bad arguments). */
+DARTREE_API size_t dartree_workspace_bytes(const dartree_params* p, int V, int H, int dtype);
+
+/* S1 alone: top-K of `rows` rows of `V` logits (dtype), written to tok/val
+ * [rows, K] ordered by (logit desc, token id asc). Uses only the workspace's
+ * status word (ws_bytes >= 256). */
+DARTREE_API int dartree_topk(const void* logits, int rows, int V, int K, int dtype,
+                 int32_t* tok, float* val, void* ws, size_t ws_bytes, void* stream);
+
+/* S2-S7: expand all depths from a given candidate table.
+ *   base_logits  unused (the candidate table carries the logits); may be NULL
+ *   block_hidden [C, L, H] dtype, H_d of the block drafter
+ *   anchor       [C] int32 anchor tokens
+ *   cand         candidate table of S1
+ *   st           supertree output */
+DARTREE_API int dartree_expand(const dartree_head* head, const dartree_params* p, const void* block_hidden,
+                   const int32_t* anchor, const dartree_candidates* cand, dartree_supertree* st,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/* S8: deferred pruning of a supertree into tree.tok/par/depth/score/n_nodes.
+ * Global order: score desc, depth asc, rank asc. tree.mask and tree.pos are not touched. */
+DARTREE_API int dartree_prune(const dartree_params* p, const dartree_supertree* st, const int32_t* anchor,
+                  dartree_tree* tree, void* stream);
+
+/* S9: tree.mask and tree.pos from tree.par, tree.depth and tree.n_nodes. */
+DARTREE_API int dartree_tree_mask(const dartree_params* p, dartree_tree* tree, void* stream);
+
+/* S1-S9: one full tree build.
+ *   base_logits  [C, L, V] dtype, L^base of the block drafter
+ *   block_hidden [C, L, H] dtype
+ *   anchor       [C] int32
+ *   tree         output (mask and pos are built when non-NULL)
+ *   st, cand     optional outputs (NULL: kept in the workspace) */
+DARTREE_API int dartree_build_tree(const dartree_head* head, const dartree_params* p, const void* base_logits,
+                       const void* block_hidden, const int32_t* anchor, dartree_tree* tree,
+                       dartree_supertree* st, dartree_candidates* cand,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* S10: greedy longest accepted prefix. From the root, t = argmax of the current
+ * slot's target row (lowest token id among equal maxima); move to the child
+ * carrying t while one exists.
+ *   target        [C, L, V] (rows = DARTREE_ROWS_PER_POSITION) or [C, B+1, V]
+ *                 (DARTREE_ROWS_PER_NODE), dtype
+ *   accepted_len  [C] accepted drafted tokens, 0..L
+ *   path          [C, L] slot ids of the accepted nodes in depth order, -1 padded
+ *   bonus         [C] the target's token after the accepted prefix (argmax of the
+ *                 last accepted slot's row), -1 when that row does not exist
+ *                 (per-position rows and a fully accepted block) */
+DARTREE_API int dartree_verify(const dartree_params* p, const dartree_tree* tree, const void* target,
+                   int rows, int V, int dtype, int32_t* accepted_len, int32_t* path,
+                   int32_t* bonus, void* ws, size_t ws_bytes, void* stream);
+
+/* Copies the device status word of `ws` to *status (synchronises `stream`). */
+DARTREE_API int dartree_read_status(const void* ws, int32_t* status, void* stream);
+
+/* Resets the device status word of `ws` to DARTREE_OK (enqueued on `stream`). */
+DARTREE_API int dartree_clear_status(void* ws, void* stream);
+
+/* Static text for a status code. */
+DARTREE_API const char* dartree_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DARTREE_H */

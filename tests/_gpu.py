@@ -1,0 +1,101 @@
+"""Helpers for the GPU parity tests: upload seeded inputs, read results back,
+and compare the CUDA path with the CPU oracle (follow mode for near-ties)."""
+import numpy as np
+import torch
+
+import diffusion_drafter_draft_gb300 as dd
+import oracle
+
+SCORE_ATOL = 2e-3
+
+
+def t(a, dtype, dev="cuda"):
+    """Stored numpy array -> torch CUDA tensor with the same bits."""
+    a = np.ascontiguousarray(a)
+    if dtype == "bf16":
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(a).to(dev)
+
+
+def upload(inp):
+    cfg = inp["cfg"]
+    d = dict(E=t(inp["E"], cfg.dtype), Wq=t(inp["Wq"], cfg.dtype), base=t(inp["base"], cfg.dtype),
+             hidden=t(inp["hidden"], cfg.dtype), anchor=torch.from_numpy(inp["anchor"]).cuda())
+    if "target" in inp:
+        d["target"] = t(inp["target"], cfg.dtype)
+    return d
+
+
+def host(x):
+    if isinstance(x, dict):
+        return {k: host(v) for k, v in x.items()}
+    return x.cpu().numpy()
+
+
+def follow_from_gpu(g, K):
+    """Follow callables that replay the GPU's per-depth and prune selections."""
+    st_tok, st_par, st_n = g["st"]["tok"], g["st"]["par"], g["st"]["n"]
+    ctok = g["cand_tok"]
+
+    def depth(i, d):
+        n = int(st_n[i, d - 1])
+        rank = {int(tk): c for c, tk in enumerate(ctok[i, d - 1])}
+        out = []
+        for k in range(n):
+            tk = int(st_tok[i, d - 1, k])
+            if tk not in rank:
+                return [-1] * n
+            out.append(int(st_par[i, d - 1, k]) * K + rank[tk])
+        return out
+
+    def prune(i):
+        rank_of_slot = {0: 0}
+        chosen = []
+        for j in range(1, int(g["n_nodes"][i])):
+            d, tk, ps = int(g["depth"][i, j]), int(g["tok"][i, j]), int(g["par"][i, j])
+            pr = rank_of_slot.get(ps, -1)
+            hit = [k for k in range(int(st_n[i, d - 1]))
+                   if int(st_tok[i, d - 1, k]) == tk and (d == 1 or int(st_par[i, d - 1, k]) == pr)]
+            if not hit:
+                return [(-1, -1)]
+            rank_of_slot[j] = hit[0]
+            chosen.append((d, hit[0]))
+        return chosen
+
+    return dict(depth=depth, prune=prune)
+
+
+def run_gpu_build(inp, dev_inputs=None):
+    cfg = inp["cfg"]
+    x = dev_inputs or upload(inp)
+    g = dd.build_tree(x["E"], x["Wq"], x["base"], x["hidden"], x["anchor"], cfg.K, cfg.W, cfg.B, cfg.beta,
+                      keep_intermediates=True)
+    torch.cuda.synchronize()
+    return host(g), x
+
+
+def compare_build(inp, g, rows=None):
+    """Element-by-element comparison of a GPU build (requests `rows` of g) with the oracle."""
+    cfg = inp["cfg"]
+    sel = np.arange(len(inp["anchor"])) if rows is None else np.asarray(rows)
+    gs = {k: (v[sel] if not isinstance(v, dict) else {kk: vv[sel] for kk, vv in v.items()}) for k, v in g.items()}
+    o = oracle.build(inp, follow=follow_from_gpu(gs, cfg.K))
+    assert not o["mismatches"], f"selections differ beyond near-ties: {o['mismatches'][:5]}"
+    np.testing.assert_array_equal(gs["cand_tok"], o["cand_tok"])
+    np.testing.assert_array_equal(gs["cand_val"], o["cand_logit"].astype(np.float32))
+    np.testing.assert_array_equal(gs["st"]["n"], o["st_n"])
+    np.testing.assert_array_equal(gs["st"]["tok"], o["st_tok"])
+    np.testing.assert_array_equal(gs["st"]["par"], o["st_par"])
+    np.testing.assert_allclose(gs["st"]["score"], o["st_s"], rtol=0, atol=SCORE_ATOL)
+    for k in ("tok", "par", "depth", "n_nodes", "mask", "pos"):
+        np.testing.assert_array_equal(gs[k], o[k], err_msg=k)
+    np.testing.assert_allclose(gs["score"], o["score"], rtol=0, atol=SCORE_ATOL)
+    return o
+
+
+def compare_verify(o, gv, target_np, cfg, rows_mode):
+    ov = oracle.verify(o, target_np, cfg.dtype, rows_mode, cfg.L)
+    np.testing.assert_array_equal(gv["accepted_len"], ov["accepted_len"])
+    np.testing.assert_array_equal(gv["path"], ov["path"])
+    np.testing.assert_array_equal(gv["bonus"], ov["bonus"])
+    return ov

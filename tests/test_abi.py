@@ -1,0 +1,64 @@
+"""The C ABI library loads, exports every declared entry point, and rejects bad
+arguments on the host (no GPU needed: argument checks run before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from diffusion_drafter_draft_gb300 import _build
+    _build.build()
+    import diffusion_drafter_draft_gb300 as dd
+    return dd.lib()
+
+
+def declared():
+    with open(os.path.join(ROOT, "include", "dartree.h")) as f:
+        src = f.read()
+    return sorted(set(re.findall(r"DARTREE_API\s+[\w\s\*]+?\b(dartree_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_exports():
+    import diffusion_drafter_draft_gb300 as dd
+    assert declared() == sorted(dd.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared():
+        assert hasattr(L, name), name
+
+
+def test_argument_errors_are_reported_on_the_host(L):
+    import diffusion_drafter_draft_gb300 as dd
+    P = dd.Params
+    fake = ctypes.c_void_p(256)  # never dereferenced: checks fail first
+    ws_ok = ctypes.c_void_p(1 << 20)
+    p = P(1, 4, 8, 2, 8, -0.1)
+    assert L.dartree_workspace_bytes(ctypes.byref(p), 100, 64, dd.F32) > 0
+    assert L.dartree_workspace_bytes(ctypes.byref(P(1, 4, 8, 2, 8, 0.5)), 100, 64, dd.F32) == 0   # beta > 0
+    assert L.dartree_workspace_bytes(ctypes.byref(P(1, 4, 200, 2, 8, -0.1)), 100, 64, dd.F32) == 0  # K > V
+    assert L.dartree_workspace_bytes(ctypes.byref(P(1, 4, 8, 2, 9, -0.1)), 100, 64, dd.F32) == 0   # B > L*W
+    assert L.dartree_workspace_bytes(ctypes.byref(p), 100, 60, dd.F32) == 0                        # H % 8
+    assert L.dartree_topk(fake, 2, 10, 11, dd.F32, fake, fake, ws_ok, 4096, None) == dd.EINVAL
+    assert L.dartree_topk(fake, 2, 10, 5, 7, fake, fake, ws_ok, 4096, None) == dd.EDTYPE
+    assert L.dartree_topk(fake, 2, 5000, 2000, dd.F32, fake, fake, ws_ok, 4096, None) == dd.EUNSUPPORTED
+    assert L.dartree_topk(fake, 2, 10, 5, dd.F32, fake, fake, ctypes.c_void_p(1 << 20 | 8), 4096, None) \
+        == dd.EWORKSPACE
+    assert L.dartree_topk(fake, 2, 10, 5, dd.F32, fake, fake, ws_ok, 16, None) == dd.EWORKSPACE
+    h = dd.Head()
+    assert L.dartree_head_init(ctypes.byref(h), fake, fake, 100, 64, dd.F32) == dd.OK
+    assert L.dartree_head_init(ctypes.byref(h), None, fake, 100, 64, dd.F32) == dd.EINVAL
+    tree = dd.Tree(256, 256, 256, 256, 256, None, None)
+    need = L.dartree_workspace_bytes(ctypes.byref(p), 100, 64, dd.F32)
+    assert L.dartree_build_tree(ctypes.byref(h), ctypes.byref(P(1, 4, 8, 2, 8, 0.1)), fake, fake, fake,
+                                ctypes.byref(tree), None, None, ws_ok, need, None) == dd.EINVAL
+    assert L.dartree_build_tree(ctypes.byref(h), ctypes.byref(p), fake, fake, fake,
+                                ctypes.byref(tree), None, None, ws_ok, need - 256, None) == dd.EWORKSPACE
+    assert L.dartree_verify(ctypes.byref(p), ctypes.byref(tree), fake, 5, 100, dd.F32, fake, fake, fake, ws_ok,
+                            need, None) == dd.EDTYPE
+    assert L.dartree_status_string(dd.ETIMEOUT) == b"a bounded device-side wait ran out"

@@ -1,0 +1,139 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Node sets, parents, depths, masks, position ids, accepted lengths, paths and bonus
+tokens must be bit-exact; scores agree within 2e-3 absolute. A per-depth or
+global selection that differs from the oracle's only on a score gap below 1e-3 is
+adopted by the oracle (follow mode) and counted, not failed.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from dartree_inputs import (breadth_first_slot_depth, make_config, make_inputs,  # noqa: E402
+                            make_target_per_node, round_to_bf16_bits, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import diffusion_drafter_draft_gb300 as dd
+    from diffusion_drafter_draft_gb300 import _build
+    _build.build()
+    dd.lib()
+
+
+from _gpu import compare_build, compare_verify, host, run_gpu_build, t, upload  # noqa: E402
+
+
+# --------------------------------------------------------------------------- S1 top-K
+
+def _topk_case(rows, V, K, dtype, kind, seed):
+    rng = np.random.default_rng(seed)
+    if kind == "gauss":
+        x = rng.standard_normal((rows, V)).astype(np.float32) * 2.5
+    elif kind == "ties":
+        x = rng.integers(-3, 4, size=(rows, V)).astype(np.float32)
+    elif kind == "const":
+        x = np.zeros((rows, V), np.float32)
+        x[:, ::3] = -0.0
+    else:  # planted peaks over heavy ties
+        x = np.round(rng.standard_normal((rows, V)).astype(np.float32) * 4) / 4
+        x[np.arange(rows), rng.integers(0, V, rows)] = 30.0
+    return round_to_bf16_bits(x) if dtype == "bf16" else x
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,V,K", [(3, 1000, 8), (5, 151936, 64), (2, 151936, 512), (4, 4099, 1024),
+                                      (7, 37, 37), (1, 9, 1), (16, 65543, 100)])
+@pytest.mark.parametrize("kind", ["gauss", "ties", "const", "peaks"])
+def test_topk_matches_oracle(dtype, rows, V, K, kind):
+    import diffusion_drafter_draft_gb300 as dd
+    x = _topk_case(rows, V, K, dtype, kind, seed=rows * 7 + V)
+    tok, val = dd.topk(t(x, dtype), K)
+    tok, val = host(tok), host(val)
+    xf = to_f64(x, dtype)
+    for r in range(rows):
+        et, ev = oracle.topk_candidates(xf[r], K)
+        np.testing.assert_array_equal(tok[r], et)
+        np.testing.assert_array_equal(val[r], ev.astype(np.float32))
+
+
+# --------------------------------------------------------------------------- S8 / S9 / S10 on oracle intermediates
+
+@pytest.mark.parametrize("name", ["cfg0_tiny", "cfg3_c4_adaptive"])
+def test_prune_mask_verify_on_oracle_supertree(name):
+    import diffusion_drafter_draft_gb300 as dd
+    cfg = make_config(name)
+    inp = make_inputs(cfg)
+    o = oracle.build(inp)
+    st = dict(tok=torch.from_numpy(o["st_tok"].astype(np.int32)).cuda(),
+              par=torch.from_numpy(o["st_par"].astype(np.int32)).cuda(),
+              score=torch.from_numpy(o["st_s"].astype(np.float32)).cuda(),
+              n=torch.from_numpy(o["st_n"].astype(np.int32)).cuda())
+    anchor = torch.from_numpy(inp["anchor"]).cuda()
+    tr = dd.prune(st, anchor, cfg.B)
+    dd.tree_mask(tr, cfg.L)
+    g = host(tr)
+    for k in ("tok", "par", "depth", "n_nodes", "mask", "pos"):
+        np.testing.assert_array_equal(g[k], o[k], err_msg=k)
+    np.testing.assert_array_equal(g["score"], o["score"].astype(np.float32))
+    target = t(inp["target"], cfg.dtype)
+    gv = host(dd.verify(tr, target, dd.ROWS_PER_POSITION, cfg.L))
+    compare_verify(o, gv, inp["target"], cfg, "position")
+
+
+# --------------------------------------------------------------------------- end to end
+
+@pytest.mark.parametrize("name", ["cfg0_tiny", "cfg1_qwen3_4b_c1", "cfg2_qwen3_8b_fixed", "cfg3_c4_adaptive",
+                                  "cfg3_c2"])
+def test_build_and_verify_match_oracle(name):
+    import diffusion_drafter_draft_gb300 as dd
+    cfg = make_config(name)
+    inp = make_inputs(cfg)
+    g, x = run_gpu_build(inp)
+    o = compare_build(inp, g)
+    tr = {k: torch.from_numpy(v).cuda() for k, v in g.items() if k in ("tok", "par", "depth", "n_nodes")}
+    gv = host(dd.verify(tr, x["target"], dd.ROWS_PER_POSITION, cfg.L))
+    compare_verify(o, gv, inp["target"], cfg, "position")
+
+
+def test_tiny_shapes_with_ragged_tails():
+    """Several small shapes whose sizes are not multiples of any tile."""
+    import diffusion_drafter_draft_gb300 as dd
+    for seed, (L, V, H, K, W, B) in enumerate([(3, 211, 24, 5, 7, 9), (5, 1031, 40, 17, 3, 11),
+                                                (2, 99, 8, 33, 40, 50), (6, 517, 72, 1, 4, 5)]):
+        for dtype in ("f32", "bf16"):
+            cfg = make_config("cfg0_tiny").replace(C=3, L=L, V=V, H=H, K=K, W=W, B=B, dtype=dtype, seed=seed,
+                                                   beta=-0.05 * seed)
+            inp = make_inputs(cfg)
+            g, x = run_gpu_build(inp)
+            o = compare_build(inp, g)
+            tr = {k: torch.from_numpy(v).cuda() for k, v in g.items() if k in ("tok", "par", "depth", "n_nodes")}
+            gv = host(dd.verify(tr, x["target"], dd.ROWS_PER_POSITION, cfg.L))
+            compare_verify(o, gv, inp["target"], cfg, "position")
+
+
+def test_stress_batch_sampled_requests():
+    """Full C=64, K=512 batch on the GPU; the oracle checks a sample of requests
+    (each request is drawn from its own stream, so a sample is bit-identical)."""
+    import diffusion_drafter_draft_gb300 as dd
+    cfg = make_config("cfg4_c64_stress")
+    full = make_inputs(cfg)
+    g, x = run_gpu_build(full)
+    sample = [0, 37, 63]
+    small = make_inputs(cfg, requests=sample)
+    o = compare_build(small, g, rows=sample)
+    # per-node target rows: sampled requests use their true slot depths, the rest a fixed layout
+    depths = np.broadcast_to(breadth_first_slot_depth(cfg), (cfg.C, cfg.B + 1)).copy()
+    for i, r in enumerate(sample):
+        depths[r] = o["depth"][i]
+    tgt = make_target_per_node(cfg, full, depths)
+    tr = {k: torch.from_numpy(v).cuda() for k, v in g.items() if k in ("tok", "par", "depth", "n_nodes")}
+    gv = host(dd.verify(tr, t(tgt, cfg.dtype), dd.ROWS_PER_NODE, cfg.L))
+    gvs = {k: v[sample] for k, v in gv.items()}
+    compare_verify(o, gvs, tgt[sample], cfg, "node")
