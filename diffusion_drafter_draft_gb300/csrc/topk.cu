@@ -2,16 +2,16 @@
 // candidate generation: keep the top-K tokens of every position).
 //
 // One thread-block cluster per row. Each CTA stages a contiguous chunk of the
-// row in shared memory with one TMA bulk copy (a single HBM read of the row),
-// then the cluster runs an exact radix select on orderable value keys:
-//   1. every thread's maximum over its owned run of elements is a "group max";
-//      the K-th largest group max c is a lower bound of the K-th largest value
-//      (K groups each hold an element >= c), so only elements >= c can matter;
-//   2. exact K-th largest value t among elements >= c, 8 bits per pass, with the
-//      per-CTA histograms summed through distributed shared memory;
-//   3. all elements > t, plus the first (K - #>t) elements == t in token order
-//      (ties go to the lower token id), are written to the leader CTA;
-//   4. the leader sorts the K composite keys (value, ~token) and writes them out.
+// row in shared memory with TMA bulk copies (a single HBM read of the row) and
+// works on orderable keys (value, ~token), so ties go to the lower token id:
+//   1. while the pieces land, every thread takes the maximum of its vectors (a
+//      "group max"); each warp's j-th largest group max, minimised over the
+//      row's warps, is a value c with at least K elements >= c (j = K / warps);
+//   2. elements >= c (typically 2-20x K of them) are written to the leader CTA
+//      through distributed shared memory at offsets from a cluster-wide scan;
+//   3. the leader sorts the candidates and writes the first K.
+// If more than TK_CAP elements pass the filter (heavy ties), the cluster falls
+// back to an exact radix select of the K-th value with ordered tie compaction.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -21,22 +21,67 @@ constexpr int TK_NT = 512;
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+constexpr int TK_CAP = 4096;      // candidate keys gathered by the leader CTA
+constexpr int TK_PIECE = 16384;   // bytes per bulk copy (one mbarrier each)
+constexpr int TK_MAXP = 16;       // at most 16 pieces (256 KB chunk)
+constexpr int TK_STASH = 4;       // candidate keys a thread keeps in registers
+
 struct TopkSmem {
     size_t hist, hsum, misc, wtot, mbar, cand, total;
 };
 
-__host__ __device__ inline TopkSmem topk_smem_layout(int chunk, int elem, int kpad) {
+__host__ __device__ inline TopkSmem topk_smem_layout(int chunk, int elem) {
     TopkSmem s{};
     size_t off = align_up(size_t(chunk) * elem, 128);
     s.hist = off; off += 2 * 256 * 4;
     s.hsum = off; off += 256 * 4;
     s.misc = off; off += 64 * 4;
     s.wtot = off; off += 32 * 4;
-    s.mbar = off; off += 16;
+    s.mbar = off; off += 8 * TK_MAXP;
     off = align_up(off, 16);
-    s.cand = off; off += size_t(kpad) * 8;
+    s.cand = off; off += size_t(TK_CAP) * 8;
     s.total = off;
     return s;
+}
+
+// Largest orderable key among the VEC elements of one 16-byte vector.
+__device__ __forceinline__ uint32_t vec_max_ord(uint4 v, bf16_t*) {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
+    const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&v.z);
+    const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&v.w);
+    const __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
+    const uint32_t mb = *reinterpret_cast<const uint32_t*>(&m);
+    const uint32_t lo = ord_bf16(mb & 0xffffu), hi = ord_bf16(mb >> 16);
+    return lo > hi ? lo : hi;
+}
+__device__ __forceinline__ uint32_t vec_max_ord(uint4 v, float*) {
+    return ord_f32(fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                         fmaxf(__uint_as_float(v.z), __uint_as_float(v.w))));
+}
+__device__ __forceinline__ uint32_t vec_elem_ord(uint4 v, int e, bf16_t*) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    return ord_bf16((w[e >> 1] >> ((e & 1) * 16)) & 0xffffu);
+}
+__device__ __forceinline__ uint32_t vec_elem_ord(uint4 v, int e, float*) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    return ord_f32(__uint_as_float(w[e]));
+}
+
+// j-th largest (1-based, j <= 32) of one value per lane.
+__device__ __forceinline__ uint32_t warp_jth_largest(uint32_t v, int j) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int m = k >> 1; m > 0; m >>= 1) {
+            const uint32_t o = __shfl_xor_sync(0xffffffffu, v, m);
+            const bool lower = (lane & m) == 0;
+            const bool desc = (lane & k) == 0;
+            v = (lower == desc) ? (o > v ? o : v) : (o < v ? o : v);
+        }
+    }
+    return __shfl_sync(0xffffffffu, v, j - 1);
 }
 
 // Calls f(index_in_chunk, ord_key) for the thread's owned run [lo, hi) in order.
@@ -100,69 +145,25 @@ __device__ bool cluster_select_kth(Each&& each, uint32_t lo, uint32_t K, uint32_
     return true;
 }
 
+// Exact selection used when the filter leaves more than TK_CAP candidates (heavy
+// ties, constant rows): radix select of the K-th largest value over the whole
+// chunk, then ordered compaction of the ties in token order. Writes the K keys
+// to the leader's cand[0..K) (unsorted).
 template <typename T>
-__global__ void __launch_bounds__(TK_NT) topk_rows_kernel(const T* __restrict__ x, int V, int K, int kpad,
-                                                          int chunk, int use_bulk, int32_t* __restrict__ out_tok,
-                                                          float* __restrict__ out_val, int* status) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+__device__ bool topk_exact_fallback(const T* buf, int n, int c0, int K, uint32_t S, uint32_t cr, uint32_t* hist,
+                                    uint32_t* hsum, uint32_t* misc, int* wtot, uint64_t* cand) {
     constexpr int VEC = ValueKey<T>::VEC;
     constexpr int KBITS = ValueKey<T>::BITS;
-    const uint32_t S = cluster_nctarank(), cr = cluster_ctarank();
-    const int row = blockIdx.x / S;
-    const int c0 = int(cr) * chunk;
-    const int n = max(0, min(V, c0 + chunk) - c0);
-    const TopkSmem L = topk_smem_layout(chunk, sizeof(T), kpad);
-    T* buf = reinterpret_cast<T*>(smem);
-    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L.hist);
-    uint32_t* hsum = reinterpret_cast<uint32_t*>(smem + L.hsum);
-    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L.misc);
-    int* wtot = reinterpret_cast<int*>(smem + L.wtot);
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + L.mbar);
-    uint64_t* cand = reinterpret_cast<uint64_t*>(smem + L.cand);
-    const T* src = x + size_t(row) * V + c0;
-
-    if (threadIdx.x < 64) misc[threadIdx.x] = 0;
-    bool loaded = true;
-    if (use_bulk) {
-        if (threadIdx.x == 0) { mbar_init(mbar, 1); fence_mbar_init(); }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const uint32_t bytes = uint32_t(n) * sizeof(T);
-            mbar_arrive_expect_tx(mbar, bytes);
-            constexpr uint32_t PIECE = 32768;
-            for (uint32_t o = 0; o < bytes; o += PIECE) {
-                const uint32_t b = bytes - o < PIECE ? bytes - o : PIECE;
-                bulk_g2s(reinterpret_cast<uint8_t*>(buf) + o, reinterpret_cast<const uint8_t*>(src) + o, b, mbar);
-            }
-        }
-        loaded = mbar_wait_bounded(mbar, 0, status);
-    } else {
-        for (int i = threadIdx.x; i < n; i += TK_NT) buf[i] = src[i];
-    }
-    __syncthreads();
-
-    // owned run of this thread (multiple of the 16-byte vector)
     const int per = int(align_up((n + TK_NT - 1) / TK_NT, VEC));
     const int lo = min(n, int(threadIdx.x) * per);
     const int hi = min(n, lo + per);
     auto each = [&](auto&& f) { for_owned<T>(buf, lo, hi, f); };
-
-    // 1. lower bound c from the group maxima
-    uint32_t gm = 0;
-    each([&](int, uint32_t o) { gm = o > gm ? o : gm; });
-    uint32_t c = 0, dummy = 0;
-    bool ok = true;
-    if (S * TK_NT >= uint32_t(K)) {
-        ok = cluster_select_kth<KBITS>([&](auto&& f) { f(0, gm); }, 0u, uint32_t(K), hist, hsum, misc, S, c, dummy);
-    }
-    // 2. exact K-th largest value t among elements >= c
+    if (threadIdx.x == 0) misc[9] = 0;
     uint32_t t = 0, rem = 0;
-    if (ok) ok = cluster_select_kth<KBITS>(each, c, uint32_t(K), hist, hsum, misc, S, t, rem);
-    if (!ok) { t = 0xffffffffu; rem = 0; }  // select nothing; the status records the failure
+    bool ok = cluster_select_kth<KBITS>(each, 0u, uint32_t(K), hist, hsum, misc, S, t, rem);
+    if (!ok) { t = 0xffffffffu; rem = 0; }
     const uint32_t n_gt = uint32_t(K) - rem;
-
-    // 3a. elements > t go to the leader in any order
-    const uint32_t leader_ctr = dsmem_addr(&misc[8], 0);
+    const uint32_t leader_ctr = dsmem_addr(&misc[9], 0);
     const uint32_t leader_cand = dsmem_addr(cand, 0);
     each([&](int i, uint32_t o) {
         if (o > t) {
@@ -170,7 +171,6 @@ __global__ void __launch_bounds__(TK_NT) topk_rows_kernel(const T* __restrict__ 
             if (p < n_gt) st_dsmem_u64(leader_cand + 8u * p, (uint64_t(o) << 32) | (0xffffffffu - uint32_t(c0 + i)));
         }
     });
-    // 3b. the first rem elements == t in token order
     int cnt = 0;
     each([&](int, uint32_t o) { cnt += (o == t); });
     const int excl = block_exclusive_scan<TK_NT>(cnt, wtot, reinterpret_cast<int*>(&misc[16]));
@@ -179,26 +179,166 @@ __global__ void __launch_bounds__(TK_NT) topk_rows_kernel(const T* __restrict__ 
     for (uint32_t q = 0; q < cr; ++q) rank += ld_dsmem_u32(dsmem_addr(&misc[16], q));
     each([&](int i, uint32_t o) {
         if (o == t) {
-            if (rank < rem) st_dsmem_u64(leader_cand + 8u * (n_gt + rank), (uint64_t(o) << 32) | (0xffffffffu - uint32_t(c0 + i)));
+            if (rank < rem)
+                st_dsmem_u64(leader_cand + 8u * (n_gt + rank), (uint64_t(o) << 32) | (0xffffffffu - uint32_t(c0 + i)));
             ++rank;
         }
     });
     cluster_sync();
+    return ok && (cr != 0 || misc[9] == n_gt);
+}
 
-    // 4. leader sorts and writes
-    if (cr == 0) {
-        if (threadIdx.x == 0 && (!ok || misc[8] != n_gt)) set_status(status, DARTREE_EINTERNAL);
-        for (int i = K + threadIdx.x; i < kpad; i += TK_NT) cand[i] = 0;
-        if (!ok) for (int i = threadIdx.x; i < K; i += TK_NT) cand[i] = 0;
+template <typename T>
+__global__ void __launch_bounds__(TK_NT) topk_rows_kernel(const T* __restrict__ x, int V, int K, int jsel,
+                                                          int chunk, int use_bulk, int32_t* __restrict__ out_tok,
+                                                          float* __restrict__ out_val, int* status) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr int VEC = ValueKey<T>::VEC;
+    const uint32_t S = cluster_nctarank(), cr = cluster_ctarank();
+    const int row = blockIdx.x / S;
+    const int c0 = int(cr) * chunk;
+    const int n = max(0, min(V, c0 + chunk) - c0);
+    const TopkSmem L = topk_smem_layout(chunk, sizeof(T));
+    T* buf = reinterpret_cast<T*>(smem);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L.hist);
+    uint32_t* hsum = reinterpret_cast<uint32_t*>(smem + L.hsum);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L.misc);
+    int* wtot = reinterpret_cast<int*>(smem + L.wtot);
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + L.mbar);
+    uint64_t* cand = reinterpret_cast<uint64_t*>(smem + L.cand);
+    const T* src = x + size_t(row) * V + c0;
+    const int nvec = n / VEC;
+    constexpr int VPP = TK_PIECE / 16;  // vectors per piece
+    const uint32_t bytes = uint32_t(n) * sizeof(T);
+    const int npieces = use_bulk ? int((bytes + TK_PIECE - 1) / TK_PIECE) : 0;
+
+    // misc: [2] CTA min, [3] leader min, [4] leader count, [8..] scans
+    if (threadIdx.x < 64) misc[threadIdx.x] = (threadIdx.x == 2 || threadIdx.x == 3) ? 0xffffffffu : 0u;
+    if (use_bulk) {
+        if (threadIdx.x == 0) {
+            for (int p = 0; p < npieces; ++p) mbar_init(&mbar[p], 1);
+            fence_mbar_init();
+        }
         __syncthreads();
-        bitonic_sort_desc<TK_NT>(cand, kpad);
+        if (threadIdx.x == 0) {
+            for (int p = 0; p < npieces; ++p) {
+                const uint32_t o = uint32_t(p) * TK_PIECE;
+                const uint32_t b = bytes - o < uint32_t(TK_PIECE) ? bytes - o : uint32_t(TK_PIECE);
+                mbar_arrive_expect_tx(&mbar[p], b);
+                bulk_g2s(reinterpret_cast<uint8_t*>(buf) + o, reinterpret_cast<const uint8_t*>(src) + o, b, &mbar[p]);
+            }
+        }
+    } else {
+        for (int i = threadIdx.x; i < n; i += TK_NT) buf[i] = src[i];
+        __syncthreads();
+    }
+
+    // pass 1: group maximum of the vectors t, t+NT, ... (piece by piece as they land)
+    uint32_t gm = 0;
+    bool loaded = true;
+    if (use_bulk) {
+        for (int p = 0; p < npieces; ++p) {
+            if (!mbar_wait_bounded(&mbar[p], 0, status)) loaded = false;
+            const int v1 = min(nvec, (p + 1) * VPP);
+            for (int v = p * VPP + int(threadIdx.x); v < v1; v += TK_NT) {
+                const uint32_t o = vec_max_ord(reinterpret_cast<const uint4*>(buf)[v], static_cast<T*>(nullptr));
+                gm = o > gm ? o : gm;
+            }
+        }
+    } else {
+        for (int v = threadIdx.x; v < nvec; v += TK_NT) {
+            const uint32_t o = vec_max_ord(reinterpret_cast<const uint4*>(buf)[v], static_cast<T*>(nullptr));
+            gm = o > gm ? o : gm;
+        }
+    }
+    for (int i = nvec * VEC + int(threadIdx.x); i < n; i += TK_NT) {
+        const uint32_t o = ValueKey<T>::ord(buf[i]);
+        gm = o > gm ? o : gm;
+    }
+    // lower bound c: every warp holds jsel groups whose maximum is >= its jsel-th
+    // largest group max, and the warps of the row number at least K / jsel, so at
+    // least K elements are >= the minimum over warps of those values.
+    uint32_t wj = jsel <= 32 ? warp_jth_largest(gm, jsel) : 0u;
+    if ((threadIdx.x & 31) == 0) atomicMin(&misc[2], wj);
+    __syncthreads();
+    cluster_sync();  // every CTA's misc is initialised before remote atomics
+    if (threadIdx.x == 0) {
+        uint32_t old;
+        asm volatile("atom.shared::cluster.min.u32 %0, [%1], %2;" : "=r"(old) : "r"(dsmem_addr(&misc[3], 0)), "r"(misc[2]) : "memory");
+    }
+    cluster_sync();
+    const uint32_t c = ld_dsmem_u32(dsmem_addr(&misc[3], 0));
+
+    // pass 2: candidates >= c; a few per thread stay in registers
+    uint64_t stash[TK_STASH];
+    int cnt = 0;
+    auto consider = [&](uint32_t o, int i) {
+        if (o >= c) {
+            const uint64_t key = (uint64_t(o) << 32) | (0xffffffffu - uint32_t(c0 + i));
+#pragma unroll
+            for (int q = 0; q < TK_STASH; ++q)
+                if (q == cnt) stash[q] = key;
+            ++cnt;
+        }
+    };
+    for (int v = threadIdx.x; v < nvec; v += TK_NT) {
+        const uint4 w = reinterpret_cast<const uint4*>(buf)[v];
+        if (vec_max_ord(w, static_cast<T*>(nullptr)) >= c) {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) consider(vec_elem_ord(w, e, static_cast<T*>(nullptr)), v * VEC + e);
+        }
+    }
+    for (int i = nvec * VEC + int(threadIdx.x); i < n; i += TK_NT) consider(ValueKey<T>::ord(buf[i]), i);
+    const int excl = block_exclusive_scan<TK_NT>(cnt, wtot, reinterpret_cast<int*>(&misc[8]));
+    cluster_sync();  // CTA totals visible
+    uint32_t base = 0, total = 0;
+    for (uint32_t q = 0; q < S; ++q) {
+        const uint32_t tq = ld_dsmem_u32(dsmem_addr(&misc[8], q));
+        base += q < cr ? tq : 0u;
+        total += tq;
+    }
+    const bool fits = total >= uint32_t(K) && total <= uint32_t(TK_CAP);
+    if (fits) {
+        const uint32_t leader_cand = dsmem_addr(cand, 0);
+        uint32_t pos = base + uint32_t(excl);
+        if (cnt <= TK_STASH) {
+#pragma unroll
+            for (int q = 0; q < TK_STASH; ++q)
+                if (q < cnt) st_dsmem_u64(leader_cand + 8u * (pos + q), stash[q]);
+        } else {  // more candidates than registers: scan this thread's vectors again
+            auto put = [&](uint32_t o, int i) {
+                if (o >= c) { st_dsmem_u64(leader_cand + 8u * pos, (uint64_t(o) << 32) | (0xffffffffu - uint32_t(c0 + i))); ++pos; }
+            };
+            for (int v = threadIdx.x; v < nvec; v += TK_NT) {
+                const uint4 w = reinterpret_cast<const uint4*>(buf)[v];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) put(vec_elem_ord(w, e, static_cast<T*>(nullptr)), v * VEC + e);
+            }
+            for (int i = nvec * VEC + int(threadIdx.x); i < n; i += TK_NT) put(ValueKey<T>::ord(buf[i]), i);
+        }
+        cluster_sync();
+    } else {
+        // uniform across the cluster: every CTA summed the same totals
+        if (!topk_exact_fallback<T>(buf, n, c0, K, S, cr, hist, hsum, misc, wtot, cand))
+            if (threadIdx.x == 0) set_status(status, DARTREE_EINTERNAL);
+    }
+
+    // leader sorts the candidates and writes the first K
+    if (cr == 0) {
+        const int m = fits ? int(total) : K;
+        int mpad = 1;
+        while (mpad < m) mpad <<= 1;
+        for (int i = m + threadIdx.x; i < mpad; i += TK_NT) cand[i] = 0;
+        __syncthreads();
+        bitonic_sort_desc<TK_NT>(cand, mpad);
         for (int i = threadIdx.x; i < K; i += TK_NT) {
             const uint64_t k = cand[i];
             out_tok[size_t(row) * K + i] = int32_t(0xffffffffu - uint32_t(k));
             out_val[size_t(row) * K + i] = ValueKey<T>::value(uint32_t(k >> 32));
         }
     }
-    if (use_bulk && !loaded && threadIdx.x == 0) mbar_wait_bounded(mbar, 0, nullptr);
+    if (use_bulk && !loaded && threadIdx.x == 0)
+        for (int p = 0; p < npieces; ++p) mbar_wait_bounded(&mbar[p], 0, nullptr);
 }
 
 // --------------------------------------------------------------------------- host side
@@ -226,9 +366,9 @@ static int launch_topk_t(const void* x, int rows, int V, int K, int32_t* tok, fl
                      (rows * S < 2 * num_sms() && size_t(chunk_of(2 * S)) * elem >= 16 * 1024)))
         S *= 2;
     const int chunk = chunk_of(S);
-    int kpad = 1;
-    while (kpad < K) kpad <<= 1;
-    const TopkSmem L = topk_smem_layout(chunk, elem, kpad);
+    const TopkSmem L = topk_smem_layout(chunk, elem);
+    const int warps = S * (TK_NT / 32);
+    const int jsel = (K + warps - 1) / warps;  // > 32 disables the filter (exact path)
     const int use_bulk = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && ((size_t(V) * elem) % 16 == 0);
     auto kern = topk_rows_kernel<T>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.total)) != cudaSuccess)
@@ -247,7 +387,7 @@ static int launch_topk_t(const void* x, int rows, int V, int K, int32_t* tok, fl
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const T*>(x), V, K, kpad, chunk, use_bulk,
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const T*>(x), V, K, jsel, chunk, use_bulk,
                                        tok, val, status);
     return e == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
