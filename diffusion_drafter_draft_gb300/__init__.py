@@ -24,7 +24,7 @@ OK, EINVAL, EDTYPE, EWORKSPACE, ECUDA, ETIMEOUT, EINTERNAL, EUNSUPPORTED = 0, -1
 
 EXPORTS = ("dartree_head_init", "dartree_workspace_bytes", "dartree_topk", "dartree_expand", "dartree_prune",
            "dartree_tree_mask", "dartree_build_tree", "dartree_verify", "dartree_read_status",
-           "dartree_clear_status", "dartree_status_string")
+           "dartree_clear_status", "dartree_status_string", "dartree_verify_static")
 
 
 class DartreeError(RuntimeError):
@@ -86,6 +86,7 @@ def lib() -> ctypes.CDLL:
         "dartree_build_tree": (i, [P(Head), P(Params), vp, vp, vp, P(Tree), P(Supertree), P(Candidates), vp, sz,
                                    vp]),
         "dartree_verify": (i, [P(Params), P(Tree), vp, i, i, i, vp, vp, vp, vp, sz, vp]),
+        "dartree_verify_static": (i, [P(Params), P(Tree), vp, i, i, i, vp, vp, vp, vp]),
         "dartree_read_status": (i, [vp, P(ctypes.c_int32), vp]),
         "dartree_clear_status": (i, [vp, vp]),
         "dartree_status_string": (ctypes.c_char_p, [i]),
@@ -288,6 +289,23 @@ def verify(tree, target, rows: int, L: int, ws=None, stream=None):
     _call("dartree_verify", ctypes.byref(p), ctypes.byref(ts), ctypes.c_void_p(target.data_ptr()), int(rows), int(V),
           _dtype_code(target), ctypes.c_void_p(out["accepted_len"].data_ptr()), ctypes.c_void_p(out["path"].data_ptr()),
           ctypes.c_void_p(out["bonus"].data_ptr()), ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
+    return out
+
+
+def verify_static(tree, target, rows: int, L: int, stream=None):
+    """S10 through dartree_verify_static (no workspace; scratch in a fixed device array)."""
+    C, S = tree["tok"].shape
+    V = target.shape[-1]
+    _need(target, "target", None, (C, L, V) if rows == ROWS_PER_POSITION else (C, S, V))
+    dev = target.device
+    out = dict(accepted_len=torch.empty((C,), dtype=torch.int32, device=dev),
+               path=torch.empty((C, L), dtype=torch.int32, device=dev),
+               bonus=torch.empty((C,), dtype=torch.int32, device=dev))
+    p = _params(C, L, 1, 1, S - 1, 0.0)
+    ts = _tree_struct(tree)
+    _call("dartree_verify_static", ctypes.byref(p), ctypes.byref(ts), ctypes.c_void_p(target.data_ptr()), int(rows),
+          int(V), _dtype_code(target), ctypes.c_void_p(out["accepted_len"].data_ptr()),
+          ctypes.c_void_p(out["path"].data_ptr()), ctypes.c_void_p(out["bonus"].data_ptr()), _stream(stream))
     return out
 
 

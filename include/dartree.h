@@ -188,6 +188,26 @@ DARTREE_API int dartree_verify(const dartree_params* p, const dartree_tree* tree
                    int rows, int V, int dtype, int32_t* accepted_len, int32_t* path,
                    int32_t* bonus, void* ws, size_t ws_bytes, void* stream);
 
+/* S10 without a workspace, for callers that cannot allocate device memory where
+ * they verify (for example a serving loop whose caching allocator holds all free
+ * HBM, or a plugin behind a plain C interface with no allocator handle). The
+ * paper has no counterpart: this is a deployment variant of dartree_verify with
+ * the same arguments, minus the workspace, and the same results.
+ * Scratch is one file-scope device array of DARTREE_STATIC_VERIFY_BYTES bytes
+ * (status word + 8 bytes per target row key), kept by every GPU that loads the
+ * library until the process exits. Limit: 256 + 8*C*max(L, B+1) bytes must fit,
+ * else DARTREE_EUNSUPPORTED (before anything is enqueued). The first call on a
+ * device looks up the array's device address with that device current (a
+ * cudaGetSymbolAddress, no allocation); make that first call before any stream
+ * capture. All calls share the one array and each starts by clearing what must
+ * start at zero: calls that overlap on the GPU (other streams, other threads)
+ * race on it and must be serialised by the caller. Allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library call. */
+#define DARTREE_STATIC_VERIFY_BYTES (256u * 1024u)
+DARTREE_API int dartree_verify_static(const dartree_params* p, const dartree_tree* tree, const void* target,
+                                      int rows, int V, int dtype, int32_t* accepted_len, int32_t* path,
+                                      int32_t* bonus, void* stream);
+
 /* Copies the device status word of `ws` to *status (synchronises `stream`). */
 DARTREE_API int dartree_read_status(const void* ws, int32_t* status, void* stream);
 
