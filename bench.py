@@ -279,6 +279,30 @@ def cpu_baseline_stress(cfg, budget_requests=1):
             "sample": f"oracle build of {budget_requests} of {cfg.C} requests ({dt:.1f} s), scaled to the batch"}
 
 
+# --------------------------------------------------------------------------- profiling mode
+
+def profile_only(args):
+    """Runs one entry point on one workload (for ncu); prints its device time."""
+    import torch
+    import diffusion_drafter_draft_gb300 as dd
+    from diffusion_drafter_draft_gb300 import _build
+    _build.build()
+    cfg = make_config(args.config or MAIN_CFG)
+    inp, x = device_inputs(cfg, torch)
+    rows = dd.ROWS_PER_POSITION if cfg.rows == "position" else dd.ROWS_PER_NODE
+    V = x["E"].shape[0]
+    if args.only == "topk":
+        ws = dd.new_workspace(256)
+        base2 = x["base"].view(cfg.C * cfg.L, V)
+        fn = lambda: dd.topk(base2, cfg.K, ws=ws)  # noqa: E731
+    else:
+        rnd = dd.Round(x["E"], x["Wq"], cfg.C, cfg.L, cfg.K, cfg.W, cfg.B, cfg.beta, rows)
+        fn = lambda: rnd.run(x["base"], x["hidden"], x["anchor"], x["target"])  # noqa: E731
+    t = time_steps(torch, fn, args.steps, max(3, args.warmup), None)
+    print(json.dumps({"only": args.only, "workload": cfg.name, "ms_median": float(np.median(t)),
+                      "ms_min": float(np.min(t))}))
+
+
 # --------------------------------------------------------------------------- main
 
 def main():
@@ -289,7 +313,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-stress", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--only", choices=["topk", "round"], default=None,
+                    help="profiling mode: run just one entry point on --config and print its timing")
+    ap.add_argument("--config", default=None, help="workload name for --only (default: the main workload)")
     args = ap.parse_args()
+    if args.only:
+        return profile_only(args)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     cfg = make_config(MAIN_CFG)

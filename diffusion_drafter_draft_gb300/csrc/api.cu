@@ -12,11 +12,13 @@ namespace {
 using namespace dartree;
 
 constexpr size_t kAlign = 256;
+constexpr int kMaxClusters = 40;  // 8-CTA clusters: up to 320 SMs
 
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-    size_t status, cand_tok, cand_val, h[2], s[2], U, z, st_tok, st_par, st_s, st_n, keys, total;
+    size_t status, cand_tok, cand_val, h[2], s[2], U, z, st_tok, st_par, st_s, st_n, keys, zpart, bar, total;
+    int zpart_clusters;
 };
 
 Layout layout_of(const dartree_params& p, int H, int dtype) {
@@ -39,6 +41,10 @@ Layout layout_of(const dartree_params& p, int H, int dtype) {
     l.st_s = take(C * L * W * 4);
     l.st_n = take(C * L * 4);
     l.keys = take((C * L > C * (B + 1) ? C * L : C * (B + 1)) * 8);
+    // per-cluster partial logits of the small-batch persistent kernel (C*W <= 48)
+    l.zpart_clusters = (C * W <= 48) ? kMaxClusters : 0;
+    l.zpart = take(size_t(l.zpart_clusters) * C * W * K * 4);
+    l.bar = take(4);
     l.total = o;
     return l;
 }
@@ -156,6 +162,9 @@ static int expand_impl(const dartree_head* head, const dartree_params* p, const 
     a.sbuf[1] = at<float>(ws, l.s[1]);
     a.U = at<float>(ws, l.U);
     a.z = at<float>(ws, l.z);
+    a.zpart = l.zpart_clusters ? at<float>(ws, l.zpart) : nullptr;
+    a.zpart_clusters = l.zpart_clusters;
+    a.bar = at<unsigned>(ws, l.bar);
     a.status = at<int>(ws, l.status);
     return launch_expand(a, stream);
 }

@@ -288,6 +288,9 @@ static int launch_expand_t(const ExpandArgs& a, cudaStream_t st) {
 }
 
 int launch_expand(const ExpandArgs& a, cudaStream_t stream) {
+    bool done = false;
+    if (int e = try_launch_expand_small(a, stream, &done)) return e;
+    if (done) return DARTREE_OK;
     if (a.dtype == DARTREE_BF16) return launch_expand_t<bf16_t>(a, stream);
     return launch_expand_t<float>(a, stream);
 }

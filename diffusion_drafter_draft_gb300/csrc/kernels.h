@@ -30,8 +30,14 @@ struct ExpandArgs {
     float* sbuf[2];           // [C, W]
     float* U;                 // [C*W, H]
     float* z;                 // [C, W, K]
+    float* zpart;             // [zpart_clusters, C*W*K] per-cluster partial logits (small-batch path)
+    int zpart_clusters;       // 0: small-batch path unavailable
+    unsigned* bar;            // grid barrier counter (small-batch path)
     int* status;
 };
+
+// Small-batch persistent path; *launched = false when the shape does not fit it.
+int try_launch_expand_small(const ExpandArgs& a, cudaStream_t stream, bool* launched);
 
 // S2-S7 over all depths.
 int launch_expand(const ExpandArgs& a, cudaStream_t stream);

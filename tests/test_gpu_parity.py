@@ -106,7 +106,8 @@ def test_tiny_shapes_with_ragged_tails():
     """Several small shapes whose sizes are not multiples of any tile."""
     import diffusion_drafter_draft_gb300 as dd
     for seed, (L, V, H, K, W, B) in enumerate([(3, 211, 24, 5, 7, 9), (5, 1031, 40, 17, 3, 11),
-                                                (2, 99, 8, 33, 40, 50), (6, 517, 72, 1, 4, 5)]):
+                                                (2, 99, 8, 33, 40, 50), (6, 517, 72, 1, 4, 5),
+                                                (4, 3001, 256, 16, 6, 12), (7, 2003, 520, 37, 5, 20)]):
         for dtype in ("f32", "bf16"):
             cfg = make_config("cfg0_tiny").replace(C=3, L=L, V=V, H=H, K=K, W=W, B=B, dtype=dtype, seed=seed,
                                                    beta=-0.05 * seed)
