@@ -288,6 +288,8 @@ def profile_only(args):
     from diffusion_drafter_draft_gb300 import _build
     _build.build()
     cfg = make_config(args.config or MAIN_CFG)
+    if args.C:
+        cfg = cfg.replace(C=args.C)
     inp, x = device_inputs(cfg, torch)
     rows = dd.ROWS_PER_POSITION if cfg.rows == "position" else dd.ROWS_PER_NODE
     V = x["E"].shape[0]
@@ -316,6 +318,7 @@ def main():
     ap.add_argument("--only", choices=["topk", "round"], default=None,
                     help="profiling mode: run just one entry point on --config and print its timing")
     ap.add_argument("--config", default=None, help="workload name for --only (default: the main workload)")
+    ap.add_argument("--C", type=int, default=None, help="--only: override the number of requests (a smaller case)")
     args = ap.parse_args()
     if args.only:
         return profile_only(args)
