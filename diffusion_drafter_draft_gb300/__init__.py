@@ -24,7 +24,7 @@ OK, EINVAL, EDTYPE, EWORKSPACE, ECUDA, ETIMEOUT, EINTERNAL, EUNSUPPORTED = 0, -1
 
 EXPORTS = ("dartree_head_init", "dartree_workspace_bytes", "dartree_topk", "dartree_expand", "dartree_prune",
            "dartree_tree_mask", "dartree_build_tree", "dartree_verify", "dartree_read_status",
-           "dartree_clear_status", "dartree_status_string", "dartree_verify_static")
+           "dartree_clear_status", "dartree_status_string", "dartree_verify_static", "dartree_gemm_bf16")
 
 
 class DartreeError(RuntimeError):
@@ -87,6 +87,7 @@ def lib() -> ctypes.CDLL:
                                    vp]),
         "dartree_verify": (i, [P(Params), P(Tree), vp, i, i, i, vp, vp, vp, vp, sz, vp]),
         "dartree_verify_static": (i, [P(Params), P(Tree), vp, i, i, i, vp, vp, vp, vp]),
+        "dartree_gemm_bf16": (i, [vp, vp, vp, i, i, i, vp, vp]),
         "dartree_read_status": (i, [vp, P(ctypes.c_int32), vp]),
         "dartree_clear_status": (i, [vp, vp]),
         "dartree_status_string": (ctypes.c_char_p, [i]),
@@ -307,6 +308,19 @@ def verify_static(tree, target, rows: int, L: int, stream=None):
           int(V), _dtype_code(target), ctypes.c_void_p(out["accepted_len"].data_ptr()),
           ctypes.c_void_p(out["path"].data_ptr()), ctypes.c_void_p(out["bonus"].data_ptr()), _stream(stream))
     return out
+
+
+def gemm_bf16(A, B, status=None, stream=None):
+    """Building block: D = A . B^T (bf16 in, fp32 out) through the tcgen05 GEMM."""
+    M, K = A.shape
+    N = B.shape[0]
+    _need(A, "A", torch.bfloat16)
+    _need(B, "B", torch.bfloat16, (N, K))
+    D = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _call("dartree_gemm_bf16", ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
+          ctypes.c_void_p(D.data_ptr()), int(M), int(N), int(K),
+          ctypes.c_void_p(status.data_ptr()) if status is not None else None, _stream(stream))
+    return D
 
 
 def build_tree(E, Wq, base, hidden, anchor, K, W, B, beta, ws=None, keep_intermediates=False, stream=None):

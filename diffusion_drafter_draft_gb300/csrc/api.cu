@@ -124,6 +124,12 @@ int dartree_clear_status(void* ws, void* stream) {
     return cudaMemsetAsync(ws, 0, sizeof(int32_t), as_stream(stream)) == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 
+int dartree_gemm_bf16(const void* A, const void* B, float* D, int M, int N, int K, int32_t* status, void* stream) {
+    if (!A || !B || !D || M < 1 || N < 1 || K < 1) return DARTREE_EINVAL;
+    if (!gemm_tc_supported(M, N, K)) return DARTREE_EUNSUPPORTED;
+    return launch_gemm_bf16_tc(A, B, M, N, K, 0, D, nullptr, 1, status, as_stream(stream));
+}
+
 int dartree_topk(const void* logits, int rows, int V, int K, int dtype, int32_t* tok, float* val, void* ws,
                  size_t ws_bytes, void* stream) {
     if (!dtype_ok(dtype)) return DARTREE_EDTYPE;

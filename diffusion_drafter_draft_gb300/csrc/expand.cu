@@ -273,7 +273,11 @@ static int launch_expand_t(const ExpandArgs& a, cudaStream_t st) {
     for (int d = 1; d <= a.L; ++d) {
         const int M = a.C * P;
         dim3 pg((a.H + PJ_TN - 1) / PJ_TN, (M + PJ_TM - 1) / PJ_TM);
-        proj_simple_kernel<T><<<pg, PJ_NT, 0, st>>>(hb[cur], Wq, a.U, M, a.H);
+        if (sizeof(T) == 2 && gemm_tc_supported(M, a.H, a.H)) {
+            if (int e = launch_gemm_bf16_tc(hb[cur], Wq, M, a.H, a.H, 0, a.U, nullptr, 1, a.status, st)) return e;
+        } else {
+            proj_simple_kernel<T><<<pg, PJ_NT, 0, st>>>(hb[cur], Wq, a.U, M, a.H);
+        }
         dim3 cg((a.K + (CT_NT / 32) * CT_CPW - 1) / ((CT_NT / 32) * CT_CPW), a.C);
         contract_simple_kernel<T><<<cg, CT_NT, 0, st>>>(a.U, E, a.cand_tok, a.cand_val, a.z, P, a.K, a.H, a.L, d,
                                                         inv_sqrt_h);

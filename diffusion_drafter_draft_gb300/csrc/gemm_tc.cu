@@ -1,0 +1,200 @@
+// tcgen05 GEMM for the per-depth parent projection (S3, DARTree blog post 3.1:
+// the correction head runs on all surviving parents of a depth in one matrix
+// operation): U[m, :] = h_m W_q^T for all C*P parents at once.
+//
+//   D[M, N] = A[M, K] . B[N, K]^T, A and B bf16 K-major, fp32 accumulation in TMEM.
+//
+// One 128 x BN tile per CTA (cta_group::1). Warp 0's elected thread streams
+// 128 x 64 and BN x 64 tiles with TMA (128-byte swizzle) into a 4-stage ring;
+// warp 1's elected thread issues tcgen05.mma (4 per 64-wide k block) and
+// releases each stage with tcgen05.commit; all 4 warps then read the
+// accumulator from TMEM (one row per thread) and write the epilogue:
+//   mode 0: fp32 D (row-major, ld = N);
+//   mode 1: the contraction's operand, U split into a bf16 pair (hi = bf16(u),
+//           lo = bf16(u - hi)), row m = r*P + p going to rows r*32 + p and
+//           r*32 + 16 + p of a [requests, 32, N] buffer.
+// Every mbarrier wait is bounded; a wait that runs out records DARTREE_ETIMEOUT.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace dartree {
+
+constexpr int GT_BM = 128, GT_BK = 64, GT_STAGES = 4, GT_NT = 128;
+
+struct GemmOut {
+    int mode;          // 0: fp32 d32; 1: hi/lo bf16 pairs into hilo
+    float* d32;
+    uint16_t* hilo;
+    int P;             // mode 1: rows per request (<= 16)
+};
+
+template <int BN>
+struct GtSmem {
+    static constexpr size_t A_BYTES = size_t(GT_BM) * GT_BK * 2;
+    static constexpr size_t B_BYTES = size_t(BN) * GT_BK * 2;
+    static constexpr size_t STAGE = A_BYTES + B_BYTES;
+    static constexpr size_t BAR = STAGE * GT_STAGES;       // full[S], empty[S], accum
+    static constexpr size_t SLOT = BAR + 8 * (2 * GT_STAGES + 1);
+    static constexpr size_t TOTAL = SLOT + 16 + 1024;      // + alignment slack
+};
+
+__device__ __forceinline__ uint16_t bf16_rn_bits(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+
+template <int BN>
+__global__ void __launch_bounds__(GT_NT, 1) gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                                                                const __grid_constant__ CUtensorMap tmB, int M,
+                                                                int N, int K, GemmOut out, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    using L = GtSmem<BN>;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR);
+    uint64_t* empty = full + GT_STAGES;
+    uint64_t* accum = empty + GT_STAGES;
+    uint32_t* slot = reinterpret_cast<uint32_t*>(smem + L::SLOT);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.y * GT_BM, n0 = blockIdx.x * BN;
+    const int nk = (K + GT_BK - 1) / GT_BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < GT_STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        mbar_init(accum, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tc::tmem_alloc(slot, BN);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *slot;
+
+    if (warp == 0 && lane == 0) {
+        // producer: TMA ring
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % GT_STAGES;
+            const uint32_t ph = uint32_t(kb / GT_STAGES) & 1u;
+            if (!mbar_wait_bounded(&empty[s], ph ^ 1u, status)) break;
+            uint8_t* sa = smem + s * L::STAGE;
+            mbar_arrive_expect_tx(&full[s], uint32_t(L::STAGE));
+            tc::tma_load_2d(sa, &tmA, kb * GT_BK, m0, &full[s]);
+            tc::tma_load_2d(sa + L::A_BYTES, &tmB, kb * GT_BK, n0, &full[s]);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer
+        constexpr uint32_t idesc = tc::idesc_bf16_f32(GT_BM, BN);
+        bool ok = true;
+        for (int kb = 0; kb < nk && ok; ++kb) {
+            const int s = kb % GT_STAGES;
+            const uint32_t ph = uint32_t(kb / GT_STAGES) & 1u;
+            if (!mbar_wait_bounded(&full[s], ph, status)) { ok = false; break; }
+            tc::fence_after_sync();
+            const uint32_t sa = smem_u32(smem + s * L::STAGE);
+            const uint64_t da = tc::desc_sw128_kmajor(sa);
+            const uint64_t db = tc::desc_sw128_kmajor(sa + uint32_t(L::A_BYTES));
+#pragma unroll
+            for (int kk = 0; kk < GT_BK / 16; ++kk)  // 16 elements = 32 B = +2 in the encoded address
+                tc::mma_bf16(tmem, da + 2u * kk, db + 2u * kk, idesc, kb > 0 || kk > 0);
+            tc::mma_commit(&empty[s]);
+        }
+        tc::mma_commit(accum);
+    }
+    __syncwarp();
+
+    // epilogue: TMEM -> registers -> global
+    const bool have = mbar_wait_bounded(accum, 0, status);
+    tc::fence_after_sync();
+    const int m = m0 + warp * 32 + lane;
+    const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t r[32];
+        tc::tmem_ld32(trow + uint32_t(c0), r);
+        const int n = n0 + c0;
+        if (!have || m >= M || n >= N) continue;
+        if (out.mode == 0) {
+            float4* dst = reinterpret_cast<float4*>(out.d32 + size_t(m) * N + n);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                     __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        } else {
+            const int rq = m / out.P, p = m % out.P;
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float u0 = __uint_as_float(r[2 * j]), u1 = __uint_as_float(r[2 * j + 1]);
+                const uint16_t h0 = bf16_rn_bits(u0), h1 = bf16_rn_bits(u1);
+                const uint16_t l0 = bf16_rn_bits(u0 - bf16_bits_to_float(h0));
+                const uint16_t l1 = bf16_rn_bits(u1 - bf16_bits_to_float(h1));
+                hi[j] = uint32_t(h0) | (uint32_t(h1) << 16);
+                lo[j] = uint32_t(l0) | (uint32_t(l1) << 16);
+            }
+            uint4* dh = reinterpret_cast<uint4*>(out.hilo + (size_t(rq) * 32 + p) * N + n);
+            uint4* dl = reinterpret_cast<uint4*>(out.hilo + (size_t(rq) * 32 + 16 + p) * N + n);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                dh[j] = make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
+                dl[j] = make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, BN);
+}
+
+// --------------------------------------------------------------------------- host
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (row-major), box = 64 columns x box_rows rows, 128-byte swizzle.
+static bool make_map(CUtensorMap* map, const void* base, int rows, int cols, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+    cuuint32_t box[2] = {cuuint32_t(GT_BK), cuuint32_t(box_rows)};
+    cuuint32_t es[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool gemm_tc_supported(int M, int N, int K) {
+    return M > 0 && N > 0 && K > 0 && N % 128 == 0 && K % 8 == 0 && encode_fn() != nullptr;
+}
+
+int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int mode, float* d32, uint16_t* hilo,
+                        int P, int* status, cudaStream_t stream) {
+    constexpr int BN = 128;
+    if (!gemm_tc_supported(M, N, K)) return DARTREE_EUNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) % 16) return DARTREE_EINVAL;
+    if (mode == 1 && (P < 1 || P > 16 || !hilo)) return DARTREE_EINVAL;
+    if (mode == 0 && !d32) return DARTREE_EINVAL;
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, A, M, K, GT_BM) || !make_map(&tb, B, N, K, BN)) return DARTREE_ECUDA;
+    GemmOut o{mode, d32, hilo, P};
+    const size_t smem = GtSmem<BN>::TOTAL;
+    auto kern = gemm_bf16_tc_kernel<BN>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+        return DARTREE_ECUDA;
+    dim3 grid(N / BN, (M + GT_BM - 1) / GT_BM);
+    kern<<<grid, GT_NT, smem, stream>>>(ta, tb, M, N, K, o, status);
+    return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
+}
+
+}  // namespace dartree

@@ -39,6 +39,12 @@ struct ExpandArgs {
 // Small-batch persistent path; *launched = false when the shape does not fit it.
 int try_launch_expand_small(const ExpandArgs& a, cudaStream_t stream, bool* launched);
 
+// tcgen05 GEMM D[M,N] = A[M,K] . B[N,K]^T (bf16 in, fp32 accumulate).
+// mode 0: fp32 d32 [M,N]; mode 1: bf16 hi/lo pairs into hilo [M/P, 32, N].
+bool gemm_tc_supported(int M, int N, int K);
+int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int mode, float* d32, uint16_t* hilo,
+                        int P, int* status, cudaStream_t stream);
+
 // S2-S7 over all depths.
 int launch_expand(const ExpandArgs& a, cudaStream_t stream);
 

@@ -208,6 +208,14 @@ DARTREE_API int dartree_verify_static(const dartree_params* p, const dartree_tre
                                       int rows, int V, int dtype, int32_t* accepted_len, int32_t* path,
                                       int32_t* bonus, void* stream);
 
+/* Building block exposed for testing: the tcgen05 GEMM used for the per-depth
+ * parent projection. D[M,N] = A[M,K] . B[N,K]^T with A, B bf16 row-major (K
+ * contiguous, 16-byte aligned, K a multiple of 8), D fp32 row-major; N must be a
+ * multiple of 128 (else DARTREE_EUNSUPPORTED). `status` (device int, may be NULL)
+ * receives DARTREE_ETIMEOUT if a bounded wait runs out. */
+DARTREE_API int dartree_gemm_bf16(const void* A, const void* B, float* D, int M, int N, int K, int32_t* status,
+                                  void* stream);
+
 /* Copies the device status word of `ws` to *status (synchronises `stream`). */
 DARTREE_API int dartree_read_status(const void* ws, int32_t* status, void* stream);
 
