@@ -17,7 +17,7 @@ constexpr int kMaxClusters = 40;  // 8-CTA clusters: up to 320 SMs
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-    size_t status, cand_tok, cand_val, h[2], s[2], U, z, st_tok, st_par, st_s, st_n, keys, zpart, bar, total;
+    size_t status, cand_tok, cand_val, h[2], s[2], U, z, st_tok, st_par, st_s, st_n, keys, zpart, bar, uhl, total;
     int zpart_clusters;
 };
 
@@ -45,6 +45,8 @@ Layout layout_of(const dartree_params& p, int H, int dtype) {
     l.zpart_clusters = (C * W <= 48) ? kMaxClusters : 0;
     l.zpart = take(size_t(l.zpart_clusters) * C * W * K * 4);
     l.bar = take(4);
+    // bf16 hi/lo projection rows for the tensor-core contraction, [C, 32, H]
+    l.uhl = take(dtype == DARTREE_BF16 ? C * 32 * size_t(H) * 2 : 0);
     l.total = o;
     return l;
 }
@@ -171,6 +173,7 @@ static int expand_impl(const dartree_head* head, const dartree_params* p, const 
     a.zpart = l.zpart_clusters ? at<float>(ws, l.zpart) : nullptr;
     a.zpart_clusters = l.zpart_clusters;
     a.bar = at<unsigned>(ws, l.bar);
+    a.uhl = head->dtype == DARTREE_BF16 ? at<uint16_t>(ws, l.uhl) : nullptr;
     a.status = at<int>(ws, l.status);
     return launch_expand(a, stream);
 }

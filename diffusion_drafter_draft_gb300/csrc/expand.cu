@@ -273,14 +273,23 @@ static int launch_expand_t(const ExpandArgs& a, cudaStream_t st) {
     for (int d = 1; d <= a.L; ++d) {
         const int M = a.C * P;
         dim3 pg((a.H + PJ_TN - 1) / PJ_TN, (M + PJ_TM - 1) / PJ_TM);
-        if (sizeof(T) == 2 && gemm_tc_supported(M, a.H, a.H)) {
-            if (int e = launch_gemm_bf16_tc(hb[cur], Wq, M, a.H, a.H, 0, a.U, nullptr, 1, a.status, st)) return e;
+        const bool tc_proj = sizeof(T) == 2 && gemm_tc_supported(M, a.H, a.H);
+        if (tc_proj && a.uhl && contract_tc_supported(P, a.H)) {
+            // tensor cores for both: U as bf16 hi/lo pairs, then the gathered contraction
+            if (int e = launch_gemm_bf16_tc(hb[cur], Wq, M, a.H, a.H, 1, nullptr, a.uhl, P, a.status, st)) return e;
+            if (int e = launch_contract_tc(E, a.uhl, a.cand_tok, a.cand_val, a.z, a.C, P, a.K, a.H, a.L, d,
+                                           inv_sqrt_h, a.status, st))
+                return e;
         } else {
-            proj_simple_kernel<T><<<pg, PJ_NT, 0, st>>>(hb[cur], Wq, a.U, M, a.H);
+            if (tc_proj) {
+                if (int e = launch_gemm_bf16_tc(hb[cur], Wq, M, a.H, a.H, 0, a.U, nullptr, 1, a.status, st)) return e;
+            } else {
+                proj_simple_kernel<T><<<pg, PJ_NT, 0, st>>>(hb[cur], Wq, a.U, M, a.H);
+            }
+            dim3 cg((a.K + (CT_NT / 32) * CT_CPW - 1) / ((CT_NT / 32) * CT_CPW), a.C);
+            contract_simple_kernel<T><<<cg, CT_NT, 0, st>>>(a.U, E, a.cand_tok, a.cand_val, a.z, P, a.K, a.H, a.L, d,
+                                                            inv_sqrt_h);
         }
-        dim3 cg((a.K + (CT_NT / 32) * CT_CPW - 1) / ((CT_NT / 32) * CT_CPW), a.C);
-        contract_simple_kernel<T><<<cg, CT_NT, 0, st>>>(a.U, E, a.cand_tok, a.cand_val, a.z, P, a.K, a.H, a.L, d,
-                                                        inv_sqrt_h);
         const int n_keep = P * a.K < a.W ? P * a.K : a.W;
         select_kernel<T><<<a.C, SL_NT, select_smem(P, a.K, a.W), st>>>(
             a.z, a.sbuf[cur], hb[cur], a.cand_tok, E, hid, P, a.K, a.W, a.H, a.L, d, a.beta, a.st_tok, a.st_par,

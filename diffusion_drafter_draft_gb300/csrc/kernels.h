@@ -30,6 +30,7 @@ struct ExpandArgs {
     float* sbuf[2];           // [C, W]
     float* U;                 // [C*W, H]
     float* z;                 // [C, W, K]
+    uint16_t* uhl;            // [C, 32, H] bf16 hi/lo projection rows (tensor-core contraction), or null
     float* zpart;             // [zpart_clusters, C*W*K] per-cluster partial logits (small-batch path)
     int zpart_clusters;       // 0: small-batch path unavailable
     unsigned* bar;            // grid barrier counter (small-batch path)
@@ -44,6 +45,11 @@ int try_launch_expand_small(const ExpandArgs& a, cudaStream_t stream, bool* laun
 bool gemm_tc_supported(int M, int N, int K);
 int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int mode, float* d32, uint16_t* hilo,
                         int P, int* status, cudaStream_t stream);
+
+// tcgen05 contraction of one depth: z[r,p,c] from gathered candidate rows and uhl.
+bool contract_tc_supported(int P, int H);
+int launch_contract_tc(const void* E, const uint16_t* uhl, const int32_t* cand_tok, const float* cand_val, float* z,
+                       int C, int P, int K, int H, int L, int d, float inv_sqrt_h, int* status, cudaStream_t stream);
 
 // S2-S7 over all depths.
 int launch_expand(const ExpandArgs& a, cudaStream_t stream);

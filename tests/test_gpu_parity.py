@@ -119,6 +119,21 @@ def test_tiny_shapes_with_ragged_tails():
             compare_verify(o, gv, inp["target"], cfg, "position")
 
 
+@pytest.mark.parametrize("C,L,V,H,K,W,B", [(5, 5, 3001, 256, 200, 12, 30), (9, 4, 1500, 128, 33, 16, 40),
+                                           (7, 6, 2048, 384, 128, 8, 25)])
+def test_large_batch_path_shapes(C, L, V, H, K, W, B):
+    """Batches with C*W > 48 take the per-depth path (tcgen05 projection and
+    tensor-core contraction when H is a multiple of 128)."""
+    import diffusion_drafter_draft_gb300 as dd
+    cfg = make_config("cfg1_qwen3_4b_c1").replace(C=C, L=L, V=V, H=H, K=K, W=W, B=B, seed=C * 100 + K)
+    inp = make_inputs(cfg)
+    g, x = run_gpu_build(inp)
+    o = compare_build(inp, g)
+    tr = {k: torch.from_numpy(v).cuda() for k, v in g.items() if k in ("tok", "par", "depth", "n_nodes")}
+    gv = host(dd.verify(tr, x["target"], dd.ROWS_PER_POSITION, cfg.L))
+    compare_verify(o, gv, inp["target"], cfg, "position")
+
+
 def test_stress_batch_sampled_requests():
     """Full C=64, K=512 batch on the GPU; the oracle checks a sample of requests
     (each request is drawn from its own stream, so a sample is bit-identical)."""
