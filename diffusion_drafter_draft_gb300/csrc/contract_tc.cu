@@ -8,23 +8,28 @@
 // 16 significant bits), and z = cand + (D[c, p] + D[c, 16+p]) / sqrt(H).
 //
 // One CTA per (request, 128-candidate tile). The candidate rows are a gather
-// (8 KB rows of a 151936-row table), so four producer warps copy each row's
-// 128-byte k-slice with 16-byte cp.async into a 128-byte-swizzled stage (the
-// layout tcgen05 reads) and arrive on the stage's mbarrier when their copies
-// land; warp 4 issues tcgen05.mma (M=128, N=32) into TMEM and frees the stage
-// with tcgen05.commit; warps 0-3 then write z from TMEM. All waits are bounded.
+// (8 KB rows of a 151936-row table). Each stage holds a 128-element k-slice of
+// every row (two 128-byte swizzle atoms, the layout tcgen05 reads); the four
+// producer warps copy it with 16-byte cp.async, 16 lanes per row so that every
+// instruction reads two whole 256-byte row segments, and arrive on the stage's
+// mbarrier when their copies land. Warp 4 issues tcgen05.mma (M=128, N=32) into
+// TMEM and frees the stage with tcgen05.commit; warps 0-3 then write z from
+// TMEM. All waits are bounded.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
 
 namespace dartree {
 
-constexpr int CC_BM = 128, CC_BN = 32, CC_BK = 64, CC_STAGES = 4, CC_NT = 160;
-constexpr size_t CC_A = size_t(CC_BM) * CC_BK * 2;   // 16 KB
-constexpr size_t CC_B = size_t(CC_BN) * CC_BK * 2;   // 4 KB
+constexpr int CC_BM = 128, CC_BN = 32, CC_BK = 128, CC_STAGES = 4, CC_NT = 160;
+constexpr int CC_ATOMS = CC_BK / 64;                  // 64-element swizzle atoms per stage row
+constexpr size_t CC_A_ATOM = size_t(CC_BM) * 128;     // 16 KB: 128 rows x 128 B
+constexpr size_t CC_B_ATOM = size_t(CC_BN) * 128;     // 4 KB
+constexpr size_t CC_A = CC_A_ATOM * CC_ATOMS;
+constexpr size_t CC_B = CC_B_ATOM * CC_ATOMS;
 constexpr size_t CC_STAGE = CC_A + CC_B;
 constexpr size_t CC_BAR = CC_STAGE * CC_STAGES;
-constexpr size_t CC_SMEM = CC_BAR + 8 * (2 * CC_STAGES + 1) + 16 + 1024;
+constexpr size_t CC_SMEM = CC_BAR + 8 * (2 * CC_STAGES + 1) + 16 + 128 * 4 + 1024;
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
@@ -62,29 +67,37 @@ __global__ void __launch_bounds__(CC_NT, 1) contract_tc_kernel(const uint16_t* _
     tc::fence_after_sync();
     const uint32_t tmem = *slot;
 
+    int* rowtok = reinterpret_cast<int*>(accum + 2);  // 128 candidate tokens of this tile (-1 = none)
     if (warp < 4) {
-        // producers: thread t copies candidate row t (8 x 16 B per k block) and 2 chunks of B
-        const int i = threadIdx.x;
-        const int c = c0 + i;
-        const bool valid = c < K;
-        const uint16_t* arow = E + size_t(cand_tok[crow + (valid ? c : 0)]) * H;
+        const int c = c0 + int(threadIdx.x);
+        rowtok[threadIdx.x] = c < K ? cand_tok[crow + c] : -1;
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // producers only
+        // producers: per stage, warp w copies rows 32w..32w+31 (two rows per instruction,
+        // 16 lanes x 16 B = one 256-byte row segment each) and 4 chunks of B per thread
+        const int half = lane >> 4, j = lane & 15;       // j: 16-byte chunk within the 256-byte slice
+        const uint32_t atom_off = uint32_t(j >> 3), jj = uint32_t(j & 7);
         const uint16_t* brow = uhl + (size_t(r) * CC_BN) * H;
-        const uint32_t sw = uint32_t(i & 7);
         for (int kb = 0; kb < nk; ++kb) {
             const int s = kb % CC_STAGES;
             const uint32_t ph = uint32_t(kb / CC_STAGES) & 1u;
             if (!mbar_wait_bounded(&empty[s], ph ^ 1u, status)) break;
             const uint32_t sa = smem_u32(smem + s * CC_STAGE);
-            const uint16_t* src = arow + kb * CC_BK;
+            const int k0 = kb * CC_BK + j * 8;
+#pragma unroll 4
+            for (int q = 0; q < 16; ++q) {
+                const int row = warp * 32 + 2 * q + half;
+                const int tk = rowtok[row];
+                const uint32_t dst = sa + atom_off * uint32_t(CC_A_ATOM) + uint32_t(row) * 128u +
+                                     ((jj ^ uint32_t(row & 7)) << 4);
+                cp_async16(dst, E + size_t(tk < 0 ? 0 : tk) * H + k0, tk < 0 ? 0u : 16u);
+            }
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                cp_async16(sa + uint32_t(i) * 128u + ((uint32_t(j) ^ sw) << 4), src + j * 8, valid ? 16u : 0u);
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int ch = i * 2 + q;          // 256 chunks: 32 rows x 8
-                const int br = ch >> 3, bj = ch & 7;
-                cp_async16(sa + uint32_t(CC_A) + uint32_t(br) * 128u + ((uint32_t(bj) ^ uint32_t(br & 7)) << 4),
-                           brow + size_t(br) * H + kb * CC_BK + bj * 8, 16u);
+            for (int q = 0; q < 4; ++q) {
+                const int ch = int(threadIdx.x) * 4 + q;   // 512 chunks: 32 rows x 16
+                const int br = ch >> 4, bj = ch & 15;
+                const uint32_t dst = sa + uint32_t(CC_A) + uint32_t(bj >> 3) * uint32_t(CC_B_ATOM) +
+                                     uint32_t(br) * 128u + ((uint32_t(bj & 7) ^ uint32_t(br & 7)) << 4);
+                cp_async16(dst, brow + size_t(br) * H + kb * CC_BK + bj * 8, 16u);
             }
             cp_async_arrive(&full[s]);
         }
@@ -98,11 +111,14 @@ __global__ void __launch_bounds__(CC_NT, 1) contract_tc_kernel(const uint16_t* _
             fence_proxy_async_smem();  // cp.async writes -> tensor-core reads
             tc::fence_after_sync();
             const uint32_t sa = smem_u32(smem + s * CC_STAGE);
-            const uint64_t da = tc::desc_sw128_kmajor(sa);
-            const uint64_t db = tc::desc_sw128_kmajor(sa + uint32_t(CC_A));
 #pragma unroll
-            for (int kk = 0; kk < CC_BK / 16; ++kk)
-                tc::mma_bf16(tmem, da + 2u * kk, db + 2u * kk, idesc, kb > 0 || kk > 0);
+            for (int kk = 0; kk < CC_BK / 16; ++kk) {
+                // 16-element step kk: atom kk/4, 32-byte offset (kk%4) inside the atom
+                const uint64_t da = tc::desc_sw128_kmajor(sa + uint32_t(kk >> 2) * uint32_t(CC_A_ATOM)) + 2u * (kk & 3);
+                const uint64_t db =
+                    tc::desc_sw128_kmajor(sa + uint32_t(CC_A) + uint32_t(kk >> 2) * uint32_t(CC_B_ATOM)) + 2u * (kk & 3);
+                tc::mma_bf16(tmem, da, db, idesc, kb > 0 || kk > 0);
+            }
             tc::mma_commit(&empty[s]);
         }
         tc::mma_commit(accum);
@@ -130,6 +146,7 @@ __global__ void __launch_bounds__(CC_NT, 1) contract_tc_kernel(const uint16_t* _
 }
 
 bool contract_tc_supported(int P, int H) { return P >= 1 && P <= 16 && H % CC_BK == 0; }
+// (H % 128 == 0: every stage is a whole 128-element k-slice)
 
 int launch_contract_tc(const void* E, const uint16_t* uhl, const int32_t* cand_tok, const float* cand_val, float* z,
                        int C, int P, int K, int H, int L, int d, float inv_sqrt_h, int* status, cudaStream_t stream) {
