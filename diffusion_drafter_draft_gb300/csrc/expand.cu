@@ -148,7 +148,57 @@ __global__ void __launch_bounds__(CT_NT) contract_simple_kernel(const float* __r
 // --------------------------------------------------------------------------- select: softmax, score, top-W, state
 
 constexpr int SL_NT = 512;
+constexpr int SL_NW = SL_NT / 32;
 
+// Warp-wide maximum of unique 64-bit keys (redux on the high word, then on the
+// low word among the lanes holding that high word).
+__device__ __forceinline__ uint64_t warp_max_key64(uint64_t v) {
+    const uint32_t hi = uint32_t(v >> 32), lo = uint32_t(v);
+    const uint32_t mh = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t ml = __reduce_max_sync(0xffffffffu, hi == mh ? lo : 0u);
+    return (uint64_t(mh) << 32) | ml;
+}
+
+// The n_keep largest keys of keys[0..n), descending, into out[0..n_keep) (all
+// threads of the block; unique keys). Two levels: every warp keeps the best
+// n_keep of its slice by rounds of "largest key below the previous one", then
+// warp 0 merges the 16 lists the same way.
+__device__ void block_top_keys(const uint64_t* keys, int n, int n_keep, uint64_t* cands, uint64_t* out) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int per = (n + SL_NW - 1) / SL_NW;
+    const int lo = wid * per, hi = min(n, lo + per);
+    uint64_t prev = ~0ull;
+    for (int k = 0; k < n_keep; ++k) {
+        uint64_t best = 0;
+        for (int f = lo + lane; f < hi; f += 32) {
+            const uint64_t v = keys[f];
+            if (v < prev && v > best) best = v;
+        }
+        best = warp_max_key64(best);
+        prev = best;
+        if (lane == 0) cands[wid * n_keep + k] = best;
+    }
+    __syncthreads();
+    if (wid == 0) {
+        const int m = SL_NW * n_keep;
+        prev = ~0ull;
+        for (int k = 0; k < n_keep; ++k) {
+            uint64_t best = 0;
+            for (int f = lane; f < m; f += 32) {
+                const uint64_t v = cands[f];
+                if (v < prev && v > best) best = v;
+            }
+            best = warp_max_key64(best);
+            prev = best;
+            if (lane == 0) out[k] = best;
+        }
+    }
+    __syncthreads();
+}
+
+// One depth's log-softmax, scores, top-W and state update for the per-depth
+// (large batch) path, one CTA per request: the selection runs once, then the
+// kept children's state rows are built in parallel, one group of warps per row.
 template <typename T>
 __global__ void __launch_bounds__(SL_NT) select_kernel(
     const float* __restrict__ z, const float* __restrict__ s_cur, const T* __restrict__ h_cur,
@@ -160,66 +210,45 @@ __global__ void __launch_bounds__(SL_NT) select_kernel(
     const int r = blockIdx.x;
     const int n = P * K;
     const int n_keep = min(W, n);
-    int kpad = 1;
-    while (kpad < n_keep) kpad <<= 1;
-    uint64_t* keys = reinterpret_cast<uint64_t*>(smem);                 // n
-    uint64_t* sel = keys + n;                                            // kpad
-    float* lse = reinterpret_cast<float*>(sel + kpad);                   // P
-    uint32_t* hist = reinterpret_cast<uint32_t*>(lse + P);               // 256
-    uint32_t* bcast = hist + 256;                                        // 8
-    int* kept_par = reinterpret_cast<int*>(bcast + 8);                   // W
-    int* kept_tok = kept_par + W;                                        // W
+    uint64_t* keys = reinterpret_cast<uint64_t*>(smem);         // n
+    uint64_t* cands = keys + n;                                  // 16 * W
+    uint64_t* sel = cands + SL_NW * W;                           // W
+    float* lse = reinterpret_cast<float*>(sel + W);              // P
+    float* red = lse + P;                                        // 16
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const float* zr = z + size_t(r) * P * K;
     const int32_t* ct = cand_tok + (size_t(r) * L + (d - 1)) * K;
+    (void)status;
 
-    for (int p = wid; p < P; p += SL_NT / 32) {
+    for (int p = wid; p < P; p += SL_NW) {
         float m = -INFINITY;
         for (int c = lane; c < K; c += 32) m = fmaxf(m, zr[size_t(p) * K + c]);
         m = warp_max(m);
-        float s = 0.f;
-        for (int c = lane; c < K; c += 32) s += expf(zr[size_t(p) * K + c] - m);
-        s = warp_sum(s);
-        if (lane == 0) lse[p] = m + logf(s);
+        float sum = 0.f;
+        for (int c = lane; c < K; c += 32) sum += expf(zr[size_t(p) * K + c] - m);
+        sum = warp_sum(sum);
+        if (lane == 0) lse[p] = m + logf(sum);
     }
-    if (threadIdx.x == 0) bcast[4] = 0;
     __syncthreads();
     for (int f = threadIdx.x; f < n; f += SL_NT) {
         const int p = f / K;
-        float s = (s_cur[size_t(r) * P + p] + (zr[f] - lse[p])) + beta;
-        s += 0.f;
-        keys[f] = (uint64_t(ord_f32(s)) << 32) | (0xffffffffu - uint32_t(f));
+        float sc = (s_cur[size_t(r) * P + p] + (zr[f] - lse[p])) + beta;
+        sc += 0.f;
+        keys[f] = (uint64_t(ord_f32(sc)) << 32) | (0xffffffffu - uint32_t(f));
     }
     __syncthreads();
-    uint64_t prefix = 0, mask = 0;
-    const bool ok = block_select_top<SL_NT>(keys, n, n_keep, hist, bcast, prefix, mask);
-    for (int f = threadIdx.x; f < n; f += SL_NT) {
-        if (ok && selected(keys[f], prefix, mask)) {
-            const uint32_t q = atomicAdd(&bcast[4], 1u);
-            if (q < uint32_t(n_keep)) sel[q] = keys[f];
-        }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0 && (!ok || bcast[4] != uint32_t(n_keep))) set_status(status, DARTREE_EINTERNAL);
-    for (int i = threadIdx.x; i < kpad; i += SL_NT)
-        if (i >= n_keep || !ok || i >= int(bcast[4])) sel[i] = 0;
-    __syncthreads();
-    bitonic_sort_desc<SL_NT>(sel, kpad);
+    block_top_keys(keys, n, n_keep, cands, sel);
 
     const size_t sto = (size_t(r) * L + (d - 1)) * W;
     for (int k = threadIdx.x; k < W; k += SL_NT) {
         if (k < n_keep) {
             const uint64_t key = sel[k];
             const uint32_t f = 0xffffffffu - uint32_t(key);
-            const int p = int(f) / K, c = int(f) % K;
-            const float s = f32_from_ord(uint32_t(key >> 32));
-            const int tk = (f < uint32_t(n)) ? ct[c] : 0;
-            st_tok[sto + k] = tk;
-            st_par[sto + k] = p;
-            st_s[sto + k] = s;
-            s_next[size_t(r) * n_keep + k] = s;
-            kept_par[k] = p;
-            kept_tok[k] = tk;
+            const float sc = f32_from_ord(uint32_t(key >> 32));
+            st_tok[sto + k] = ct[f % uint32_t(K)];
+            st_par[sto + k] = int(f / uint32_t(K));
+            st_s[sto + k] = sc;
+            s_next[size_t(r) * n_keep + k] = sc;
         } else {
             st_tok[sto + k] = -1;
             st_par[sto + k] = -1;
@@ -227,33 +256,90 @@ __global__ void __launch_bounds__(SL_NT) select_kernel(
         }
     }
     if (threadIdx.x == 0) st_n[size_t(r) * L + (d - 1)] = n_keep;
-    if (!update_state) return;
-    __syncthreads();
+    (void)h_cur; (void)E; (void)hidden; (void)H; (void)h_next; (void)update_state;
+}
+
+// State rows of the kept children of one depth: h = RMSNorm(h_p + E[tok] +
+// H_d[d-1]) in the storage type. Grid (n_keep, C), one CTA per row; parent and
+// token come from the supertree entries just written. Every thread holds up to
+// two 16-byte vectors of each input in registers, so all loads are in flight
+// together.
+constexpr int SU_NT = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(SU_NT) state_kernel(const T* __restrict__ h_cur, const T* __restrict__ E,
+                                                      const T* __restrict__ hidden,
+                                                      const int32_t* __restrict__ st_tok,
+                                                      const int32_t* __restrict__ st_par, int P, int W, int H, int L,
+                                                      int d, T* __restrict__ h_next) {
+    __shared__ float red[SU_NT / 32];
+    const int k = blockIdx.x, r = blockIdx.y, n_keep = gridDim.x;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const size_t o = (size_t(r) * L + (d - 1)) * W + k;
+    const T* hp = h_cur + (size_t(r) * P + st_par[o]) * H;
+    const T* e = E + size_t(st_tok[o]) * H;
     const T* hd = hidden + (size_t(r) * L + (d - 1)) * H;
-    for (int k = wid; k < n_keep; k += SL_NT / 32) {
-        const T* hp = h_cur + (size_t(r) * P + kept_par[k]) * H;
-        const T* e = E + size_t(kept_tok[k]) * H;
-        float ss = 0.f;
-        for (int j = lane; j < H; j += 32) {
-            const float x = (to_float(hp[j]) + to_float(e[j])) + to_float(hd[j]);
-            ss = fmaf(x, x, ss);
-        }
-        ss = warp_sum(ss);
-        const float rs = sqrtf(ss / float(H) + 1e-6f);
-        T* out = h_next + (size_t(r) * n_keep + k) * H;
-        for (int j = lane; j < H; j += 32) {
-            const float x = (to_float(hp[j]) + to_float(e[j])) + to_float(hd[j]);
-            out[j] = from_float<T>(x / rs);
+    T* out = h_next + (size_t(r) * n_keep + k) * H;
+    constexpr int VE = 16 / sizeof(T), VR = 2;
+    const int nv = H / VE;
+    float xr[VR][VE];
+    float ss = 0.f;
+    uint4 vo[VR], ve[VR], vh[VR];
+#pragma unroll
+    for (int i = 0; i < VR; ++i) {
+        const int v = threadIdx.x + i * SU_NT;
+        if (v < nv) {
+            vo[i] = __ldcg(reinterpret_cast<const uint4*>(hp) + v);  // written by the previous depth
+            ve[i] = reinterpret_cast<const uint4*>(e)[v];
+            vh[i] = reinterpret_cast<const uint4*>(hd)[v];
         }
     }
+#pragma unroll
+    for (int i = 0; i < VR; ++i) {
+        if (int(threadIdx.x) + i * SU_NT < nv) {
+            const T* po = reinterpret_cast<const T*>(&vo[i]);
+            const T* pe = reinterpret_cast<const T*>(&ve[i]);
+            const T* ph = reinterpret_cast<const T*>(&vh[i]);
+#pragma unroll
+            for (int j = 0; j < VE; ++j) {
+                xr[i][j] = (to_float(po[j]) + to_float(pe[j])) + to_float(ph[j]);
+                ss = fmaf(xr[i][j], xr[i][j], ss);
+            }
+        }
+    }
+    for (int v = threadIdx.x + VR * SU_NT; v < nv; v += SU_NT)  // rows wider than the registers
+        for (int j = 0; j < VE; ++j) {
+            const float x = (to_float(hp[v * VE + j]) + to_float(e[v * VE + j])) + to_float(hd[v * VE + j]);
+            ss = fmaf(x, x, ss);
+        }
+    ss = warp_sum(ss);
+    if (lane == 0) red[wid] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < SU_NT / 32; ++w) tot += red[w];
+    const float rs = sqrtf(tot / float(H) + 1e-6f);
+#pragma unroll
+    for (int i = 0; i < VR; ++i) {
+        const int v = threadIdx.x + i * SU_NT;
+        if (v < nv) {
+            uint4 ov;
+            T* pw = reinterpret_cast<T*>(&ov);
+#pragma unroll
+            for (int j = 0; j < VE; ++j) pw[j] = from_float<T>(xr[i][j] / rs);
+            reinterpret_cast<uint4*>(out)[v] = ov;
+        }
+    }
+    for (int v = threadIdx.x + VR * SU_NT; v < nv; v += SU_NT)
+        for (int j = 0; j < VE; ++j) {
+            const float x = (to_float(hp[v * VE + j]) + to_float(e[v * VE + j])) + to_float(hd[v * VE + j]);
+            out[v * VE + j] = from_float<T>(x / rs);
+        }
 }
 
 static size_t select_smem(int P, int K, int W) {
-    const int n = P * K;
-    const int n_keep = n < W ? n : W;
-    int kpad = 1;
-    while (kpad < n_keep) kpad <<= 1;
-    return size_t(n) * 8 + size_t(kpad) * 8 + size_t(P) * 4 + 256 * 4 + 8 * 4 + 2 * size_t(W) * 4 + 16;
+    const size_t n = size_t(P) * K;
+    return n * 8 + size_t(SL_NW) * W * 8 + size_t(W) * 8 + size_t(P) * 4 + SL_NW * 4 + 16;
 }
 
 // --------------------------------------------------------------------------- host loop
@@ -294,6 +380,9 @@ static int launch_expand_t(const ExpandArgs& a, cudaStream_t st) {
         select_kernel<T><<<a.C, SL_NT, select_smem(P, a.K, a.W), st>>>(
             a.z, a.sbuf[cur], hb[cur], a.cand_tok, E, hid, P, a.K, a.W, a.H, a.L, d, a.beta, a.st_tok, a.st_par,
             a.st_s, a.st_n, hb[1 - cur], a.sbuf[1 - cur], d < a.L ? 1 : 0, a.status);
+        if (d < a.L)
+            state_kernel<T><<<dim3(n_keep, a.C), SU_NT, 0, st>>>(hb[cur], E, hid, a.st_tok, a.st_par, P, a.W, a.H,
+                                                               a.L, d, hb[1 - cur]);
         cur = 1 - cur;
         P = n_keep;
     }

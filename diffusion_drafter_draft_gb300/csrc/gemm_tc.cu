@@ -178,16 +178,11 @@ bool gemm_tc_supported(int M, int N, int K) {
     return M > 0 && N > 0 && K > 0 && N % 128 == 0 && K % 8 == 0 && encode_fn() != nullptr;
 }
 
-int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int mode, float* d32, uint16_t* hilo,
-                        int P, int* status, cudaStream_t stream) {
-    constexpr int BN = 128;
-    if (!gemm_tc_supported(M, N, K)) return DARTREE_EUNSUPPORTED;
-    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) % 16) return DARTREE_EINVAL;
-    if (mode == 1 && (P < 1 || P > 16 || !hilo)) return DARTREE_EINVAL;
-    if (mode == 0 && !d32) return DARTREE_EINVAL;
+template <int BN>
+static int launch_gemm_bn(const void* A, const void* B, int M, int N, int K, const GemmOut& o, int* status,
+                          cudaStream_t stream) {
     CUtensorMap ta, tb;
     if (!make_map(&ta, A, M, K, GT_BM) || !make_map(&tb, B, N, K, BN)) return DARTREE_ECUDA;
-    GemmOut o{mode, d32, hilo, P};
     const size_t smem = GtSmem<BN>::TOTAL;
     auto kern = gemm_bf16_tc_kernel<BN>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
@@ -195,6 +190,18 @@ int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int m
     dim3 grid(N / BN, (M + GT_BM - 1) / GT_BM);
     kern<<<grid, GT_NT, smem, stream>>>(ta, tb, M, N, K, o, status);
     return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
+}
+
+int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int mode, float* d32, uint16_t* hilo,
+                        int P, int* status, cudaStream_t stream) {
+    if (!gemm_tc_supported(M, N, K)) return DARTREE_EUNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) % 16) return DARTREE_EINVAL;
+    if (mode == 1 && (P < 1 || P > 16 || !hilo)) return DARTREE_EINVAL;
+    if (mode == 0 && !d32) return DARTREE_EINVAL;
+    GemmOut o{mode, d32, hilo, P};
+    // wider tiles halve the L2 traffic of the operand both tile rows share
+    if (N % 256 == 0) return launch_gemm_bn<256>(A, B, M, N, K, o, status, stream);
+    return launch_gemm_bn<128>(A, B, M, N, K, o, status, stream);
 }
 
 }  // namespace dartree
