@@ -270,6 +270,65 @@ __device__ bool block_select_top(const uint64_t* keys, int n, int N, uint32_t* h
     return true;
 }
 
+// Same contract as block_select_top, for keys that share long common prefixes
+// (candidate scores cluster in a narrow range): the bytes above the highest bit
+// where any two keys differ are skipped, and each warp adds one count per
+// distinct digit (lanes with equal digits are merged with match.any), which keeps
+// shared-memory atomics uncontended.
+template <int NT>
+__device__ bool block_select_top_agg(const uint64_t* keys, int n, int N, uint32_t* hist, uint32_t* bcast,
+                                     uint64_t* orand, uint64_t& prefix_out, uint64_t& mask_out) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    // bits where the keys differ: OR of (key ^ keys[0])
+    uint64_t x = 0;
+    const uint64_t k0 = n > 0 ? keys[0] : 0ull;
+    for (int i = threadIdx.x; i < n; i += NT) x |= keys[i] ^ k0;
+    for (int m = 16; m; m >>= 1) x |= shfl_xor_u64(x, m);
+    if (lane == 0) orand[wid] = x;
+    __syncthreads();
+    uint64_t diff = 0;
+    for (int w = 0; w < NT / 32; ++w) diff |= orand[w];
+    __syncthreads();
+    if (diff == 0) {  // a single distinct key (n == 1)
+        prefix_out = k0;
+        mask_out = ~0ull;
+        return N <= n;
+    }
+    const int top = 63 - __clzll(static_cast<long long>(diff));
+    int shift = (top / 8) * 8;
+    uint64_t mask = (shift + 8 >= 64) ? 0ull : (~0ull << (shift + 8));
+    uint64_t prefix = k0 & mask;
+    uint32_t rem = uint32_t(N);
+    const int nfull = (n + NT - 1) / NT * NT;
+    for (; shift >= 0; shift -= 8) {
+        for (int i = threadIdx.x; i < 256; i += NT) hist[i] = 0;
+        __syncthreads();
+        for (int i = threadIdx.x; i < nfull; i += NT) {
+            const bool in = i < n && (keys[i] & mask) == prefix;
+            const uint32_t dg = in ? uint32_t(keys[i] >> shift) & 255u : 256u;
+            const uint32_t peers = __match_any_sync(0xffffffffu, dg);
+            if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], uint32_t(__popc(peers)));
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            uint32_t r = rem, d;
+            pick_digit_warp(hist, r, d);
+            if (threadIdx.x == 0) { bcast[0] = d; bcast[1] = r; bcast[2] = d == 0xffffffffu ? 0 : hist[d]; }
+        }
+        __syncthreads();
+        const uint32_t d = bcast[0], r = bcast[1], cnt = bcast[2];
+        __syncthreads();
+        if (d == 0xffffffffu) return false;
+        prefix |= uint64_t(d) << shift;
+        mask |= uint64_t(0xffu) << shift;
+        rem = r;
+        if (cnt == rem) break;  // every key of this bin is selected
+    }
+    prefix_out = prefix;
+    mask_out = mask;
+    return true;
+}
+
 __device__ __forceinline__ bool selected(uint64_t k, uint64_t prefix, uint64_t mask) {
     return (k & mask) >= prefix;
 }

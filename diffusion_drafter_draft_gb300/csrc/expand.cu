@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(SL_NT) select_kernel(
     uint64_t* cands = keys + n;                                  // 16 * W
     uint64_t* sel = cands + SL_NW * W;                           // W
     float* lse = reinterpret_cast<float*>(sel + W);              // P
-    float* red = lse + P;                                        // 16
+    // (no reduction scratch: state rows are built by state_kernel)
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const float* zr = z + size_t(r) * P * K;
     const int32_t* ct = cand_tok + (size_t(r) * L + (d - 1)) * K;

@@ -17,30 +17,39 @@
 
 namespace dartree {
 
-constexpr int TK_NT = 512;
+constexpr int TK_NT = 256;
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-constexpr int TK_CAP = 4096;      // candidate keys gathered by the leader CTA
+constexpr int TK_CAP = 4096;      // at most this many candidate keys gathered by the leader CTA
+constexpr int TK_FB = 1024;       // keys of the exact fallback (K <= 1024)
 constexpr int TK_PIECE = 16384;   // bytes per bulk copy (one mbarrier each)
 constexpr int TK_MAXP = 16;       // at most 16 pieces (256 KB chunk)
-constexpr int TK_STASH = 4;       // candidate keys a thread keeps in registers
+constexpr int TK_STASH = 8;       // candidate keys a thread keeps in registers
 
+// The data chunk doubles as the leader's candidate buffer once the filter pass
+// has read it (peers write candidates only after the pass, behind a cluster
+// barrier), so a CTA needs little more than its chunk of shared memory.
 struct TopkSmem {
-    size_t hist, hsum, misc, wtot, mbar, cand, total;
+    size_t data, hist, hsum, misc, wtot, mbar, fb, total;
+    int cap;  // candidate keys the data region holds
 };
 
 __host__ __device__ inline TopkSmem topk_smem_layout(int chunk, int elem) {
     TopkSmem s{};
-    size_t off = align_up(size_t(chunk) * elem, 128);
+    const size_t data = align_up(size_t(chunk) * elem, 128);
+    s.data = 0;
+    size_t off = data;
     s.hist = off; off += 2 * 256 * 4;
     s.hsum = off; off += 256 * 4;
     s.misc = off; off += 64 * 4;
     s.wtot = off; off += 32 * 4;
     s.mbar = off; off += 8 * TK_MAXP;
     off = align_up(off, 16);
-    s.cand = off; off += size_t(TK_CAP) * 8;
+    s.fb = off; off += size_t(TK_FB) * 8;
     s.total = off;
+    const size_t cap = data / 8;
+    s.cap = int(cap < size_t(TK_CAP) ? cap : size_t(TK_CAP));
     return s;
 }
 
@@ -145,6 +154,76 @@ __device__ bool cluster_select_kth(Each&& each, uint32_t lo, uint32_t K, uint32_
     return true;
 }
 
+// Bitonic sort, descending, of n (a power of two, <= EPT*NT) keys: thread t holds
+// elements t + e*NT (e < EPT) in registers. Partners closer than 32 are exchanged
+// with warp shuffles, partners in the same thread directly, and only strides of
+// 32..NT/2 go through shared memory.
+template <int NT, int EPT>
+__device__ __forceinline__ void sort_desc_regs(uint64_t* a, int n) {
+    const int t = threadIdx.x;
+    uint64_t v[EPT];
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) v[e] = (t + e * NT < n) ? a[t + e * NT] : 0ull;
+    for (int k = 2; k <= n; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j >= NT) {
+                const int ej = j / NT;
+#pragma unroll
+                for (int es = 1; es < EPT; es <<= 1) {  // static partner slots (register indices)
+                    if (es != ej) continue;
+#pragma unroll
+                    for (int e = 0; e < EPT; ++e) {
+                        const int pe = e ^ es;
+                        if (pe > e) {
+                            const int i = t + e * NT;
+                            const bool desc = (i & k) == 0;
+                            const uint64_t x = v[e], y = v[pe];
+                            const bool sw = desc ? (x < y) : (x > y);
+                            v[e] = sw ? y : x;
+                            v[pe] = sw ? x : y;
+                        }
+                    }
+                }
+            } else if (j >= 32) {
+                __syncthreads();
+#pragma unroll
+                for (int e = 0; e < EPT; ++e)
+                    if (t + e * NT < n) a[t + e * NT] = v[e];
+                __syncthreads();
+#pragma unroll
+                for (int e = 0; e < EPT; ++e) {
+                    const int i = t + e * NT;
+                    if (i < n) {
+                        const uint64_t p = a[i ^ j];
+                        const bool lower = (i & j) == 0, desc = (i & k) == 0;
+                        v[e] = (lower == desc) ? (p > v[e] ? p : v[e]) : (p < v[e] ? p : v[e]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPT; ++e) {
+                    const int i = t + e * NT;
+                    const uint64_t p = shfl_xor_u64(v[e], j);
+                    const bool lower = (i & j) == 0, desc = (i & k) == 0;
+                    v[e] = (lower == desc) ? (p > v[e] ? p : v[e]) : (p < v[e] ? p : v[e]);
+                }
+            }
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < EPT; ++e)
+        if (t + e * NT < n) a[t + e * NT] = v[e];
+    __syncthreads();
+}
+
+template <int NT>
+__device__ __forceinline__ void sort_desc(uint64_t* a, int n) {
+    if (n <= NT) sort_desc_regs<NT, 1>(a, n);
+    else if (n <= 2 * NT) sort_desc_regs<NT, 2>(a, n);
+    else sort_desc_regs<NT, 4>(a, n);  // callers sort at most 1024 keys
+}
+
 // Exact selection used when the filter leaves more than TK_CAP candidates (heavy
 // ties, constant rows): radix select of the K-th largest value over the whole
 // chunk, then ordered compaction of the ties in token order. Writes the K keys
@@ -158,12 +237,12 @@ __device__ bool topk_exact_fallback(const T* buf, int n, int c0, int K, uint32_t
     const int lo = min(n, int(threadIdx.x) * per);
     const int hi = min(n, lo + per);
     auto each = [&](auto&& f) { for_owned<T>(buf, lo, hi, f); };
-    if (threadIdx.x == 0) misc[9] = 0;
+    if (threadIdx.x == 0) misc[10] = 0;
     uint32_t t = 0, rem = 0;
     bool ok = cluster_select_kth<KBITS>(each, 0u, uint32_t(K), hist, hsum, misc, S, t, rem);
     if (!ok) { t = 0xffffffffu; rem = 0; }
     const uint32_t n_gt = uint32_t(K) - rem;
-    const uint32_t leader_ctr = dsmem_addr(&misc[9], 0);
+    const uint32_t leader_ctr = dsmem_addr(&misc[10], 0);
     const uint32_t leader_cand = dsmem_addr(cand, 0);
     each([&](int i, uint32_t o) {
         if (o > t) {
@@ -185,11 +264,11 @@ __device__ bool topk_exact_fallback(const T* buf, int n, int c0, int K, uint32_t
         }
     });
     cluster_sync();
-    return ok && (cr != 0 || misc[9] == n_gt);
+    return ok && (cr != 0 || misc[10] == n_gt);
 }
 
 template <typename T>
-__global__ void __launch_bounds__(TK_NT) topk_rows_kernel(const T* __restrict__ x, int V, int K, int jsel,
+__global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict__ x, int V, int K, int jsel,
                                                           int chunk, int use_bulk, int32_t* __restrict__ out_tok,
                                                           float* __restrict__ out_val, int* status) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -205,7 +284,8 @@ __global__ void __launch_bounds__(TK_NT) topk_rows_kernel(const T* __restrict__ 
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L.misc);
     int* wtot = reinterpret_cast<int*>(smem + L.wtot);
     uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + L.mbar);
-    uint64_t* cand = reinterpret_cast<uint64_t*>(smem + L.cand);
+    uint64_t* cand = reinterpret_cast<uint64_t*>(smem + L.data);  // after the filter pass
+    uint64_t* fb = reinterpret_cast<uint64_t*>(smem + L.fb);
     const T* src = x + size_t(row) * V + c0;
     const int nvec = n / VEC;
     constexpr int VPP = TK_PIECE / 16;  // vectors per piece
@@ -289,50 +369,58 @@ __global__ void __launch_bounds__(TK_NT) topk_rows_kernel(const T* __restrict__ 
         }
     }
     for (int i = nvec * VEC + int(threadIdx.x); i < n; i += TK_NT) consider(ValueKey<T>::ord(buf[i]), i);
+    const int over = __syncthreads_or(cnt > TK_STASH);  // a thread with more candidates than registers
+    if (threadIdx.x == 0) misc[9] = uint32_t(over);
     const int excl = block_exclusive_scan<TK_NT>(cnt, wtot, reinterpret_cast<int*>(&misc[8]));
     cluster_sync();  // CTA totals visible
-    uint32_t base = 0, total = 0;
+    uint32_t base = 0, total = 0, anyover = 0;
     for (uint32_t q = 0; q < S; ++q) {
         const uint32_t tq = ld_dsmem_u32(dsmem_addr(&misc[8], q));
+        anyover |= ld_dsmem_u32(dsmem_addr(&misc[9], q));
         base += q < cr ? tq : 0u;
         total += tq;
     }
-    const bool fits = total >= uint32_t(K) && total <= uint32_t(TK_CAP);
+    // the same decision in every CTA: the totals and flags are shared
+    const bool fits = total >= uint32_t(K) && total <= uint32_t(L.cap) && !anyover;
     if (fits) {
         const uint32_t leader_cand = dsmem_addr(cand, 0);
-        uint32_t pos = base + uint32_t(excl);
-        if (cnt <= TK_STASH) {
+        const uint32_t pos = base + uint32_t(excl);
 #pragma unroll
-            for (int q = 0; q < TK_STASH; ++q)
-                if (q < cnt) st_dsmem_u64(leader_cand + 8u * (pos + q), stash[q]);
-        } else {  // more candidates than registers: scan this thread's vectors again
-            auto put = [&](uint32_t o, int i) {
-                if (o >= c) { st_dsmem_u64(leader_cand + 8u * pos, (uint64_t(o) << 32) | (0xffffffffu - uint32_t(c0 + i))); ++pos; }
-            };
-            for (int v = threadIdx.x; v < nvec; v += TK_NT) {
-                const uint4 w = reinterpret_cast<const uint4*>(buf)[v];
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) put(vec_elem_ord(w, e, static_cast<T*>(nullptr)), v * VEC + e);
-            }
-            for (int i = nvec * VEC + int(threadIdx.x); i < n; i += TK_NT) put(ValueKey<T>::ord(buf[i]), i);
-        }
+        for (int q = 0; q < TK_STASH; ++q)
+            if (q < cnt) st_dsmem_u64(leader_cand + 8u * (pos + q), stash[q]);
         cluster_sync();
     } else {
         // uniform across the cluster: every CTA summed the same totals
-        if (!topk_exact_fallback<T>(buf, n, c0, K, S, cr, hist, hsum, misc, wtot, cand))
+        if (!topk_exact_fallback<T>(buf, n, c0, K, S, cr, hist, hsum, misc, wtot, fb))
             if (threadIdx.x == 0) set_status(status, DARTREE_EINTERNAL);
     }
 
-    // leader sorts the candidates and writes the first K
+    // leader: exactly the K best candidates (radix select), then sort those K
     if (cr == 0) {
-        const int m = fits ? int(total) : K;
-        int mpad = 1;
-        while (mpad < m) mpad <<= 1;
-        for (int i = m + threadIdx.x; i < mpad; i += TK_NT) cand[i] = 0;
+        if (fits) {
+            uint64_t prefix = 0, mask = 0;
+            uint64_t* orand = reinterpret_cast<uint64_t*>(hsum);  // 16 words of scratch
+            const bool ok = block_select_top_agg<TK_NT>(cand, int(total), K, hist, misc + 32, orand, prefix, mask);
+            if (threadIdx.x == 0) { misc[40] = 0; if (!ok) set_status(status, DARTREE_EINTERNAL); }
+            __syncthreads();
+            for (int i = threadIdx.x; i < int(total); i += TK_NT) {
+                const uint64_t k = cand[i];
+                if (ok && selected(k, prefix, mask)) {
+                    const uint32_t q = atomicAdd(&misc[40], 1u);
+                    if (q < uint32_t(K)) fb[q] = k;
+                }
+            }
+            __syncthreads();
+            if (threadIdx.x == 0 && misc[40] != uint32_t(K)) set_status(status, DARTREE_EINTERNAL);
+            for (int i = min(int(misc[40]), K) + threadIdx.x; i < K; i += TK_NT) fb[i] = 0;
+        }
+        int kp = 1;
+        while (kp < K) kp <<= 1;
+        for (int i = K + threadIdx.x; i < kp; i += TK_NT) fb[i] = 0;
         __syncthreads();
-        bitonic_sort_desc<TK_NT>(cand, mpad);
+        sort_desc<TK_NT>(fb, kp);
         for (int i = threadIdx.x; i < K; i += TK_NT) {
-            const uint64_t k = cand[i];
+            const uint64_t k = fb[i];
             out_tok[size_t(row) * K + i] = int32_t(0xffffffffu - uint32_t(k));
             out_val[size_t(row) * K + i] = ValueKey<T>::value(uint32_t(k >> 32));
         }
@@ -357,14 +445,15 @@ int num_sms() {
 
 template <typename T>
 static int launch_topk_t(const void* x, int rows, int V, int K, int32_t* tok, float* val, int* status,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, int max_s = 16) {
     const int elem = sizeof(T);
     const int VEC = 16 / elem;
     int S = 1;
     auto chunk_of = [&](int s) { return int(align_up((V + s - 1) / s, VEC)); };
-    while (S < 8 && (size_t(chunk_of(S)) * elem > 96 * 1024 ||
-                     (rows * S < 2 * num_sms() && size_t(chunk_of(2 * S)) * elem >= 16 * 1024)))
-        S *= 2;
+    // ~40 KB chunks: several CTAs per SM overlap their loads with the other CTAs'
+    // passes; with few rows, up to 16-CTA clusters so that the rows still cover the GPU
+    while (S < 8 && size_t(chunk_of(S)) * elem > 40 * 1024) S *= 2;
+    while (S < max_s && rows * S < 2 * num_sms() && size_t(chunk_of(2 * S)) * elem >= 16 * 1024) S *= 2;
     const int chunk = chunk_of(S);
     const TopkSmem L = topk_smem_layout(chunk, elem);
     const int warps = S * (TK_NT / 32);
@@ -375,6 +464,24 @@ static int launch_topk_t(const void* x, int rows, int V, int K, int32_t* tok, fl
         return DARTREE_ECUDA;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
         return DARTREE_ECUDA;
+    if (S > 8) {  // 16-CTA clusters need a GPC with 16 free SMs: keep 8 when none can run
+        cudaLaunchConfig_t q{};
+        q.gridDim = dim3(unsigned(S));
+        q.blockDim = dim3(TK_NT);
+        q.dynamicSmemBytes = L.total;
+        cudaLaunchAttribute qa[1];
+        qa[0].id = cudaLaunchAttributeClusterDimension;
+        qa[0].val.clusterDim.x = S;
+        qa[0].val.clusterDim.y = 1;
+        qa[0].val.clusterDim.z = 1;
+        q.attrs = qa;
+        q.numAttrs = 1;
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, kern, &q) != cudaSuccess || nc < 1) {
+            cudaGetLastError();
+            return launch_topk_t<T>(x, rows, V, K, tok, val, status, stream, 8);
+        }
+    }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(unsigned(rows) * S);
     cfg.blockDim = dim3(TK_NT);
