@@ -24,7 +24,8 @@ OK, EINVAL, EDTYPE, EWORKSPACE, ECUDA, ETIMEOUT, EINTERNAL, EUNSUPPORTED = 0, -1
 
 EXPORTS = ("dartree_head_init", "dartree_workspace_bytes", "dartree_topk", "dartree_expand", "dartree_prune",
            "dartree_tree_mask", "dartree_build_tree", "dartree_verify", "dartree_read_status",
-           "dartree_clear_status", "dartree_status_string", "dartree_verify_static", "dartree_gemm_bf16")
+           "dartree_clear_status", "dartree_status_string", "dartree_verify_static", "dartree_gemm_bf16",
+           "dartree_head_prepare")
 
 
 class DartreeError(RuntimeError):
@@ -35,7 +36,7 @@ class DartreeError(RuntimeError):
 
 class Head(ctypes.Structure):
     _fields_ = [("E", ctypes.c_void_p), ("Wq", ctypes.c_void_p), ("V", ctypes.c_int), ("H", ctypes.c_int),
-                ("dtype", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("WqT", ctypes.c_void_p)]
 
 
 class Params(ctypes.Structure):
@@ -78,6 +79,7 @@ def lib() -> ctypes.CDLL:
     P = ctypes.POINTER
     sig = {
         "dartree_head_init": (i, [P(Head), vp, vp, i, i, i]),
+        "dartree_head_prepare": (i, [P(Head), vp, vp]),
         "dartree_workspace_bytes": (sz, [P(Params), i, i, i]),
         "dartree_topk": (i, [vp, i, i, i, i, vp, vp, vp, sz, vp]),
         "dartree_expand": (i, [P(Head), P(Params), vp, vp, P(Candidates), P(Supertree), vp, sz, vp]),
@@ -142,6 +144,16 @@ def _stream(stream=None) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _keep(stream, *tensors) -> None:
+    """Tensors allocated here and used by work enqueued on a side stream are not
+    reused by the caching allocator before that work is done."""
+    if stream is None or stream == torch.cuda.current_stream():
+        return
+    for t in tensors:
+        if t is not None:
+            t.record_stream(stream)
+
+
 def _params(C, L, K, W, B, beta) -> Params:
     return Params(int(C), int(L), int(K), int(W), int(B), float(beta))
 
@@ -170,14 +182,21 @@ def clear_status(ws: torch.Tensor, stream=None) -> None:
     _call("dartree_clear_status", ctypes.c_void_p(ws.data_ptr()), _stream(stream))
 
 
-def _head(E: torch.Tensor, Wq: torch.Tensor) -> Head:
+def _head(E: torch.Tensor, Wq: torch.Tensor, prepare: bool = False, stream=None):
+    """(head description, W_q^T tensor or None). With prepare, bf16 heads get W_q^T
+    for the small-batch path; the caller keeps the returned tensor alive while the
+    head is used."""
     V, H = E.shape
     _need(E, "E")
     _need(Wq, "Wq", E.dtype, (H, H))
     h = Head()
     _call("dartree_head_init", ctypes.byref(h), ctypes.c_void_p(E.data_ptr()), ctypes.c_void_p(Wq.data_ptr()),
           int(V), int(H), _dtype_code(E))
-    return h
+    wqt = None
+    if prepare and E.dtype == torch.bfloat16:
+        wqt = torch.empty((H, H), dtype=E.dtype, device=E.device)
+        _call("dartree_head_prepare", ctypes.byref(h), ctypes.c_void_p(wqt.data_ptr()), _stream(stream))
+    return h, wqt
 
 
 # --------------------------------------------------------------------------- steps
@@ -229,7 +248,7 @@ def expand(E, Wq, hidden, anchor, cand_tok, cand_val, W, beta, ws=None, stream=N
     """S2-S7 from a candidate table -> supertree dict (tok, par, score, n)."""
     C, L, H = hidden.shape
     K = cand_tok.shape[-1]
-    head = _head(E, Wq)
+    head, wqt = _head(E, Wq, prepare=True, stream=stream)
     _need(hidden, "hidden", E.dtype, (C, L, H))
     _need(anchor, "anchor", torch.int32, (C,))
     _need(cand_tok, "cand_tok", torch.int32, (C, L, K))
@@ -243,6 +262,7 @@ def expand(E, Wq, hidden, anchor, cand_tok, cand_val, W, beta, ws=None, stream=N
     _call("dartree_expand", ctypes.byref(head), ctypes.byref(p), ctypes.c_void_p(hidden.data_ptr()),
           ctypes.c_void_p(anchor.data_ptr()), ctypes.byref(cand), ctypes.byref(sts), ctypes.c_void_p(ws.data_ptr()),
           ws.numel(), _stream(stream))
+    _keep(stream, ws, wqt)
     return st
 
 
@@ -327,7 +347,7 @@ def build_tree(E, Wq, base, hidden, anchor, K, W, B, beta, ws=None, keep_interme
     """S1-S9: one tree build -> tree dict (+ 'cand_tok', 'cand_val', 'st' when keep_intermediates)."""
     C, L, V = base.shape
     H = E.shape[1]
-    head = _head(E, Wq)
+    head, wqt = _head(E, Wq, prepare=True, stream=stream)
     _need(base, "base", E.dtype, (C, L, V))
     _need(hidden, "hidden", E.dtype, (C, L, H))
     _need(anchor, "anchor", torch.int32, (C,))
@@ -347,6 +367,7 @@ def build_tree(E, Wq, base, hidden, anchor, K, W, B, beta, ws=None, keep_interme
     _call("dartree_build_tree", ctypes.byref(head), ctypes.byref(p), ctypes.c_void_p(base.data_ptr()),
           ctypes.c_void_p(hidden.data_ptr()), ctypes.c_void_p(anchor.data_ptr()), ctypes.byref(ts), st_p, cand_p,
           ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
+    _keep(stream, ws, wqt)
     return t
 
 
@@ -362,7 +383,7 @@ class Round:
         self.V, self.H = E.shape
         self.C, self.L, self.K, self.W, self.B, self.beta, self.rows = C, L, K, W, B, beta, rows
         dev = device or E.device
-        self.head = _head(E, Wq)
+        self.head, self.wqt = _head(E, Wq, prepare=True)
         self.p = _params(C, L, K, W, B, beta)
         self.ws = new_workspace(workspace_bytes(C, L, K, W, B, beta, self.V, self.H, self.head.dtype), dev)
         self.tree = _alloc_tree(C, B, dev)

@@ -13,12 +13,14 @@ using namespace dartree;
 
 constexpr size_t kAlign = 256;
 constexpr int kMaxClusters = 40;  // 8-CTA clusters: up to 320 SMs
+constexpr int kMaxGRows = 8192;   // candidate rows of the candidate-side projection path
 
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-    size_t status, cand_tok, cand_val, h[2], s[2], U, z, st_tok, st_par, st_s, st_n, keys, zpart, bar, uhl, total;
-    int zpart_clusters;
+    size_t status, cand_tok, cand_val, h[2], s[2], U, z, st_tok, st_par, st_s, st_n, keys, zpart, bar, uhl, Eg, Ghi, Glo,
+        total;
+    int zpart_clusters, g_rows;
 };
 
 Layout layout_of(const dartree_params& p, int H, int dtype) {
@@ -47,6 +49,13 @@ Layout layout_of(const dartree_params& p, int H, int dtype) {
     l.bar = take(4);
     // bf16 hi/lo projection rows for the tensor-core contraction, [C, 32, H]
     l.uhl = take(dtype == DARTREE_BF16 ? C * 32 * size_t(H) * 2 : 0);
+    // candidate-side projection path (prepared bf16 heads, small batches): gathered
+    // candidate rows and G = E[cand] W_q as a bf16 pair, [C*L*K, H] each
+    const size_t g = C * L * K;
+    l.g_rows = (dtype == DARTREE_BF16 && K <= 64 && W <= 16 && g <= size_t(kMaxGRows)) ? int(g) : 0;
+    l.Eg = take(size_t(l.g_rows) * H * 2);
+    l.Ghi = take(size_t(l.g_rows) * H * 2);
+    l.Glo = take(size_t(l.g_rows) * H * 2);
     l.total = o;
     return l;
 }
@@ -103,6 +112,16 @@ int dartree_head_init(dartree_head* head, const void* E, const void* Wq, int V, 
     head->V = V;
     head->H = H;
     head->dtype = dtype;
+    head->WqT = nullptr;
+    return DARTREE_OK;
+}
+
+int dartree_head_prepare(dartree_head* head, void* wqt, void* stream) {
+    if (!head || !head->Wq || !wqt || head->H < 8 || (reinterpret_cast<uintptr_t>(wqt) % 16) != 0)
+        return DARTREE_EINVAL;
+    if (head->dtype != DARTREE_BF16) return DARTREE_EUNSUPPORTED;
+    if (int e = launch_transpose_bf16(head->Wq, wqt, head->H, as_stream(stream))) return e;
+    head->WqT = wqt;
     return DARTREE_OK;
 }
 
@@ -174,6 +193,11 @@ static int expand_impl(const dartree_head* head, const dartree_params* p, const 
     a.zpart_clusters = l.zpart_clusters;
     a.bar = at<unsigned>(ws, l.bar);
     a.uhl = head->dtype == DARTREE_BF16 ? at<uint16_t>(ws, l.uhl) : nullptr;
+    a.WqT = head->WqT;
+    a.g_rows = l.g_rows;
+    a.Eg = l.g_rows ? at<uint16_t>(ws, l.Eg) : nullptr;
+    a.Ghi = l.g_rows ? at<uint16_t>(ws, l.Ghi) : nullptr;
+    a.Glo = l.g_rows ? at<uint16_t>(ws, l.Glo) : nullptr;
     a.status = at<int>(ws, l.status);
     return launch_expand(a, stream);
 }

@@ -333,4 +333,51 @@ __device__ __forceinline__ bool selected(uint64_t k, uint64_t prefix, uint64_t m
     return (k & mask) >= prefix;
 }
 
+// Warp-wide maximum of unique 64-bit keys (redux on the high word, then on the
+// low word among the lanes holding that high word).
+__device__ __forceinline__ uint64_t warp_max_key64(uint64_t v) {
+    const uint32_t hi = uint32_t(v >> 32), lo = uint32_t(v);
+    const uint32_t mh = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t ml = __reduce_max_sync(0xffffffffu, hi == mh ? lo : 0u);
+    return (uint64_t(mh) << 32) | ml;
+}
+
+// The n_keep largest keys of keys[0..n), descending, into out[0..n_keep) (all
+// threads of the block; unique keys). Two levels: every warp keeps the best
+// n_keep of its slice by rounds of "largest key below the previous one", then
+// warp 0 merges the per-warp lists the same way.
+template <int NT>
+__device__ void block_top_keys(const uint64_t* keys, int n, int n_keep, uint64_t* cands, uint64_t* out) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int per = (n + (NT / 32) - 1) / (NT / 32);
+    const int lo = wid * per, hi = min(n, lo + per);
+    uint64_t prev = ~0ull;
+    for (int k = 0; k < n_keep; ++k) {
+        uint64_t best = 0;
+        for (int f = lo + lane; f < hi; f += 32) {
+            const uint64_t v = keys[f];
+            if (v < prev && v > best) best = v;
+        }
+        best = warp_max_key64(best);
+        prev = best;
+        if (lane == 0) cands[wid * n_keep + k] = best;
+    }
+    __syncthreads();
+    if (wid == 0) {
+        const int m = (NT / 32) * n_keep;
+        prev = ~0ull;
+        for (int k = 0; k < n_keep; ++k) {
+            uint64_t best = 0;
+            for (int f = lane; f < m; f += 32) {
+                const uint64_t v = cands[f];
+                if (v < prev && v > best) best = v;
+            }
+            best = warp_max_key64(best);
+            prev = best;
+            if (lane == 0) out[k] = best;
+        }
+    }
+    __syncthreads();
+}
+
 }  // namespace dartree

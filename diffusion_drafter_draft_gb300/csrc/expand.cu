@@ -150,52 +150,6 @@ __global__ void __launch_bounds__(CT_NT) contract_simple_kernel(const float* __r
 constexpr int SL_NT = 512;
 constexpr int SL_NW = SL_NT / 32;
 
-// Warp-wide maximum of unique 64-bit keys (redux on the high word, then on the
-// low word among the lanes holding that high word).
-__device__ __forceinline__ uint64_t warp_max_key64(uint64_t v) {
-    const uint32_t hi = uint32_t(v >> 32), lo = uint32_t(v);
-    const uint32_t mh = __reduce_max_sync(0xffffffffu, hi);
-    const uint32_t ml = __reduce_max_sync(0xffffffffu, hi == mh ? lo : 0u);
-    return (uint64_t(mh) << 32) | ml;
-}
-
-// The n_keep largest keys of keys[0..n), descending, into out[0..n_keep) (all
-// threads of the block; unique keys). Two levels: every warp keeps the best
-// n_keep of its slice by rounds of "largest key below the previous one", then
-// warp 0 merges the 16 lists the same way.
-__device__ void block_top_keys(const uint64_t* keys, int n, int n_keep, uint64_t* cands, uint64_t* out) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int per = (n + SL_NW - 1) / SL_NW;
-    const int lo = wid * per, hi = min(n, lo + per);
-    uint64_t prev = ~0ull;
-    for (int k = 0; k < n_keep; ++k) {
-        uint64_t best = 0;
-        for (int f = lo + lane; f < hi; f += 32) {
-            const uint64_t v = keys[f];
-            if (v < prev && v > best) best = v;
-        }
-        best = warp_max_key64(best);
-        prev = best;
-        if (lane == 0) cands[wid * n_keep + k] = best;
-    }
-    __syncthreads();
-    if (wid == 0) {
-        const int m = SL_NW * n_keep;
-        prev = ~0ull;
-        for (int k = 0; k < n_keep; ++k) {
-            uint64_t best = 0;
-            for (int f = lane; f < m; f += 32) {
-                const uint64_t v = cands[f];
-                if (v < prev && v > best) best = v;
-            }
-            best = warp_max_key64(best);
-            prev = best;
-            if (lane == 0) out[k] = best;
-        }
-    }
-    __syncthreads();
-}
-
 // One depth's log-softmax, scores, top-W and state update for the per-depth
 // (large batch) path, one CTA per request: the selection runs once, then the
 // kept children's state rows are built in parallel, one group of warps per row.
@@ -237,7 +191,7 @@ __global__ void __launch_bounds__(SL_NT) select_kernel(
         keys[f] = (uint64_t(ord_f32(sc)) << 32) | (0xffffffffu - uint32_t(f));
     }
     __syncthreads();
-    block_top_keys(keys, n, n_keep, cands, sel);
+    block_top_keys<SL_NT>(keys, n, n_keep, cands, sel);
 
     const size_t sto = (size_t(r) * L + (d - 1)) * W;
     for (int k = threadIdx.x; k < W; k += SL_NT) {
@@ -391,6 +345,8 @@ static int launch_expand_t(const ExpandArgs& a, cudaStream_t st) {
 
 int launch_expand(const ExpandArgs& a, cudaStream_t stream) {
     bool done = false;
+    if (int e = try_launch_expand_g(a, stream, &done)) return e;
+    if (done) return DARTREE_OK;
     if (int e = try_launch_expand_small(a, stream, &done)) return e;
     if (done) return DARTREE_OK;
     if (a.dtype == DARTREE_BF16) return launch_expand_t<bf16_t>(a, stream);

@@ -27,9 +27,10 @@ namespace dartree {
 constexpr int GT_BM = 128, GT_BK = 64, GT_STAGES = 4, GT_NT = 128;
 
 struct GemmOut {
-    int mode;          // 0: fp32 d32; 1: hi/lo bf16 pairs into hilo
+    int mode;          // 0: fp32 d32; 1: hi/lo bf16 pairs into hilo (row remap); 2: hi -> hilo, lo -> lo2
     float* d32;
     uint16_t* hilo;
+    uint16_t* lo2;     // mode 2: [M, N]
     int P;             // mode 1: rows per request (<= 16)
 };
 
@@ -120,7 +121,7 @@ __global__ void __launch_bounds__(GT_NT, 1) gemm_bf16_tc_kernel(const __grid_con
                 dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                                      __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
         } else {
-            const int rq = m / out.P, p = m % out.P;
+            const int rq = out.mode == 1 ? m / out.P : 0, p = out.mode == 1 ? m % out.P : 0;
             uint32_t hi[16], lo[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -131,8 +132,10 @@ __global__ void __launch_bounds__(GT_NT, 1) gemm_bf16_tc_kernel(const __grid_con
                 hi[j] = uint32_t(h0) | (uint32_t(h1) << 16);
                 lo[j] = uint32_t(l0) | (uint32_t(l1) << 16);
             }
-            uint4* dh = reinterpret_cast<uint4*>(out.hilo + (size_t(rq) * 32 + p) * N + n);
-            uint4* dl = reinterpret_cast<uint4*>(out.hilo + (size_t(rq) * 32 + 16 + p) * N + n);
+            uint4* dh = out.mode == 2 ? reinterpret_cast<uint4*>(out.hilo + size_t(m) * N + n)
+                                      : reinterpret_cast<uint4*>(out.hilo + (size_t(rq) * 32 + p) * N + n);
+            uint4* dl = out.mode == 2 ? reinterpret_cast<uint4*>(out.lo2 + size_t(m) * N + n)
+                                      : reinterpret_cast<uint4*>(out.hilo + (size_t(rq) * 32 + 16 + p) * N + n);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 dh[j] = make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
@@ -193,12 +196,13 @@ static int launch_gemm_bn(const void* A, const void* B, int M, int N, int K, con
 }
 
 int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int mode, float* d32, uint16_t* hilo,
-                        int P, int* status, cudaStream_t stream) {
+                        int P, int* status, cudaStream_t stream, uint16_t* lo2) {
     if (!gemm_tc_supported(M, N, K)) return DARTREE_EUNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) % 16) return DARTREE_EINVAL;
     if (mode == 1 && (P < 1 || P > 16 || !hilo)) return DARTREE_EINVAL;
     if (mode == 0 && !d32) return DARTREE_EINVAL;
-    GemmOut o{mode, d32, hilo, P};
+    if (mode == 2 && (!hilo || !lo2)) return DARTREE_EINVAL;
+    GemmOut o{mode, d32, hilo, lo2, P};
     // wider tiles halve the L2 traffic of the operand both tile rows share
     if (N % 256 == 0) return launch_gemm_bn<256>(A, B, M, N, K, o, status, stream);
     return launch_gemm_bn<128>(A, B, M, N, K, o, status, stream);

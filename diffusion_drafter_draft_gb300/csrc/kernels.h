@@ -31,20 +31,33 @@ struct ExpandArgs {
     float* U;                 // [C*W, H]
     float* z;                 // [C, W, K]
     uint16_t* uhl;            // [C, 32, H] bf16 hi/lo projection rows (tensor-core contraction), or null
+    const void* WqT;          // [H, H] W_q transposed (prepared head), or null
+    uint16_t* Eg;             // [C*L*K, H] gathered candidate rows (candidate-side projection path)
+    uint16_t* Ghi;            // [C*L*K, H] G = E[cand] W_q, bf16 high part
+    uint16_t* Glo;            // [C*L*K, H] low part
+    int g_rows;               // rows the Eg/G buffers hold (0: path unavailable)
     float* zpart;             // [zpart_clusters, C*W*K] per-cluster partial logits (small-batch path)
     int zpart_clusters;       // 0: small-batch path unavailable
     unsigned* bar;            // grid barrier counter (small-batch path)
     int* status;
 };
 
+// Transpose of an H x H bf16 matrix (head preparation).
+int launch_transpose_bf16(const void* src, void* dst, int H, cudaStream_t stream);
+
+// Candidate-side projection path (small batches, prepared bf16 head); *launched = false
+// when the shape does not fit it.
+int try_launch_expand_g(const ExpandArgs& a, cudaStream_t stream, bool* launched);
+
 // Small-batch persistent path; *launched = false when the shape does not fit it.
 int try_launch_expand_small(const ExpandArgs& a, cudaStream_t stream, bool* launched);
 
 // tcgen05 GEMM D[M,N] = A[M,K] . B[N,K]^T (bf16 in, fp32 accumulate).
-// mode 0: fp32 d32 [M,N]; mode 1: bf16 hi/lo pairs into hilo [M/P, 32, N].
+// mode 0: fp32 d32 [M,N]; mode 1: bf16 hi/lo pairs into hilo [M/P, 32, N];
+// mode 2: bf16 hi into hilo [M,N] and lo into lo2 [M,N].
 bool gemm_tc_supported(int M, int N, int K);
 int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int mode, float* d32, uint16_t* hilo,
-                        int P, int* status, cudaStream_t stream);
+                        int P, int* status, cudaStream_t stream, uint16_t* lo2 = nullptr);
 
 // tcgen05 contraction of one depth: z[r,p,c] from gathered candidate rows and uhl.
 bool contract_tc_supported(int P, int H);

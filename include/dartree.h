@@ -88,6 +88,7 @@ typedef struct {
     int V;
     int H;           /* multiple of 8 */
     int dtype;       /* dartree_dtype of E, Wq, base logits and block hidden states */
+    const void* WqT; /* [H, H] W_q transposed, filled by dartree_head_prepare; NULL until then */
 } dartree_head;
 
 /* Shape of one round. */
@@ -135,6 +136,13 @@ typedef struct {
 /* Checks and stores the head description. E and Wq must stay valid while the
  * head is used. Returns DARTREE_OK or a negative status. */
 DARTREE_API int dartree_head_init(dartree_head* head, const void* E, const void* Wq, int V, int H, int dtype);
+
+/* Derived per-model data for the small-batch path: writes W_q^T into `wqt`
+ * (caller-owned device memory of H*H elements of the head's dtype, valid while the
+ * head is used) on `stream` and records it in head->WqT. Call once after
+ * dartree_head_init and again whenever W_q changes. Without it, every batch takes
+ * the per-depth projection path. bf16 heads only (DARTREE_EUNSUPPORTED otherwise). */
+DARTREE_API int dartree_head_prepare(dartree_head* head, void* wqt, void* stream);
 
 /* Workspace bytes needed by every call below for this shape (0 on bad arguments). */
 DARTREE_API size_t dartree_workspace_bytes(const dartree_params* p, int V, int H, int dtype);

@@ -134,6 +134,22 @@ def test_large_batch_path_shapes(C, L, V, H, K, W, B):
     compare_verify(o, gv, inp["target"], cfg, "position")
 
 
+@pytest.mark.parametrize("C,L,V,H,K,W,B", [(2, 5, 3001, 512, 64, 16, 40), (3, 3, 2000, 384, 24, 5, 10),
+                                           (1, 16, 4096, 1024, 8, 1, 16), (4, 7, 1500, 256, 64, 12, 30)])
+def test_candidate_side_projection_shapes(C, L, V, H, K, W, B):
+    """Small bf16 batches with K <= 64 and W <= 16 take the candidate-side
+    projection path (G = E[cand] W_q once per round, one cluster per request);
+    H = 384 runs it with 8-CTA clusters, the others with 16."""
+    import diffusion_drafter_draft_gb300 as dd
+    cfg = make_config("cfg1_qwen3_4b_c1").replace(C=C, L=L, V=V, H=H, K=K, W=W, B=B, seed=C * 1000 + K)
+    inp = make_inputs(cfg)
+    g, x = run_gpu_build(inp)
+    o = compare_build(inp, g)
+    tr = {k: torch.from_numpy(v).cuda() for k, v in g.items() if k in ("tok", "par", "depth", "n_nodes")}
+    gv = host(dd.verify(tr, x["target"], dd.ROWS_PER_POSITION, cfg.L))
+    compare_verify(o, gv, inp["target"], cfg, "position")
+
+
 def test_stress_batch_sampled_requests():
     """Full C=64, K=512 batch on the GPU; the oracle checks a sample of requests
     (each request is drawn from its own stream, so a sample is bit-identical)."""
