@@ -107,6 +107,12 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_u32(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
 // Address of the same shared variable in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
     uint32_t r; asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
@@ -161,6 +167,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+// 1-D bulk copy from own shared memory into a peer CTA's shared memory; completion
+// (bytes) is counted on the peer's mbarrier. remote_dst and remote_bar are
+// shared::cluster addresses (mapa); all addresses and bytes multiples of 16.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t remote_dst, const void* src, uint32_t bytes,
+                                               uint32_t remote_bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(remote_dst), "r"(smem_u32(src)), "r"(bytes), "r"(remote_bar) : "memory");
 }
 
 // ----------------------------------------------------------------------------- block helpers

@@ -12,47 +12,68 @@
 // Each depth then contracts the P parents with the K candidates of its position
 // in one batch: z = h . G_hi^T + h . G_lo^T (mma.sync, fp32 accumulation), with
 // no dependence on W_q, so one thread-block cluster per request runs all L
-// depths: CTA q of the cluster owns H/CS features of h and G, the partial logits
-// are summed through distributed shared memory, every CTA selects the same top-W
-// children, and each CTA normalises its own feature slice of the new states
-// (the RMSNorm sum of squares is all-reduced across the cluster). Nothing leaves
-// the cluster between depths.
+// depths. CTA q of the cluster owns H/CS features of h, G and E, and parent
+// rows p with p mod CS = q. Per depth, separated by three cluster barriers:
+//
+//   1. partial logits over the CTA's features (mma.sync), each parent row sent
+//      to its owner's shared memory (reduce-scatter);
+//   2. the owner sums the CS partials of its rows in a fixed order, takes the
+//      log-softmax and scores, ranks the row's candidates by counting, and
+//      broadcasts the row's best min(W, K) keys, sorted, to every CTA;
+//   3. every CTA merges the P sorted lists (rank = position in its own list +
+//      binary searches in the others), so all of them take the same top-W; the
+//      kept children's state slices x = h_p + E[tok] + H_d[d-1] are formed,
+//      partial sums of squares exchanged, and the slices normalised into the
+//      next parent buffer.
+//
+// The candidate table of the request sits in shared memory. The G, E and H_d
+// slices of the next position arrive by TMA while the current depth runs: G as
+// 32-column tiles with 64-byte swizzle (conflict-free ldmatrix), E as one tile
+// of the gathered candidate rows, H_d as one bulk copy, all completing on one
+// mbarrier. Waits are bounded; a wait that runs out records a timeout and the
+// CTA keeps taking part in every cluster barrier, so no peer is left waiting.
 #include <math.h>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace dartree {
 
 constexpr int XG_NT = 256;
 constexpr int XG_NW = XG_NT / 32;
-constexpr int XG_MAXK = 64;   // candidates per position (one 8-candidate mma tile per warp)
-constexpr int XG_MAXW = 16;   // parents per depth (one 16-row mma tile)
-constexpr int XG_MAXCAND = 8192;
+constexpr int XG_MAXK = 64;   // candidates per position: two per lane in the score pass
+constexpr int XG_MAXW = 16;   // parents per depth: one 16-row mma tile
 
 __host__ __device__ constexpr size_t xg_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct XgLayout {
-    size_t hs, gs, es, hds, zp, zfull, keys, ssp, sel, cands, misc, total;
+    size_t gs, hs, es, hds, ctok, cval, zred, rkeys, lists, mrg, ssq, sel, spar, mbar, total;
 };
 
-// fs: features per CTA, fp = fs + 8 (padded row), cs: cluster size
-__host__ __device__ inline XgLayout xg_layout(int fs, int K, int cs) {
-    const int fp = fs + 8;
+constexpr int XG_GB = 32;  // columns of one swizzled G tile (64 bytes)
+
+// fs: features per CTA (a multiple of 32, at most 256), cs: cluster size
+__host__ __device__ inline XgLayout xg_layout(int fs, int K, int cs, int L) {
+    const size_t fp = size_t(fs) + 8;
+    const size_t rpo = XG_MAXW / cs;  // parent rows per owner
     XgLayout l{};
     size_t o = 0;
-    auto take = [&](size_t b) { size_t at = o; o = xg_up(o + b, 16); return at; };
-    l.hs = take(size_t(2) * XG_MAXW * fp * 2);   // h slices, current and next
-    l.gs = take(size_t(2) * K * fp * 2);         // G_hi, G_lo slices of one position
-    l.es = take(size_t(K) * fs * 2);             // E slices of one position
-    l.hds = take(size_t(fs) * 2);                // H_d slice of one position
-    l.zp = take(size_t(XG_MAXW) * K * 4);
-    l.zfull = take(size_t(XG_MAXW) * K * 4);
-    l.keys = take(size_t(XG_MAXW) * K * 8);
-    l.ssp = take(size_t(cs) * XG_MAXW * 4);
-    l.sel = take(size_t(XG_MAXW) * 16);
-    l.cands = take(size_t(XG_NW) * XG_MAXW * 8);
-    l.misc = take(64 * 4);
+    auto take = [&](size_t b, size_t al) { o = xg_up(o, al); size_t at = o; o += b; return at; };
+    l.gs = take(2 * size_t(K) * fs * 2, 1024);        // G_hi, G_lo: fs/32 swizzled tiles [K][32] each
+    l.hs = take(2 * XG_MAXW * fp * 2, 128);          // parent state slices, two buffers of 16 padded rows
+    l.es = take(2 * size_t(K) * fs * 2, 128);        // E slices [K][fs], two positions
+    l.hds = take(2 * size_t(fs) * 2, 128);           // H_d slices, two positions
+    l.ctok = take(size_t(L) * K * 4, 16);            // candidate table of the request
+    l.cval = take(size_t(L) * K * 4, 16);
+    l.zred = take(size_t(cs) * rpo * K * 4, 16);     // partial logits of the owned rows [q][slot][c]
+    l.rkeys = take(rpo * size_t(K) * 8, 16);         // keys of the owned rows
+    l.lists = take(size_t(XG_MAXW) * XG_MAXW * 8, 16);  // best keys of every row, sorted [p][j]
+    l.mrg = take(2 * size_t(XG_NW) * 16 * 8, 16);        // merge tree levels, ping-pong
+    l.ssq = take(size_t(cs) * XG_MAXW * 4, 16);      // partial sums of squares [q][k]
+    l.sel = take(size_t(XG_MAXW) * 8 + 2 * XG_MAXW * 4, 16);
+    l.spar = take(size_t(XG_MAXW) * 4, 16);
+    l.mbar = take(8, 8);                             // prefetch barrier
     l.total = o;
     return l;
 }
@@ -63,9 +84,7 @@ struct XgArgs {
     const int32_t* anchor;
     const int32_t* cand_tok;
     const float* cand_val;
-    const uint16_t* Ghi;
-    const uint16_t* Glo;
-    int H, L, K, W, cs;
+    int H, L, K, W;
     float beta, inv_sqrt_h;
     int32_t* st_tok;
     int32_t* st_par;
@@ -74,15 +93,9 @@ struct XgArgs {
     int* status;
 };
 
-__device__ __forceinline__ void xg_cp16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void xg_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void xg_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ void xg_ldsm_x4(uint32_t (&r)[4], const void* p) {
+__device__ __forceinline__ void xg_ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
 }
 __device__ __forceinline__ void xg_mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -91,200 +104,292 @@ __device__ __forceinline__ void xg_mma(float (&d)[4], const uint32_t (&a)[4], ui
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ void st_dsmem_f32x(uint32_t addr, float v) {
+__device__ __forceinline__ void xg_st_remote_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
 }
-__device__ __forceinline__ float ld_dsmem_f32x(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
+__device__ __forceinline__ void xg_st_remote_v2(uint32_t addr, float x, float y) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" :: "r"(addr), "f"(x), "f"(y) : "memory");
 }
 
-// G_hi/G_lo slices of position pos, by cp.async (one group).
-__device__ __forceinline__ void xg_load_g(const XgArgs& a, int r, int pos, int f0, int fs, uint16_t* gs) {
-    const int fp = fs + 8, K = a.K, H = a.H;
-    const int cpr = fs / 8;  // 16-byte chunks per slice row
-    const size_t crow = (size_t(r) * a.L + pos) * K;
-    for (int i = threadIdx.x; i < 2 * K * cpr; i += XG_NT) {
-        const int hl = i / (K * cpr), c = (i / cpr) % K, j = i % cpr;
-        const uint16_t* src = (hl ? a.Glo : a.Ghi) + (crow + c) * H + f0 + j * 8;
-        xg_cp16(gs + (size_t(hl) * K + c) * fp + j * 8, src);
+// Top 16 of two descending 16-key lists held by the two half-warps (lane l of
+// half-warp h holds element l of list h), sorted descending into lanes 0..15:
+// the element-wise maximum of one list and the other reversed is bitonic and
+// holds the 16 largest; a bitonic merge (distances 8, 4, 2, 1) sorts it.
+__device__ __forceinline__ uint64_t xg_merge16(uint64_t v) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t lo = __shfl_sync(0xffffffffu, uint32_t(v), 31 - lane);
+    const uint32_t hi = __shfl_sync(0xffffffffu, uint32_t(v >> 32), 31 - lane);
+    const uint64_t o = (uint64_t(hi) << 32) | lo;
+    uint64_t c = v > o ? v : o;
+#pragma unroll
+    for (int d = 8; d; d >>= 1) {
+        const uint64_t p = shfl_xor_u64(c, d);
+        c = ((lane & d) == 0) ? (c > p ? c : p) : (c < p ? c : p);
     }
-    xg_commit();
+    return c;
 }
 
-// E slices of the candidates of position pos and the H_d slice of pos (one group).
-__device__ __forceinline__ void xg_load_e(const XgArgs& a, int r, int pos, int f0, int fs, uint16_t* es,
-                                          uint16_t* hds) {
-    const int K = a.K, H = a.H;
-    const int cpr = fs / 8;
-    const size_t crow = (size_t(r) * a.L + pos) * K;
-    for (int i = threadIdx.x; i < K * cpr; i += XG_NT) {
-        const int c = i / cpr, j = i % cpr;
-        xg_cp16(es + size_t(c) * fs + j * 8, a.E + size_t(a.cand_tok[crow + c]) * H + f0 + j * 8);
-    }
-    for (int j = threadIdx.x; j < cpr; j += XG_NT)
-        xg_cp16(hds + j * 8, a.hidden + (size_t(r) * a.L + pos) * H + f0 + j * 8);
-    xg_commit();
-}
-
-__global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    const int CS = a.cs, H = a.H, L = a.L, K = a.K, W = a.W;
-    const int fs = H / CS, fp = fs + 8;
-    const XgLayout lay = xg_layout(fs, K, CS);
+template <int CS>
+__global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __grid_constant__ CUtensorMap tm_ghi,
+                                                             const __grid_constant__ CUtensorMap tm_glo,
+                                                             const __grid_constant__ CUtensorMap tm_eg) {
+    constexpr int RPO = XG_MAXW / CS;  // parent rows per owner
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int H = a.H, L = a.L, K = a.K, W = a.W;
+    const int fs = H / CS, fp = fs + 8, cpr = fs / 8, nb = fs / XG_GB;
+    const XgLayout lay = xg_layout(fs, K, CS, L);
+    uint8_t* gs = smem + lay.gs;
     uint16_t* hs = reinterpret_cast<uint16_t*>(smem + lay.hs);
-    uint16_t* gs = reinterpret_cast<uint16_t*>(smem + lay.gs);
     uint16_t* es = reinterpret_cast<uint16_t*>(smem + lay.es);
     uint16_t* hds = reinterpret_cast<uint16_t*>(smem + lay.hds);
-    float* zp = reinterpret_cast<float*>(smem + lay.zp);
-    float* zfull = reinterpret_cast<float*>(smem + lay.zfull);
-    uint64_t* keys = reinterpret_cast<uint64_t*>(smem + lay.keys);
-    float* ssp = reinterpret_cast<float*>(smem + lay.ssp);
-    uint64_t* selk = reinterpret_cast<uint64_t*>(smem + lay.sel);   // kept keys, descending
-    int* selx = reinterpret_cast<int*>(selk + XG_MAXW);             // [0..W): parent rank, [W..2W): candidate
-    uint64_t* cands = reinterpret_cast<uint64_t*>(smem + lay.cands);
-    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + lay.misc);
-    float* spar = reinterpret_cast<float*>(misc + 32);              // parent scores (<= 16)
+    int32_t* ctok = reinterpret_cast<int32_t*>(smem + lay.ctok);
+    float* cval = reinterpret_cast<float*>(smem + lay.cval);
+    float* zred = reinterpret_cast<float*>(smem + lay.zred);
+    uint64_t* rkeys = reinterpret_cast<uint64_t*>(smem + lay.rkeys);
+    uint64_t* lists = reinterpret_cast<uint64_t*>(smem + lay.lists);
+    uint64_t* mrg = reinterpret_cast<uint64_t*>(smem + lay.mrg);
+    float* ssq = reinterpret_cast<float*>(smem + lay.ssq);
+    uint64_t* selk = reinterpret_cast<uint64_t*>(smem + lay.sel);  // kept keys, descending
+    int* selx = reinterpret_cast<int*>(selk + XG_MAXW);            // [0..16): parent rank, [16..32): candidate
+    float* spar = reinterpret_cast<float*>(smem + lay.spar);       // parent scores
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + lay.mbar);
 
     const uint32_t cr = cluster_ctarank();
     const int r = blockIdx.x / CS;
     const int f0 = int(cr) * fs;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 
-    // root: h = E[anchor] (this CTA's slice), s = 0; rows 1..15 zero
-    for (int i = threadIdx.x; i < 2 * XG_MAXW * fp; i += XG_NT) hs[i] = 0;
-    __syncthreads();
+    // G (and, with_e, the E and H_d slices) of position pos; one thread
+    auto prefetch = [&](int pos, bool with_e) {
+        const int row = (r * L + pos) * K;  // first candidate row of the position in G and E[cand]
+        mbar_arrive_expect_tx(mbar, uint32_t((2 + (with_e ? 1 : 0)) * K * fs * 2 + (with_e ? fs * 2 : 0)));
+        for (int b = 0; b < nb; ++b) {
+            tc::tma_load_2d(gs + size_t(b) * K * 64, &tm_ghi, f0 + b * XG_GB, row, mbar);
+            tc::tma_load_2d(gs + size_t(nb + b) * K * 64, &tm_glo, f0 + b * XG_GB, row, mbar);
+        }
+        if (with_e) {
+            tc::tma_load_2d(es + size_t(pos & 1) * K * fs, &tm_eg, f0, row, mbar);
+            bulk_g2s(hds + size_t(pos & 1) * fs, a.hidden + (size_t(r) * L + pos) * H + f0, uint32_t(fs * 2), mbar);
+        }
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(mbar, 1);
+        fence_mbar_init();
+    }
+    for (int i = threadIdx.x; i < L * K; i += XG_NT) {
+        ctok[i] = a.cand_tok[size_t(r) * L * K + i];
+        cval[i] = a.cand_val[size_t(r) * L * K + i];
+    }
+    // root: h = E[anchor] (this CTA's slice), s = 0
     for (int f = threadIdx.x; f < fs; f += XG_NT) hs[f] = a.E[size_t(a.anchor[r]) * H + f0 + f];
-    if (threadIdx.x < XG_MAXW) spar[threadIdx.x] = 0.f;
-    xg_load_g(a, r, 0, f0, fs, gs);
-    xg_load_e(a, r, 0, f0, fs, es, hds);
+    if (threadIdx.x == 0) spar[0] = 0.f;
+    __syncthreads();
+    if (threadIdx.x == 0) prefetch(0, L > 1);
+    int issued = 1, waited = 0;  // prefetch phases (uniform across the CTA)
+    bool pf_ok = true;           // false once a prefetch wait ran out: no further prefetches
     int cur = 0, P = 1;
 
     for (int d = 1; d <= L; ++d) {
         const int pos = d - 1;
-        xg_wait_all();
-        __syncthreads();
-        // ---- partial logits over this CTA's features: zp[p][c] = h_p . (G_hi + G_lo)_c
+        const int ne = P * K;
+        const int n_keep = min(W, ne);
+        const int m = min(n_keep, K);  // keys per row list
+        // a timed-out wait records ETIMEOUT and the CTA carries on, so that every
+        // CTA of the cluster reaches the same barriers
+        if (pf_ok) pf_ok = __syncthreads_and(mbar_wait_bounded(mbar, uint32_t(waited) & 1u, a.status) ? 1 : 0) != 0;
+        else __syncthreads();
+        if (pf_ok) waited = issued;
+        // ---- 1. partial logits over this CTA's features, each row to its owner
         {
             const uint16_t* hb = hs + size_t(cur) * XG_MAXW * fp;
             const int lm = lane >> 3, lr = lane & 7, g = lane >> 2, t = lane & 3;
+            const uint32_t z0 = smem_u32(zred), g0 = smem_u32(gs);
             for (int ct = wid; ct * 8 < K; ct += XG_NW) {  // 8 candidates per tile
+                const int n = ct * 8 + lr;                 // candidate row this lane addresses
+                // matrices: (hi, k lo), (hi, k hi), (lo, k lo), (lo, k hi)
+                const uint32_t brow = g0 + uint32_t(((lm >> 1) * nb * K + n) * 64);
+                const uint32_t sw = uint32_t((n >> 1) & 3);
                 float acc_hi[4] = {0.f, 0.f, 0.f, 0.f}, acc_lo[4] = {0.f, 0.f, 0.f, 0.f};
                 for (int k0 = 0; k0 < fs; k0 += 16) {
                     uint32_t af[4], bf[4];
-                    xg_ldsm_x4(af, hb + size_t((lm & 1) * 8 + lr) * fp + k0 + (lm >> 1) * 8);
-                    // matrices: (hi, k lo), (hi, k hi), (lo, k lo), (lo, k hi)
-                    xg_ldsm_x4(bf, gs + (size_t(lm >> 1) * K + ct * 8 + lr) * fp + k0 + (lm & 1) * 8);
+                    xg_ldsm_x4(af, smem_u32(hb + size_t((lm & 1) * 8 + lr) * fp + k0 + (lm >> 1) * 8));
+                    const uint32_t chunk = uint32_t(((k0 & 31) >> 3) + (lm & 1));
+                    xg_ldsm_x4(bf, brow + uint32_t((k0 >> 5) * K * 64) + ((chunk ^ sw) << 4));
                     xg_mma(acc_hi, af, bf[0], bf[1]);
                     xg_mma(acc_lo, af, bf[2], bf[3]);
                 }
                 const int c = ct * 8 + 2 * t;
-                if (g < P) {
-                    zp[g * K + c] = acc_hi[0] + acc_lo[0];
-                    zp[g * K + c + 1] = acc_hi[1] + acc_lo[1];
-                }
-                if (g + 8 < P) {
-                    zp[(g + 8) * K + c] = acc_hi[2] + acc_lo[2];
-                    zp[(g + 8) * K + c + 1] = acc_hi[3] + acc_lo[3];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int p = g + 8 * hh;
+                    if (p < P) {
+                        const uint32_t off = z0 + uint32_t(((int(cr) * RPO + p / CS) * K + c) * 4);
+                        xg_st_remote_v2(mapa_u32(off, uint32_t(p % CS)), acc_hi[2 * hh] + acc_lo[2 * hh],
+                                        acc_hi[2 * hh + 1] + acc_lo[2 * hh + 1]);
+                    }
                 }
             }
         }
+        cluster_sync();  // A: partials with their owners; gs free
+        // ---- 2. owned rows: z, log-softmax, scores (warp s: row slot s)
+        if (wid < RPO) {
+            const int p = int(cr) + CS * wid;
+            if (p < P) {
+                float zv[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c = lane + 32 * h;
+                    zv[h] = -INFINITY;
+                    if (c < K) {
+                        float sacc = 0.f;
+#pragma unroll
+                        for (int q = 0; q < CS; ++q) sacc += zred[(q * RPO + wid) * K + c];
+                        zv[h] = cval[pos * K + c] + sacc * a.inv_sqrt_h;
+                    }
+                }
+                const float mx = f32_from_ord(__reduce_max_sync(0xffffffffu, ord_f32(fmaxf(zv[0], zv[1]))));
+                float se = 0.f;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    if (lane + 32 * h < K) se += expf(zv[h] - mx);
+                se = warp_sum(se);
+                const float lse = mx + logf(se);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c = lane + 32 * h;
+                    if (c < K) {
+                        float sc = (spar[p] + (zv[h] - lse)) + a.beta;
+                        sc += 0.f;  // -0 -> +0
+                        const uint32_t f = uint32_t(p * K + c);
+                        rkeys[wid * K + c] = (uint64_t(ord_f32(sc)) << 32) | (0xffffffffu - f);
+                    }
+                }
+            }
+        } else if (threadIdx.x == 32 * RPO && pf_ok && d < L) {
+            prefetch(pos + 1, d + 1 < L);
+        }
+        if (pf_ok && d < L) ++issued;
         __syncthreads();
-        if (d < L) xg_load_g(a, r, pos + 1, f0, fs, gs);  // this depth is done with gs
-        cluster_sync();
-        // ---- cluster sum of this CTA's share of the entries, broadcast to every peer
-        const int ne = P * K;
+        // rank of every owned key within its row (4 lanes per key), best m broadcast
+        for (int item = threadIdx.x >> 2; item < RPO * K; item += XG_NT / 4) {
+            const int slot = item / K, i = item % K, qd = threadIdx.x & 3;
+            const int p = int(cr) + CS * slot;
+            const bool live = p < P;
+            int cnt = 0;
+            uint64_t x = 0;
+            if (live) {
+                x = rkeys[slot * K + i];
+                for (int j = qd; j < K; j += 4) cnt += rkeys[slot * K + j] > x;
+            }
+            cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
+            cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
+            if (live && cnt < m) {
+                // lane qd writes the key to CTAs qd, qd + 4, ...
+                const uint32_t off = smem_u32(lists + p * XG_MAXW + cnt);
+                for (int q = qd; q < CS; q += 4) st_dsmem_u64(mapa_u32(off, uint32_t(q)), x);
+            }
+        }
+        cluster_sync();  // B: every row list everywhere
+        // ---- 3. top-W: bitonic merge tree over the 16 row lists (slots past m or P
+        //         are empty = 0); level 1: warp w merges lists 2w and 2w + 1
         {
-            const int share = (ne + CS - 1) / CS;
-            const int e0 = int(cr) * share, e1 = min(ne, e0 + share);
-            for (int e = e0 + threadIdx.x; e < e1; e += XG_NT) {
-                float s = 0.f;
-                for (int q = 0; q < CS; ++q) s += ld_dsmem_f32x(dsmem_addr(&zp[e], uint32_t(q)));
-                const float z = a.cand_val[(size_t(r) * L + pos) * K + e % K] + s * a.inv_sqrt_h;
-                for (int q = 0; q < CS; ++q) st_dsmem_f32x(dsmem_addr(&zfull[e], uint32_t(q)), z);
-            }
-        }
-        cluster_sync();
-        // ---- log-softmax, scores, top-W (identical in every CTA)
-        for (int p = wid; p < P; p += XG_NW) {
-            const float* zr = zfull + p * K;
-            float mx = -INFINITY;
-            for (int c = lane; c < K; c += 32) mx = fmaxf(mx, zr[c]);
-            mx = warp_max(mx);
-            float se = 0.f;
-            for (int c = lane; c < K; c += 32) se += expf(zr[c] - mx);
-            se = warp_sum(se);
-            const float lse = mx + logf(se);
-            for (int c = lane; c < K; c += 32) {
-                float s = (spar[p] + (zr[c] - lse)) + a.beta;
-                s += 0.f;
-                const uint32_t f = uint32_t(p * K + c);
-                keys[f] = (uint64_t(ord_f32(s)) << 32) | (0xffffffffu - f);
-            }
-        }
-        __syncthreads();
-        const int n_keep = min(W, ne);
-        block_top_keys<XG_NT>(keys, ne, n_keep, cands, selk);
-        if (threadIdx.x < n_keep) {
-            const uint32_t f = 0xffffffffu - uint32_t(selk[threadIdx.x]);
-            selx[threadIdx.x] = int(f) / K;
-            selx[XG_MAXW + threadIdx.x] = int(f) % K;
-        }
-        __syncthreads();
-        if (cr == 0) {
-            for (int k = threadIdx.x; k < W; k += XG_NT) {
-                const size_t o = (size_t(r) * L + pos) * W + k;
-                if (k < n_keep) {
-                    a.st_tok[o] = a.cand_tok[(size_t(r) * L + pos) * K + selx[XG_MAXW + k]];
-                    a.st_par[o] = selx[k];
-                    a.st_s[o] = f32_from_ord(uint32_t(selk[k] >> 32));
-                } else {
-                    a.st_tok[o] = -1;
-                    a.st_par[o] = -1;
-                    a.st_s[o] = 0.f;
+            const int hl = lane & 15, q = 2 * wid + (lane >> 4);
+            uint64_t v = (q < P && hl < m) ? lists[q * XG_MAXW + hl] : 0ull;
+            v = xg_merge16(v);
+            if (lane < 16) mrg[wid * 16 + lane] = v;
+            __syncthreads();
+            int in = 0;
+            for (int nm = XG_NW / 2; nm >= 1; nm >>= 1) {  // merges at this level
+                if (wid < nm) {
+                    v = mrg[in * XG_NW * 16 + (2 * wid + (lane >> 4)) * 16 + hl];
+                    v = xg_merge16(v);
+                    if (lane < 16) mrg[(1 - in) * XG_NW * 16 + wid * 16 + lane] = v;
                 }
+                in = 1 - in;
+                __syncthreads();
             }
-            if (threadIdx.x == 0) a.st_n[size_t(r) * L + pos] = n_keep;
+            if (threadIdx.x < n_keep) {
+                const uint64_t x = mrg[in * XG_NW * 16 + threadIdx.x];
+                const uint32_t f = 0xffffffffu - uint32_t(x);
+                selk[threadIdx.x] = x;
+                selx[threadIdx.x] = int(f) / K;
+                selx[XG_MAXW + threadIdx.x] = int(f) % K;
+            }
         }
-        if (d == L) break;
-        // ---- state update of this CTA's feature slice; the RMSNorm sum of squares
-        // is all-reduced over the cluster
+        __syncthreads();
+        // supertree entries: entry k is written by CTA k mod CS
+        if (threadIdx.x < W && int(threadIdx.x) % CS == int(cr)) {
+            const int k = threadIdx.x;
+            const size_t o = (size_t(r) * L + pos) * W + k;
+            if (k < n_keep) {
+                a.st_tok[o] = ctok[pos * K + selx[XG_MAXW + k]];
+                a.st_par[o] = selx[k];
+                a.st_s[o] = f32_from_ord(uint32_t(selk[k] >> 32));
+            } else {
+                a.st_tok[o] = -1;
+                a.st_par[o] = -1;
+                a.st_s[o] = 0.f;
+            }
+        }
+        if (threadIdx.x == 0 && cr == 0) a.st_n[size_t(r) * L + pos] = n_keep;
+        if (d == L) break;  // no remote access follows barrier B of the last depth
+        // ---- state slices of the kept children: warp w owns rows w and w + 8,
+        //      lane j the 8-feature chunk j
         const uint16_t* hb = hs + size_t(cur) * XG_MAXW * fp;
         uint16_t* hn = hs + size_t(1 - cur) * XG_MAXW * fp;
-        for (int k = wid; k < n_keep; k += XG_NW) {
-            const uint16_t* hp = hb + size_t(selx[k]) * fp;
-            const uint16_t* er = es + size_t(selx[XG_MAXW + k]) * fs;
-            float ss = 0.f;
-            for (int f = lane; f < fs; f += 32) {
-                const float x = (bf16_bits_to_float(hp[f]) + bf16_bits_to_float(er[f])) + bf16_bits_to_float(hds[f]);
-                ss = fmaf(x, x, ss);
+        const uint16_t* eb = es + size_t(pos & 1) * K * fs;
+        const uint16_t* hdb = hds + size_t(pos & 1) * fs;
+        float x[2][8];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int k = wid + rr * XG_NW;
+            if (k < n_keep) {
+                float ss = 0.f;
+                if (lane < cpr) {
+                    const uint4 vp = *reinterpret_cast<const uint4*>(hb + size_t(selx[k]) * fp + lane * 8);
+                    const uint4 ve = *reinterpret_cast<const uint4*>(eb + size_t(selx[XG_MAXW + k]) * fs + lane * 8);
+                    const uint4 vh = *reinterpret_cast<const uint4*>(hdb + lane * 8);
+                    const uint32_t* wp = reinterpret_cast<const uint32_t*>(&vp);
+                    const uint32_t* we = reinterpret_cast<const uint32_t*>(&ve);
+                    const uint32_t* wh = reinterpret_cast<const uint32_t*>(&vh);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int sh = (i & 1) ? 16 : 0;
+                        const float xv = (bf16_bits_to_float((wp[i >> 1] >> sh) & 0xffffu) +
+                                          bf16_bits_to_float((we[i >> 1] >> sh) & 0xffffu)) +
+                                         bf16_bits_to_float((wh[i >> 1] >> sh) & 0xffffu);
+                        x[rr][i] = xv;
+                        ss = fmaf(xv, xv, ss);
+                    }
+                }
+                ss = warp_sum(ss);
+                if (lane < CS) xg_st_remote_f32(mapa_u32(smem_u32(ssq + int(cr) * XG_MAXW + k), uint32_t(lane)), ss);
             }
-            ss = warp_sum(ss);
-            if (lane < CS) st_dsmem_f32x(dsmem_addr(&ssp[int(cr) * XG_MAXW + k], uint32_t(lane)), ss);
         }
-        cluster_sync();
-        for (int k = wid; k < n_keep; k += XG_NW) {
-            float tot = 0.f;
-            for (int q = 0; q < CS; ++q) tot += ssp[q * XG_MAXW + k];
-            const float rs = sqrtf(tot / float(H) + 1e-6f);
-            const uint16_t* hp = hb + size_t(selx[k]) * fp;
-            const uint16_t* er = es + size_t(selx[XG_MAXW + k]) * fs;
-            for (int f = lane; f < fs; f += 32) {
-                const float x = (bf16_bits_to_float(hp[f]) + bf16_bits_to_float(er[f])) + bf16_bits_to_float(hds[f]);
-                hn[size_t(k) * fp + f] = __bfloat16_as_ushort(__float2bfloat16_rn(x / rs));
+        cluster_sync();  // C: every partial sum of squares everywhere
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int k = wid + rr * XG_NW;
+            if (k < n_keep && lane < cpr) {
+                float tot = 0.f;
+#pragma unroll
+                for (int q = 0; q < CS; ++q) tot += ssq[q * XG_MAXW + k];
+                const float inv = 1.0f / sqrtf(tot / float(H) + 1e-6f);
+                uint32_t w4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    w4[i] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(x[rr][2 * i] * inv))) |
+                            (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(x[rr][2 * i + 1] * inv))) << 16);
+                *reinterpret_cast<uint4*>(hn + size_t(k) * fp + lane * 8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
         }
-        for (int i = threadIdx.x; i < (XG_MAXW - n_keep) * fs; i += XG_NT)  // unused rows stay zero
-            hn[size_t(n_keep + i / fs) * fp + i % fs] = 0;
         if (threadIdx.x < n_keep) spar[threadIdx.x] = f32_from_ord(uint32_t(selk[threadIdx.x] >> 32));
-        __syncthreads();
-        xg_load_e(a, r, pos + 1, f0, fs, es, hds);  // this depth is done with es, hds
         cur = 1 - cur;
         P = n_keep;
     }
-    xg_wait_all();
-    cluster_sync();  // no CTA leaves while a peer may still address its shared memory
+    // a prefetch still in flight (only after a timed-out wait) lands before the CTA leaves
+    if (!pf_ok) mbar_wait_bounded(mbar, uint32_t(waited) & 1u, a.status);
 }
 
 // --------------------------------------------------------------------------- gathers, transpose
@@ -319,20 +424,21 @@ int launch_transpose_bf16(const void* src, void* dst, int H, cudaStream_t stream
 
 // --------------------------------------------------------------------------- host
 
-static bool xg_cluster_ok(int cs, size_t smem) {
-    auto kern = expand_g_kernel;
+template <int CS>
+static bool xg_cluster_ok(size_t smem) {
+    auto kern = expand_g_kernel<CS>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess ||
-        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        (CS > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)) {
         cudaGetLastError();
         return false;
     }
     cudaLaunchConfig_t q{};
-    q.gridDim = dim3(unsigned(cs));
+    q.gridDim = dim3(unsigned(CS));
     q.blockDim = dim3(XG_NT);
     q.dynamicSmemBytes = smem;
     cudaLaunchAttribute qa[1];
     qa[0].id = cudaLaunchAttributeClusterDimension;
-    qa[0].val.clusterDim.x = cs;
+    qa[0].val.clusterDim.x = CS;
     qa[0].val.clusterDim.y = 1;
     qa[0].val.clusterDim.z = 1;
     q.attrs = qa;
@@ -345,6 +451,28 @@ static bool xg_cluster_ok(int cs, size_t smem) {
     return nc >= 1;
 }
 
+template <int CS>
+static int xg_launch(const XgArgs& x, const CUtensorMap& ghi, const CUtensorMap& glo, const CUtensorMap& eg, int C,
+                     size_t smem, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(unsigned(C) * CS);
+    cfg.blockDim = dim3(XG_NT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, expand_g_kernel<CS>, x, ghi, glo, eg) == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
+}
+
+// Features per CTA for cluster size cs: whole 32-column G tiles, at most 256 (one
+// 16-byte chunk per lane in the state update, one E tile).
+static bool xg_fs_ok(int H, int cs) { return H % (cs * XG_GB) == 0 && H / cs <= 256; }
+
 int try_launch_expand_g(const ExpandArgs& a, cudaStream_t stream, bool* launched) {
     *launched = false;
     if (a.dtype != DARTREE_BF16 || !a.WqT || !a.Eg || !a.Ghi || !a.Glo) return DARTREE_OK;
@@ -353,29 +481,35 @@ int try_launch_expand_g(const ExpandArgs& a, cudaStream_t stream, bool* launched
     if (!gemm_tc_supported(M, a.H, a.H)) return DARTREE_OK;
     int cs = 0;
     size_t smem = 0;
-    for (int c : {16, 8}) {
-        if (a.H % (c * 16) != 0) continue;
-        const size_t sm = xg_layout(a.H / c, a.K, c).total;
-        if (sm <= 227 * 1024 && xg_cluster_ok(c, sm)) { cs = c; smem = sm; break; }
+    if (xg_fs_ok(a.H, 16)) {
+        const size_t sm = xg_layout(a.H / 16, a.K, 16, a.L).total;
+        if (sm <= 227 * 1024 && xg_cluster_ok<16>(sm)) { cs = 16; smem = sm; }
+    }
+    if (!cs && xg_fs_ok(a.H, 8)) {
+        const size_t sm = xg_layout(a.H / 8, a.K, 8, a.L).total;
+        if (sm <= 227 * 1024 && xg_cluster_ok<8>(sm)) { cs = 8; smem = sm; }
     }
     if (!cs) return DARTREE_OK;
     *launched = true;
     gather_rows_kernel<<<M, 256, 0, stream>>>(static_cast<const uint16_t*>(a.E), a.cand_tok, a.H, a.Eg);
     if (cudaGetLastError() != cudaSuccess) return DARTREE_ECUDA;
     if (int e = launch_gemm_bf16_tc(a.Eg, a.WqT, M, a.H, a.H, 2, nullptr, a.Ghi, 1, a.status, stream, a.Glo)) return e;
+    const int fs = a.H / cs;
+    CUtensorMap ghi, glo, eg;
+    if (!make_tensor_map_bf16(&ghi, a.Ghi, M, a.H, XG_GB, a.K, 64) ||
+        !make_tensor_map_bf16(&glo, a.Glo, M, a.H, XG_GB, a.K, 64) ||
+        !make_tensor_map_bf16(&eg, a.Eg, M, a.H, fs, a.K, 0))
+        return DARTREE_ECUDA;
     XgArgs x{};
     x.E = static_cast<const uint16_t*>(a.E);
     x.hidden = static_cast<const uint16_t*>(a.hidden);
     x.anchor = a.anchor;
     x.cand_tok = a.cand_tok;
     x.cand_val = a.cand_val;
-    x.Ghi = a.Ghi;
-    x.Glo = a.Glo;
     x.H = a.H;
     x.L = a.L;
     x.K = a.K;
     x.W = a.W;
-    x.cs = cs;
     x.beta = a.beta;
     x.inv_sqrt_h = 1.0f / sqrtf(float(a.H));
     x.st_tok = a.st_tok;
@@ -383,19 +517,7 @@ int try_launch_expand_g(const ExpandArgs& a, cudaStream_t stream, bool* launched
     x.st_s = a.st_s;
     x.st_n = a.st_n;
     x.status = a.status;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(unsigned(a.C) * cs);
-    cfg.blockDim = dim3(XG_NT);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, expand_g_kernel, x) == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
+    return cs == 16 ? xg_launch<16>(x, ghi, glo, eg, a.C, smem, stream) : xg_launch<8>(x, ghi, glo, eg, a.C, smem, stream);
 }
 
 }  // namespace dartree

@@ -164,17 +164,27 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D bf16 tensor [rows, cols] (row-major), box = 64 columns x box_rows rows, 128-byte swizzle.
-static bool make_map(CUtensorMap* map, const void* base, int rows, int cols, int box_rows) {
+bool make_tensor_map_bf16(CUtensorMap* map, const void* base, int rows, int cols, int box_cols, int box_rows,
+                          int swizzle_bytes) {
     auto fn = encode_fn();
     if (!fn) return false;
+    CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
+    if (swizzle_bytes == 32) sw = CU_TENSOR_MAP_SWIZZLE_32B;
+    else if (swizzle_bytes == 64) sw = CU_TENSOR_MAP_SWIZZLE_64B;
+    else if (swizzle_bytes == 128) sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    else if (swizzle_bytes != 0) return false;
     cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
     cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
-    cuuint32_t box[2] = {cuuint32_t(GT_BK), cuuint32_t(box_rows)};
+    cuuint32_t box[2] = {cuuint32_t(box_cols), cuuint32_t(box_rows)};
     cuuint32_t es[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Operand tiles of the GEMM: box = 64 columns x box_rows rows, 128-byte swizzle.
+static bool make_map(CUtensorMap* map, const void* base, int rows, int cols, int box_rows) {
+    return make_tensor_map_bf16(map, base, rows, cols, GT_BK, box_rows, 128);
 }
 
 bool gemm_tc_supported(int M, int N, int K) {

@@ -1,6 +1,7 @@
 // Host-side launchers of the DARTree kernels (internal to the library).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -43,6 +44,10 @@ struct ExpandArgs {
 };
 
 // Transpose of an H x H bf16 matrix (head preparation).
+// 2-D bf16 TMA descriptor of a row-major [rows, cols] tensor, box box_cols x box_rows,
+// swizzle 0 (none), 32, 64 or 128 bytes. False when the driver refuses it.
+bool make_tensor_map_bf16(CUtensorMap* map, const void* base, int rows, int cols, int box_cols, int box_rows,
+                          int swizzle_bytes);
 int launch_transpose_bf16(const void* src, void* dst, int H, cudaStream_t stream);
 
 // Candidate-side projection path (small batches, prepared bf16 head); *launched = false

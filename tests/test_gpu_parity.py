@@ -134,12 +134,12 @@ def test_large_batch_path_shapes(C, L, V, H, K, W, B):
     compare_verify(o, gv, inp["target"], cfg, "position")
 
 
-@pytest.mark.parametrize("C,L,V,H,K,W,B", [(2, 5, 3001, 512, 64, 16, 40), (3, 3, 2000, 384, 24, 5, 10),
+@pytest.mark.parametrize("C,L,V,H,K,W,B", [(2, 5, 3001, 512, 64, 16, 40), (3, 3, 2000, 768, 24, 5, 10),
                                            (1, 16, 4096, 1024, 8, 1, 16), (4, 7, 1500, 256, 64, 12, 30)])
 def test_candidate_side_projection_shapes(C, L, V, H, K, W, B):
     """Small bf16 batches with K <= 64 and W <= 16 take the candidate-side
     projection path (G = E[cand] W_q once per round, one cluster per request);
-    H = 384 runs it with 8-CTA clusters, the others with 16."""
+    H = 768 and H = 256 run it with 8-CTA clusters, the others with 16."""
     import diffusion_drafter_draft_gb300 as dd
     cfg = make_config("cfg1_qwen3_4b_c1").replace(C=C, L=L, V=V, H=H, K=K, W=W, B=B, seed=C * 1000 + K)
     inp = make_inputs(cfg)
