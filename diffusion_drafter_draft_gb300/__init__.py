@@ -25,7 +25,7 @@ OK, EINVAL, EDTYPE, EWORKSPACE, ECUDA, ETIMEOUT, EINTERNAL, EUNSUPPORTED = 0, -1
 EXPORTS = ("dartree_head_init", "dartree_workspace_bytes", "dartree_topk", "dartree_expand", "dartree_prune",
            "dartree_tree_mask", "dartree_build_tree", "dartree_verify", "dartree_read_status",
            "dartree_clear_status", "dartree_status_string", "dartree_verify_static", "dartree_gemm_bf16",
-           "dartree_head_prepare")
+           "dartree_head_prepare", "dartree_round")
 
 
 class DartreeError(RuntimeError):
@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
     P = ctypes.POINTER
     sig = {
         "dartree_head_init": (i, [P(Head), vp, vp, i, i, i]),
+        "dartree_round": (i, [P(Head), P(Params), vp, vp, vp, vp, i, P(Tree), vp, vp, vp, vp, sz, vp]),
         "dartree_head_prepare": (i, [P(Head), vp, vp]),
         "dartree_workspace_bytes": (sz, [P(Params), i, i, i]),
         "dartree_topk": (i, [vp, i, i, i, i, vp, vp, vp, sz, vp]),
@@ -394,6 +395,17 @@ class Round:
         self.dtype_code = self.head.dtype
 
     def run(self, base, hidden, anchor, target, stream=None):
+        """dartree_round: build + verify in one call."""
+        _call("dartree_round", ctypes.byref(self.head), ctypes.byref(self.p), ctypes.c_void_p(base.data_ptr()),
+              ctypes.c_void_p(hidden.data_ptr()), ctypes.c_void_p(anchor.data_ptr()),
+              ctypes.c_void_p(target.data_ptr()), int(self.rows), ctypes.byref(self._ts),
+              ctypes.c_void_p(self.out["accepted_len"].data_ptr()), ctypes.c_void_p(self.out["path"].data_ptr()),
+              ctypes.c_void_p(self.out["bonus"].data_ptr()), ctypes.c_void_p(self.ws.data_ptr()), self.ws.numel(),
+              _stream(stream))
+        return self.out
+
+    def run_two_calls(self, base, hidden, anchor, target, stream=None):
+        """The same round as dartree_build_tree followed by dartree_verify."""
         s = _stream(stream)
         _call("dartree_build_tree", ctypes.byref(self.head), ctypes.byref(self.p), ctypes.c_void_p(base.data_ptr()),
               ctypes.c_void_p(hidden.data_ptr()), ctypes.c_void_p(anchor.data_ptr()), ctypes.byref(self._ts), None,

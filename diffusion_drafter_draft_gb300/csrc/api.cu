@@ -7,6 +7,8 @@
 #include "dartree.h"
 #include "kernels.h"
 
+#include <mutex>
+
 namespace {
 
 using namespace dartree;
@@ -85,6 +87,22 @@ template <typename P>
 P* at(void* ws, size_t off) { return reinterpret_cast<P*>(static_cast<uint8_t*>(ws) + off); }
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+// S8 + S9 from a supertree: the fused one-CTA-per-request kernel when the
+// supertree holds at most 256 nodes, else the radix prune and the mask kernel.
+int finish_tree(const dartree_params* p, const dartree_supertree* sp, const int32_t* anchor, dartree_tree* tree,
+                int* status, cudaStream_t s) {
+    if (finish_supported(p->L, p->W))
+        return launch_finish(p->C, p->L, p->W, p->B, sp->tok, sp->par, sp->score, sp->n, anchor, tree->tok,
+                             tree->par, tree->depth, tree->score, tree->n_nodes, tree->mask, tree->pos, nullptr,
+                             nullptr, nullptr, nullptr, status, s);
+    if (int e = launch_prune(p->C, p->L, p->W, p->B, sp->tok, sp->par, sp->score, sp->n, anchor, tree->tok, tree->par,
+                             tree->depth, tree->score, tree->n_nodes, status, s))
+        return e;
+    if (tree->mask)
+        return launch_mask(p->C, p->L, p->B, tree->par, tree->depth, tree->n_nodes, tree->mask, tree->pos, s);
+    return DARTREE_OK;
+}
 
 }  // namespace
 
@@ -259,12 +277,84 @@ int dartree_build_tree(const dartree_head* head, const dartree_params* p, const 
     int* status = at<int>(ws, l.status);
     if (int e = launch_topk(base_logits, p->C * p->L, head->V, p->K, head->dtype, ct, cv, status, s)) return e;
     if (int e = expand_impl(head, p, block_hidden, anchor, ct, cv, sp, ws, l, s)) return e;
-    if (int e = launch_prune(p->C, p->L, p->W, p->B, sp->tok, sp->par, sp->score, sp->n, anchor, tree->tok, tree->par,
-                             tree->depth, tree->score, tree->n_nodes, status, s))
-        return e;
-    if (tree->mask)
-        return launch_mask(p->C, p->L, p->B, tree->par, tree->depth, tree->n_nodes, tree->mask, tree->pos, s);
-    return DARTREE_OK;
+    return finish_tree(p, sp, anchor, tree, status, s);
+}
+
+// Side stream and events per device: the target-row maxima of a round run there,
+// overlapping the build. Created on first use; calls that fork are serialised.
+struct SidePool {
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    bool ok = false;
+};
+static std::mutex g_side_mu;
+static SidePool g_side[64];
+
+static SidePool* side_pool() {  // with g_side_mu held
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    SidePool& sp = g_side[dev];
+    if (!sp.ok) {
+        if (cudaStreamCreateWithFlags(&sp.side, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&sp.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&sp.join, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        sp.ok = true;
+    }
+    return &sp;
+}
+
+int dartree_round(const dartree_head* head, const dartree_params* p, const void* base_logits,
+                  const void* block_hidden, const int32_t* anchor, const void* target, int rows, dartree_tree* tree,
+                  int32_t* accepted_len, int32_t* path, int32_t* bonus, void* ws, size_t ws_bytes, void* stream) {
+    if (!head) return DARTREE_EINVAL;
+    if (int e = check_params(p, head->V, head->H, head->dtype)) return e;
+    if (rows != DARTREE_ROWS_PER_POSITION && rows != DARTREE_ROWS_PER_NODE) return DARTREE_EDTYPE;
+    if (p->C == 0) return DARTREE_OK;
+    if (!head->E || !head->Wq || !base_logits || !block_hidden || !anchor || !target || !tree || !tree->tok ||
+        !tree->par || !tree->depth || !tree->score || !tree->n_nodes || !accepted_len || !path || !bonus)
+        return DARTREE_EINVAL;
+    if ((tree->mask == nullptr) != (tree->pos == nullptr)) return DARTREE_EINVAL;
+    const Layout l = layout_of(*p, head->H, head->dtype);
+    if (int e = check_ws(ws, ws_bytes, l.total)) return e;
+    cudaStream_t s = as_stream(stream);
+    int32_t* ct = at<int32_t>(ws, l.cand_tok);
+    float* cv = at<float>(ws, l.cand_val);
+    const dartree_supertree st{at<int32_t>(ws, l.st_tok), at<int32_t>(ws, l.st_par), at<float>(ws, l.st_s),
+                               at<int32_t>(ws, l.st_n)};
+    int* status = at<int>(ws, l.status);
+    unsigned long long* rowkeys = at<unsigned long long>(ws, l.keys);
+    const bool per_pos = rows == DARTREE_ROWS_PER_POSITION;
+    std::unique_lock<std::mutex> lock(g_side_mu, std::defer_lock);
+    SidePool* side = nullptr;
+    if (per_pos) {
+        lock.lock();
+        side = side_pool();
+        if (side) {
+            if (cudaEventRecord(side->fork, s) != cudaSuccess || cudaStreamWaitEvent(side->side, side->fork, 0) != cudaSuccess)
+                return DARTREE_ECUDA;
+            if (int e = launch_rowmax_position(p->C, p->L, head->V, head->dtype, target, rowkeys, side->side)) return e;
+            if (cudaEventRecord(side->join, side->side) != cudaSuccess) return DARTREE_ECUDA;
+        } else {
+            lock.unlock();
+            if (int e = launch_rowmax_position(p->C, p->L, head->V, head->dtype, target, rowkeys, s)) return e;
+        }
+    }
+    if (int e = launch_topk(base_logits, p->C * p->L, head->V, p->K, head->dtype, ct, cv, status, s)) return e;
+    if (int e = expand_impl(head, p, block_hidden, anchor, ct, cv, &st, ws, l, s)) return e;
+    if (side && cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess) return DARTREE_ECUDA;
+    if (per_pos && finish_supported(p->L, p->W))
+        return launch_finish(p->C, p->L, p->W, p->B, st.tok, st.par, st.score, st.n, anchor, tree->tok, tree->par,
+                             tree->depth, tree->score, tree->n_nodes, tree->mask, tree->pos, rowkeys, accepted_len,
+                             path, bonus, status, s);
+    if (int e = finish_tree(p, &st, anchor, tree, status, s)) return e;
+    if (per_pos)
+        return launch_walk_position(p->C, p->L, p->B, tree->tok, tree->par, tree->depth, tree->n_nodes, rowkeys,
+                                    accepted_len, path, bonus, s);
+    return launch_verify(p->C, p->L, p->B, tree->tok, tree->par, tree->depth, tree->n_nodes, target, rows, head->V,
+                         head->dtype, rowkeys, accepted_len, path, bonus, status, s);
 }
 
 int dartree_verify(const dartree_params* p, const dartree_tree* tree, const void* target, int rows, int V, int dtype,

@@ -395,4 +395,35 @@ __device__ void block_top_keys(const uint64_t* keys, int n, int n_keep, uint64_t
     __syncthreads();
 }
 
+// Bitonic sort, descending, of the 32*EPL keys a warp holds (element lane*EPL + j
+// in register j; EPL a power of two); partners in other lanes come by shuffles.
+template <int EPL>
+__device__ __forceinline__ void warp_bitonic_desc(uint64_t (&v)[EPL]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= 32 * EPL; k <<= 1) {
+#pragma unroll
+        for (int d = k >> 1; d >= 1; d >>= 1) {
+            if (d >= EPL) {
+#pragma unroll
+                for (int j = 0; j < EPL; ++j) {
+                    const int e = lane * EPL + j;
+                    const uint64_t o = shfl_xor_u64(v[j], d / EPL);
+                    const bool keep_max = ((e & d) == 0) == ((e & k) == 0);
+                    v[j] = keep_max ? (v[j] > o ? v[j] : o) : (v[j] < o ? v[j] : o);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < EPL; ++j) {
+                    if ((j & d) == 0) {
+                        const bool desc = ((lane * EPL + j) & k) == 0;
+                        const uint64_t x = v[j], y = v[j | d];
+                        if (desc ? (x < y) : (x > y)) { v[j] = y; v[j | d] = x; }
+                    }
+                }
+            }
+        }
+    }
+}
+
 }  // namespace dartree

@@ -82,6 +82,23 @@ int launch_mask(int C, int L, int B, const int32_t* par, const int32_t* depth, c
                 uint8_t* mask, int32_t* pos, cudaStream_t stream);
 
 // S10: verification.
+// Row maxima (value, ~token) of per-position target rows [C*L, V] (keys zeroed first).
+int launch_rowmax_position(int C, int L, int V, int dtype, const void* target, unsigned long long* keys,
+                           cudaStream_t stream);
+
+// S10 walk over per-position row maxima computed by launch_rowmax_position.
+int launch_walk_position(int C, int L, int B, const int32_t* tok, const int32_t* par, const int32_t* depth,
+                         const int32_t* n_nodes, const unsigned long long* keys, int32_t* accepted, int32_t* path,
+                         int32_t* bonus, cudaStream_t stream);
+
+// S8-S9 (and S10 with per-position row maxima when rowkeys is not null) for one
+// request per CTA; supertrees of at most 256 nodes (finish_supported).
+bool finish_supported(int L, int W);
+int launch_finish(int C, int L, int W, int B, const int32_t* st_tok, const int32_t* st_par, const float* st_s,
+                  const int32_t* st_n, const int32_t* anchor, int32_t* tok, int32_t* par, int32_t* depth,
+                  float* score, int32_t* n_nodes, uint8_t* mask, int32_t* pos, const unsigned long long* rowkeys,
+                  int32_t* accepted, int32_t* path, int32_t* bonus, int* status, cudaStream_t stream);
+
 int launch_verify(int C, int L, int B, const int32_t* tok, const int32_t* par, const int32_t* depth,
                   const int32_t* n_nodes, const void* target, int rows_mode, int V, int dtype,
                   unsigned long long* keys, int32_t* accepted, int32_t* path, int32_t* bonus, int* status,

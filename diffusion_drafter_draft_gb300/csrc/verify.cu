@@ -163,6 +163,37 @@ __global__ void __launch_bounds__(WK_NT) walk_node_kernel(int L, int B, int V, i
 
 // ----------------------------------------------------------------------------- host
 
+// Row maxima of per-position target rows [C*L, V] into keys (value, ~token).
+template <typename T>
+static int launch_rowmax_t(int rows, int V, const void* target, unsigned long long* keys, cudaStream_t stream) {
+    if (cudaMemsetAsync(keys, 0, size_t(rows) * sizeof(unsigned long long), stream) != cudaSuccess)
+        return DARTREE_ECUDA;
+    int splits = (2 * num_sms() + rows - 1) / rows;
+    const int min_seg = 4096;
+    if (splits > (V + min_seg - 1) / min_seg) splits = (V + min_seg - 1) / min_seg;
+    if (splits < 1) splits = 1;
+    int seg = (V + splits - 1) / splits;
+    seg = (seg + 7) / 8 * 8;
+    splits = (V + seg - 1) / seg;
+    rowmax_kernel<T><<<dim3(splits, rows), RM_NT, 0, stream>>>(static_cast<const T*>(target), V, seg, keys);
+    return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
+}
+
+int launch_walk_position(int C, int L, int B, const int32_t* tok, const int32_t* par, const int32_t* depth,
+                         const int32_t* n_nodes, const unsigned long long* keys, int32_t* accepted, int32_t* path,
+                         int32_t* bonus, cudaStream_t stream) {
+    if (C == 0) return DARTREE_OK;
+    walk_position_kernel<<<C, 32, 0, stream>>>(L, B, tok, par, depth, n_nodes, keys, accepted, path, bonus);
+    return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
+}
+
+int launch_rowmax_position(int C, int L, int V, int dtype, const void* target, unsigned long long* keys,
+                           cudaStream_t stream) {
+    if (C == 0) return DARTREE_OK;
+    return dtype == DARTREE_BF16 ? launch_rowmax_t<bf16_t>(C * L, V, target, keys, stream)
+                                 : launch_rowmax_t<float>(C * L, V, target, keys, stream);
+}
+
 template <typename T>
 static int launch_verify_t(int C, int L, int B, const int32_t* tok, const int32_t* par, const int32_t* depth,
                            const int32_t* n_nodes, const void* target, int rows_mode, int V,
@@ -170,17 +201,7 @@ static int launch_verify_t(int C, int L, int B, const int32_t* tok, const int32_
                            cudaStream_t stream) {
     const T* tg = static_cast<const T*>(target);
     if (rows_mode == DARTREE_ROWS_PER_POSITION) {
-        const int rows = C * L;
-        if (cudaMemsetAsync(keys, 0, size_t(rows) * sizeof(unsigned long long), stream) != cudaSuccess)
-            return DARTREE_ECUDA;
-        int splits = (2 * num_sms() + rows - 1) / rows;
-        const int min_seg = 4096;
-        if (splits > (V + min_seg - 1) / min_seg) splits = (V + min_seg - 1) / min_seg;
-        if (splits < 1) splits = 1;
-        int seg = (V + splits - 1) / splits;
-        seg = (seg + 7) / 8 * 8;
-        splits = (V + seg - 1) / seg;
-        rowmax_kernel<T><<<dim3(splits, rows), RM_NT, 0, stream>>>(tg, V, seg, keys);
+        if (int e = launch_rowmax_t<T>(C * L, V, target, keys, stream)) return e;
         walk_position_kernel<<<C, 32, 0, stream>>>(L, B, tok, par, depth, n_nodes, keys, accepted, path, bonus);
         return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
     }

@@ -196,6 +196,21 @@ DARTREE_API int dartree_verify(const dartree_params* p, const dartree_tree* tree
                    int rows, int V, int dtype, int32_t* accepted_len, int32_t* path,
                    int32_t* bonus, void* ws, size_t ws_bytes, void* stream);
 
+/* S1-S10 in one call: dartree_build_tree (no supertree or candidate outputs)
+ * followed by dartree_verify, with the same results as those two calls.
+ * target, rows: as for dartree_verify, with V and dtype of the head. With
+ * per-position rows the target-row maxima do not depend on the tree, so they are
+ * computed on a library-owned side stream (one per device, created on the first
+ * call; make that call before any stream capture) forked from `stream` and
+ * joined before the walk; the fork is captured with the rest when `stream` is
+ * being captured into a CUDA graph. Calls are serialised on the host while they
+ * enqueue. The row maxima go to a workspace region of their own (the workspace of
+ * dartree_workspace_bytes suffices). Errors as for the two calls. */
+DARTREE_API int dartree_round(const dartree_head* head, const dartree_params* p, const void* base_logits,
+                              const void* block_hidden, const int32_t* anchor, const void* target, int rows,
+                              dartree_tree* tree, int32_t* accepted_len, int32_t* path, int32_t* bonus,
+                              void* ws, size_t ws_bytes, void* stream);
+
 /* S10 without a workspace, for callers that cannot allocate device memory where
  * they verify (for example a serving loop whose caching allocator holds all free
  * HBM, or a plugin behind a plain C interface with no allocator handle). The

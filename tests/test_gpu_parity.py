@@ -169,3 +169,38 @@ def test_stress_batch_sampled_requests():
     gv = host(dd.verify(tr, t(tgt, cfg.dtype), dd.ROWS_PER_NODE, cfg.L))
     gvs = {k: v[sample] for k, v in gv.items()}
     compare_verify(o, gvs, tgt[sample], cfg, "node")
+
+
+@pytest.mark.parametrize("name,C,rows", [("cfg1_qwen3_4b_c1", None, "position"), ("cfg3_c4_adaptive", None, "position"),
+                                         ("cfg0_tiny", 3, "position"), ("cfg2_qwen3_8b_fixed", 2, "node"),
+                                         ("cfg4_c64_stress", 4, "node"), ("cfg4_c64_stress", 3, "position")])
+def test_round_entry_point(name, C, rows):
+    """dartree_round (row maxima on a side stream, fused finish kernel) gives the
+    same tree and verification as dartree_build_tree + dartree_verify, and that
+    tree matches the oracle."""
+    import diffusion_drafter_draft_gb300 as dd
+    cfg = make_config(name)
+    if C:
+        cfg = cfg.replace(C=C)
+    cfg = cfg.replace(rows=rows)
+    inp = make_inputs(cfg)
+    x = upload(inp)
+    if rows == "node":
+        depths = np.broadcast_to(breadth_first_slot_depth(cfg), (cfg.C, cfg.B + 1)).copy()
+        x["target"] = t(make_target_per_node(cfg, inp, depths), cfg.dtype)
+    mode = dd.ROWS_PER_POSITION if rows == "position" else dd.ROWS_PER_NODE
+    rnd = dd.Round(x["E"], x["Wq"], cfg.C, cfg.L, cfg.K, cfg.W, cfg.B, cfg.beta, mode)
+    a = {k: v.clone() for k, v in rnd.run(x["base"], x["hidden"], x["anchor"], x["target"]).items()}
+    ta = {k: v.clone() for k, v in rnd.tree.items()}
+    b = {k: v.clone() for k, v in rnd.run_two_calls(x["base"], x["hidden"], x["anchor"], x["target"]).items()}
+    tb = {k: v.clone() for k, v in rnd.tree.items()}
+    torch.cuda.synchronize()
+    assert dd.read_status(rnd.ws) == 0
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+    for k in ta:
+        assert torch.equal(ta[k], tb[k]), k
+    g, _ = run_gpu_build(inp, dev_inputs=x)
+    compare_build(inp, g)
+    for k in ("tok", "par", "depth", "n_nodes", "mask", "pos"):
+        np.testing.assert_array_equal(host(ta[k]), g[k], err_msg=k)
