@@ -4,11 +4,12 @@
 // and position ids (3.2), and, with per-position target rows, the greedy
 // longest accepted prefix (3.2).
 //
-// The supertree's keys (score desc, depth asc, rank asc) are sorted by one warp
-// (bitonic, 8 keys per lane); the B-th key is the threshold and the chosen nodes
-// take slots in (depth, rank) order by a block scan. Tree arrays, ancestor table
-// and mask are built in shared memory, and the walk follows the row maxima
-// computed beforehand (on a side stream, overlapping the build).
+// Every supertree node's global rank under (score desc, depth asc, rank asc) is
+// counted against all keys in shared memory (broadcast reads); the nodes of rank
+// below B are chosen and take slots in (depth, rank) order by a block scan. Tree
+// arrays, ancestor table and mask are built in shared memory, and the walk
+// follows the row maxima computed beforehand (on a side stream, overlapping the
+// build), read into shared memory first.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -17,7 +18,7 @@ namespace dartree {
 constexpr int FN_NT = 256;  // one supertree node per thread
 
 struct FnSmem {
-    size_t keys, slot, ttok, tpar, tdep, anc, wtot, misc, bytes;
+    size_t keys, slot, ttok, tpar, tdep, anc, rowk, next, wtot, misc, bytes;
 };
 __host__ __device__ inline FnSmem fn_smem(int L, int B) {
     const size_t S = size_t(B) + 1;
@@ -30,6 +31,8 @@ __host__ __device__ inline FnSmem fn_smem(int L, int B) {
     f.tpar = take(S * 4);
     f.tdep = take(S * 4);
     f.anc = take(S * (size_t(L) + 1) * 2);
+    f.rowk = take(size_t(L) * 8);
+    f.next = take(S * 4);
     f.wtot = take(32 * 4);
     f.misc = take(16);
     f.bytes = o;
@@ -57,7 +60,9 @@ __global__ void __launch_bounds__(FN_NT) finish_kernel(int L, int W, int B, cons
     int* tdep = reinterpret_cast<int*>(smem + fl.tdep);
     int16_t* anc = reinterpret_cast<int16_t*>(smem + fl.anc);
     int* wtot = reinterpret_cast<int*>(smem + fl.wtot);
-    int* misc = reinterpret_cast<int*>(smem + fl.misc);  // [0] scan total, [2..3] threshold
+    int* misc = reinterpret_cast<int*>(smem + fl.misc);  // [0] scan total
+    uint64_t* rowk = reinterpret_cast<uint64_t*>(smem + fl.rowk);
+    int* next = reinterpret_cast<int*>(smem + fl.next);  // accepted child of every slot, or INT_MAX
     const int r = blockIdx.x, n = L * W, S = B + 1, q = threadIdx.x;
     const int lane = q & 31, wid = q >> 5;
     const size_t base = size_t(r) * L * W;
@@ -78,23 +83,22 @@ __global__ void __launch_bounds__(FN_NT) finish_kernel(int L, int W, int B, cons
         }
     }
     keys[q] = key;
+    if (WALK)
+        for (int d = q; d < L; d += FN_NT) rowk[d] = rowkeys[size_t(r) * L + d];
     const int nv = __syncthreads_count(key != 0);
     const int N = min(B, nv);
-    // ---- threshold: the N-th largest key (warp 0 sorts all 256)
-    if (wid == 0) {
-        uint64_t v[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = keys[lane * 8 + j];
-        warp_bitonic_desc<8>(v);
-        if (N > 0 && lane == (N - 1) / 8) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (j == (N - 1) % 8) *reinterpret_cast<uint64_t*>(misc + 2) = v[j];
+    // ---- global rank: keys above this one (all threads read the same pair at once)
+    int above = 0;
+    {
+        const ulonglong2* k2 = reinterpret_cast<const ulonglong2*>(keys);
+        const int n2 = (n + 1) / 2;
+#pragma unroll 4
+        for (int i = 0; i < n2; ++i) {
+            const ulonglong2 v = k2[i];
+            above += (v.x > key) + (v.y > key);
         }
     }
-    __syncthreads();
-    const uint64_t thr = N > 0 ? *reinterpret_cast<const uint64_t*>(misc + 2) : ~0ull;
-    const bool ch = key != 0 && key >= thr;
+    const bool ch = key != 0 && above < N;
     // ---- slots in (depth, rank) order
     const int ex = block_exclusive_scan<FN_NT>(ch ? 1 : 0, wtot, misc);
     const int chosen = misc[0];
@@ -153,14 +157,18 @@ __global__ void __launch_bounds__(FN_NT) finish_kernel(int L, int W, int B, cons
         const int total = S * S;
         for (int e = q * 4; e < total; e += FN_NT * 4) {
             uint32_t word = 0;
+            const int i0 = e / S;
+            int i = i0, j = e - i0 * S;  // (row, column) of byte e, then stepped
+            const int di = i < nn ? tdep[i] : -1;
+            const int di2 = i + 1 < nn ? tdep[i + 1] : -1;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int x = e + u;
-                if (x >= total) break;
-                const int i = x / S, j = x % S;
-                const int di = i < nn ? tdep[i] : -1, dj = j < nn ? tdep[j] : -1;
-                const bool on = di >= 0 && dj >= 0 && dj <= di && anc[size_t(i) * (L + 1) + dj] == j;
+                if (e + u >= total) break;
+                const int dii = i == i0 ? di : di2;
+                const int dj = j < nn ? tdep[j] : -1;
+                const bool on = dii >= 0 && dj >= 0 && dj <= dii && anc[size_t(i) * (L + 1) + dj] == j;
                 word |= uint32_t(on) << (8 * u);
+                if (++j == S) { j = 0; ++i; }
             }
             if (e + 4 <= total && (reinterpret_cast<uintptr_t>(m + e) & 3) == 0) {
                 *reinterpret_cast<uint32_t*>(m + e) = word;
@@ -169,27 +177,35 @@ __global__ void __launch_bounds__(FN_NT) finish_kernel(int L, int W, int B, cons
             }
         }
     }
-    // ---- greedy walk with per-position row maxima
-    if (WALK && wid == 0) {
-        int cur = 0, acc = 0, bon = -1;
-        for (int step = 0; step <= L; ++step) {
-            const int d = tdep[cur];
-            if (d < 0 || d >= L) break;
-            const int t = int(0xffffffffu - uint32_t(rowkeys[size_t(r) * L + d]));
-            int found = -1;
-            for (int j0 = 1; j0 < nn && found < 0; j0 += 32) {
-                const int j = j0 + lane;
-                const bool hit = j < nn && tpar[j] == cur && ttok[j] == t;
-                const uint32_t b = __ballot_sync(0xffffffffu, hit);
-                if (b) found = j0 + __ffs(b) - 1;
-            }
-            if (found < 0) { bon = t; break; }
-            if (lane == 0 && acc < L) path[size_t(r) * L + acc] = found;
-            ++acc;
-            cur = found;
+    // ---- greedy walk with per-position row maxima: every slot's accepted child
+    //      (the lowest slot whose parent it is and whose token is the argmax of
+    //      the parent's row) in parallel, then one thread follows the chain
+    if (WALK) {
+        for (int j = q; j < S; j += FN_NT) next[j] = 0x7fffffff;
+        __syncthreads();
+        for (int j = 1 + q; j < nn; j += FN_NT) {
+            const int p = tpar[j];
+            const int dp = (p >= 0 && p < nn) ? tdep[p] : -1;
+            if (dp >= 0 && dp < L && ttok[j] == int(0xffffffffu - uint32_t(rowk[dp]))) atomicMin(&next[p], j);
         }
-        for (int u = acc + lane; u < L; u += 32) path[size_t(r) * L + u] = -1;
-        if (lane == 0) { accepted[r] = acc; bonus[r] = bon; }
+        __syncthreads();
+        if (q == 0) {
+            int cur = 0, acc = 0, bon = -1;
+            for (int step = 0; step <= L; ++step) {
+                const int d = tdep[cur];
+                if (d < 0 || d >= L) break;
+                const int f = next[cur];
+                if (f == 0x7fffffff) { bon = int(0xffffffffu - uint32_t(rowk[d])); break; }
+                if (acc < L) path[size_t(r) * L + acc] = f;
+                ++acc;
+                cur = f;
+            }
+            accepted[r] = acc;
+            bonus[r] = bon;
+            misc[1] = acc;
+        }
+        __syncthreads();
+        for (int u = misc[1] + q; u < L; u += FN_NT) path[size_t(r) * L + u] = -1;
     }
 }
 
