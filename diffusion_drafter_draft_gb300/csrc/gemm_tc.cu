@@ -5,7 +5,8 @@
 //   D[M, N] = A[M, K] . B[N, K]^T, A and B bf16 K-major, fp32 accumulation in TMEM.
 //
 // One 128 x BN tile per CTA (cta_group::1). Warp 0's elected thread streams
-// 128 x 64 and BN x 64 tiles with TMA (128-byte swizzle) into a 4-stage ring;
+// 128 x 64 and BN x 64 tiles with TMA (128-byte swizzle) into a ring of as many
+// stages as shared memory holds (4 for BN = 256, 6 for BN = 160 or 128);
 // warp 1's elected thread issues tcgen05.mma (4 per 64-wide k block) and
 // releases each stage with tcgen05.commit; all 4 warps then read the
 // accumulator from TMEM (one row per thread) and write the epilogue:
@@ -24,7 +25,7 @@
 
 namespace dartree {
 
-constexpr int GT_BM = 128, GT_BK = 64, GT_STAGES = 4, GT_NT = 128;
+constexpr int GT_BM = 128, GT_BK = 64, GT_NT = 128;
 
 struct GemmOut {
     int mode;          // 0: fp32 d32; 1: hi/lo bf16 pairs into hilo (row remap); 2: hi -> hilo, lo -> lo2
@@ -38,10 +39,13 @@ template <int BN>
 struct GtSmem {
     static constexpr size_t A_BYTES = size_t(GT_BM) * GT_BK * 2;
     static constexpr size_t B_BYTES = size_t(BN) * GT_BK * 2;
-    static constexpr size_t STAGE = A_BYTES + B_BYTES;
-    static constexpr size_t BAR = STAGE * GT_STAGES;       // full[S], empty[S], accum
-    static constexpr size_t SLOT = BAR + 8 * (2 * GT_STAGES + 1);
+    static constexpr size_t STAGE = A_BYTES + B_BYTES;      // a multiple of 1024 (swizzle atoms)
+    // as many stages as fit next to the barriers (more bytes in flight per SM)
+    static constexpr int STAGES = int((220 * 1024) / STAGE) > 8 ? 8 : int((220 * 1024) / STAGE);
+    static constexpr size_t BAR = STAGE * STAGES;          // full[S], empty[S], accum
+    static constexpr size_t SLOT = BAR + 8 * (2 * STAGES + 1);
     static constexpr size_t TOTAL = SLOT + 16 + 1024;      // + alignment slack
+    static constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
 };
 
 __device__ __forceinline__ uint16_t bf16_rn_bits(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
@@ -54,19 +58,19 @@ __global__ void __launch_bounds__(GT_NT, 1) gemm_bf16_tc_kernel(const __grid_con
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     using L = GtSmem<BN>;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR);
-    uint64_t* empty = full + GT_STAGES;
-    uint64_t* accum = empty + GT_STAGES;
+    uint64_t* empty = full + L::STAGES;
+    uint64_t* accum = empty + L::STAGES;
     uint32_t* slot = reinterpret_cast<uint32_t*>(smem + L::SLOT);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * GT_BM, n0 = blockIdx.x * BN;
     const int nk = (K + GT_BK - 1) / GT_BK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < GT_STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int s = 0; s < L::STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         mbar_init(accum, 1);
         fence_mbar_init();
     }
-    if (warp == 0) tc::tmem_alloc(slot, BN);
+    if (warp == 0) tc::tmem_alloc(slot, L::TMEM_COLS);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -75,8 +79,8 @@ __global__ void __launch_bounds__(GT_NT, 1) gemm_bf16_tc_kernel(const __grid_con
     if (warp == 0 && lane == 0) {
         // producer: TMA ring
         for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % GT_STAGES;
-            const uint32_t ph = uint32_t(kb / GT_STAGES) & 1u;
+            const int s = kb % L::STAGES;
+            const uint32_t ph = uint32_t(kb / L::STAGES) & 1u;
             if (!mbar_wait_bounded(&empty[s], ph ^ 1u, status)) break;
             uint8_t* sa = smem + s * L::STAGE;
             mbar_arrive_expect_tx(&full[s], uint32_t(L::STAGE));
@@ -88,8 +92,8 @@ __global__ void __launch_bounds__(GT_NT, 1) gemm_bf16_tc_kernel(const __grid_con
         constexpr uint32_t idesc = tc::idesc_bf16_f32(GT_BM, BN);
         bool ok = true;
         for (int kb = 0; kb < nk && ok; ++kb) {
-            const int s = kb % GT_STAGES;
-            const uint32_t ph = uint32_t(kb / GT_STAGES) & 1u;
+            const int s = kb % L::STAGES;
+            const uint32_t ph = uint32_t(kb / L::STAGES) & 1u;
             if (!mbar_wait_bounded(&full[s], ph, status)) { ok = false; break; }
             tc::fence_after_sync();
             const uint32_t sa = smem_u32(smem + s * L::STAGE);
@@ -145,7 +149,7 @@ __global__ void __launch_bounds__(GT_NT, 1) gemm_bf16_tc_kernel(const __grid_con
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, BN);
+    if (warp == 0) tc::tmem_dealloc(tmem, L::TMEM_COLS);
 }
 
 // --------------------------------------------------------------------------- host
@@ -213,8 +217,19 @@ int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int m
     if (mode == 0 && !d32) return DARTREE_EINVAL;
     if (mode == 2 && (!hilo || !lo2)) return DARTREE_EINVAL;
     GemmOut o{mode, d32, hilo, lo2, P};
-    // wider tiles halve the L2 traffic of the operand both tile rows share
-    if (N % 256 == 0) return launch_gemm_bn<256>(A, B, M, N, K, o, status, stream);
+    // Tile width: the operand bytes a CTA streams per k block (its ingest time)
+    // times the number of waves of CTAs over the SMs, smallest wins.
+    const int mt = (M + GT_BM - 1) / GT_BM, sms = num_sms();
+    int best = 128;
+    long best_cost = -1;
+    for (int bn : {256, 160, 128}) {
+        if (N % bn != 0) continue;
+        const long tiles = long(mt) * (N / bn), waves = (tiles + sms - 1) / sms;
+        const long cost = waves * (GT_BM + bn);
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = bn; }
+    }
+    if (best == 256) return launch_gemm_bn<256>(A, B, M, N, K, o, status, stream);
+    if (best == 160) return launch_gemm_bn<160>(A, B, M, N, K, o, status, stream);
     return launch_gemm_bn<128>(A, B, M, N, K, o, status, stream);
 }
 

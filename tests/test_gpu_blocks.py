@@ -21,7 +21,9 @@ def dd():
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 64), (1, 128, 64), (200, 256, 200), (64, 4096, 4096),
-                                   (768, 512, 4096), (300, 384, 2560)])
+                                   (768, 512, 4096), (300, 384, 2560),
+                                   # 128 x 160 tiles with a 6-stage ring (one wave of 128 CTAs)
+                                   (1024, 2560, 512), (1001, 2560, 136)])
 def test_tcgen05_gemm_matches_float64(dd, M, N, K):
     g = torch.Generator().manual_seed(M * 7 + N + K)
     A = torch.randn(M, K, generator=g).to(torch.bfloat16)
