@@ -429,6 +429,214 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
         for (int p = 0; p < npieces; ++p) mbar_wait_bounded(&mbar[p], 0, nullptr);
 }
 
+// --------------------------------------------------------------------------- many rows: one CTA per row
+
+// With at least two rows per SM, one CTA per row reads its row once with 16-byte
+// vector loads, several in flight per thread, and needs no cluster barrier:
+//   1. every thread keeps the 4 largest maxima of the vectors it reads (a
+//      branch-free min/max network), and the 16-bit maximum of every 32-byte
+//      group of the row goes to shared memory; the largest c such that
+//      ceil(K/4) threads hold a 4th-largest vector maximum >= c (a bitwise
+//      search with __syncthreads_count) has at least K elements >= c: that
+//      many threads each read 4 vectors holding an element >= c;
+//   2. only the groups whose maximum reaches c (a few percent) are read again
+//      and their elements >= c written to a candidate buffer at block-scan
+//      offsets;
+//   3. exactly the K best are selected (radix) and sorted as in the cluster
+//      kernel. More than TS_CAP candidates (heavy ties) take the exact radix
+//      select over the row instead.
+// Four CTAs share an SM.
+constexpr int TS_NT = 256;
+constexpr int TS_UNROLL = 8;    // vector loads in flight per thread
+constexpr int TS_CAP = 2048;    // candidate keys
+
+struct TsSmem {
+    size_t gmax, cand, fb, hist, hsum, misc, wtot, total;
+};
+// nvec: 16-byte vectors per row (two per group)
+__host__ __device__ inline TsSmem ts_smem(int nvec) {
+    TsSmem s{};
+    size_t o = 0;
+    auto take = [&](size_t b, size_t a) { o = align_up(o, a); size_t at = o; o += b; return at; };
+    s.gmax = take(size_t((nvec + 1) / 2) * 2, 16);
+    s.cand = take(size_t(TS_CAP) * 8, 16);
+    s.fb = take(size_t(TK_FB) * 8, 16);
+    s.hist = take(2 * 256 * 4, 16);
+    s.hsum = take(256 * 4, 16);
+    s.misc = take(64 * 4, 16);
+    s.wtot = take(32 * 4, 16);
+    s.total = o;
+    return s;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(TS_NT, 4) topk_stream_kernel(const T* __restrict__ x, int V, int K,
+                                                            int32_t* __restrict__ out_tok,
+                                                            float* __restrict__ out_val, int* status) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr int VEC = ValueKey<T>::VEC;
+    constexpr int KBITS = ValueKey<T>::BITS;
+    const int nvec = int(size_t(V) * sizeof(T) / 16);
+    const TsSmem L = ts_smem(nvec);
+    uint16_t* gmax = reinterpret_cast<uint16_t*>(smem + L.gmax);  // 16-bit key maximum of vectors 2g, 2g + 1
+    uint64_t* cand = reinterpret_cast<uint64_t*>(smem + L.cand);
+    uint64_t* fb = reinterpret_cast<uint64_t*>(smem + L.fb);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L.hist);
+    uint32_t* hsum = reinterpret_cast<uint32_t*>(smem + L.hsum);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L.misc);
+    int* wtot = reinterpret_cast<int*>(smem + L.wtot);
+    const int row = blockIdx.x;
+    const T* src = x + size_t(row) * V;
+    const uint4* rv = reinterpret_cast<const uint4*>(src);
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x < 64) misc[threadIdx.x] = 0;
+    __syncthreads();
+    // ---- pass 1: vectors t, t + NT, ... (TS_UNROLL loads issued before any is
+    //      used): the thread's 4 largest vector maxima and the group maxima
+    uint32_t t0 = 0, t1 = 0, t2 = 0, t3 = 0;
+    auto insert = [&](uint32_t vm) {  // t0 >= t1 >= t2 >= t3: the 4 largest vector maxima
+        t3 = max(t3, min(t2, vm));
+        t2 = max(t2, min(t1, vm));
+        t1 = max(t1, min(t0, vm));
+        t0 = max(t0, vm);
+    };
+    constexpr int SHIFT16 = KBITS - 16;  // 16-bit group keys: the top bits of the key
+    // lanes 2i and 2i+1 hold the two vectors of one group (v = base + lane, base even)
+    auto group_max = [&](int v, uint32_t vm, bool valid) {
+        uint32_t g16 = valid ? (vm >> SHIFT16) : 0u;
+        g16 = max(g16, __shfl_xor_sync(0xffffffffu, g16, 1));
+        if ((lane & 1) == 0 && v < nvec) gmax[v >> 1] = uint16_t(g16);
+    };
+    {
+        int v0 = int(threadIdx.x) & ~31;  // warp-uniform trip counts (group maxima use shuffles)
+        for (; v0 + (TS_UNROLL - 1) * TS_NT < nvec; v0 += TS_UNROLL * TS_NT) {
+            uint4 w[TS_UNROLL];
+            bool ok[TS_UNROLL];
+#pragma unroll
+            for (int u = 0; u < TS_UNROLL; ++u) {
+                const int v = v0 + lane + u * TS_NT;
+                ok[u] = v < nvec;
+                w[u] = ok[u] ? __ldg(rv + v) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < TS_UNROLL; ++u) {
+                const uint32_t vm = ok[u] ? vec_max_ord(w[u], static_cast<T*>(nullptr)) : 0u;
+                insert(vm);
+                group_max(v0 + lane + u * TS_NT, vm, ok[u]);
+            }
+        }
+        for (; v0 < nvec; v0 += TS_NT) {
+            const int v = v0 + lane;
+            const bool ok = v < nvec;
+            const uint4 w = ok ? __ldg(rv + v) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t vm = ok ? vec_max_ord(w, static_cast<T*>(nullptr)) : 0u;
+            insert(vm);
+            group_max(v, vm, ok);
+        }
+    }
+    // ---- lower bound: largest c with at least ceil(K/4) threads' 4th-largest
+    //      vector maximum >= c
+    const int j4 = (K + 3) / 4;
+    uint32_t c = 0;
+    for (int b = KBITS - 1; b >= 0; --b) {
+        const uint32_t trial = c | (1u << b);
+        if (__syncthreads_count(t3 >= trial) >= j4) c = trial;
+    }
+    // ---- pass 2: only the groups whose maximum reaches c are read again (gmax is
+    //      complete: the bound's barriers follow pass 1). Their indices are placed
+    //      in fb by a block scan; then every thread counts the elements >= c of
+    //      its hit groups (two groups' loads in flight), a second scan gives the
+    //      offsets, and the same groups (now in L1) are read once more to write
+    //      the candidate keys.
+    const uint32_t c16 = c >> SHIFT16;
+    const int ngroups = (nvec + 1) / 2;
+    int nh = 0;
+    for (int g = threadIdx.x; g < ngroups; g += TS_NT) nh += uint32_t(gmax[g]) >= c16;
+    const int hx = block_exclusive_scan<TS_NT>(nh, wtot, reinterpret_cast<int*>(&misc[4]));
+    const int nhits = int(misc[4]);
+    uint32_t* hits = reinterpret_cast<uint32_t*>(fb);
+    constexpr int TS_HITCAP = TK_FB * 2;  // u32 entries of fb
+    const bool hits_fit = nhits <= TS_HITCAP;
+    if (hits_fit) {
+        int o = hx;
+        for (int g = threadIdx.x; g < ngroups; g += TS_NT)
+            if (uint32_t(gmax[g]) >= c16) hits[o++] = uint32_t(g);
+    }
+    __syncthreads();
+    // f(vector index, vector) over the vectors of this thread's hit groups
+    auto over_hits = [&](auto&& f) {
+        for (int h = threadIdx.x; h < nhits; h += 2 * TS_NT) {
+            const int h2 = h + TS_NT;
+            const int va = 2 * int(hits[h]), vb = h2 < nhits ? 2 * int(hits[h2]) : -1;
+            const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+            const uint4 w0 = __ldg(rv + va);
+            const uint4 w1 = va + 1 < nvec ? __ldg(rv + va + 1) : zero;
+            const uint4 w2 = vb >= 0 ? __ldg(rv + vb) : zero;
+            const uint4 w3 = (vb >= 0 && vb + 1 < nvec) ? __ldg(rv + vb + 1) : zero;
+            f(va, w0);
+            if (va + 1 < nvec) f(va + 1, w1);
+            if (vb >= 0) {
+                f(vb, w2);
+                if (vb + 1 < nvec) f(vb + 1, w3);
+            }
+        }
+    };
+    int cnt = 0;
+    if (hits_fit)
+        over_hits([&](int, uint4 w) {
+            if (vec_max_ord(w, static_cast<T*>(nullptr)) < c) return;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) cnt += vec_elem_ord(w, e, static_cast<T*>(nullptr)) >= c;
+        });
+    const int excl = block_exclusive_scan<TS_NT>(cnt, wtot, reinterpret_cast<int*>(&misc[0]));
+    const uint32_t total = hits_fit ? misc[0] : 0xffffffffu;
+    if (total <= uint32_t(TS_CAP)) {
+        uint32_t pos = uint32_t(excl);
+        over_hits([&](int vi, uint4 w) {
+            if (vec_max_ord(w, static_cast<T*>(nullptr)) < c) return;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const uint32_t o = vec_elem_ord(w, e, static_cast<T*>(nullptr));
+                if (o >= c) cand[pos++] = (uint64_t(o) << 32) | (0xffffffffu - uint32_t(vi * VEC + e));
+            }
+        });
+    }
+    __syncthreads();
+    if (total >= uint32_t(K) && total <= uint32_t(TS_CAP)) {
+        uint64_t prefix = 0, mask = 0;
+        uint64_t* orand = reinterpret_cast<uint64_t*>(hsum);
+        const bool ok = block_select_top_agg<TS_NT>(cand, int(total), K, hist, misc + 32, orand, prefix, mask);
+        if (threadIdx.x == 0) { misc[40] = 0; if (!ok) set_status(status, DARTREE_EINTERNAL); }
+        __syncthreads();
+        for (int i = threadIdx.x; i < int(total); i += TS_NT) {
+            const uint64_t k = cand[i];
+            if (ok && selected(k, prefix, mask)) {
+                const uint32_t q = atomicAdd(&misc[40], 1u);
+                if (q < uint32_t(K)) fb[q] = k;
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0 && misc[40] != uint32_t(K)) set_status(status, DARTREE_EINTERNAL);
+        for (int i = min(int(misc[40]), K) + threadIdx.x; i < K; i += TS_NT) fb[i] = 0;
+    } else {
+        // heavy ties: exact radix select over the row read from global memory
+        // (a one-CTA cluster)
+        if (!topk_exact_fallback<T>(src, V, 0, K, 1u, 0u, hist, hsum, misc, wtot, fb))
+            if (threadIdx.x == 0) set_status(status, DARTREE_EINTERNAL);
+    }
+    int kp = 1;
+    while (kp < K) kp <<= 1;
+    for (int i = K + threadIdx.x; i < kp; i += TS_NT) fb[i] = 0;
+    __syncthreads();
+    sort_desc<TS_NT>(fb, kp);
+    for (int i = threadIdx.x; i < K; i += TS_NT) {
+        const uint64_t k = fb[i];
+        out_tok[size_t(row) * K + i] = int32_t(0xffffffffu - uint32_t(k));
+        out_val[size_t(row) * K + i] = ValueKey<T>::value(uint32_t(k >> 32));
+    }
+}
+
 // --------------------------------------------------------------------------- host side
 
 static int g_num_sms = 0;
@@ -499,9 +707,43 @@ static int launch_topk_t(const void* x, int rows, int V, int K, int32_t* tok, fl
     return e == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 
+template <typename T>
+static int launch_topk_stream(const void* x, int rows, int V, int K, int32_t* tok, float* val, int* status,
+                              cudaStream_t stream) {
+    const TsSmem L = ts_smem(int(size_t(V) * sizeof(T) / 16));
+    auto kern = topk_stream_kernel<T>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.total)) != cudaSuccess)
+        return DARTREE_ECUDA;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(unsigned(rows));
+    cfg.blockDim = dim3(TS_NT);
+    cfg.dynamicSmemBytes = L.total;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];  // a one-CTA cluster: the exact fallback uses cluster barriers
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const T*>(x), V, K, tok, val, status);
+    // (rows are read with plain vector loads: 16-byte aligned rows)
+    return e == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
+}
+
+// One CTA per row once the rows cover the SMs twice and every row starts on a
+// 16-byte boundary; else one cluster per row.
+static bool use_stream(const void* x, int rows, int V, int K, int elem) {
+    return rows >= 2 * num_sms() && K <= 4 * TS_NT && reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
+           (size_t(V) * elem) % 16 == 0;
+}
+
 int launch_topk(const void* x, int rows, int V, int K, int dtype, int32_t* tok, float* val, int* status,
                 cudaStream_t stream) {
     if (rows == 0) return DARTREE_OK;
+    if (use_stream(x, rows, V, K, dtype == DARTREE_BF16 ? 2 : 4))
+        return dtype == DARTREE_BF16 ? launch_topk_stream<bf16_t>(x, rows, V, K, tok, val, status, stream)
+                                     : launch_topk_stream<float>(x, rows, V, K, tok, val, status, stream);
     if (dtype == DARTREE_BF16) return launch_topk_t<bf16_t>(x, rows, V, K, tok, val, status, stream);
     return launch_topk_t<float>(x, rows, V, K, tok, val, status, stream);
 }

@@ -63,6 +63,25 @@ def test_topk_matches_oracle(dtype, rows, V, K, kind):
         np.testing.assert_array_equal(val[r], ev.astype(np.float32))
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,V,K,kind", [(320, 151936, 512, "gauss"), (320, 151936, 512, "const"),
+                                           (304, 151936, 64, "ties"), (400, 4104, 100, "gauss"),
+                                           (400, 4104, 100, "peaks"), (400, 4104, 1024, "ties")])
+def test_topk_many_rows(dtype, rows, V, K, kind):
+    """At least two rows per SM: one CTA per row streams its row twice (heavy
+    ties take the exact radix fallback). Rows are independent, so a sample of
+    rows is checked against the oracle."""
+    import diffusion_drafter_draft_gb300 as dd
+    x = _topk_case(rows, V, K, dtype, kind, seed=rows + V + K)
+    tok, val = dd.topk(t(x, dtype), K)
+    tok, val = host(tok), host(val)
+    xf = to_f64(x, dtype)
+    for r in sorted(set(range(0, rows, max(1, rows // 24))) | {rows - 1}):
+        et, ev = oracle.topk_candidates(xf[r], K)
+        np.testing.assert_array_equal(tok[r], et)
+        np.testing.assert_array_equal(val[r], ev.astype(np.float32))
+
+
 # --------------------------------------------------------------------------- S8 / S9 / S10 on oracle intermediates
 
 @pytest.mark.parametrize("name", ["cfg0_tiny", "cfg3_c4_adaptive"])
