@@ -25,7 +25,7 @@ OK, EINVAL, EDTYPE, EWORKSPACE, ECUDA, ETIMEOUT, EINTERNAL, EUNSUPPORTED = 0, -1
 EXPORTS = ("dartree_head_init", "dartree_workspace_bytes", "dartree_topk", "dartree_expand", "dartree_prune",
            "dartree_tree_mask", "dartree_build_tree", "dartree_verify", "dartree_read_status",
            "dartree_clear_status", "dartree_status_string", "dartree_verify_static", "dartree_gemm_bf16",
-           "dartree_head_prepare", "dartree_round")
+           "dartree_head_prepare", "dartree_round", "dartree_selftest_wait")
 
 
 class DartreeError(RuntimeError):
@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
     sig = {
         "dartree_head_init": (i, [P(Head), vp, vp, i, i, i]),
         "dartree_round": (i, [P(Head), P(Params), vp, vp, vp, vp, i, P(Tree), vp, vp, vp, vp, sz, vp]),
+        "dartree_selftest_wait": (i, [vp, sz, i, ctypes.c_uint, vp]),
         "dartree_head_prepare": (i, [P(Head), vp, vp]),
         "dartree_workspace_bytes": (sz, [P(Params), i, i, i]),
         "dartree_topk": (i, [vp, i, i, i, i, vp, vp, vp, sz, vp]),
@@ -177,6 +178,13 @@ def read_status(ws: torch.Tensor, stream=None) -> int:
     v = ctypes.c_int32(0)
     _call("dartree_read_status", ctypes.c_void_p(ws.data_ptr()), ctypes.byref(v), _stream(stream))
     return int(v.value)
+
+
+def selftest_wait(ws: torch.Tensor, which: int, limit_us: int, stream=None) -> None:
+    """Enqueues a bounded wait on something never signalled (0: mbarrier, 1: grid
+    barrier); it must end after limit_us with DARTREE_ETIMEOUT in ws's status word."""
+    _call("dartree_selftest_wait", ctypes.c_void_p(ws.data_ptr()), ws.numel(), int(which), int(limit_us),
+          _stream(stream))
 
 
 def clear_status(ws: torch.Tensor, stream=None) -> None:

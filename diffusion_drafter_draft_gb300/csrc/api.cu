@@ -163,6 +163,14 @@ int dartree_clear_status(void* ws, void* stream) {
     return cudaMemsetAsync(ws, 0, sizeof(int32_t), as_stream(stream)) == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 
+int dartree_selftest_wait(void* ws, size_t ws_bytes, int which, unsigned limit_us, void* stream) {
+    if (which != 0 && which != 1) return DARTREE_EINVAL;
+    if (limit_us < 1 || limit_us > 1000000u) return DARTREE_EINVAL;
+    if (int e = check_ws(ws, ws_bytes, 2 * kAlign)) return e;
+    return launch_selftest_wait(which, at<unsigned>(ws, kAlign), at<int>(ws, 0), uint64_t(limit_us) * 1000ull,
+                                as_stream(stream));
+}
+
 int dartree_gemm_bf16(const void* A, const void* B, float* D, int M, int N, int K, int32_t* status, void* stream) {
     if (!A || !B || !D || M < 1 || N < 1 || K < 1) return DARTREE_EINVAL;
     if (!gemm_tc_supported(M, N, K)) return DARTREE_EUNSUPPORTED;

@@ -153,12 +153,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 // Bounded wait on an mbarrier phase. Returns false (and records ETIMEOUT) when
-// the phase did not complete within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status) {
+// the phase did not complete within limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) { set_status(status, DARTREE_ETIMEOUT); return false; }
+        if (globaltimer_ns() - t0 > limit_ns) { set_status(status, DARTREE_ETIMEOUT); return false; }
     }
     return true;
 }
@@ -176,6 +177,40 @@ __device__ __forceinline__ void bulk_s2cluster(uint32_t remote_dst, const void* 
                                                uint32_t remote_bar) {
     asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  :: "r"(remote_dst), "r"(smem_u32(src)), "r"(bytes), "r"(remote_bar) : "memory");
+}
+
+// ----------------------------------------------------------------------------- grid barrier
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+// Grid-wide barrier on a monotonic counter; target = G * epoch. The wait is
+// bounded: after limit_ns it records DARTREE_ETIMEOUT and gives up (later
+// barriers of the same launch then skip their waits).
+__device__ __forceinline__ void grid_barrier(unsigned* ctr, unsigned target, int* status, unsigned* timed_out,
+                                             uint64_t limit_ns = kWaitLimitNs) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        red_release_gpu_add(ctr, 1u);
+        if (!*timed_out) {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_gpu(ctr) < target) {
+                if (globaltimer_ns() - t0 > limit_ns) {
+                    set_status(status, DARTREE_ETIMEOUT);
+                    *timed_out = 1;
+                    break;
+                }
+            }
+        }
+    }
+    __syncthreads();
 }
 
 // ----------------------------------------------------------------------------- block helpers

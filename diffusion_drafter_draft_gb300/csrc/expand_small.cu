@@ -96,37 +96,6 @@ struct XsArgs {
     int G, Q, hp, nfp, use_mma, wq_smem;
 };
 
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void red_release_gpu_add(unsigned* p, unsigned v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
-}
-
-// Grid-wide barrier on a monotonic counter; target = G * epoch. The wait is
-// bounded: after kWaitLimitNs it records DARTREE_ETIMEOUT and gives up (later
-// barriers of the same launch then skip their waits).
-__device__ __forceinline__ void grid_barrier(unsigned* ctr, unsigned target, int* status, unsigned* timed_out) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        red_release_gpu_add(ctr, 1u);
-        if (!*timed_out) {
-            const uint64_t t0 = globaltimer_ns();
-            while (ld_acquire_gpu(ctr) < target) {
-                if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                    set_status(status, DARTREE_ETIMEOUT);
-                    *timed_out = 1;
-                    break;
-                }
-            }
-        }
-    }
-    __syncthreads();
-}
-
 __device__ __forceinline__ void st_dsmem_v4(uint32_t addr, uint4 v) {
     asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w) : "memory");

@@ -104,4 +104,7 @@ int launch_verify(int C, int L, int B, const int32_t* tok, const int32_t* par, c
                   unsigned long long* keys, int32_t* accepted, int32_t* path, int32_t* bonus, int* status,
                   cudaStream_t stream);
 
+// Bounded-wait self-test (which = 0: mbarrier, 1: grid barrier on ctr).
+int launch_selftest_wait(int which, unsigned* ctr, int* status, uint64_t limit_ns, cudaStream_t stream);
+
 }  // namespace dartree

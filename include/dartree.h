@@ -231,6 +231,17 @@ DARTREE_API int dartree_verify_static(const dartree_params* p, const dartree_tre
                                       int rows, int V, int dtype, int32_t* accepted_len, int32_t* path,
                                       int32_t* bonus, void* stream);
 
+/* Self-test of the bounded device-side waits (failure detection without a GPU
+ * fault). The library's own wait helpers wait for something that is never
+ * signalled: which = 0, an mbarrier phase that nothing completes; which = 1, a
+ * grid barrier whose target counts one CTA more than the launch has. The wait
+ * gives up after limit_us microseconds (1..1000000), records DARTREE_ETIMEOUT in
+ * the status word at the start of ws (read it with dartree_read_status) and the
+ * kernel returns; the context stays usable. ws: >= 512 bytes, 256-byte aligned
+ * (its second 256-byte block holds the barrier counter). Returns DARTREE_OK once
+ * enqueued, DARTREE_EINVAL for a bad `which` or limit. */
+DARTREE_API int dartree_selftest_wait(void* ws, size_t ws_bytes, int which, unsigned limit_us, void* stream);
+
 /* Building block exposed for testing: the tcgen05 GEMM used for the per-depth
  * parent projection. D[M,N] = A[M,K] . B[N,K]^T with A, B bf16 row-major (K
  * contiguous, 16-byte aligned, K a multiple of 8), D fp32 row-major; N must be a

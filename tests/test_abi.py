@@ -62,3 +62,14 @@ def test_argument_errors_are_reported_on_the_host(L):
     assert L.dartree_verify(ctypes.byref(p), ctypes.byref(tree), fake, 5, 100, dd.F32, fake, fake, fake, ws_ok,
                             need, None) == dd.EDTYPE
     assert L.dartree_status_string(dd.ETIMEOUT) == b"a bounded device-side wait ran out"
+    # bounded-wait self-test: argument checks come before any launch
+    assert L.dartree_selftest_wait(ws_ok, 4096, 2, 1000, None) == dd.EINVAL          # which
+    assert L.dartree_selftest_wait(ws_ok, 4096, 0, 0, None) == dd.EINVAL             # limit 0
+    assert L.dartree_selftest_wait(ws_ok, 4096, 1, 2000000, None) == dd.EINVAL       # limit > 1 s
+    assert L.dartree_selftest_wait(ws_ok, 256, 0, 1000, None) == dd.EWORKSPACE       # < 512 bytes
+    assert L.dartree_selftest_wait(None, 4096, 0, 1000, None) == dd.EWORKSPACE
+    # dartree_round checks like build + verify
+    assert L.dartree_round(ctypes.byref(h), ctypes.byref(p), fake, fake, fake, fake, 5, ctypes.byref(tree), fake,
+                           fake, fake, ws_ok, need, None) == dd.EDTYPE
+    assert L.dartree_round(ctypes.byref(h), ctypes.byref(p), fake, fake, fake, fake, 0, ctypes.byref(tree), fake,
+                           fake, fake, ws_ok, need - 256, None) == dd.EWORKSPACE

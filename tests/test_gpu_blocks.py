@@ -1,6 +1,6 @@
 """GPU building blocks against plain references: the tcgen05 GEMM of the parent
 projection (D = A . B^T, bf16 in, fp32 accumulate) against a float64 matmul of the
-same bf16 values."""
+same bf16 values; the bounded device-side waits against a wait that never ends."""
 import numpy as np
 import pytest
 
@@ -35,3 +35,25 @@ def test_tcgen05_gemm_matches_float64(dd, M, N, K):
     ref = A.double() @ B.double().T
     err = (D.cpu().double() - ref).abs().max().item()
     assert err <= 1e-4 * max(1.0, ref.abs().max().item()), err
+
+
+@pytest.mark.parametrize("which", [0, 1])
+def test_bounded_waits_time_out_and_leave_the_context_usable(dd, which):
+    """The library's wait helpers wait for something nothing signals (0: an
+    mbarrier phase, 1: a grid-barrier target one CTA above the grid); each gives up
+    after 20 ms with DARTREE_ETIMEOUT in the status word, and later work runs."""
+    import time
+    ws = dd.new_workspace(4096, torch.device("cuda"))
+    dd.clear_status(ws)
+    t0 = time.time()
+    dd.selftest_wait(ws, which, 20000)
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 5.0
+    assert dd.read_status(ws) == dd.ETIMEOUT
+    dd.clear_status(ws)
+    x = torch.randn(4, 1000, device="cuda")
+    tok, val = dd.topk(x, 8, ws=ws)
+    torch.cuda.synchronize()
+    ref = torch.topk(x, 8, dim=1)
+    assert torch.equal(val, ref.values)
+    assert dd.read_status(ws) == 0
