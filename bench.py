@@ -191,8 +191,18 @@ def measure(cfg, steps, warmup, torch, dd, graphs=True):
                         flush)
     t_verify = time_steps(torch, graphed(torch, lambda: dd.verify(rnd.tree, x["target"], rows, cfg.L, ws=rnd.ws),
                                          graphs), steps, warmup, flush)
+    # per-kernel device time: the library brackets each launch with CUDA events on
+    # its own stream while timing is on (same rounds, not graph-captured)
+    n_prof = max(5, min(steps, 20))
+    dd.timing(True)
+    for _ in range(n_prof):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    kt = dd.kernel_times()
+    dd.timing(False)
     return dict(inp=inp, x=x, rnd=rnd, t_round=t_round, t_topk=t_topk, t_verify=t_verify, clocks=clk,
-                accepted_mean=acc, rows=rows)
+                accepted_mean=acc, rows=rows, kernel_times=kt, n_prof=n_prof)
 
 
 def measure_e2e(cfg, m, steps, torch, dd):
@@ -226,9 +236,71 @@ def measure_e2e(cfg, m, steps, torch, dd):
     return ms, h2d, d2h
 
 
-def launches_per_round(cfg) -> int:
-    # topk 1 + root 1 + 3 per depth + prune 1 + mask 1 + verify 2 (per-position) or 1 (per-node)
-    return 1 + 1 + 3 * cfg.L + 2 + (2 if cfg.rows == "position" else 1)
+# DRAM bytes per launch (read + write) from one ncu capture of the current kernel on
+# this workload; the C=64 contraction and top-K were captured on fewer requests (8
+# and 20 of them) and scaled by the requests processed (their traffic is per request).
+NCU_TRAFFIC = {
+    ("cfg1_qwen3_4b_c1", "expand_g_kernel"): 15542272,
+    ("cfg1_qwen3_4b_c1", "gemm_bf16_tc_kernel"): 18364928,
+    ("cfg4_c64_stress", "contract_tc_kernel"): 35337472 * 8,
+    ("cfg4_c64_stress", "topk_stream_kernel"): int((100288256 + 3384576) * 64 / 20),
+}
+
+
+def kernel_work(cfg, name, accepted_mean, g_path):
+    """Algorithmic work of ONE launch of a kernel family: ("hbm", bytes) or ("tensor", flops)."""
+    eb = 2 if cfg.dtype == "bf16" else 4
+    C, L, V, H, K, W, B = cfg.C, cfg.L, cfg.V, cfg.H, cfg.K, cfg.W, cfg.B
+    P = [1]
+    for _ in range(L - 1):
+        P.append(min(W, P[-1] * K))
+    if name in ("topk_rows_kernel", "topk_stream_kernel", "rowmax_kernel"):
+        return "hbm", C * L * V * eb
+    if name == "gather_rows_kernel":
+        return "hbm", 2 * C * L * K * H * eb
+    if name == "gemm_bf16_tc_kernel":
+        if g_path:
+            return "tensor", 2 * (C * L * K) * H * H
+        return "tensor", sum(2 * C * p * H * H for p in P) / L
+    if name == "contract_tc_kernel":
+        return "hbm", C * K * H * eb + C * 32 * H * 2
+    if name == "expand_g_kernel":
+        return "hbm", 3 * C * L * K * H * 2 + C * L * H * 2
+    if name == "select_kernel":
+        return "hbm", sum(C * p * K * 4 for p in P) / L
+    if name == "state_kernel":
+        return "hbm", 4 * C * W * H * eb
+    if name == "walk_kernel":
+        rows_walked = (accepted_mean + 1) if cfg.rows == "node" else L
+        return "hbm", C * rows_walked * V * eb
+    if name == "finish_kernel":
+        return "hbm", C * (L * W * 16 + (B + 1) * (B + 1) + (B + 1) * 20)
+    return "hbm", 0
+
+
+def kernel_roofline(cfg, m, hbm_peak, tf_peak):
+    """Roofline of the kernel with the largest device time per round."""
+    kt, n = m["kernel_times"], m["n_prof"]
+    g_path = "expand_g_kernel" in kt
+    dom = max(kt, key=lambda k: kt[k][1])
+    launches, ms_total = kt[dom]
+    ms_launch = ms_total / launches
+    bound, work = kernel_work(cfg, dom, m["accepted_mean"], g_path)
+    traffic = NCU_TRAFFIC.get((cfg.name, dom))
+    if bound == "tensor":
+        achieved = work / (ms_launch * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": round(achieved / tf_peak, 4), "traffic": traffic, "flops_per_launch": int(work)}
+    else:
+        achieved = work / (ms_launch * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "traffic": traffic, "bytes_per_launch": int(work)}
+    roof.update({"kernel": dom, "ms_per_launch": round(ms_launch, 5), "launches_per_round": launches / n,
+                 "share_of_kernel_time": round(ms_total / sum(v[1] for v in kt.values()), 4)})
+    per_kernel = {k: {"launches_per_round": round(v[0] / n, 2), "ms_per_round": round(v[1] / n, 4)}
+                  for k, v in sorted(kt.items(), key=lambda kv: -kv[1][1])}
+    launches_per_round = sum(v[0] for v in kt.values()) / n
+    return roof, per_kernel, launches_per_round
 
 
 def roofline(cfg, m, hbm_peak):
@@ -375,7 +447,8 @@ def main():
         ms_local = float(tt.item())
     ms = ms_local / args.steps
     value = world * 1e3 / ms
-    dom, roof, alg, parts = roofline(cfg, m, hbm_peak)
+    dom, _, alg, parts = roofline(cfg, m, hbm_peak)
+    roof, per_kernel, lpr = kernel_roofline(cfg, m, hbm_peak, tf_peak)
     e2e_ms, h2d, d2h = measure_e2e(cfg, m, min(args.steps, 20), torch, dd)
     line = {
         "metric": "draft-tree rounds/sec (build+verify)", "value": round(value, 3), "unit": "rounds/s",
@@ -389,8 +462,9 @@ def main():
                    "cuda_graph": not args.no_graph, "parallelism": "replicas" if world > 1 else "single"},
         "roofline": dict(roof, peak_kind=peak_kind),
         "breakdown_ms": {k: round(v[1], 4) for k, v in parts.items()},
+        "kernels": per_kernel,
         "accepted_mean": m["accepted_mean"],
-        "gpu_launches": launches_per_round(cfg) * args.steps,
+        "gpu_launches": int(round(lpr * args.steps)),
         "e2e": {"value": round(1e3 / e2e_ms, 3), "unit": "rounds/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "clocks": m["clocks"],
@@ -400,7 +474,8 @@ def main():
     if not args.no_stress:
         scfg = make_config(STRESS_CFG)
         sm = measure(scfg, max(5, min(args.steps, 20)), 3, torch, dd, graphs=not args.no_graph)
-        sdom, sroof, salg, sparts = roofline(scfg, sm, hbm_peak)
+        sdom, _, salg, sparts = roofline(scfg, sm, hbm_peak)
+        sroof, sper_kernel, _ = kernel_roofline(scfg, sm, hbm_peak, tf_peak)
         sms = float(np.median(sm["t_round"]))
         line["c64"] = {"workload": scfg.name, "value": round(1e3 / sms, 3), "unit": "rounds/s",
                        "request_rounds_per_s": round(scfg.C * 1e3 / sms, 1), "us_per_round_p50": round(sms * 1e3, 1),
@@ -408,6 +483,7 @@ def main():
                        "round_hbm_frac": round(salg["total"] / (sms * 1e-3) / 1e9 / hbm_peak, 4),
                        "round_tensor_frac": round(salg["flops"] / (sms * 1e-3) / 1e12 / tf_peak, 4),
                        "breakdown_ms": {k: round(v[1], 4) for k, v in sparts.items()},
+                       "kernels": sper_kernel,
                        "accepted_mean": sm["accepted_mean"], "clocks": sm["clocks"]}
         del sm
         torch.cuda.empty_cache()

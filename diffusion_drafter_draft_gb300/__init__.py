@@ -25,7 +25,8 @@ OK, EINVAL, EDTYPE, EWORKSPACE, ECUDA, ETIMEOUT, EINTERNAL, EUNSUPPORTED = 0, -1
 EXPORTS = ("dartree_head_init", "dartree_workspace_bytes", "dartree_topk", "dartree_expand", "dartree_prune",
            "dartree_tree_mask", "dartree_build_tree", "dartree_verify", "dartree_read_status",
            "dartree_clear_status", "dartree_status_string", "dartree_verify_static", "dartree_gemm_bf16",
-           "dartree_head_prepare", "dartree_round", "dartree_selftest_wait")
+           "dartree_head_prepare", "dartree_round", "dartree_selftest_wait", "dartree_timing",
+           "dartree_timing_read", "dartree_kernel_name")
 
 
 class DartreeError(RuntimeError):
@@ -81,6 +82,9 @@ def lib() -> ctypes.CDLL:
         "dartree_head_init": (i, [P(Head), vp, vp, i, i, i]),
         "dartree_round": (i, [P(Head), P(Params), vp, vp, vp, vp, i, P(Tree), vp, vp, vp, vp, sz, vp]),
         "dartree_selftest_wait": (i, [vp, sz, i, ctypes.c_uint, vp]),
+        "dartree_timing": (i, [i]),
+        "dartree_timing_read": (i, [i, P(ctypes.c_int), P(ctypes.c_double)]),
+        "dartree_kernel_name": (ctypes.c_char_p, [i]),
         "dartree_head_prepare": (i, [P(Head), vp, vp]),
         "dartree_workspace_bytes": (sz, [P(Params), i, i, i]),
         "dartree_topk": (i, [vp, i, i, i, i, vp, vp, vp, sz, vp]),
@@ -185,6 +189,25 @@ def selftest_wait(ws: torch.Tensor, which: int, limit_us: int, stream=None) -> N
     barrier); it must end after limit_us with DARTREE_ETIMEOUT in ws's status word."""
     _call("dartree_selftest_wait", ctypes.c_void_p(ws.data_ptr()), ws.numel(), int(which), int(limit_us),
           _stream(stream))
+
+
+NUM_KERNEL_IDS = 15
+
+
+def timing(enable: bool) -> None:
+    """Starts (clearing earlier records) or stops per-kernel launch timing."""
+    _call("dartree_timing", int(bool(enable)))
+
+
+def kernel_times() -> dict:
+    """{kernel family: (launches, total device ms)} recorded since timing(True)."""
+    out = {}
+    for k in range(NUM_KERNEL_IDS):
+        n, ms = ctypes.c_int(0), ctypes.c_double(0.0)
+        _call("dartree_timing_read", k, ctypes.byref(n), ctypes.byref(ms))
+        if n.value:
+            out[lib().dartree_kernel_name(k).decode()] = (int(n.value), float(ms.value))
+    return out
 
 
 def clear_status(ws: torch.Tensor, stream=None) -> None:

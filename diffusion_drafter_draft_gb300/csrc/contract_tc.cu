@@ -155,8 +155,11 @@ int launch_contract_tc(const void* E, const uint16_t* uhl, const int32_t* cand_t
         cudaSuccess)
         return DARTREE_ECUDA;
     dim3 grid((K + CC_BM - 1) / CC_BM, C);
-    contract_tc_kernel<<<grid, CC_NT, CC_SMEM, stream>>>(static_cast<const uint16_t*>(E), uhl, cand_tok, cand_val, z,
-                                                         P, K, H, L, d, inv_sqrt_h, status);
+    {
+        KTimer kt_(KID_CONTRACT, stream);
+        contract_tc_kernel<<<grid, CC_NT, CC_SMEM, stream>>>(static_cast<const uint16_t*>(E), uhl, cand_tok, cand_val, z,
+                                                             P, K, H, L, d, inv_sqrt_h, status);
+    }
     return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 

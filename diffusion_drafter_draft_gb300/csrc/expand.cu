@@ -304,7 +304,10 @@ static int launch_expand_t(const ExpandArgs& a, cudaStream_t st) {
     const T* Wq = static_cast<const T*>(a.Wq);
     const T* hid = static_cast<const T*>(a.hidden);
     T* hb[2] = {static_cast<T*>(a.hbuf[0]), static_cast<T*>(a.hbuf[1])};
-    root_init_kernel<T><<<a.C, 256, 0, st>>>(E, a.anchor, a.H, hb[0], a.sbuf[0]);
+    {
+        KTimer kt_(KID_OTHER, st);
+        root_init_kernel<T><<<a.C, 256, 0, st>>>(E, a.anchor, a.H, hb[0], a.sbuf[0]);
+    }
     const size_t smax = select_smem(a.W, a.K, a.W);
     if (cudaFuncSetAttribute(select_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smax)) != cudaSuccess)
         return DARTREE_ECUDA;
@@ -324,19 +327,31 @@ static int launch_expand_t(const ExpandArgs& a, cudaStream_t st) {
             if (tc_proj) {
                 if (int e = launch_gemm_bf16_tc(hb[cur], Wq, M, a.H, a.H, 0, a.U, nullptr, 1, a.status, st)) return e;
             } else {
-                proj_simple_kernel<T><<<pg, PJ_NT, 0, st>>>(hb[cur], Wq, a.U, M, a.H);
+                {
+                    KTimer kt_(KID_OTHER, st);
+                    proj_simple_kernel<T><<<pg, PJ_NT, 0, st>>>(hb[cur], Wq, a.U, M, a.H);
+                }
             }
             dim3 cg((a.K + (CT_NT / 32) * CT_CPW - 1) / ((CT_NT / 32) * CT_CPW), a.C);
-            contract_simple_kernel<T><<<cg, CT_NT, 0, st>>>(a.U, E, a.cand_tok, a.cand_val, a.z, P, a.K, a.H, a.L, d,
-                                                            inv_sqrt_h);
+            {
+                KTimer kt_(KID_CONTRACT, st);
+                contract_simple_kernel<T><<<cg, CT_NT, 0, st>>>(a.U, E, a.cand_tok, a.cand_val, a.z, P, a.K, a.H, a.L, d,
+                                                                inv_sqrt_h);
+            }
         }
         const int n_keep = P * a.K < a.W ? P * a.K : a.W;
-        select_kernel<T><<<a.C, SL_NT, select_smem(P, a.K, a.W), st>>>(
-            a.z, a.sbuf[cur], hb[cur], a.cand_tok, E, hid, P, a.K, a.W, a.H, a.L, d, a.beta, a.st_tok, a.st_par,
-            a.st_s, a.st_n, hb[1 - cur], a.sbuf[1 - cur], d < a.L ? 1 : 0, a.status);
+        {
+            KTimer kt_(KID_SELECT, st);
+            select_kernel<T><<<a.C, SL_NT, select_smem(P, a.K, a.W), st>>>(
+                a.z, a.sbuf[cur], hb[cur], a.cand_tok, E, hid, P, a.K, a.W, a.H, a.L, d, a.beta, a.st_tok, a.st_par,
+                a.st_s, a.st_n, hb[1 - cur], a.sbuf[1 - cur], d < a.L ? 1 : 0, a.status);
+        }
         if (d < a.L)
-            state_kernel<T><<<dim3(n_keep, a.C), SU_NT, 0, st>>>(hb[cur], E, hid, a.st_tok, a.st_par, P, a.W, a.H,
-                                                               a.L, d, hb[1 - cur]);
+            {
+                KTimer kt_(KID_STATE, st);
+                state_kernel<T><<<dim3(n_keep, a.C), SU_NT, 0, st>>>(hb[cur], E, hid, a.st_tok, a.st_par, P, a.W, a.H,
+                                                                   a.L, d, hb[1 - cur]);
+            }
         cur = 1 - cur;
         P = n_keep;
     }

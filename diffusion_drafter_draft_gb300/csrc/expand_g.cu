@@ -418,7 +418,10 @@ __global__ void transpose_bf16_kernel(const uint16_t* __restrict__ src, uint16_t
 
 int launch_transpose_bf16(const void* src, void* dst, int H, cudaStream_t stream) {
     dim3 grid((H + 31) / 32, (H + 31) / 32), block(32, 8);
-    transpose_bf16_kernel<<<grid, block, 0, stream>>>(static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst), H);
+    {
+        KTimer kt_(KID_OTHER, stream);
+        transpose_bf16_kernel<<<grid, block, 0, stream>>>(static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst), H);
+    }
     return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 
@@ -466,6 +469,7 @@ static int xg_launch(const XgArgs& x, const CUtensorMap& ghi, const CUtensorMap&
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    KTimer kt_(KID_EXPAND_G, stream);
     return cudaLaunchKernelEx(&cfg, expand_g_kernel<CS>, x, ghi, glo, eg) == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 
@@ -491,7 +495,10 @@ int try_launch_expand_g(const ExpandArgs& a, cudaStream_t stream, bool* launched
     }
     if (!cs) return DARTREE_OK;
     *launched = true;
-    gather_rows_kernel<<<M, 256, 0, stream>>>(static_cast<const uint16_t*>(a.E), a.cand_tok, a.H, a.Eg);
+    {
+        KTimer kt_(KID_GATHER, stream);
+        gather_rows_kernel<<<M, 256, 0, stream>>>(static_cast<const uint16_t*>(a.E), a.cand_tok, a.H, a.Eg);
+    }
     if (cudaGetLastError() != cudaSuccess) return DARTREE_ECUDA;
     if (int e = launch_gemm_bf16_tc(a.Eg, a.WqT, M, a.H, a.H, 2, nullptr, a.Ghi, 1, a.status, stream, a.Glo)) return e;
     const int fs = a.H / cs;

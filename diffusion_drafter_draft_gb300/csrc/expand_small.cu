@@ -755,6 +755,7 @@ static int launch_small_t(const ExpandArgs& a, const XsPlan& pl, cudaStream_t st
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    KTimer kt_(KID_EXPAND_SMALL, st);
     return cudaLaunchKernelEx(&cfg, expand_small_kernel<T>, x) == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 

@@ -222,8 +222,11 @@ int launch_finish(int C, int L, int W, int B, const int32_t* st_tok, const int32
     auto kern = walk ? finish_kernel<true> : finish_kernel<false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
         return DARTREE_ECUDA;
-    kern<<<C, FN_NT, smem, stream>>>(L, W, B, st_tok, st_par, st_s, st_n, anchor, tok, par, depth, score, n_nodes,
-                                     mask, pos, rowkeys, accepted, path, bonus, status);
+    {
+        KTimer kt_(KID_FINISH, stream);
+        kern<<<C, FN_NT, smem, stream>>>(L, W, B, st_tok, st_par, st_s, st_n, anchor, tok, par, depth, score, n_nodes,
+                                         mask, pos, rowkeys, accepted, path, bonus, status);
+    }
     return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 

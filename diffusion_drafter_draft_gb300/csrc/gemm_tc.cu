@@ -205,7 +205,10 @@ static int launch_gemm_bn(const void* A, const void* B, int M, int N, int K, con
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
         return DARTREE_ECUDA;
     dim3 grid(N / BN, (M + GT_BM - 1) / GT_BM);
-    kern<<<grid, GT_NT, smem, stream>>>(ta, tb, M, N, K, o, status);
+    {
+        KTimer kt_(KID_GEMM, stream);
+        kern<<<grid, GT_NT, smem, stream>>>(ta, tb, M, N, K, o, status);
+    }
     return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 

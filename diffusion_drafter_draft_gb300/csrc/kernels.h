@@ -7,6 +7,23 @@
 
 namespace dartree {
 
+// Kernel ids of the launch timing (dartree_timing): one per kernel family.
+enum KernelId {
+    KID_TOPK_ROWS = 0, KID_TOPK_STREAM, KID_GEMM, KID_CONTRACT, KID_EXPAND_G, KID_GATHER, KID_SELECT,
+    KID_STATE, KID_EXPAND_SMALL, KID_FINISH, KID_PRUNE, KID_MASK, KID_ROWMAX, KID_WALK, KID_OTHER,
+    KID_COUNT
+};
+// Brackets the launches of its scope with timing events when timing is enabled.
+struct KTimer {
+    KTimer(int id, cudaStream_t s);
+    ~KTimer();
+    KTimer(const KTimer&) = delete;
+    KTimer& operator=(const KTimer&) = delete;
+    int id_;
+    cudaStream_t s_;
+    void* b_;
+};
+
 int num_sms();
 
 // S1: top-K of `rows` rows of V values.

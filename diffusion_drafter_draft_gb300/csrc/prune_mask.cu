@@ -106,8 +106,11 @@ int launch_prune(int C, int L, int W, int B, const int32_t* st_tok, const int32_
     const size_t smem = n * 8 + n * 4 + 256 * 4 + 8 * 4 + 32 * 4 + 8 * 4 + 16;
     if (cudaFuncSetAttribute(prune_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
         return DARTREE_ECUDA;
-    prune_kernel<<<C, PR_NT, smem, stream>>>(L, W, B, st_tok, st_par, st_s, st_n, anchor, tok, par, depth, score,
-                                            n_nodes, status);
+    {
+        KTimer kt_(KID_PRUNE, stream);
+        prune_kernel<<<C, PR_NT, smem, stream>>>(L, W, B, st_tok, st_par, st_s, st_n, anchor, tok, par, depth, score,
+                                                n_nodes, status);
+    }
     return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 
@@ -170,7 +173,10 @@ int launch_mask(int C, int L, int B, const int32_t* par, const int32_t* depth, c
     const size_t smem = size_t(S) * (L + 1) * 2 + size_t(S) * 2 + 16;
     if (cudaFuncSetAttribute(mask_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
         return DARTREE_ECUDA;
-    mask_kernel<<<C, MK_NT, smem, stream>>>(L, B, par, depth, n_nodes, mask, pos);
+    {
+        KTimer kt_(KID_MASK, stream);
+        mask_kernel<<<C, MK_NT, smem, stream>>>(L, B, par, depth, n_nodes, mask, pos);
+    }
     return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 

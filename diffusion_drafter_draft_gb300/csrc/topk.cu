@@ -702,8 +702,12 @@ static int launch_topk_t(const void* x, int rows, int V, int K, int32_t* tok, fl
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const T*>(x), V, K, jsel, chunk, use_bulk,
-                                       tok, val, status);
+    cudaError_t e;
+    {
+        KTimer kt_(KID_TOPK_ROWS, stream);
+        e = cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const T*>(x), V, K, jsel, chunk, use_bulk, tok, val,
+                               status);
+    }
     return e == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 
@@ -726,7 +730,11 @@ static int launch_topk_stream(const void* x, int rows, int V, int K, int32_t* to
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const T*>(x), V, K, tok, val, status);
+    cudaError_t e;
+    {
+        KTimer kt_(KID_TOPK_STREAM, stream);
+        e = cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const T*>(x), V, K, tok, val, status);
+    }
     // (rows are read with plain vector loads: 16-byte aligned rows)
     return e == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }

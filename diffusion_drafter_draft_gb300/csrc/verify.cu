@@ -175,7 +175,10 @@ static int launch_rowmax_t(int rows, int V, const void* target, unsigned long lo
     int seg = (V + splits - 1) / splits;
     seg = (seg + 7) / 8 * 8;
     splits = (V + seg - 1) / seg;
-    rowmax_kernel<T><<<dim3(splits, rows), RM_NT, 0, stream>>>(static_cast<const T*>(target), V, seg, keys);
+    {
+        KTimer kt_(KID_ROWMAX, stream);
+        rowmax_kernel<T><<<dim3(splits, rows), RM_NT, 0, stream>>>(static_cast<const T*>(target), V, seg, keys);
+    }
     return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 
@@ -183,7 +186,10 @@ int launch_walk_position(int C, int L, int B, const int32_t* tok, const int32_t*
                          const int32_t* n_nodes, const unsigned long long* keys, int32_t* accepted, int32_t* path,
                          int32_t* bonus, cudaStream_t stream) {
     if (C == 0) return DARTREE_OK;
-    walk_position_kernel<<<C, 32, 0, stream>>>(L, B, tok, par, depth, n_nodes, keys, accepted, path, bonus);
+    {
+        KTimer kt_(KID_WALK, stream);
+        walk_position_kernel<<<C, 32, 0, stream>>>(L, B, tok, par, depth, n_nodes, keys, accepted, path, bonus);
+    }
     return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 
@@ -202,7 +208,10 @@ static int launch_verify_t(int C, int L, int B, const int32_t* tok, const int32_
     const T* tg = static_cast<const T*>(target);
     if (rows_mode == DARTREE_ROWS_PER_POSITION) {
         if (int e = launch_rowmax_t<T>(C * L, V, target, keys, stream)) return e;
-        walk_position_kernel<<<C, 32, 0, stream>>>(L, B, tok, par, depth, n_nodes, keys, accepted, path, bonus);
+        {
+            KTimer kt_(KID_WALK, stream);
+            walk_position_kernel<<<C, 32, 0, stream>>>(L, B, tok, par, depth, n_nodes, keys, accepted, path, bonus);
+        }
         return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
     }
     const int S = 8;
@@ -220,8 +229,11 @@ static int launch_verify_t(int C, int L, int B, const int32_t* tok, const int32_
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, walk_node_kernel<T>, L, B, V, seg, tg, tok, par, n_nodes, accepted,
-                                       path, bonus);
+    cudaError_t e;
+    {
+        KTimer kt_(KID_WALK, stream);
+        e = cudaLaunchKernelEx(&cfg, walk_node_kernel<T>, L, B, V, seg, tg, tok, par, n_nodes, accepted, path, bonus);
+    }
     return e == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 

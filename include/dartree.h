@@ -242,6 +242,18 @@ DARTREE_API int dartree_verify_static(const dartree_params* p, const dartree_tre
  * enqueued, DARTREE_EINVAL for a bad `which` or limit. */
 DARTREE_API int dartree_selftest_wait(void* ws, size_t ws_bytes, int which, unsigned limit_us, void* stream);
 
+/* Per-kernel launch timing (profiling). dartree_timing(1) clears the records and
+ * starts bracketing every library kernel launch with two CUDA events on the
+ * launch's stream; dartree_timing(0) stops. dartree_timing_read synchronises the
+ * recorded events of one kernel family and returns its launch count and summed
+ * device time. Kernel ids 0..DARTREE_NUM_KERNEL_IDS-1, named by
+ * dartree_kernel_name. Not for launches captured into a CUDA graph; adds two
+ * event records per launch while on. */
+#define DARTREE_NUM_KERNEL_IDS 15
+DARTREE_API int dartree_timing(int enable);
+DARTREE_API int dartree_timing_read(int kernel_id, int* launches, double* total_ms);
+DARTREE_API const char* dartree_kernel_name(int kernel_id);
+
 /* Building block exposed for testing: the tcgen05 GEMM used for the per-depth
  * parent projection. D[M,N] = A[M,K] . B[N,K]^T with A, B bf16 row-major (K
  * contiguous, 16-byte aligned, K a multiple of 8), D fp32 row-major; N must be a
