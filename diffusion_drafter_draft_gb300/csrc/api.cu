@@ -288,32 +288,6 @@ int dartree_build_tree(const dartree_head* head, const dartree_params* p, const 
     return finish_tree(p, sp, anchor, tree, status, s);
 }
 
-// Side stream and events per device: the target-row maxima of a round run there,
-// overlapping the build. Created on first use; calls that fork are serialised.
-struct SidePool {
-    cudaStream_t side = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-    bool ok = false;
-};
-static std::mutex g_side_mu;
-static SidePool g_side[64];
-
-static SidePool* side_pool() {  // with g_side_mu held
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    SidePool& sp = g_side[dev];
-    if (!sp.ok) {
-        if (cudaStreamCreateWithFlags(&sp.side, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaEventCreateWithFlags(&sp.fork, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&sp.join, cudaEventDisableTiming) != cudaSuccess) {
-            cudaGetLastError();
-            return nullptr;
-        }
-        sp.ok = true;
-    }
-    return &sp;
-}
-
 int dartree_round(const dartree_head* head, const dartree_params* p, const void* base_logits,
                   const void* block_hidden, const int32_t* anchor, const void* target, int rows, dartree_tree* tree,
                   int32_t* accepted_len, int32_t* path, int32_t* bonus, void* ws, size_t ws_bytes, void* stream) {
@@ -335,24 +309,28 @@ int dartree_round(const dartree_head* head, const dartree_params* p, const void*
     int* status = at<int>(ws, l.status);
     unsigned long long* rowkeys = at<unsigned long long>(ws, l.keys);
     const bool per_pos = rows == DARTREE_ROWS_PER_POSITION;
-    std::unique_lock<std::mutex> lock(g_side_mu, std::defer_lock);
-    SidePool* side = nullptr;
+    // S1 first; the target-row maxima (per-position rows) then run on a side
+    // stream forked here, overlapping the expansion, which leaves most SMs idle
+    // for small batches (forked before S1 they would compete with it for HBM)
+    if (int e = launch_topk(base_logits, p->C * p->L, head->V, p->K, head->dtype, ct, cv, status, s)) return e;
+    std::unique_lock<std::recursive_mutex> lock(side_mutex(), std::defer_lock);
+    SideStreams* side = nullptr;
     if (per_pos) {
         lock.lock();
-        side = side_pool();
+        side = side_streams();
         if (side) {
-            if (cudaEventRecord(side->fork, s) != cudaSuccess || cudaStreamWaitEvent(side->side, side->fork, 0) != cudaSuccess)
+            if (cudaEventRecord(side->fork[0], s) != cudaSuccess ||
+                cudaStreamWaitEvent(side->s[0], side->fork[0], 0) != cudaSuccess)
                 return DARTREE_ECUDA;
-            if (int e = launch_rowmax_position(p->C, p->L, head->V, head->dtype, target, rowkeys, side->side)) return e;
-            if (cudaEventRecord(side->join, side->side) != cudaSuccess) return DARTREE_ECUDA;
+            if (int e = launch_rowmax_position(p->C, p->L, head->V, head->dtype, target, rowkeys, side->s[0])) return e;
+            if (cudaEventRecord(side->join[0], side->s[0]) != cudaSuccess) return DARTREE_ECUDA;
         } else {
             lock.unlock();
             if (int e = launch_rowmax_position(p->C, p->L, head->V, head->dtype, target, rowkeys, s)) return e;
         }
     }
-    if (int e = launch_topk(base_logits, p->C * p->L, head->V, p->K, head->dtype, ct, cv, status, s)) return e;
     if (int e = expand_impl(head, p, block_hidden, anchor, ct, cv, &st, ws, l, s)) return e;
-    if (side && cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess) return DARTREE_ECUDA;
+    if (side && cudaStreamWaitEvent(s, side->join[0], 0) != cudaSuccess) return DARTREE_ECUDA;
     if (per_pos && finish_supported(p->L, p->W))
         return launch_finish(p->C, p->L, p->W, p->B, st.tok, st.par, st.score, st.n, anchor, tree->tok, tree->par,
                              tree->depth, tree->score, tree->n_nodes, tree->mask, tree->pos, rowkeys, accepted_len,

@@ -358,14 +358,52 @@ static int launch_expand_t(const ExpandArgs& a, cudaStream_t st) {
     return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 
+constexpr int kSplitMinC = 32;  // requests from which a batch expands as two halves
+
 int launch_expand(const ExpandArgs& a, cudaStream_t stream) {
     bool done = false;
     if (int e = try_launch_expand_g(a, stream, &done)) return e;
     if (done) return DARTREE_OK;
     if (int e = try_launch_expand_small(a, stream, &done)) return e;
     if (done) return DARTREE_OK;
-    if (a.dtype == DARTREE_BF16) return launch_expand_t<bf16_t>(a, stream);
-    return launch_expand_t<float>(a, stream);
+    auto run = [&](const ExpandArgs& x, cudaStream_t st) {
+        return x.dtype == DARTREE_BF16 ? launch_expand_t<bf16_t>(x, st) : launch_expand_t<float>(x, st);
+    };
+    // A large batch runs as two halves of requests on two streams, so that one
+    // half's projection GEMM (tensor cores, L2) overlaps the other half's
+    // candidate-row contraction (HBM). Requests are independent; every
+    // per-request buffer is indexed from the half's first request.
+    std::unique_lock<std::recursive_mutex> lock(side_mutex());
+    SideStreams* side = a.C >= kSplitMinC ? side_streams() : nullptr;
+    if (!side) return run(a, stream);
+    const int c0 = a.C / 2, r0 = c0;
+    const size_t eb = a.dtype == DARTREE_BF16 ? 2 : 4;
+    ExpandArgs h0 = a, h1 = a;
+    h0.C = c0;
+    h1.C = a.C - c0;
+    h1.hidden = static_cast<const uint8_t*>(a.hidden) + size_t(r0) * a.L * a.H * eb;
+    h1.anchor = a.anchor + r0;
+    h1.cand_tok = a.cand_tok + size_t(r0) * a.L * a.K;
+    h1.cand_val = a.cand_val + size_t(r0) * a.L * a.K;
+    h1.st_tok = a.st_tok + size_t(r0) * a.L * a.W;
+    h1.st_par = a.st_par + size_t(r0) * a.L * a.W;
+    h1.st_s = a.st_s + size_t(r0) * a.L * a.W;
+    h1.st_n = a.st_n + size_t(r0) * a.L;
+    for (int i = 0; i < 2; ++i) {
+        h1.hbuf[i] = static_cast<uint8_t*>(a.hbuf[i]) + size_t(r0) * a.W * a.H * eb;
+        h1.sbuf[i] = a.sbuf[i] + size_t(r0) * a.W;
+    }
+    h1.U = a.U + size_t(r0) * a.W * a.H;
+    h1.z = a.z + size_t(r0) * a.W * a.K;
+    if (a.uhl) h1.uhl = a.uhl + size_t(r0) * 32 * a.H;
+    if (cudaEventRecord(side->fork[1], stream) != cudaSuccess ||
+        cudaStreamWaitEvent(side->s[1], side->fork[1], 0) != cudaSuccess)
+        return DARTREE_ECUDA;
+    if (int e = run(h0, stream)) return e;
+    if (int e = run(h1, side->s[1])) return e;
+    if (cudaEventRecord(side->join[1], side->s[1]) != cudaSuccess || cudaStreamWaitEvent(stream, side->join[1], 0) != cudaSuccess)
+        return DARTREE_ECUDA;
+    return DARTREE_OK;
 }
 
 }  // namespace dartree

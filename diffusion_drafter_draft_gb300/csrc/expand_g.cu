@@ -48,7 +48,7 @@ constexpr int XG_MAXW = 16;   // parents per depth: one 16-row mma tile
 __host__ __device__ constexpr size_t xg_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct XgLayout {
-    size_t gs, hs, es, hds, ctok, cval, zred, rkeys, lists, mrg, ssq, sel, spar, mbar, total;
+    size_t gs, hs, es, hds, ctok, cval, zred, rkeys, lists, mrg, ssq, sel, spar, stout, mbar, total;
 };
 
 constexpr int XG_GB = 32;  // columns of one swizzled G tile (64 bytes)
@@ -73,6 +73,7 @@ __host__ __device__ inline XgLayout xg_layout(int fs, int K, int cs, int L) {
     l.ssq = take(size_t(cs) * XG_MAXW * 4, 16);      // partial sums of squares [q][k]
     l.sel = take(size_t(XG_MAXW) * 8 + 2 * XG_MAXW * 4, 16);
     l.spar = take(size_t(XG_MAXW) * 4, 16);
+    l.stout = take(size_t(L) * XG_MAXW * 8 + size_t(L) * 4, 16);  // supertree of the request, written at the end
     l.mbar = take(8, 8);                             // prefetch barrier
     l.total = o;
     return l;
@@ -153,6 +154,8 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
     int* selx = reinterpret_cast<int*>(selk + XG_MAXW);            // [0..16): parent rank, [16..32): candidate
     float* spar = reinterpret_cast<float*>(smem + lay.spar);       // parent scores
     uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + lay.mbar);
+    uint64_t* stkey = reinterpret_cast<uint64_t*>(smem + lay.stout);  // [L][16] kept keys (0 = none)
+    int* stn = reinterpret_cast<int*>(stkey + size_t(L) * XG_MAXW);    // [L] kept per depth
 
     const uint32_t cr = cluster_ctarank();
     const int r = blockIdx.x / CS;
@@ -318,21 +321,10 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
             }
         }
         __syncthreads();
-        // supertree entries: entry k is written by CTA k mod CS
-        if (threadIdx.x < W && int(threadIdx.x) % CS == int(cr)) {
-            const int k = threadIdx.x;
-            const size_t o = (size_t(r) * L + pos) * W + k;
-            if (k < n_keep) {
-                a.st_tok[o] = ctok[pos * K + selx[XG_MAXW + k]];
-                a.st_par[o] = selx[k];
-                a.st_s[o] = f32_from_ord(uint32_t(selk[k] >> 32));
-            } else {
-                a.st_tok[o] = -1;
-                a.st_par[o] = -1;
-                a.st_s[o] = 0.f;
-            }
-        }
-        if (threadIdx.x == 0 && cr == 0) a.st_n[size_t(r) * L + pos] = n_keep;
+        // supertree entries stay in shared memory until the depth loop ends (global
+        // stores inside the loop would hold up the release of the next cluster barrier)
+        if (threadIdx.x < XG_MAXW) stkey[pos * XG_MAXW + threadIdx.x] = threadIdx.x < n_keep ? selk[threadIdx.x] : 0ull;
+        if (threadIdx.x == 0) stn[pos] = n_keep;
         if (d == L) break;  // no remote access follows barrier B of the last depth
         // ---- state slices of the kept children: warp w owns rows w and w + 8,
         //      lane j the 8-feature chunk j
@@ -388,18 +380,60 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
         cur = 1 - cur;
         P = n_keep;
     }
+    // the supertree: CTA q writes depths q, q + CS, ...
+    __syncthreads();
+    for (int pd = int(cr); pd < L; pd += CS) {
+        const int nk = stn[pd];
+        for (int k = threadIdx.x; k < W; k += XG_NT) {
+            const size_t o = (size_t(r) * L + pd) * W + k;
+            const uint64_t key = k < XG_MAXW ? stkey[pd * XG_MAXW + k] : 0ull;
+            if (k < nk) {
+                const uint32_t f = 0xffffffffu - uint32_t(key);
+                a.st_tok[o] = ctok[pd * K + int(f) % K];
+                a.st_par[o] = int(f) / K;
+                a.st_s[o] = f32_from_ord(uint32_t(key >> 32));
+            } else {
+                a.st_tok[o] = -1;
+                a.st_par[o] = -1;
+                a.st_s[o] = 0.f;
+            }
+        }
+        if (threadIdx.x == 0) a.st_n[size_t(r) * L + pd] = nk;
+    }
     // a prefetch still in flight (only after a timed-out wait) lands before the CTA leaves
     if (!pf_ok) mbar_wait_bounded(mbar, uint32_t(waited) & 1u, a.status);
 }
 
 // --------------------------------------------------------------------------- gathers, transpose
 
-__global__ void gather_rows_kernel(const uint16_t* __restrict__ E, const int32_t* __restrict__ idx, int H,
-                                   uint16_t* __restrict__ out) {
-    const int m = blockIdx.x;
-    const uint4* src = reinterpret_cast<const uint4*>(E + size_t(idx[m]) * H);
-    uint4* dst = reinterpret_cast<uint4*>(out + size_t(m) * H);
-    for (int v = threadIdx.x; v < H / 8; v += blockDim.x) dst[v] = src[v];
+// out[m] = E[idx[m]]: GR_ROWS rows per CTA, every load of a thread issued before
+// its stores.
+constexpr int GR_ROWS = 8, GR_NT = 256, GR_MAXV = 3;  // rows of up to GR_MAXV * GR_NT vectors
+__global__ void __launch_bounds__(GR_NT) gather_rows_kernel(const uint16_t* __restrict__ E,
+                                                            const int32_t* __restrict__ idx, int H, int M,
+                                                            uint16_t* __restrict__ out) {
+    const int nv = H / 8;
+    uint4 v[GR_ROWS][GR_MAXV];
+#pragma unroll
+    for (int i = 0; i < GR_ROWS; ++i) {
+        const int m = blockIdx.x * GR_ROWS + i;
+        if (m < M) {
+            const uint4* src = reinterpret_cast<const uint4*>(E + size_t(idx[m]) * H);
+#pragma unroll
+            for (int j = 0; j < GR_MAXV; ++j)
+                if (int(threadIdx.x) + j * GR_NT < nv) v[i][j] = __ldg(src + threadIdx.x + j * GR_NT);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < GR_ROWS; ++i) {
+        const int m = blockIdx.x * GR_ROWS + i;
+        if (m < M) {
+            uint4* dst = reinterpret_cast<uint4*>(out + size_t(m) * H);
+#pragma unroll
+            for (int j = 0; j < GR_MAXV; ++j)
+                if (int(threadIdx.x) + j * GR_NT < nv) dst[threadIdx.x + j * GR_NT] = v[i][j];
+        }
+    }
 }
 
 __global__ void transpose_bf16_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst, int H) {
@@ -482,7 +516,7 @@ int try_launch_expand_g(const ExpandArgs& a, cudaStream_t stream, bool* launched
     if (a.dtype != DARTREE_BF16 || !a.WqT || !a.Eg || !a.Ghi || !a.Glo) return DARTREE_OK;
     const int M = a.C * a.L * a.K;
     if (M > a.g_rows || a.K > XG_MAXK || a.K % 8 != 0 || a.W > XG_MAXW) return DARTREE_OK;
-    if (!gemm_tc_supported(M, a.H, a.H)) return DARTREE_OK;
+    if (!gemm_tc_supported(M, a.H, a.H) || a.H / 8 > GR_MAXV * GR_NT) return DARTREE_OK;
     int cs = 0;
     size_t smem = 0;
     if (xg_fs_ok(a.H, 16)) {
@@ -497,7 +531,8 @@ int try_launch_expand_g(const ExpandArgs& a, cudaStream_t stream, bool* launched
     *launched = true;
     {
         KTimer kt_(KID_GATHER, stream);
-        gather_rows_kernel<<<M, 256, 0, stream>>>(static_cast<const uint16_t*>(a.E), a.cand_tok, a.H, a.Eg);
+        gather_rows_kernel<<<(M + GR_ROWS - 1) / GR_ROWS, GR_NT, 0, stream>>>(static_cast<const uint16_t*>(a.E),
+                                                                              a.cand_tok, a.H, M, a.Eg);
     }
     if (cudaGetLastError() != cudaSuccess) return DARTREE_ECUDA;
     if (int e = launch_gemm_bf16_tc(a.Eg, a.WqT, M, a.H, a.H, 2, nullptr, a.Ghi, 1, a.status, stream, a.Glo)) return e;

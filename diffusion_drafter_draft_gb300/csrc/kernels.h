@@ -3,9 +3,21 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 #include <stdint.h>
 
 namespace dartree {
+
+// Side streams for forks inside one call (0: target-row maxima of a round, 1: the
+// second half of a large batch's expansion). Enqueue under side_mutex().
+struct SideStreams {
+    cudaStream_t s[2] = {nullptr, nullptr};
+    cudaEvent_t fork[2] = {nullptr, nullptr}, join[2] = {nullptr, nullptr};
+    bool ok = false;
+};
+SideStreams* side_streams();  // nullptr when they cannot be created
+std::recursive_mutex& side_mutex();
 
 // Kernel ids of the launch timing (dartree_timing): one per kernel family.
 enum KernelId {
@@ -60,11 +72,11 @@ struct ExpandArgs {
     int* status;
 };
 
-// Transpose of an H x H bf16 matrix (head preparation).
 // 2-D bf16 TMA descriptor of a row-major [rows, cols] tensor, box box_cols x box_rows,
 // swizzle 0 (none), 32, 64 or 128 bytes. False when the driver refuses it.
 bool make_tensor_map_bf16(CUtensorMap* map, const void* base, int rows, int cols, int box_cols, int box_rows,
                           int swizzle_bytes);
+// Transpose of an H x H bf16 matrix (head preparation).
 int launch_transpose_bf16(const void* src, void* dst, int H, cudaStream_t stream);
 
 // Candidate-side projection path (small batches, prepared bf16 head); *launched = false
