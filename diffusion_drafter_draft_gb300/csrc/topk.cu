@@ -4,12 +4,15 @@
 // One thread-block cluster per row. Each CTA stages a contiguous chunk of the
 // row in shared memory with TMA bulk copies (a single HBM read of the row) and
 // works on orderable keys (value, ~token), so ties go to the lower token id:
-//   1. while the pieces land, every thread takes the maximum of its vectors (a
-//      "group max"); each warp's j-th largest group max, minimised over the
-//      row's warps, is a value c with at least K elements >= c (j = K / warps);
+//   1. while the pieces land, every thread keeps the 4 largest maxima of its
+//      vectors (a branch-free min/max network); each CTA takes the j-th largest
+//      of its threads' 4th-largest values (a bitwise search, j = ceil(K / 4S)),
+//      and the minimum over the cluster is a value c with at least K elements
+//      >= c (every CTA holds j threads with 4 vectors reaching it);
 //   2. elements >= c (typically 2-20x K of them) are written to the leader CTA
 //      through distributed shared memory at offsets from a cluster-wide scan;
-//   3. the leader sorts the candidates and writes the first K.
+//   3. the leader sorts the candidates (after a radix select of exactly K when
+//      more than 1024 passed) and writes the first K.
 // If more than TK_CAP elements pass the filter (heavy ties), the cluster falls
 // back to an exact radix select of the K-th value with ordered tie compaction.
 #include "common.cuh"
@@ -75,22 +78,6 @@ __device__ __forceinline__ uint32_t vec_elem_ord(uint4 v, int e, bf16_t*) {
 __device__ __forceinline__ uint32_t vec_elem_ord(uint4 v, int e, float*) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     return ord_f32(__uint_as_float(w[e]));
-}
-
-// j-th largest (1-based, j <= 32) of one value per lane.
-__device__ __forceinline__ uint32_t warp_jth_largest(uint32_t v, int j) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-        for (int m = k >> 1; m > 0; m >>= 1) {
-            const uint32_t o = __shfl_xor_sync(0xffffffffu, v, m);
-            const bool lower = (lane & m) == 0;
-            const bool desc = (lane & k) == 0;
-            v = (lower == desc) ? (o > v ? o : v) : (o < v ? o : v);
-        }
-    }
-    return __shfl_sync(0xffffffffu, v, j - 1);
 }
 
 // Calls f(index_in_chunk, ord_key) for the thread's owned run [lo, hi) in order.
@@ -313,33 +300,48 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
         __syncthreads();
     }
 
-    // pass 1: group maximum of the vectors t, t+NT, ... (piece by piece as they land)
-    uint32_t gm = 0;
+    // pass 1: the 4 largest maxima of the vectors t, t+NT, ... (piece by piece as they land)
+    uint32_t t0 = 0, t1 = 0, t2 = 0, t3 = 0;
+    auto ins = [&](uint32_t vm) {
+        t3 = max(t3, min(t2, vm));
+        t2 = max(t2, min(t1, vm));
+        t1 = max(t1, min(t0, vm));
+        t0 = max(t0, vm);
+    };
     bool loaded = true;
     if (use_bulk) {
         for (int p = 0; p < npieces; ++p) {
             if (!mbar_wait_bounded(&mbar[p], 0, status)) loaded = false;
             const int v1 = min(nvec, (p + 1) * VPP);
-            for (int v = p * VPP + int(threadIdx.x); v < v1; v += TK_NT) {
-                const uint32_t o = vec_max_ord(reinterpret_cast<const uint4*>(buf)[v], static_cast<T*>(nullptr));
-                gm = o > gm ? o : gm;
-            }
+            for (int v = p * VPP + int(threadIdx.x); v < v1; v += TK_NT)
+                ins(vec_max_ord(reinterpret_cast<const uint4*>(buf)[v], static_cast<T*>(nullptr)));
         }
     } else {
-        for (int v = threadIdx.x; v < nvec; v += TK_NT) {
-            const uint32_t o = vec_max_ord(reinterpret_cast<const uint4*>(buf)[v], static_cast<T*>(nullptr));
-            gm = o > gm ? o : gm;
+        for (int v = threadIdx.x; v < nvec; v += TK_NT)
+            ins(vec_max_ord(reinterpret_cast<const uint4*>(buf)[v], static_cast<T*>(nullptr)));
+    }
+    for (int i = nvec * VEC + int(threadIdx.x); i < n; i += TK_NT) ins(ValueKey<T>::ord(buf[i]));
+    // lower bound c, per CTA the larger of two bounds, then minimised over the
+    // cluster: the CTA's j1-th largest vector maximum (j1 = ceil(K / S): j1 distinct
+    // elements reach it) and its jsel-th largest 4th-largest vector maximum (4 * jsel
+    // elements reach it, 4 * jsel * S >= K). Every CTA then has at least K / S
+    // elements >= c. The first bound is the tighter one when a thread reads few
+    // vectors, the second when it reads many.
+    {
+        constexpr int KB = ValueKey<T>::BITS;
+        const int j1 = (K + int(S) - 1) / int(S);
+        uint32_t c1 = 0, c4 = 0;
+        if (j1 <= TK_NT)
+            for (int b = KB - 1; b >= 0; --b) {
+                const uint32_t trial = c1 | (1u << b);
+                if (__syncthreads_count(t0 >= trial) >= j1) c1 = trial;
+            }
+        for (int b = KB - 1; b >= 0; --b) {
+            const uint32_t trial = c4 | (1u << b);
+            if (__syncthreads_count(t3 >= trial) >= jsel) c4 = trial;
         }
+        if (threadIdx.x == 0) misc[2] = c1 > c4 ? c1 : c4;
     }
-    for (int i = nvec * VEC + int(threadIdx.x); i < n; i += TK_NT) {
-        const uint32_t o = ValueKey<T>::ord(buf[i]);
-        gm = o > gm ? o : gm;
-    }
-    // lower bound c: every warp holds jsel groups whose maximum is >= its jsel-th
-    // largest group max, and the warps of the row number at least K / jsel, so at
-    // least K elements are >= the minimum over warps of those values.
-    uint32_t wj = jsel <= 32 ? warp_jth_largest(gm, jsel) : 0u;
-    if ((threadIdx.x & 31) == 0) atomicMin(&misc[2], wj);
     __syncthreads();
     cluster_sync();  // every CTA's misc is initialised before remote atomics
     if (threadIdx.x == 0) {
@@ -395,8 +397,20 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
             if (threadIdx.x == 0) set_status(status, DARTREE_EINTERNAL);
     }
 
-    // leader: exactly the K best candidates (radix select), then sort those K
-    if (cr == 0) {
+    // leader: up to TK_FB candidates are sorted directly; more are cut to exactly K
+    // by a radix select first
+    int np = 1;
+    while (np < int(total)) np <<= 1;
+    if (cr == 0 && fits && np <= TK_FB && np <= L.cap) {
+        for (int i = int(total) + threadIdx.x; i < np; i += TK_NT) cand[i] = 0;
+        __syncthreads();
+        sort_desc<TK_NT>(cand, np);
+        for (int i = threadIdx.x; i < K; i += TK_NT) {
+            const uint64_t k = cand[i];
+            out_tok[size_t(row) * K + i] = int32_t(0xffffffffu - uint32_t(k));
+            out_val[size_t(row) * K + i] = ValueKey<T>::value(uint32_t(k >> 32));
+        }
+    } else if (cr == 0) {
         if (fits) {
             uint64_t prefix = 0, mask = 0;
             uint64_t* orand = reinterpret_cast<uint64_t*>(hsum);  // 16 words of scratch
@@ -664,8 +678,7 @@ static int launch_topk_t(const void* x, int rows, int V, int K, int32_t* tok, fl
     while (S < max_s && rows * S < 2 * num_sms() && size_t(chunk_of(2 * S)) * elem >= 16 * 1024) S *= 2;
     const int chunk = chunk_of(S);
     const TopkSmem L = topk_smem_layout(chunk, elem);
-    const int warps = S * (TK_NT / 32);
-    const int jsel = (K + warps - 1) / warps;  // > 32 disables the filter (exact path)
+    const int jsel = (K + 4 * S - 1) / (4 * S);  // threads per CTA holding the bound (<= TK_NT)
     const int use_bulk = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && ((size_t(V) * elem) % 16 == 0);
     auto kern = topk_rows_kernel<T>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.total)) != cudaSuccess)
