@@ -213,14 +213,27 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
                 // matrices: (hi, k lo), (hi, k hi), (lo, k lo), (lo, k hi)
                 const uint32_t brow = g0 + uint32_t(((lm >> 1) * nb * K + n) * 64);
                 const uint32_t sw = uint32_t((n >> 1) & 3);
+                // two accumulator chains per operand (even and odd k-steps), summed in a
+                // fixed order at the end
                 float acc_hi[4] = {0.f, 0.f, 0.f, 0.f}, acc_lo[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int k0 = 0; k0 < fs; k0 += 16) {
+                float acc_hi2[4] = {0.f, 0.f, 0.f, 0.f}, acc_lo2[4] = {0.f, 0.f, 0.f, 0.f};
+                auto kstep = [&](int k0, float (&ah)[4], float (&al)[4]) {
                     uint32_t af[4], bf[4];
                     xg_ldsm_x4(af, smem_u32(hb + size_t((lm & 1) * 8 + lr) * fp + k0 + (lm >> 1) * 8));
                     const uint32_t chunk = uint32_t(((k0 & 31) >> 3) + (lm & 1));
                     xg_ldsm_x4(bf, brow + uint32_t((k0 >> 5) * K * 64) + ((chunk ^ sw) << 4));
-                    xg_mma(acc_hi, af, bf[0], bf[1]);
-                    xg_mma(acc_lo, af, bf[2], bf[3]);
+                    xg_mma(ah, af, bf[0], bf[1]);
+                    xg_mma(al, af, bf[2], bf[3]);
+                };
+                int k0 = 0;
+                for (; k0 + 16 < fs; k0 += 32) {  // fs is a multiple of 32
+                    kstep(k0, acc_hi, acc_lo);
+                    kstep(k0 + 16, acc_hi2, acc_lo2);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc_hi[i] += acc_hi2[i];
+                    acc_lo[i] += acc_lo2[i];
                 }
                 const int c = ct * 8 + 2 * t;
 #pragma unroll
