@@ -242,13 +242,13 @@ def measure_e2e(cfg, m, steps, torch, dd):
 NCU_TRAFFIC = {
     ("cfg1_qwen3_4b_c1", "expand_g_kernel"): 15542272,
     ("cfg1_qwen3_4b_c1", "gemm_bf16_tc_kernel"): 18364928,
-    ("cfg4_c64_stress", "contract_tc_kernel"): 35337472 * 8,
+    ("cfg4_c64_stress", "contract_tc_kernel"): 35337472 * 8,   # one launch over all 64 requests
     ("cfg4_c64_stress", "topk_stream_kernel"): int((100288256 + 3384576) * 64 / 20),
 }
 
 
 def kernel_work(cfg, name, accepted_mean, g_path):
-    """Algorithmic work of ONE launch of a kernel family: ("hbm", bytes) or ("tensor", flops)."""
+    """Algorithmic work of a kernel family over ONE round: ("hbm", bytes) or ("tensor", flops)."""
     eb = 2 if cfg.dtype == "bf16" else 4
     C, L, V, H, K, W, B = cfg.C, cfg.L, cfg.V, cfg.H, cfg.K, cfg.W, cfg.B
     P = [1]
@@ -261,15 +261,15 @@ def kernel_work(cfg, name, accepted_mean, g_path):
     if name == "gemm_bf16_tc_kernel":
         if g_path:
             return "tensor", 2 * (C * L * K) * H * H
-        return "tensor", sum(2 * C * p * H * H for p in P) / L
+        return "tensor", sum(2 * C * p * H * H for p in P)
     if name == "contract_tc_kernel":
-        return "hbm", C * K * H * eb + C * 32 * H * 2
+        return "hbm", L * (C * K * H * eb + C * 32 * H * 2)
     if name == "expand_g_kernel":
         return "hbm", 3 * C * L * K * H * 2 + C * L * H * 2
     if name == "select_kernel":
-        return "hbm", sum(C * p * K * 4 for p in P) / L
+        return "hbm", sum(C * p * K * 4 for p in P)
     if name == "state_kernel":
-        return "hbm", 4 * C * W * H * eb
+        return "hbm", (L - 1) * 4 * C * W * H * eb
     if name == "walk_kernel":
         rows_walked = (accepted_mean + 1) if cfg.rows == "node" else L
         return "hbm", C * rows_walked * V * eb
@@ -278,15 +278,29 @@ def kernel_work(cfg, name, accepted_mean, g_path):
     return "hbm", 0
 
 
+# Batches of at least this many requests expand as two halves on two streams.
+SPLIT_MIN_C = 32
+
+
 def kernel_roofline(cfg, m, hbm_peak, tf_peak):
-    """Roofline of the kernel with the largest device time per round."""
+    """Roofline of the kernel family with the largest device time per round:
+    algorithmic work of one launch (the round's work / launches per round) over the
+    average launch time. When the batch expands as two halves on two streams
+    ("concurrent_halves": 2), a launch covers half of the requests and shares the
+    GPU with its sibling, so its own rate understates the pair's."""
     kt, n = m["kernel_times"], m["n_prof"]
     g_path = "expand_g_kernel" in kt
     dom = max(kt, key=lambda k: kt[k][1])
     launches, ms_total = kt[dom]
+    lpr = launches / n
     ms_launch = ms_total / launches
-    bound, work = kernel_work(cfg, dom, m["accepted_mean"], g_path)
+    bound, work_round = kernel_work(cfg, dom, m["accepted_mean"], g_path)
+    work = work_round / lpr
     traffic = NCU_TRAFFIC.get((cfg.name, dom))
+    split = (not g_path) and cfg.C >= SPLIT_MIN_C and dom in ("contract_tc_kernel", "gemm_bf16_tc_kernel",
+                                                               "select_kernel", "state_kernel")
+    if split and traffic is not None:
+        traffic //= 2  # the capture processed whole-batch launches; a launch here is half of them
     if bound == "tensor":
         achieved = work / (ms_launch * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": tf_peak, "unit": "TFLOP/s",
@@ -295,8 +309,10 @@ def kernel_roofline(cfg, m, hbm_peak, tf_peak):
         achieved = work / (ms_launch * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "traffic": traffic, "bytes_per_launch": int(work)}
-    roof.update({"kernel": dom, "ms_per_launch": round(ms_launch, 5), "launches_per_round": launches / n,
+    roof.update({"kernel": dom, "ms_per_launch": round(ms_launch, 5), "launches_per_round": lpr,
                  "share_of_kernel_time": round(ms_total / sum(v[1] for v in kt.values()), 4)})
+    if split:
+        roof["concurrent_halves"] = 2
     per_kernel = {k: {"launches_per_round": round(v[0] / n, 2), "ms_per_round": round(v[1] / n, 4)}
                   for k, v in sorted(kt.items(), key=lambda kv: -kv[1][1])}
     launches_per_round = sum(v[0] for v in kt.values()) / n

@@ -461,4 +461,22 @@ __device__ __forceinline__ void warp_bitonic_desc(uint64_t (&v)[EPL]) {
     }
 }
 
+// Top 16 of two descending 16-key lists held by the two half-warps (lane l of
+// half-warp h holds element l of list h), sorted descending into lanes 0..15:
+// the element-wise maximum of one list and the other reversed is bitonic and
+// holds the 16 largest; a bitonic merge (distances 8, 4, 2, 1) sorts it.
+__device__ __forceinline__ uint64_t xg_merge16(uint64_t v) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t lo = __shfl_sync(0xffffffffu, uint32_t(v), 31 - lane);
+    const uint32_t hi = __shfl_sync(0xffffffffu, uint32_t(v >> 32), 31 - lane);
+    const uint64_t o = (uint64_t(hi) << 32) | lo;
+    uint64_t c = v > o ? v : o;
+#pragma unroll
+    for (int d = 8; d; d >>= 1) {
+        const uint64_t p = shfl_xor_u64(c, d);
+        c = ((lane & d) == 0) ? (c > p ? c : p) : (c < p ? c : p);
+    }
+    return c;
+}
+
 }  // namespace dartree

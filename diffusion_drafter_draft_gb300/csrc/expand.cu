@@ -213,6 +213,124 @@ __global__ void __launch_bounds__(SL_NT) select_kernel(
     (void)h_cur; (void)E; (void)hidden; (void)H; (void)h_next; (void)update_state;
 }
 
+// The same selection for W <= 16, P <= 16 and K <= 1024, one CTA per request:
+// warp p takes parent row p with its K logits in registers (EPL per lane): the
+// log-softmax and scores (the same arithmetic in the same order as above), then
+// the row's best m = min(W, K) keys by m rounds of "largest remaining key of the
+// warp", sorted into a list. The 16 lists (empty beyond P) are merged by a
+// bitonic tree of 16-key merges.
+template <int EPL>
+__global__ void __launch_bounds__(SL_NT) select_rows_kernel(
+    const float* __restrict__ z, const float* __restrict__ s_cur, const int32_t* __restrict__ cand_tok, int P, int K,
+    int W, int L, int d, float beta, int32_t* __restrict__ st_tok, int32_t* __restrict__ st_par,
+    float* __restrict__ st_s, int32_t* __restrict__ st_n, float* __restrict__ s_next) {
+    __shared__ uint64_t lists[16 * 16];
+    __shared__ uint64_t mrg[2 * 8 * 16];
+    const int r = blockIdx.x;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int n = P * K, n_keep = min(W, n), m = min(n_keep, K);
+    if (wid < P) {
+        const int p = wid;
+        const float* zr = z + (size_t(r) * P + p) * K;
+        float zv[EPL];
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            const int c = lane + 32 * j;
+            zv[j] = c < K ? zr[c] : -INFINITY;
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) mx = fmaxf(mx, zv[j]);
+        mx = warp_max(mx);
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j)
+            if (lane + 32 * j < K) sum += expf(zv[j] - mx);
+        sum = warp_sum(sum);
+        const float lse = mx + logf(sum);
+        const float sp = s_cur[size_t(r) * P + p];
+        uint64_t v[EPL];
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            const int c = lane + 32 * j;
+            v[j] = 0ull;
+            if (c < K) {
+                float sc = (sp + (zv[j] - lse)) + beta;
+                sc += 0.f;
+                v[j] = (uint64_t(ord_f32(sc)) << 32) | (0xffffffffu - uint32_t(p * K + c));
+            }
+        }
+        for (int k = 0; k < m; ++k) {
+            uint64_t lm = 0;
+#pragma unroll
+            for (int j = 0; j < EPL; ++j) lm = v[j] > lm ? v[j] : lm;
+            const uint64_t w = warp_max_key64(lm);
+            if (w != 0 && lm == w) {
+#pragma unroll
+                for (int j = 0; j < EPL; ++j)
+                    if (v[j] == w) v[j] = 0;
+            }
+            if (lane == 0) lists[p * 16 + k] = w;
+        }
+    }
+    __syncthreads();
+    // merge tree: level 1, warp w merges lists 2w and 2w + 1
+    const int hl = lane & 15;
+    uint64_t v = 0;
+    if (wid < 8) {
+        const int q = 2 * wid + (lane >> 4);
+        v = (q < P && hl < m) ? lists[q * 16 + hl] : 0ull;
+        v = xg_merge16(v);
+        if (lane < 16) mrg[wid * 16 + lane] = v;
+    }
+    __syncthreads();
+    int in = 0;
+    for (int nm = 4; nm >= 1; nm >>= 1) {
+        if (wid < nm) {
+            v = mrg[in * 128 + (2 * wid + (lane >> 4)) * 16 + hl];
+            v = xg_merge16(v);
+            if (lane < 16) mrg[(1 - in) * 128 + wid * 16 + lane] = v;
+        }
+        in = 1 - in;
+        __syncthreads();
+    }
+    const int32_t* ct = cand_tok + (size_t(r) * L + (d - 1)) * K;
+    const size_t sto = (size_t(r) * L + (d - 1)) * W;
+    for (int k = threadIdx.x; k < W; k += SL_NT) {
+        if (k < n_keep) {
+            const uint64_t key = mrg[in * 128 + k];
+            const uint32_t f = 0xffffffffu - uint32_t(key);
+            const float sc = f32_from_ord(uint32_t(key >> 32));
+            st_tok[sto + k] = ct[f % uint32_t(K)];
+            st_par[sto + k] = int(f / uint32_t(K));
+            st_s[sto + k] = sc;
+            s_next[size_t(r) * n_keep + k] = sc;
+        } else {
+            st_tok[sto + k] = -1;
+            st_par[sto + k] = -1;
+            st_s[sto + k] = 0.f;
+        }
+    }
+    if (threadIdx.x == 0) st_n[size_t(r) * L + (d - 1)] = n_keep;
+}
+
+template <int EPL>
+static void launch_select_rows(const ExpandArgs& a, const float* s_cur, int P, int d, float* s_next, cudaStream_t st) {
+    select_rows_kernel<EPL><<<a.C, SL_NT, 0, st>>>(a.z, s_cur, a.cand_tok, P, a.K, a.W, a.L, d, a.beta, a.st_tok,
+                                                   a.st_par, a.st_s, a.st_n, s_next);
+}
+
+// true when select_rows_kernel covers the shape (and was launched)
+static bool select_rows(const ExpandArgs& a, const float* s_cur, int P, int d, float* s_next, cudaStream_t st) {
+    if (P > 16 || a.W > 16 || a.K > 1024) return false;
+    if (a.K <= 64) launch_select_rows<2>(a, s_cur, P, d, s_next, st);
+    else if (a.K <= 128) launch_select_rows<4>(a, s_cur, P, d, s_next, st);
+    else if (a.K <= 256) launch_select_rows<8>(a, s_cur, P, d, s_next, st);
+    else if (a.K <= 512) launch_select_rows<16>(a, s_cur, P, d, s_next, st);
+    else launch_select_rows<32>(a, s_cur, P, d, s_next, st);
+    return true;
+}
+
 // State rows of the kept children of one depth: h = RMSNorm(h_p + E[tok] +
 // H_d[d-1]) in the storage type. Grid (n_keep, C), one CTA per row; parent and
 // token come from the supertree entries just written. Every thread holds up to
@@ -342,9 +460,10 @@ static int launch_expand_t(const ExpandArgs& a, cudaStream_t st) {
         const int n_keep = P * a.K < a.W ? P * a.K : a.W;
         {
             KTimer kt_(KID_SELECT, st);
-            select_kernel<T><<<a.C, SL_NT, select_smem(P, a.K, a.W), st>>>(
-                a.z, a.sbuf[cur], hb[cur], a.cand_tok, E, hid, P, a.K, a.W, a.H, a.L, d, a.beta, a.st_tok, a.st_par,
-                a.st_s, a.st_n, hb[1 - cur], a.sbuf[1 - cur], d < a.L ? 1 : 0, a.status);
+            if (!select_rows(a, a.sbuf[cur], P, d, a.sbuf[1 - cur], st))
+                select_kernel<T><<<a.C, SL_NT, select_smem(P, a.K, a.W), st>>>(
+                    a.z, a.sbuf[cur], hb[cur], a.cand_tok, E, hid, P, a.K, a.W, a.H, a.L, d, a.beta, a.st_tok,
+                    a.st_par, a.st_s, a.st_n, hb[1 - cur], a.sbuf[1 - cur], d < a.L ? 1 : 0, a.status);
         }
         if (d < a.L)
             {
