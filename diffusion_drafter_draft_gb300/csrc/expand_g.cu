@@ -13,7 +13,10 @@
 // in one batch: z = h . G_hi^T + h . G_lo^T (mma.sync, fp32 accumulation), with
 // no dependence on W_q, so one thread-block cluster per request runs all L
 // depths. CTA q of the cluster owns H/CS features of h, G and E, and parent
-// rows p with p mod CS = q. Per depth, separated by three cluster barriers:
+// rows p with p mod CS = q. Per depth, three exchanges through distributed
+// shared memory, each made of st.async stores that count their bytes on the
+// receiver's mbarrier (no cluster barrier: a receiver waits for exactly the
+// data it needs, and a sender never waits):
 //
 //   1. partial logits over the CTA's features (mma.sync), each parent row sent
 //      to its owner's shared memory (reduce-scatter);
@@ -74,7 +77,7 @@ __host__ __device__ inline XgLayout xg_layout(int fs, int K, int cs, int L) {
     l.sel = take(size_t(XG_MAXW) * 8 + 2 * XG_MAXW * 4, 16);
     l.spar = take(size_t(XG_MAXW) * 4, 16);
     l.stout = take(size_t(L) * XG_MAXW * 8 + size_t(L) * 4, 16);  // supertree of the request, written at the end
-    l.mbar = take(8, 8);                             // prefetch barrier
+    l.mbar = take(4 * 8, 8);                         // prefetch barrier; exchanges A, B, C
     l.total = o;
     return l;
 }
@@ -105,11 +108,19 @@ __device__ __forceinline__ void xg_mma(float (&d)[4], const uint32_t (&a)[4], ui
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ void xg_st_remote_f32(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
+// Remote stores into a peer CTA's shared memory that count their bytes on the
+// peer's mbarrier (addr and bar: shared::cluster addresses from mapa).
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];"
+                 :: "r"(addr), "f"(v), "r"(bar) : "memory");
 }
-__device__ __forceinline__ void xg_st_remote_v2(uint32_t addr, float x, float y) {
-    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" :: "r"(addr), "f"(x), "f"(y) : "memory");
+__device__ __forceinline__ void st_async_v2f32(uint32_t addr, float x, float y, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+                 :: "r"(addr), "f"(x), "f"(y), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void st_async_b64(uint32_t addr, uint64_t v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];"
+                 :: "r"(addr), "l"(v), "r"(bar) : "memory");
 }
 
 template <int CS>
@@ -135,7 +146,10 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
     uint64_t* selk = reinterpret_cast<uint64_t*>(smem + lay.sel);  // kept keys, descending
     int* selx = reinterpret_cast<int*>(selk + XG_MAXW);            // [0..16): parent rank, [16..32): candidate
     float* spar = reinterpret_cast<float*>(smem + lay.spar);       // parent scores
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + lay.mbar);
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + lay.mbar);  // prefetch
+    uint64_t* mbA = mbar + 1;  // partial logits of the owned rows
+    uint64_t* mbB = mbar + 2;  // row lists
+    uint64_t* mbC = mbar + 3;  // partial sums of squares
     uint64_t* stkey = reinterpret_cast<uint64_t*>(smem + lay.stout);  // [L][16] kept keys (0 = none)
     int* stn = reinterpret_cast<int*>(stkey + size_t(L) * XG_MAXW);    // [L] kept per depth
 
@@ -159,7 +173,7 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
     };
 
     if (threadIdx.x == 0) {
-        mbar_init(mbar, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&mbar[i], 1);
         fence_mbar_init();
     }
     for (int i = threadIdx.x; i < L * K; i += XG_NT) {
@@ -170,6 +184,7 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
     for (int f = threadIdx.x; f < fs; f += XG_NT) hs[f] = a.E[size_t(a.anchor[r]) * H + f0 + f];
     if (threadIdx.x == 0) spar[0] = 0.f;
     __syncthreads();
+    cluster_sync();  // every peer's exchange barriers are initialised before any store targets them
     if (threadIdx.x == 0) prefetch(0, L > 1);
     int issued = 1, waited = 0;  // prefetch phases (uniform across the CTA)
     bool pf_ok = true;           // false once a prefetch wait ran out: no further prefetches
@@ -180,6 +195,20 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
         const int ne = P * K;
         const int n_keep = min(W, ne);
         const int m = min(n_keep, K);  // keys per row list
+        const uint32_t par = uint32_t(pos) & 1u;
+        int owned = 0;  // owned rows of this depth
+        for (int sl = 0; sl < RPO; ++sl) owned += int(cr) + CS * sl < P;
+        if (threadIdx.x == 0) {
+            // one arrival per phase: a barrier whose previous phase did not complete
+            // (a wait that ran out) gets none, and the status records the timeout
+            auto arm = [&](uint64_t* b, uint32_t bytes) {
+                if (mbar_try_wait(b, par ^ 1u)) mbar_arrive_expect_tx(b, bytes);
+                else set_status(a.status, DARTREE_ETIMEOUT);
+            };
+            arm(mbA, uint32_t(owned * CS * K * 4));
+            arm(mbB, uint32_t(P * m * 8));
+            if (d < L) arm(mbC, uint32_t(CS * n_keep * 4));
+        }
         // a timed-out wait records ETIMEOUT and the CTA carries on, so that every
         // CTA of the cluster reaches the same barriers
         if (pf_ok) pf_ok = __syncthreads_and(mbar_wait_bounded(mbar, uint32_t(waited) & 1u, a.status) ? 1 : 0) != 0;
@@ -223,17 +252,19 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
                     const int p = g + 8 * hh;
                     if (p < P) {
                         const uint32_t off = z0 + uint32_t(((int(cr) * RPO + p / CS) * K + c) * 4);
-                        xg_st_remote_v2(mapa_u32(off, uint32_t(p % CS)), acc_hi[2 * hh] + acc_lo[2 * hh],
-                                        acc_hi[2 * hh + 1] + acc_lo[2 * hh + 1]);
+                        const uint32_t ow = uint32_t(p % CS);
+                        st_async_v2f32(mapa_u32(off, ow), acc_hi[2 * hh] + acc_lo[2 * hh],
+                                       acc_hi[2 * hh + 1] + acc_lo[2 * hh + 1], mapa_u32(smem_u32(mbA), ow));
                     }
                 }
             }
         }
-        cluster_sync();  // A: partials with their owners; gs free
+        __syncthreads();  // gs free
         // ---- 2. owned rows: z, log-softmax, scores (warp s: row slot s)
         if (wid < RPO) {
             const int p = int(cr) + CS * wid;
             if (p < P) {
+                mbar_wait_bounded(mbA, par, a.status);  // the CS partials of the owned rows
                 float zv[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -285,10 +316,11 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
             if (live && cnt < m) {
                 // lane qd writes the key to CTAs qd, qd + 4, ...
                 const uint32_t off = smem_u32(lists + p * XG_MAXW + cnt);
-                for (int q = qd; q < CS; q += 4) st_dsmem_u64(mapa_u32(off, uint32_t(q)), x);
+                for (int q = qd; q < CS; q += 4)
+                    st_async_b64(mapa_u32(off, uint32_t(q)), x, mapa_u32(smem_u32(mbB), uint32_t(q)));
             }
         }
-        cluster_sync();  // B: every row list everywhere
+        mbar_wait_bounded(mbB, par, a.status);  // every row list
         // ---- 3. top-W: bitonic merge tree over the 16 row lists (slots past m or P
         //         are empty = 0); level 1: warp w merges lists 2w and 2w + 1
         {
@@ -351,10 +383,12 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
                     }
                 }
                 ss = warp_sum(ss);
-                if (lane < CS) xg_st_remote_f32(mapa_u32(smem_u32(ssq + int(cr) * XG_MAXW + k), uint32_t(lane)), ss);
+                if (lane < CS)
+                    st_async_f32(mapa_u32(smem_u32(ssq + int(cr) * XG_MAXW + k), uint32_t(lane)), ss,
+                                 mapa_u32(smem_u32(mbC), uint32_t(lane)));
             }
         }
-        cluster_sync();  // C: every partial sum of squares everywhere
+        mbar_wait_bounded(mbC, par, a.status);  // every partial sum of squares
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
             const int k = wid + rr * XG_NW;

@@ -87,29 +87,16 @@ __global__ void __launch_bounds__(FN_NT) finish_kernel(int L, int W, int B, cons
         for (int d = q; d < L; d += FN_NT) rowk[d] = rowkeys[size_t(r) * L + d];
     const int nv = __syncthreads_count(key != 0);
     const int N = min(B, nv);
-    // ---- global rank: keys above this one. Four lanes share a key (every lane
-    //      counts a quarter of the keys, reading the same pair as its neighbours)
-    //      and four passes cover the 256 keys; the quarter counts meet by shuffles.
+    // ---- global rank: keys above this one (all threads read the same pair at once)
     int above = 0;
     {
         const ulonglong2* k2 = reinterpret_cast<const ulonglong2*>(keys);
-        const int n2 = (n + 1) / 2, qd = q & 3;
-        for (int pass = 0; pass < 4; ++pass) {
-            const int kq = (q >> 2) + 64 * pass;  // the key these four lanes rank
-            const uint64_t x = keys[kq];
-            int cnt = 0;
+        const int n2 = (n + 1) / 2;
 #pragma unroll 4
-            for (int i = qd; i < n2; i += 4) {
-                const ulonglong2 v = k2[i];
-                cnt += (v.x > x) + (v.y > x);
-            }
-            cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
-            cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
-            if (qd == 0) slot[kq] = cnt;
+        for (int i = 0; i < n2; ++i) {
+            const ulonglong2 v = k2[i];
+            above += (v.x > key) + (v.y > key);
         }
-        __syncthreads();
-        above = slot[q];
-        __syncthreads();
     }
     const bool ch = key != 0 && above < N;
     // ---- slots in (depth, rank) order
