@@ -123,6 +123,13 @@ __device__ __forceinline__ void st_async_b64(uint32_t addr, uint64_t v, uint32_t
                  :: "r"(addr), "l"(v), "r"(bar) : "memory");
 }
 
+// Sum over the 16 lanes of a half-warp (every lane of the warp takes part).
+__device__ __forceinline__ float half_sum(float v) {
+#pragma unroll
+    for (int m = 8; m; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+
 template <int CS>
 __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __grid_constant__ CUtensorMap tm_ghi,
                                                              const __grid_constant__ CUtensorMap tm_glo,
@@ -353,56 +360,64 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
         if (threadIdx.x < XG_MAXW) stkey[pos * XG_MAXW + threadIdx.x] = threadIdx.x < n_keep ? selk[threadIdx.x] : 0ull;
         if (threadIdx.x == 0) stn[pos] = n_keep;
         if (d == L) break;  // no remote access follows barrier B of the last depth
-        // ---- state slices of the kept children: warp w owns rows w and w + 8,
-        //      lane j the 8-feature chunk j
+        // ---- state slices of the kept children: half-warp k owns row k, its lane
+        //      j the 8-feature chunks j and j + 16
         const uint16_t* hb = hs + size_t(cur) * XG_MAXW * fp;
         uint16_t* hn = hs + size_t(1 - cur) * XG_MAXW * fp;
         const uint16_t* eb = es + size_t(pos & 1) * K * fs;
         const uint16_t* hdb = hds + size_t(pos & 1) * fs;
+        const int k = threadIdx.x >> 4, hl = threadIdx.x & 15;
+        const bool row_ok = k < n_keep;
         float x[2][8];
+        {
+            float ss = 0.f;
+            if (row_ok) {
+                const uint16_t* hp = hb + size_t(selx[k]) * fp;
+                const uint16_t* er = eb + size_t(selx[XG_MAXW + k]) * fs;
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            const int k = wid + rr * XG_NW;
-            if (k < n_keep) {
-                float ss = 0.f;
-                if (lane < cpr) {
-                    const uint4 vp = *reinterpret_cast<const uint4*>(hb + size_t(selx[k]) * fp + lane * 8);
-                    const uint4 ve = *reinterpret_cast<const uint4*>(eb + size_t(selx[XG_MAXW + k]) * fs + lane * 8);
-                    const uint4 vh = *reinterpret_cast<const uint4*>(hdb + lane * 8);
-                    const uint32_t* wp = reinterpret_cast<const uint32_t*>(&vp);
-                    const uint32_t* we = reinterpret_cast<const uint32_t*>(&ve);
-                    const uint32_t* wh = reinterpret_cast<const uint32_t*>(&vh);
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int j = hl + 16 * cc;
+                    if (j < cpr) {
+                        const uint4 vp = *reinterpret_cast<const uint4*>(hp + j * 8);
+                        const uint4 ve = *reinterpret_cast<const uint4*>(er + j * 8);
+                        const uint4 vh = *reinterpret_cast<const uint4*>(hdb + j * 8);
+                        const uint32_t* wp = reinterpret_cast<const uint32_t*>(&vp);
+                        const uint32_t* we = reinterpret_cast<const uint32_t*>(&ve);
+                        const uint32_t* wh = reinterpret_cast<const uint32_t*>(&vh);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int sh = (i & 1) ? 16 : 0;
-                        const float xv = (bf16_bits_to_float((wp[i >> 1] >> sh) & 0xffffu) +
-                                          bf16_bits_to_float((we[i >> 1] >> sh) & 0xffffu)) +
-                                         bf16_bits_to_float((wh[i >> 1] >> sh) & 0xffffu);
-                        x[rr][i] = xv;
-                        ss = fmaf(xv, xv, ss);
+                        for (int i = 0; i < 8; ++i) {
+                            const int sh = (i & 1) ? 16 : 0;
+                            const float xv = (bf16_bits_to_float((wp[i >> 1] >> sh) & 0xffffu) +
+                                              bf16_bits_to_float((we[i >> 1] >> sh) & 0xffffu)) +
+                                             bf16_bits_to_float((wh[i >> 1] >> sh) & 0xffffu);
+                            x[cc][i] = xv;
+                            ss = fmaf(xv, xv, ss);
+                        }
                     }
                 }
-                ss = warp_sum(ss);
-                if (lane < CS)
-                    st_async_f32(mapa_u32(smem_u32(ssq + int(cr) * XG_MAXW + k), uint32_t(lane)), ss,
-                                 mapa_u32(smem_u32(mbC), uint32_t(lane)));
             }
+            ss = half_sum(ss);  // both half-warps of a warp take part
+            if (row_ok && hl < CS)
+                st_async_f32(mapa_u32(smem_u32(ssq + int(cr) * XG_MAXW + k), uint32_t(hl)), ss,
+                             mapa_u32(smem_u32(mbC), uint32_t(hl)));
         }
         mbar_wait_bounded(mbC, par, a.status);  // every partial sum of squares
+        if (row_ok) {
+            float tot = 0.f;
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            const int k = wid + rr * XG_NW;
-            if (k < n_keep && lane < cpr) {
-                float tot = 0.f;
+            for (int q = 0; q < CS; ++q) tot += ssq[q * XG_MAXW + k];
+            const float inv = 1.0f / sqrtf(tot / float(H) + 1e-6f);
 #pragma unroll
-                for (int q = 0; q < CS; ++q) tot += ssq[q * XG_MAXW + k];
-                const float inv = 1.0f / sqrtf(tot / float(H) + 1e-6f);
-                uint32_t w4[4];
+            for (int cc = 0; cc < 2; ++cc) {
+                const int j = hl + 16 * cc;
+                if (j < cpr) {
+                    uint32_t w4[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    w4[i] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(x[rr][2 * i] * inv))) |
-                            (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(x[rr][2 * i + 1] * inv))) << 16);
-                *reinterpret_cast<uint4*>(hn + size_t(k) * fp + lane * 8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    for (int i = 0; i < 4; ++i)
+                        w4[i] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(x[cc][2 * i] * inv))) |
+                                (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(x[cc][2 * i + 1] * inv))) << 16);
+                    *reinterpret_cast<uint4*>(hn + size_t(k) * fp + j * 8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
             }
         }
         if (threadIdx.x < n_keep) spar[threadIdx.x] = f32_from_ord(uint32_t(selk[threadIdx.x] >> 32));
