@@ -205,19 +205,8 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
         const uint32_t par = uint32_t(pos) & 1u;
         int owned = 0;  // owned rows of this depth
         for (int sl = 0; sl < RPO; ++sl) owned += int(cr) + CS * sl < P;
-        if (threadIdx.x == 0) {
-            // one arrival per phase: a barrier whose previous phase did not complete
-            // (a wait that ran out) gets none, and the status records the timeout
-            auto arm = [&](uint64_t* b, uint32_t bytes) {
-                if (mbar_try_wait(b, par ^ 1u)) mbar_arrive_expect_tx(b, bytes);
-                else set_status(a.status, DARTREE_ETIMEOUT);
-            };
-            arm(mbA, uint32_t(owned * CS * K * 4));
-            arm(mbB, uint32_t(P * m * 8));
-            if (d < L) arm(mbC, uint32_t(CS * n_keep * 4));
-        }
-        // a timed-out wait records ETIMEOUT and the CTA carries on, so that every
-        // CTA of the cluster reaches the same barriers
+        // a timed-out prefetch wait records ETIMEOUT and the CTA carries on with the
+        // exchanges, so that no peer is left waiting for its data
         if (pf_ok) pf_ok = __syncthreads_and(mbar_wait_bounded(mbar, uint32_t(waited) & 1u, a.status) ? 1 : 0) != 0;
         else __syncthreads();
         if (pf_ok) waited = issued;
@@ -265,6 +254,19 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
                     }
                 }
             }
+        }
+        // arm this depth's exchange barriers (data that lands before the arrival
+        // only drives the transaction count negative for a while)
+        if (threadIdx.x == 0) {
+            // one arrival per phase: a barrier whose previous phase did not complete
+            // (a wait that ran out) gets none, and the status records the timeout
+            auto arm = [&](uint64_t* b, uint32_t bytes) {
+                if (mbar_try_wait(b, par ^ 1u)) mbar_arrive_expect_tx(b, bytes);
+                else set_status(a.status, DARTREE_ETIMEOUT);
+            };
+            arm(mbA, uint32_t(owned * CS * K * 4));
+            arm(mbB, uint32_t(P * m * 8));
+            if (d < L) arm(mbC, uint32_t(CS * n_keep * 4));
         }
         __syncthreads();  // gs free
         // ---- 2. owned rows: z, log-softmax, scores (warp s: row slot s)
@@ -336,22 +338,26 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
             v = xg_merge16(v);
             if (lane < 16) mrg[wid * 16 + lane] = v;
             __syncthreads();
-            int in = 0;
-            for (int nm = XG_NW / 2; nm >= 1; nm >>= 1) {  // merges at this level
-                if (wid < nm) {
-                    v = mrg[in * XG_NW * 16 + (2 * wid + (lane >> 4)) * 16 + hl];
-                    v = xg_merge16(v);
-                    if (lane < 16) mrg[(1 - in) * XG_NW * 16 + wid * 16 + lane] = v;
-                }
-                in = 1 - in;
-                __syncthreads();
+            // level 2: warps 0..3
+            if (wid < 4) {
+                v = mrg[(2 * wid + (lane >> 4)) * 16 + hl];
+                v = xg_merge16(v);
+                if (lane < 16) mrg[XG_NW * 16 + wid * 16 + lane] = v;
             }
-            if (threadIdx.x < n_keep) {
-                const uint64_t x = mrg[in * XG_NW * 16 + threadIdx.x];
-                const uint32_t f = 0xffffffffu - uint32_t(x);
-                selk[threadIdx.x] = x;
-                selx[threadIdx.x] = int(f) / K;
-                selx[XG_MAXW + threadIdx.x] = int(f) % K;
+            __syncthreads();
+            // levels 3 and 4 in warp 0: lists 0+1 and 2+3, then the two results
+            if (wid == 0) {
+                const uint64_t ab = xg_merge16(mrg[XG_NW * 16 + (lane >> 4) * 16 + hl]);
+                const uint64_t cd = xg_merge16(mrg[XG_NW * 16 + (2 + (lane >> 4)) * 16 + hl]);
+                const uint32_t lo = __shfl_up_sync(0xffffffffu, uint32_t(cd), 16);
+                const uint32_t hi = __shfl_up_sync(0xffffffffu, uint32_t(cd >> 32), 16);
+                const uint64_t x = xg_merge16(lane < 16 ? ab : ((uint64_t(hi) << 32) | lo));
+                if (lane < n_keep) {
+                    const uint32_t f = 0xffffffffu - uint32_t(x);
+                    selk[lane] = x;
+                    selx[lane] = int(f) / K;
+                    selx[XG_MAXW + lane] = int(f) % K;
+                }
             }
         }
         __syncthreads();
