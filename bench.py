@@ -240,7 +240,7 @@ def measure_e2e(cfg, m, steps, torch, dd):
 # this workload; the C=64 contraction and top-K were captured on fewer requests (8
 # and 20 of them) and scaled by the requests processed (their traffic is per request).
 NCU_TRAFFIC = {
-    ("cfg1_qwen3_4b_c1", "expand_g_kernel"): 15542272,
+    ("cfg1_qwen3_4b_c1", "expand_g_kernel"): 15546112,
     ("cfg1_qwen3_4b_c1", "gemm_bf16_tc_kernel"): 18364928,
     ("cfg4_c64_stress", "contract_tc_kernel"): 35337472 * 8,   # one launch over all 64 requests
     ("cfg4_c64_stress", "topk_stream_kernel"): int((100288256 + 3384576) * 64 / 20),
