@@ -247,15 +247,17 @@ NCU_TRAFFIC = {
 }
 
 
-def kernel_work(cfg, name, accepted_mean, g_path):
-    """Algorithmic work of a kernel family over ONE round: ("hbm", bytes) or ("tensor", flops)."""
+def kernel_work(cfg, name, accepted_mean, g_path, fused_gather=False):
+    """Algorithmic work of a kernel family over ONE round: ("hbm", bytes) or ("tensor", flops).
+    fused_gather: the cluster top-K also copied the candidates' rows of E."""
     eb = 2 if cfg.dtype == "bf16" else 4
     C, L, V, H, K, W, B = cfg.C, cfg.L, cfg.V, cfg.H, cfg.K, cfg.W, cfg.B
     P = [1]
     for _ in range(L - 1):
         P.append(min(W, P[-1] * K))
     if name in ("topk_rows_kernel", "topk_stream_kernel", "rowmax_kernel"):
-        return "hbm", C * L * V * eb
+        gather = 2 * C * L * K * H * 2 if (fused_gather and name == "topk_rows_kernel") else 0
+        return "hbm", C * L * V * eb + gather
     if name == "gather_rows_kernel":
         return "hbm", 2 * C * L * K * H * eb
     if name == "gemm_bf16_tc_kernel":
@@ -294,7 +296,8 @@ def kernel_roofline(cfg, m, hbm_peak, tf_peak):
     launches, ms_total = kt[dom]
     lpr = launches / n
     ms_launch = ms_total / launches
-    bound, work_round = kernel_work(cfg, dom, m["accepted_mean"], g_path)
+    fused = g_path and "gather_rows_kernel" not in kt
+    bound, work_round = kernel_work(cfg, dom, m["accepted_mean"], g_path, fused)
     work = work_round / lpr
     traffic = NCU_TRAFFIC.get((cfg.name, dom))
     split = (not g_path) and cfg.C >= SPLIT_MIN_C and dom in ("contract_tc_kernel", "gemm_bf16_tc_kernel",

@@ -95,7 +95,7 @@ int finish_tree(const dartree_params* p, const dartree_supertree* sp, const int3
     if (finish_supported(p->L, p->W))
         return launch_finish(p->C, p->L, p->W, p->B, sp->tok, sp->par, sp->score, sp->n, anchor, tree->tok,
                              tree->par, tree->depth, tree->score, tree->n_nodes, tree->mask, tree->pos, nullptr,
-                             nullptr, nullptr, nullptr, status, s);
+                             nullptr, nullptr, nullptr, status, s, true);
     if (int e = launch_prune(p->C, p->L, p->W, p->B, sp->tok, sp->par, sp->score, sp->n, anchor, tree->tok, tree->par,
                              tree->depth, tree->score, tree->n_nodes, status, s))
         return e;
@@ -187,9 +187,9 @@ int dartree_topk(const void* logits, int rows, int V, int K, int dtype, int32_t*
     return launch_topk(logits, rows, V, K, dtype, tok, val, at<int>(ws, 0), as_stream(stream));
 }
 
-static int expand_impl(const dartree_head* head, const dartree_params* p, const void* hidden, const int32_t* anchor,
-                       const int32_t* cand_tok, const float* cand_val, const dartree_supertree* st, void* ws,
-                       const Layout& l, cudaStream_t stream) {
+static ExpandArgs expand_args(const dartree_head* head, const dartree_params* p, const void* hidden,
+                              const int32_t* anchor, const int32_t* cand_tok, const float* cand_val,
+                              const dartree_supertree* st, void* ws, const Layout& l) {
     ExpandArgs a{};
     a.E = head->E;
     a.Wq = head->Wq;
@@ -225,7 +225,28 @@ static int expand_impl(const dartree_head* head, const dartree_params* p, const 
     a.Ghi = l.g_rows ? at<uint16_t>(ws, l.Ghi) : nullptr;
     a.Glo = l.g_rows ? at<uint16_t>(ws, l.Glo) : nullptr;
     a.status = at<int>(ws, l.status);
-    return launch_expand(a, stream);
+    return a;
+}
+
+static int expand_impl(const dartree_head* head, const dartree_params* p, const void* hidden, const int32_t* anchor,
+                       const int32_t* cand_tok, const float* cand_val, const dartree_supertree* st, void* ws,
+                       const Layout& l, cudaStream_t stream) {
+    return launch_expand(expand_args(head, p, hidden, anchor, cand_tok, cand_val, st, ws, l), stream);
+}
+
+// S1 of a whole tree build into ct/cv; when the expansion a describes takes the
+// candidate-side projection path, the same launch may also copy the candidates'
+// rows of E into a.Eg (a.eg_ready says whether it did).
+static int topk_for_expand(const dartree_head* head, const dartree_params* p, const void* base_logits, int32_t* ct,
+                           float* cv, int* status, ExpandArgs& a, cudaStream_t s) {
+    const TopkGather g{static_cast<const uint16_t*>(head->E), head->H, a.Eg};
+    bool gathered = false;
+    const bool want = expand_g_fits(a);
+    if (int e = launch_topk(base_logits, p->C * p->L, head->V, p->K, head->dtype, ct, cv, status, s,
+                            want ? &g : nullptr, &gathered))
+        return e;
+    a.eg_ready = gathered;
+    return DARTREE_OK;
 }
 
 static bool st_ok(const dartree_supertree* st) { return st && st->tok && st->par && st->score && st->n; }
@@ -283,8 +304,9 @@ int dartree_build_tree(const dartree_head* head, const dartree_params* p, const 
                           at<int32_t>(ws, l.st_n)};
     const dartree_supertree* sp = st ? st : &wst;
     int* status = at<int>(ws, l.status);
-    if (int e = launch_topk(base_logits, p->C * p->L, head->V, p->K, head->dtype, ct, cv, status, s)) return e;
-    if (int e = expand_impl(head, p, block_hidden, anchor, ct, cv, sp, ws, l, s)) return e;
+    ExpandArgs a = expand_args(head, p, block_hidden, anchor, ct, cv, sp, ws, l);
+    if (int e = topk_for_expand(head, p, base_logits, ct, cv, status, a, s)) return e;
+    if (int e = launch_expand(a, s)) return e;
     return finish_tree(p, sp, anchor, tree, status, s);
 }
 
@@ -312,7 +334,8 @@ int dartree_round(const dartree_head* head, const dartree_params* p, const void*
     // S1 first; the target-row maxima (per-position rows) then run on a side
     // stream forked here, overlapping the expansion, which leaves most SMs idle
     // for small batches (forked before S1 they would compete with it for HBM)
-    if (int e = launch_topk(base_logits, p->C * p->L, head->V, p->K, head->dtype, ct, cv, status, s)) return e;
+    ExpandArgs a = expand_args(head, p, block_hidden, anchor, ct, cv, &st, ws, l);
+    if (int e = topk_for_expand(head, p, base_logits, ct, cv, status, a, s)) return e;
     std::unique_lock<std::recursive_mutex> lock(side_mutex(), std::defer_lock);
     SideStreams* side = nullptr;
     if (per_pos) {
@@ -329,12 +352,12 @@ int dartree_round(const dartree_head* head, const dartree_params* p, const void*
             if (int e = launch_rowmax_position(p->C, p->L, head->V, head->dtype, target, rowkeys, s)) return e;
         }
     }
-    if (int e = expand_impl(head, p, block_hidden, anchor, ct, cv, &st, ws, l, s)) return e;
+    if (int e = launch_expand(a, s)) return e;
     if (side && cudaStreamWaitEvent(s, side->join[0], 0) != cudaSuccess) return DARTREE_ECUDA;
-    if (per_pos && finish_supported(p->L, p->W))
+    if (per_pos && finish_supported(p->L, p->W))  // (set-up overlapping the expansion's tail)
         return launch_finish(p->C, p->L, p->W, p->B, st.tok, st.par, st.score, st.n, anchor, tree->tok, tree->par,
                              tree->depth, tree->score, tree->n_nodes, tree->mask, tree->pos, rowkeys, accepted_len,
-                             path, bonus, status, s);
+                             path, bonus, status, s, true);
     if (int e = finish_tree(p, &st, anchor, tree, status, s)) return e;
     if (per_pos)
         return launch_walk_position(p->C, p->L, p->B, tree->tok, tree->par, tree->depth, tree->n_nodes, rowkeys,

@@ -179,20 +179,24 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
         }
     };
 
+    griddep_launch_dependents();
     if (threadIdx.x == 0) {
         for (int i = 0; i < 4; ++i) mbar_init(&mbar[i], 1);
         fence_mbar_init();
-    }
-    for (int i = threadIdx.x; i < L * K; i += XG_NT) {
-        ctok[i] = a.cand_tok[size_t(r) * L * K + i];
-        cval[i] = a.cand_val[size_t(r) * L * K + i];
     }
     // root: h = E[anchor] (this CTA's slice), s = 0
     for (int f = threadIdx.x; f < fs; f += XG_NT) hs[f] = a.E[size_t(a.anchor[r]) * H + f0 + f];
     if (threadIdx.x == 0) spar[0] = 0.f;
     __syncthreads();
     cluster_sync();  // every peer's exchange barriers are initialised before any store targets them
+    // the candidates, their rows and G come from the kernels before this one
+    griddep_wait();
     if (threadIdx.x == 0) prefetch(0, L > 1);
+    for (int i = threadIdx.x; i < L * K; i += XG_NT) {
+        ctok[i] = a.cand_tok[size_t(r) * L * K + i];
+        cval[i] = a.cand_val[size_t(r) * L * K + i];
+    }
+    __syncthreads();
     int issued = 1, waited = 0;  // prefetch phases (uniform across the CTA)
     bool pf_ok = true;           // false once a prefetch wait ran out: no further prefetches
     int cur = 0, P = 1;
@@ -546,13 +550,14 @@ static int xg_launch(const XgArgs& x, const CUtensorMap& ghi, const CUtensorMap&
     cfg.blockDim = dim3(XG_NT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();  // the prologue overlaps the GEMM's tail
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     KTimer kt_(KID_EXPAND_G, stream);
     return cudaLaunchKernelEx(&cfg, expand_g_kernel<CS>, x, ghi, glo, eg) == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
@@ -561,31 +566,47 @@ static int xg_launch(const XgArgs& x, const CUtensorMap& ghi, const CUtensorMap&
 // 16-byte chunk per lane in the state update, one E tile).
 static bool xg_fs_ok(int H, int cs) { return H % (cs * XG_GB) == 0 && H / cs <= 256; }
 
-int try_launch_expand_g(const ExpandArgs& a, cudaStream_t stream, bool* launched) {
-    *launched = false;
-    if (a.dtype != DARTREE_BF16 || !a.WqT || !a.Eg || !a.Ghi || !a.Glo) return DARTREE_OK;
+// Cluster size of the path for these arguments (0: it does not apply) and its
+// shared memory.
+static int xg_plan(const ExpandArgs& a, size_t* smem) {
+    if (a.dtype != DARTREE_BF16 || !a.WqT || !a.Eg || !a.Ghi || !a.Glo) return 0;
     const int M = a.C * a.L * a.K;
-    if (M > a.g_rows || a.K > XG_MAXK || a.K % 8 != 0 || a.W > XG_MAXW) return DARTREE_OK;
-    if (!gemm_tc_supported(M, a.H, a.H) || a.H / 8 > GR_MAXV * GR_NT) return DARTREE_OK;
-    int cs = 0;
-    size_t smem = 0;
+    if (M > a.g_rows || a.K > XG_MAXK || a.K % 8 != 0 || a.W > XG_MAXW) return 0;
+    if (!gemm_tc_supported(M, a.H, a.H) || a.H / 8 > GR_MAXV * GR_NT) return 0;
     if (xg_fs_ok(a.H, 16)) {
         const size_t sm = xg_layout(a.H / 16, a.K, 16, a.L).total;
-        if (sm <= 227 * 1024 && xg_cluster_ok<16>(sm)) { cs = 16; smem = sm; }
+        if (sm <= 227 * 1024 && xg_cluster_ok<16>(sm)) { *smem = sm; return 16; }
     }
-    if (!cs && xg_fs_ok(a.H, 8)) {
+    if (xg_fs_ok(a.H, 8)) {
         const size_t sm = xg_layout(a.H / 8, a.K, 8, a.L).total;
-        if (sm <= 227 * 1024 && xg_cluster_ok<8>(sm)) { cs = 8; smem = sm; }
+        if (sm <= 227 * 1024 && xg_cluster_ok<8>(sm)) { *smem = sm; return 8; }
     }
+    return 0;
+}
+
+bool expand_g_fits(const ExpandArgs& a) {
+    size_t smem = 0;
+    return xg_plan(a, &smem) != 0;
+}
+
+int try_launch_expand_g(const ExpandArgs& a, cudaStream_t stream, bool* launched) {
+    *launched = false;
+    size_t smem = 0;
+    const int cs = xg_plan(a, &smem);
     if (!cs) return DARTREE_OK;
+    const int M = a.C * a.L * a.K;
     *launched = true;
-    {
-        KTimer kt_(KID_GATHER, stream);
-        gather_rows_kernel<<<(M + GR_ROWS - 1) / GR_ROWS, GR_NT, 0, stream>>>(static_cast<const uint16_t*>(a.E),
-                                                                              a.cand_tok, a.H, M, a.Eg);
+    if (!a.eg_ready) {
+        {
+            KTimer kt_(KID_GATHER, stream);
+            gather_rows_kernel<<<(M + GR_ROWS - 1) / GR_ROWS, GR_NT, 0, stream>>>(
+                static_cast<const uint16_t*>(a.E), a.cand_tok, a.H, M, a.Eg);
+        }
+        if (cudaGetLastError() != cudaSuccess) return DARTREE_ECUDA;
     }
-    if (cudaGetLastError() != cudaSuccess) return DARTREE_ECUDA;
-    if (int e = launch_gemm_bf16_tc(a.Eg, a.WqT, M, a.H, a.H, 2, nullptr, a.Ghi, 1, a.status, stream, a.Glo)) return e;
+    // the GEMM's W_q^T tiles and set-up overlap the previous kernel's tail
+    if (int e = launch_gemm_bf16_tc(a.Eg, a.WqT, M, a.H, a.H, 2, nullptr, a.Ghi, 1, a.status, stream, a.Glo, true))
+        return e;
     const int fs = a.H / cs;
     CUtensorMap ghi, glo, eg;
     if (!make_tensor_map_bf16(&ghi, a.Ghi, M, a.H, XG_GB, a.K, 64) ||

@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(FN_NT) finish_kernel(int L, int W, int B, cons
                                                        int32_t* __restrict__ accepted, int32_t* __restrict__ path,
                                                        int32_t* __restrict__ bonus, int* status) {
     extern __shared__ __align__(16) uint8_t smem[];
+    griddep_wait();  // the supertree comes from the kernel before this one
     const FnSmem fl = fn_smem(L, B);
     uint64_t* keys = reinterpret_cast<uint64_t*>(smem + fl.keys);
     int* slot = reinterpret_cast<int*>(smem + fl.slot);
@@ -214,7 +215,7 @@ bool finish_supported(int L, int W) { return L * W <= FN_NT; }
 int launch_finish(int C, int L, int W, int B, const int32_t* st_tok, const int32_t* st_par, const float* st_s,
                   const int32_t* st_n, const int32_t* anchor, int32_t* tok, int32_t* par, int32_t* depth,
                   float* score, int32_t* n_nodes, uint8_t* mask, int32_t* pos, const unsigned long long* rowkeys,
-                  int32_t* accepted, int32_t* path, int32_t* bonus, int* status, cudaStream_t stream) {
+                  int32_t* accepted, int32_t* path, int32_t* bonus, int* status, cudaStream_t stream, bool pdl) {
     if (C == 0) return DARTREE_OK;
     if (!finish_supported(L, W)) return DARTREE_EUNSUPPORTED;
     const size_t smem = fn_smem(L, B).bytes;
@@ -222,12 +223,21 @@ int launch_finish(int C, int L, int W, int B, const int32_t* st_tok, const int32
     auto kern = walk ? finish_kernel<true> : finish_kernel<false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
         return DARTREE_ECUDA;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(unsigned(C));
+    cfg.blockDim = dim3(FN_NT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e;
     {
         KTimer kt_(KID_FINISH, stream);
-        kern<<<C, FN_NT, smem, stream>>>(L, W, B, st_tok, st_par, st_s, st_n, anchor, tok, par, depth, score, n_nodes,
-                                         mask, pos, rowkeys, accepted, path, bonus, status);
+        e = cudaLaunchKernelEx(&cfg, kern, L, W, B, st_tok, st_par, st_s, st_n, anchor, tok, par, depth, score,
+                               n_nodes, mask, pos, rowkeys, accepted, path, bonus, status);
     }
-    return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
+    return e == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 
 }  // namespace dartree

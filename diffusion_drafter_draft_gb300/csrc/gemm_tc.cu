@@ -76,19 +76,30 @@ __global__ void __launch_bounds__(GT_NT, 1) gemm_bf16_tc_kernel(const __grid_con
     tc::fence_after_sync();
     const uint32_t tmem = *slot;
 
+    griddep_launch_dependents();
     if (warp == 0 && lane == 0) {
-        // producer: TMA ring
+        // producer: TMA ring. B is not written by the previous kernel of the stream:
+        // the first stages' B tiles load before the dependency wait, A after it.
+        const int npre = nk < L::STAGES ? nk : L::STAGES;
+        for (int kb = 0; kb < npre; ++kb) {
+            mbar_arrive_expect_tx(&full[kb], uint32_t(L::STAGE));
+            tc::tma_load_2d(smem + kb * L::STAGE + L::A_BYTES, &tmB, kb * GT_BK, n0, &full[kb]);
+        }
+        griddep_wait();
         for (int kb = 0; kb < nk; ++kb) {
             const int s = kb % L::STAGES;
             const uint32_t ph = uint32_t(kb / L::STAGES) & 1u;
-            if (!mbar_wait_bounded(&empty[s], ph ^ 1u, status)) break;
             uint8_t* sa = smem + s * L::STAGE;
-            mbar_arrive_expect_tx(&full[s], uint32_t(L::STAGE));
+            if (kb >= npre) {
+                if (!mbar_wait_bounded(&empty[s], ph ^ 1u, status)) break;
+                mbar_arrive_expect_tx(&full[s], uint32_t(L::STAGE));
+                tc::tma_load_2d(sa + L::A_BYTES, &tmB, kb * GT_BK, n0, &full[s]);
+            }
             tc::tma_load_2d(sa, &tmA, kb * GT_BK, m0, &full[s]);
-            tc::tma_load_2d(sa + L::A_BYTES, &tmB, kb * GT_BK, n0, &full[s]);
         }
     } else if (warp == 1 && lane == 0) {
-        // MMA issuer
+        // MMA issuer (its bounded waits start once the operands can arrive)
+        griddep_wait();
         constexpr uint32_t idesc = tc::idesc_bf16_f32(GT_BM, BN);
         bool ok = true;
         for (int kb = 0; kb < nk && ok; ++kb) {
@@ -107,6 +118,7 @@ __global__ void __launch_bounds__(GT_NT, 1) gemm_bf16_tc_kernel(const __grid_con
         tc::mma_commit(accum);
     }
     __syncwarp();
+    griddep_wait();  // (the producer's wait already covers the operands; this orders the stores)
 
     // epilogue: TMEM -> registers -> global
     const bool have = mbar_wait_bounded(accum, 0, status);
@@ -197,23 +209,31 @@ bool gemm_tc_supported(int M, int N, int K) {
 
 template <int BN>
 static int launch_gemm_bn(const void* A, const void* B, int M, int N, int K, const GemmOut& o, int* status,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool pdl) {
     CUtensorMap ta, tb;
     if (!make_map(&ta, A, M, K, GT_BM) || !make_map(&tb, B, N, K, BN)) return DARTREE_ECUDA;
     const size_t smem = GtSmem<BN>::TOTAL;
     auto kern = gemm_bf16_tc_kernel<BN>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
         return DARTREE_ECUDA;
-    dim3 grid(N / BN, (M + GT_BM - 1) / GT_BM);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(N / BN, (M + GT_BM - 1) / GT_BM);
+    cfg.blockDim = dim3(GT_NT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e;
     {
         KTimer kt_(KID_GEMM, stream);
-        kern<<<grid, GT_NT, smem, stream>>>(ta, tb, M, N, K, o, status);
+        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, M, N, K, o, status);
     }
-    return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
+    return e == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
 
 int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int mode, float* d32, uint16_t* hilo,
-                        int P, int* status, cudaStream_t stream, uint16_t* lo2) {
+                        int P, int* status, cudaStream_t stream, uint16_t* lo2, bool pdl) {
     if (!gemm_tc_supported(M, N, K)) return DARTREE_EUNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) % 16) return DARTREE_EINVAL;
     if (mode == 1 && (P < 1 || P > 16 || !hilo)) return DARTREE_EINVAL;
@@ -231,9 +251,9 @@ int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int m
         const long cost = waves * (GT_BM + bn);
         if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = bn; }
     }
-    if (best == 256) return launch_gemm_bn<256>(A, B, M, N, K, o, status, stream);
-    if (best == 160) return launch_gemm_bn<160>(A, B, M, N, K, o, status, stream);
-    return launch_gemm_bn<128>(A, B, M, N, K, o, status, stream);
+    if (best == 256) return launch_gemm_bn<256>(A, B, M, N, K, o, status, stream, pdl);
+    if (best == 160) return launch_gemm_bn<160>(A, B, M, N, K, o, status, stream, pdl);
+    return launch_gemm_bn<128>(A, B, M, N, K, o, status, stream, pdl);
 }
 
 }  // namespace dartree

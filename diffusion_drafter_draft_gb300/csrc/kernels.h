@@ -38,9 +38,28 @@ struct KTimer {
 
 int num_sms();
 
-// S1: top-K of `rows` rows of V values.
+// Launch attribute of programmatic dependent launch: the kernel may start while the
+// previous kernel of the stream finishes; it calls griddep_wait before it touches
+// anything that kernel (or one before it) writes.
+inline cudaLaunchAttribute pdl_attribute() {
+    cudaLaunchAttribute a{};
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+    return a;
+}
+
+// Rows of a bf16 [V, H] matrix copied, per top-K row r and rank i, to out[r*K + i]
+// by the top-K launch itself (the candidate rows of the candidate-side projection).
+struct TopkGather {
+    const uint16_t* E;
+    int H;
+    uint16_t* out;
+};
+
+// S1: top-K of `rows` rows of V values. With g, *gathered tells whether the rows of
+// g->E were copied too (only some launch shapes do; otherwise the caller copies them).
 int launch_topk(const void* x, int rows, int V, int K, int dtype, int32_t* tok, float* val, int* status,
-                cudaStream_t stream);
+                cudaStream_t stream, const TopkGather* g = nullptr, bool* gathered = nullptr);
 
 struct ExpandArgs {
     const void* E;
@@ -63,6 +82,7 @@ struct ExpandArgs {
     uint16_t* uhl;            // [C, 32, H] bf16 hi/lo projection rows (tensor-core contraction), or null
     const void* WqT;          // [H, H] W_q transposed (prepared head), or null
     uint16_t* Eg;             // [C*L*K, H] gathered candidate rows (candidate-side projection path)
+    bool eg_ready;            // Eg already holds E[cand_tok] (copied by the top-K launch)
     uint16_t* Ghi;            // [C*L*K, H] G = E[cand] W_q, bf16 high part
     uint16_t* Glo;            // [C*L*K, H] low part
     int g_rows;               // rows the Eg/G buffers hold (0: path unavailable)
@@ -80,7 +100,8 @@ bool make_tensor_map_bf16(CUtensorMap* map, const void* base, int rows, int cols
 int launch_transpose_bf16(const void* src, void* dst, int H, cudaStream_t stream);
 
 // Candidate-side projection path (small batches, prepared bf16 head); *launched = false
-// when the shape does not fit it.
+// when the shape does not fit it. expand_g_fits: whether it would launch.
+bool expand_g_fits(const ExpandArgs& a);
 int try_launch_expand_g(const ExpandArgs& a, cudaStream_t stream, bool* launched);
 
 // Small-batch persistent path; *launched = false when the shape does not fit it.
@@ -89,9 +110,11 @@ int try_launch_expand_small(const ExpandArgs& a, cudaStream_t stream, bool* laun
 // tcgen05 GEMM D[M,N] = A[M,K] . B[N,K]^T (bf16 in, fp32 accumulate).
 // mode 0: fp32 d32 [M,N]; mode 1: bf16 hi/lo pairs into hilo [M/P, 32, N];
 // mode 2: bf16 hi into hilo [M,N] and lo into lo2 [M,N].
+// pdl: programmatic dependent launch (A may be written by the previous kernel; B and
+// the outputs are not touched by it).
 bool gemm_tc_supported(int M, int N, int K);
 int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int mode, float* d32, uint16_t* hilo,
-                        int P, int* status, cudaStream_t stream, uint16_t* lo2 = nullptr);
+                        int P, int* status, cudaStream_t stream, uint16_t* lo2 = nullptr, bool pdl = false);
 
 // tcgen05 contraction of one depth: z[r,p,c] from gathered candidate rows and uhl.
 bool contract_tc_supported(int P, int H);
@@ -126,7 +149,8 @@ bool finish_supported(int L, int W);
 int launch_finish(int C, int L, int W, int B, const int32_t* st_tok, const int32_t* st_par, const float* st_s,
                   const int32_t* st_n, const int32_t* anchor, int32_t* tok, int32_t* par, int32_t* depth,
                   float* score, int32_t* n_nodes, uint8_t* mask, int32_t* pos, const unsigned long long* rowkeys,
-                  int32_t* accepted, int32_t* path, int32_t* bonus, int* status, cudaStream_t stream);
+                  int32_t* accepted, int32_t* path, int32_t* bonus, int* status, cudaStream_t stream,
+                  bool pdl = false);
 
 int launch_verify(int C, int L, int B, const int32_t* tok, const int32_t* par, const int32_t* depth,
                   const int32_t* n_nodes, const void* target, int rows_mode, int V, int dtype,

@@ -257,8 +257,11 @@ __device__ bool topk_exact_fallback(const T* buf, int n, int c0, int K, uint32_t
 template <typename T>
 __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict__ x, int V, int K, int jsel,
                                                           int chunk, int use_bulk, int32_t* __restrict__ out_tok,
-                                                          float* __restrict__ out_val, int* status) {
+                                                          float* __restrict__ out_val, int* status,
+                                                          const uint16_t* __restrict__ gE, int gH,
+                                                          uint16_t* __restrict__ gout) {
     extern __shared__ __align__(1024) uint8_t smem[];
+    griddep_launch_dependents();
     constexpr int VEC = ValueKey<T>::VEC;
     const uint32_t S = cluster_nctarank(), cr = cluster_ctarank();
     const int row = blockIdx.x / S;
@@ -407,8 +410,10 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
         sort_desc<TK_NT>(cand, np);
         for (int i = threadIdx.x; i < K; i += TK_NT) {
             const uint64_t k = cand[i];
-            out_tok[size_t(row) * K + i] = int32_t(0xffffffffu - uint32_t(k));
+            const int32_t t = int32_t(0xffffffffu - uint32_t(k));
+            out_tok[size_t(row) * K + i] = t;
             out_val[size_t(row) * K + i] = ValueKey<T>::value(uint32_t(k >> 32));
+            if (gout) reinterpret_cast<int32_t*>(hist)[i] = t;
         }
     } else if (cr == 0) {
         if (fits) {
@@ -435,9 +440,48 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
         sort_desc<TK_NT>(fb, kp);
         for (int i = threadIdx.x; i < K; i += TK_NT) {
             const uint64_t k = fb[i];
-            out_tok[size_t(row) * K + i] = int32_t(0xffffffffu - uint32_t(k));
+            const int32_t t = int32_t(0xffffffffu - uint32_t(k));
+            out_tok[size_t(row) * K + i] = t;
             out_val[size_t(row) * K + i] = ValueKey<T>::value(uint32_t(k >> 32));
+            if (gout) reinterpret_cast<int32_t*>(hist)[i] = t;
         }
+    }
+    if (gout) {
+        // rows of E for the K tokens, ranks cr, cr + S, ... copied by this CTA: the
+        // leader's tokens (its hist, K <= 512) are read first, then the cluster
+        // barrier's arrival releases them while the copies run
+        int32_t* mine = reinterpret_cast<int32_t*>(fb);  // TK_FB * 2 >= 512 entries
+        cluster_sync();
+        const int nmine = (K - int(cr) + int(S) - 1) / int(S);
+        const uint32_t ltok = dsmem_addr(hist, 0);
+        for (int j = threadIdx.x; j < nmine; j += TK_NT) {
+            const int32_t t = int32_t(ld_dsmem_u32(ltok + 4u * uint32_t(int(cr) + j * int(S))));
+            mine[j] = (t >= 0 && t < V) ? t : 0;  // an invalid token (error status set) reads row 0
+        }
+        __syncthreads();
+        cluster_arrive_release();
+        const int nv = gH / 8, total = nmine * nv;
+        constexpr int GU = 8;  // 16-byte loads in flight per thread
+        for (int b = threadIdx.x; b < total; b += GU * TK_NT) {
+            uint4 v[GU];
+#pragma unroll
+            for (int u = 0; u < GU; ++u) {
+                const int i = b + u * TK_NT;
+                if (i < total) {
+                    const int j = i / nv, c = i - j * nv;
+                    v[u] = __ldg(reinterpret_cast<const uint4*>(gE + size_t(mine[j]) * gH) + c);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < GU; ++u) {
+                const int i = b + u * TK_NT;
+                if (i < total) {
+                    const int j = i / nv, c = i - j * nv;
+                    reinterpret_cast<uint4*>(gout + (size_t(row) * K + int(cr) + j * int(S)) * gH)[c] = v[u];
+                }
+            }
+        }
+        cluster_wait_acquire();
     }
     if (use_bulk && !loaded && threadIdx.x == 0)
         for (int p = 0; p < npieces; ++p) mbar_wait_bounded(&mbar[p], 0, nullptr);
@@ -667,7 +711,7 @@ int num_sms() {
 
 template <typename T>
 static int launch_topk_t(const void* x, int rows, int V, int K, int32_t* tok, float* val, int* status,
-                         cudaStream_t stream, int max_s = 16) {
+                         cudaStream_t stream, const TopkGather* g, int max_s = 16) {
     const int elem = sizeof(T);
     const int VEC = 16 / elem;
     int S = 1;
@@ -700,7 +744,7 @@ static int launch_topk_t(const void* x, int rows, int V, int K, int32_t* tok, fl
         int nc = 0;
         if (cudaOccupancyMaxActiveClusters(&nc, kern, &q) != cudaSuccess || nc < 1) {
             cudaGetLastError();
-            return launch_topk_t<T>(x, rows, V, K, tok, val, status, stream, 8);
+            return launch_topk_t<T>(x, rows, V, K, tok, val, status, stream, g, 8);
         }
     }
     cudaLaunchConfig_t cfg{};
@@ -719,7 +763,7 @@ static int launch_topk_t(const void* x, int rows, int V, int K, int32_t* tok, fl
     {
         KTimer kt_(KID_TOPK_ROWS, stream);
         e = cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const T*>(x), V, K, jsel, chunk, use_bulk, tok, val,
-                               status);
+                               status, g ? g->E : nullptr, g ? g->H : 0, g ? g->out : nullptr);
     }
     return e == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
@@ -759,14 +803,25 @@ static bool use_stream(const void* x, int rows, int V, int K, int elem) {
            (size_t(V) * elem) % 16 == 0;
 }
 
+// The cluster kernel copies the gathered rows itself (K <= 512 tokens fit the
+// leader's histogram, rows of whole 16-byte vectors).
+static bool gather_ok(const TopkGather* g, int K) {
+    return g && g->E && g->out && K <= 512 && g->H > 0 && g->H % 8 == 0 &&
+           (reinterpret_cast<uintptr_t>(g->E) | reinterpret_cast<uintptr_t>(g->out)) % 16 == 0;
+}
+
 int launch_topk(const void* x, int rows, int V, int K, int dtype, int32_t* tok, float* val, int* status,
-                cudaStream_t stream) {
+                cudaStream_t stream, const TopkGather* g, bool* gathered) {
+    if (gathered) *gathered = false;
     if (rows == 0) return DARTREE_OK;
     if (use_stream(x, rows, V, K, dtype == DARTREE_BF16 ? 2 : 4))
         return dtype == DARTREE_BF16 ? launch_topk_stream<bf16_t>(x, rows, V, K, tok, val, status, stream)
                                      : launch_topk_stream<float>(x, rows, V, K, tok, val, status, stream);
-    if (dtype == DARTREE_BF16) return launch_topk_t<bf16_t>(x, rows, V, K, tok, val, status, stream);
-    return launch_topk_t<float>(x, rows, V, K, tok, val, status, stream);
+    const TopkGather* gg = gather_ok(g, K) ? g : nullptr;
+    const int e = dtype == DARTREE_BF16 ? launch_topk_t<bf16_t>(x, rows, V, K, tok, val, status, stream, gg)
+                                        : launch_topk_t<float>(x, rows, V, K, tok, val, status, stream, gg);
+    if (gathered) *gathered = e == DARTREE_OK && gg != nullptr;
+    return e;
 }
 
 }  // namespace dartree

@@ -154,11 +154,15 @@ def test_large_batch_path_shapes(C, L, V, H, K, W, B):
 
 
 @pytest.mark.parametrize("C,L,V,H,K,W,B", [(2, 5, 3001, 512, 64, 16, 40), (3, 3, 2000, 768, 24, 5, 10),
-                                           (1, 16, 4096, 1024, 8, 1, 16), (4, 7, 1500, 256, 64, 12, 30)])
+                                           (1, 16, 4096, 1024, 8, 1, 16), (4, 7, 1500, 256, 64, 12, 30),
+                                           (1, 4, 151936, 512, 8, 4, 8), (2, 3, 50000, 256, 24, 6, 12)])
 def test_candidate_side_projection_shapes(C, L, V, H, K, W, B):
     """Small bf16 batches with K <= 64 and W <= 16 take the candidate-side
     projection path (G = E[cand] W_q once per round, one cluster per request);
-    H = 768 and H = 256 run it with 8-CTA clusters, the others with 16."""
+    H = 768 and H = 256 run it with 8-CTA clusters, the others with 16. The top-K
+    launch copies the candidates' rows of E itself: with one CTA per row (small V),
+    with 4-CTA clusters (V = 50000, 6 ranks per CTA) and with 16-CTA clusters where
+    only half of the CTAs have a rank to copy (V = 151936, K = 8)."""
     import diffusion_drafter_draft_gb300 as dd
     cfg = make_config("cfg1_qwen3_4b_c1").replace(C=C, L=L, V=V, H=H, K=K, W=W, B=B, seed=C * 1000 + K)
     inp = make_inputs(cfg)
