@@ -330,18 +330,37 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
     // elements reach it, 4 * jsel * S >= K). Every CTA then has at least K / S
     // elements >= c. The first bound is the tighter one when a thread reads few
     // vectors, the second when it reads many.
+    // Both are found 4 bits at a time: per digit value d, each warp counts (ballots)
+    // its threads reaching prefix | d, lanes 1..15 for c1 and 17..31 for c4; after
+    // one barrier every warp sums the warps' counts and takes the largest digit
+    // whose count suffices (the counts fall with d), so all warps agree.
     {
         constexpr int KB = ValueKey<T>::BITS;
+        static_assert(KB % 4 == 0, "whole digits");
         const int j1 = (K + int(S) - 1) / int(S);
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         uint32_t c1 = 0, c4 = 0;
-        if (j1 <= TK_NT)
-            for (int b = KB - 1; b >= 0; --b) {
-                const uint32_t trial = c1 | (1u << b);
-                if (__syncthreads_count(t0 >= trial) >= j1) c1 = trial;
+        uint32_t* wc = hist;  // [2][TK_NT / 32][32] per-warp counts, double-buffered
+        for (int sh = KB - 4, it = 0; sh >= 0; sh -= 4, ++it) {
+            uint32_t mine = 0;
+#pragma unroll
+            for (uint32_t d = 1; d < 16; ++d) {
+                const uint32_t b1 = __ballot_sync(0xffffffffu, t0 >= (c1 | (d << sh)));
+                const uint32_t b4 = __ballot_sync(0xffffffffu, t3 >= (c4 | (d << sh)));
+                if (uint32_t(lane) == d) mine = __popc(b1);
+                if (uint32_t(lane) == d + 16) mine = __popc(b4);
             }
-        for (int b = KB - 1; b >= 0; --b) {
-            const uint32_t trial = c4 | (1u << b);
-            if (__syncthreads_count(t3 >= trial) >= jsel) c4 = trial;
+            uint32_t* buf = wc + (it & 1) * TK_NT;
+            buf[warp * 32 + lane] = mine;
+            __syncthreads();
+            uint32_t tot = 0;
+#pragma unroll
+            for (int w = 0; w < TK_NT / 32; ++w) tot += buf[w * 32 + lane];
+            const bool ok1 = lane >= 1 && lane < 16 && j1 <= TK_NT && tot >= uint32_t(j1);
+            const bool ok4 = lane >= 17 && tot >= uint32_t(jsel);
+            const uint32_t m1 = __ballot_sync(0xffffffffu, ok1), m4 = __ballot_sync(0xffffffffu, ok4);
+            if (m1) c1 |= uint32_t(31 - __clz(m1)) << sh;
+            if (m4) c4 |= uint32_t(31 - __clz(m4) - 16) << sh;
         }
         if (threadIdx.x == 0) misc[2] = c1 > c4 ? c1 : c4;
     }
@@ -387,6 +406,9 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
     }
     // the same decision in every CTA: the totals and flags are shared
     const bool fits = total >= uint32_t(K) && total <= uint32_t(L.cap) && !anyover;
+    // few candidates (one per thread): every CTA ranks the leader's list itself
+    // (no sort, no further exchange); else the leader sorts or selects
+    const bool spread = fits && total <= uint32_t(TK_NT);
     if (fits) {
         const uint32_t leader_cand = dsmem_addr(cand, 0);
         const uint32_t pos = base + uint32_t(excl);
@@ -402,6 +424,63 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
 
     // leader: up to TK_FB candidates are sorted directly; more are cut to exactly K
     // by a radix select first
+    if (spread) {
+        // rank of a key = number of larger keys (keys are distinct: the index is
+        // in the low half). Every CTA copies the leader's list, then arrives on the
+        // cluster barrier (the leader's shared memory may go once all have), ranks
+        // every key, and copies the rows of ranks cr, cr + S, ... < K; the leader
+        // writes the K outputs.
+        const int n = int(total);
+        uint64_t key = 0;
+        if (int(threadIdx.x) < n) key = cr == 0 ? cand[threadIdx.x] : ld_dsmem_u64(dsmem_addr(&cand[threadIdx.x], 0));
+        if (cr != 0 && int(threadIdx.x) < n) cand[threadIdx.x] = key;
+        cluster_arrive_release();
+        __syncthreads();
+        int32_t* ranked = reinterpret_cast<int32_t*>(fb);  // token of each rank < K
+        if (int(threadIdx.x) < n) {
+            int larger = 0;
+            for (int j = 0; j < n; ++j) larger += cand[j] > key ? 1 : 0;
+            if (larger < K) {
+                const int32_t t = int32_t(0xffffffffu - uint32_t(key));
+                if (cr == 0) {
+                    out_tok[size_t(row) * K + larger] = t;
+                    out_val[size_t(row) * K + larger] = ValueKey<T>::value(uint32_t(key >> 32));
+                }
+                ranked[larger] = (t >= 0 && t < V) ? t : 0;
+            }
+        }
+        if (gout) {
+            __syncthreads();
+            const int nmine = (K - int(cr) + int(S) - 1) / int(S);
+            const int nv = gH / 8, tot = nmine * nv;
+            constexpr int GU = 8;  // 16-byte loads in flight per thread
+            for (int b = threadIdx.x; b < tot; b += GU * TK_NT) {
+                uint4 v[GU];
+#pragma unroll
+                for (int u = 0; u < GU; ++u) {
+                    const int i = b + u * TK_NT;
+                    if (i < tot) {
+                        const int j = i / nv, c = i - j * nv;
+                        const int32_t t = ranked[int(cr) + j * int(S)];
+                        v[u] = __ldg(reinterpret_cast<const uint4*>(gE + size_t(t) * gH) + c);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < GU; ++u) {
+                    const int i = b + u * TK_NT;
+                    if (i < tot) {
+                        const int j = i / nv, c = i - j * nv;
+                        reinterpret_cast<uint4*>(gout + (size_t(row) * K + int(cr) + j * int(S)) * gH)[c] = v[u];
+                    }
+                }
+            }
+        }
+        cluster_wait_acquire();
+        if (use_bulk && !loaded && threadIdx.x == 0)
+            for (int p = 0; p < npieces; ++p) mbar_wait_bounded(&mbar[p], 0, nullptr);
+        return;
+    }
+
     int np = 1;
     while (np < int(total)) np <<= 1;
     if (cr == 0 && fits && np <= TK_FB && np <= L.cap) {
