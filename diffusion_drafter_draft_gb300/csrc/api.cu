@@ -237,13 +237,16 @@ static int expand_impl(const dartree_head* head, const dartree_params* p, const 
 // S1 of a whole tree build into ct/cv; when the expansion a describes takes the
 // candidate-side projection path, the same launch may also copy the candidates'
 // rows of E into a.Eg (a.eg_ready says whether it did).
+// With rm, the launch may also write the per-position target row maxima
+// (*rm_done says whether it did).
 static int topk_for_expand(const dartree_head* head, const dartree_params* p, const void* base_logits, int32_t* ct,
-                           float* cv, int* status, ExpandArgs& a, cudaStream_t s) {
+                           float* cv, int* status, ExpandArgs& a, cudaStream_t s, const TopkRowmax* rm = nullptr,
+                           bool* rm_done = nullptr) {
     const TopkGather g{static_cast<const uint16_t*>(head->E), head->H, a.Eg};
     bool gathered = false;
     const bool want = expand_g_fits(a);
     if (int e = launch_topk(base_logits, p->C * p->L, head->V, p->K, head->dtype, ct, cv, status, s,
-                            want ? &g : nullptr, &gathered))
+                            want ? &g : nullptr, &gathered, rm, rm_done))
         return e;
     a.eg_ready = gathered;
     return DARTREE_OK;
@@ -331,14 +334,18 @@ int dartree_round(const dartree_head* head, const dartree_params* p, const void*
     int* status = at<int>(ws, l.status);
     unsigned long long* rowkeys = at<unsigned long long>(ws, l.keys);
     const bool per_pos = rows == DARTREE_ROWS_PER_POSITION;
-    // S1 first; the target-row maxima (per-position rows) then run on a side
-    // stream forked here, overlapping the expansion, which leaves most SMs idle
-    // for small batches (forked before S1 they would compete with it for HBM)
+    // S1 first. The target-row maxima (per-position rows) come from the cluster
+    // top-K launch itself when it can; otherwise they run on a side stream forked
+    // after S1, overlapping the expansion, which leaves most SMs idle for small
+    // batches (forked before S1 they would compete with it for HBM)
     ExpandArgs a = expand_args(head, p, block_hidden, anchor, ct, cv, &st, ws, l);
-    if (int e = topk_for_expand(head, p, base_logits, ct, cv, status, a, s)) return e;
+    const TopkRowmax rm{target, rowkeys};
+    bool rm_done = false;
+    if (int e = topk_for_expand(head, p, base_logits, ct, cv, status, a, s, per_pos ? &rm : nullptr, &rm_done))
+        return e;
     std::unique_lock<std::recursive_mutex> lock(side_mutex(), std::defer_lock);
     SideStreams* side = nullptr;
-    if (per_pos) {
+    if (per_pos && !rm_done) {
         lock.lock();
         side = side_streams();
         if (side) {

@@ -187,6 +187,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                  :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
+// Prefetch of `bytes` (a multiple of 16, 16-byte aligned address) into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
+}
+
 // 1-D bulk copy from own shared memory into a peer CTA's shared memory; completion
 // (bytes) is counted on the peer's mbarrier. remote_dst and remote_bar are
 // shared::cluster addresses (mapa); all addresses and bytes multiples of 16.

@@ -56,10 +56,19 @@ struct TopkGather {
     uint16_t* out;
 };
 
+// Maxima keys (ord(value) << 32 | ~index) of per-position target rows [rows, V],
+// the same dtype as the top-K rows, computed by the top-K launch itself.
+struct TopkRowmax {
+    const void* target;
+    unsigned long long* keys;  // [rows]
+};
+
 // S1: top-K of `rows` rows of V values. With g, *gathered tells whether the rows of
-// g->E were copied too (only some launch shapes do; otherwise the caller copies them).
+// g->E were copied too, with rm, *rm_done whether the target row maxima were
+// written (only some launch shapes do either; otherwise the caller does).
 int launch_topk(const void* x, int rows, int V, int K, int dtype, int32_t* tok, float* val, int* status,
-                cudaStream_t stream, const TopkGather* g = nullptr, bool* gathered = nullptr);
+                cudaStream_t stream, const TopkGather* g = nullptr, bool* gathered = nullptr,
+                const TopkRowmax* rm = nullptr, bool* rm_done = nullptr);
 
 struct ExpandArgs {
     const void* E;

@@ -254,12 +254,28 @@ __device__ bool topk_exact_fallback(const T* buf, int n, int c0, int K, uint32_t
     return ok && (cr != 0 || misc[10] == n_gt);
 }
 
+// Bitonic sort, descending, of one 32-bit value per lane.
+__device__ __forceinline__ uint32_t warp_sort_desc_u32(uint32_t v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int d = k >> 1; d >= 1; d >>= 1) {
+            const uint32_t o = __shfl_xor_sync(0xffffffffu, v, d);
+            const bool keep_max = ((lane & d) == 0) == ((lane & k) == 0);
+            v = keep_max ? max(v, o) : min(v, o);
+        }
+    }
+    return v;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict__ x, int V, int K, int jsel,
                                                           int chunk, int use_bulk, int32_t* __restrict__ out_tok,
                                                           float* __restrict__ out_val, int* status,
                                                           const uint16_t* __restrict__ gE, int gH,
-                                                          uint16_t* __restrict__ gout) {
+                                                          uint16_t* __restrict__ gout, const T* __restrict__ tgt,
+                                                          unsigned long long* __restrict__ tkeys) {
     extern __shared__ __align__(1024) uint8_t smem[];
     griddep_launch_dependents();
     constexpr int VEC = ValueKey<T>::VEC;
@@ -303,6 +319,30 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
         __syncthreads();
     }
 
+    // maximum key (ord(value) << 32 | ~index) of this chunk of the row's target
+    // logits (verification), read while the chunk's copy is in flight; rows of
+    // whole 16-byte vectors
+    uint64_t tbest = 0;
+    if (tgt) {
+        const T* ts = tgt + size_t(row) * V + c0;
+#pragma unroll 4
+        for (int v = threadIdx.x; v < nvec; v += TK_NT) {
+            const uint4 w = __ldg(reinterpret_cast<const uint4*>(ts) + v);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const uint64_t k = (uint64_t(vec_elem_ord(w, e, static_cast<T*>(nullptr))) << 32) |
+                                   (0xffffffffu - uint32_t(c0 + v * VEC + e));
+                tbest = k > tbest ? k : tbest;
+            }
+        }
+        for (int i = nvec * VEC + int(threadIdx.x); i < n; i += TK_NT) {
+            const uint64_t k = (uint64_t(ValueKey<T>::ord(ts[i])) << 32) | (0xffffffffu - uint32_t(c0 + i));
+            tbest = k > tbest ? k : tbest;
+        }
+        tbest = warp_max_u64(tbest);
+        if ((threadIdx.x & 31) == 0) reinterpret_cast<uint64_t*>(hsum)[threadIdx.x >> 5] = tbest;
+    }
+
     // pass 1: the 4 largest maxima of the vectors t, t+NT, ... (piece by piece as they land)
     uint32_t t0 = 0, t1 = 0, t2 = 0, t3 = 0;
     auto ins = [&](uint32_t vm) {
@@ -334,10 +374,22 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
     // its threads reaching prefix | d, lanes 1..15 for c1 and 17..31 for c4; after
     // one barrier every warp sums the warps' counts and takes the largest digit
     // whose count suffices (the counts fall with d), so all warps agree.
-    {
+    // With j1, jsel <= 4 (few keys per CTA) the bounds are read off sorted lists
+    // instead: each warp sorts its t0 and t3, its 4 largest of each go to shared
+    // memory, and every warp sorts those 32 (they hold the CTA's 4 largest).
+    const int j1 = (K + int(S) - 1) / int(S);
+    if (j1 <= 4 && jsel <= 4) {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        static_assert(TK_NT / 32 * 4 == 32, "8 warps x 4 keys");
+        const uint32_t s0 = warp_sort_desc_u32(t0), s3 = warp_sort_desc_u32(t3);
+        if (lane < 4) { hist[warp * 4 + lane] = s0; hist[32 + warp * 4 + lane] = s3; }
+        __syncthreads();
+        const uint32_t a0 = warp_sort_desc_u32(hist[lane]), a3 = warp_sort_desc_u32(hist[32 + lane]);
+        const uint32_t c1 = __shfl_sync(0xffffffffu, a0, j1 - 1), c4 = __shfl_sync(0xffffffffu, a3, jsel - 1);
+        if (threadIdx.x == 0) misc[2] = c1 > c4 ? c1 : c4;
+    } else {
         constexpr int KB = ValueKey<T>::BITS;
         static_assert(KB % 4 == 0, "whole digits");
-        const int j1 = (K + int(S) - 1) / int(S);
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         uint32_t c1 = 0, c4 = 0;
         uint32_t* wc = hist;  // [2][TK_NT / 32][32] per-warp counts, double-buffered
@@ -369,6 +421,14 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
     if (threadIdx.x == 0) {
         uint32_t old;
         asm volatile("atom.shared::cluster.min.u32 %0, [%1], %2;" : "=r"(old) : "r"(dsmem_addr(&misc[3], 0)), "r"(misc[2]) : "memory");
+        if (tgt) {  // the CTA's target maximum into its slot misc[32 + 2 cr] of the leader
+            uint64_t m = 0;
+            for (int w = 0; w < TK_NT / 32; ++w) {
+                const uint64_t x = reinterpret_cast<const uint64_t*>(hsum)[w];
+                m = x > m ? x : m;
+            }
+            st_dsmem_u64(dsmem_addr(&misc[32 + 2 * cr], 0), m);
+        }
     }
     cluster_sync();
     const uint32_t c = ld_dsmem_u32(dsmem_addr(&misc[3], 0));
@@ -393,10 +453,23 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
         }
     }
     for (int i = nvec * VEC + int(threadIdx.x); i < n; i += TK_NT) consider(ValueKey<T>::ord(buf[i]), i);
+    if (gout) {  // the rows of E the copy at the end may need: into L2 now
+#pragma unroll
+        for (int q = 0; q < TK_STASH; ++q)
+            if (q < cnt) prefetch_l2_bulk(gE + size_t(0xffffffffu - uint32_t(stash[q])) * gH, uint32_t(gH) * 2u);
+    }
     const int over = __syncthreads_or(cnt > TK_STASH);  // a thread with more candidates than registers
     if (threadIdx.x == 0) misc[9] = uint32_t(over);
     const int excl = block_exclusive_scan<TK_NT>(cnt, wtot, reinterpret_cast<int*>(&misc[8]));
     cluster_sync();  // CTA totals visible
+    if (tgt && cr == 0 && threadIdx.x == 0) {
+        uint64_t m = 0;
+        for (uint32_t q = 0; q < S; ++q) {
+            const uint64_t x = *reinterpret_cast<const uint64_t*>(&misc[32 + 2 * q]);
+            m = x > m ? x : m;
+        }
+        tkeys[row] = m;
+    }
     uint32_t base = 0, total = 0, anyover = 0;
     for (uint32_t q = 0; q < S; ++q) {
         const uint32_t tq = ld_dsmem_u32(dsmem_addr(&misc[8], q));
@@ -790,7 +863,7 @@ int num_sms() {
 
 template <typename T>
 static int launch_topk_t(const void* x, int rows, int V, int K, int32_t* tok, float* val, int* status,
-                         cudaStream_t stream, const TopkGather* g, int max_s = 16) {
+                         cudaStream_t stream, const TopkGather* g, const TopkRowmax* rm, int max_s = 16) {
     const int elem = sizeof(T);
     const int VEC = 16 / elem;
     int S = 1;
@@ -823,7 +896,7 @@ static int launch_topk_t(const void* x, int rows, int V, int K, int32_t* tok, fl
         int nc = 0;
         if (cudaOccupancyMaxActiveClusters(&nc, kern, &q) != cudaSuccess || nc < 1) {
             cudaGetLastError();
-            return launch_topk_t<T>(x, rows, V, K, tok, val, status, stream, g, 8);
+            return launch_topk_t<T>(x, rows, V, K, tok, val, status, stream, g, rm, 8);
         }
     }
     cudaLaunchConfig_t cfg{};
@@ -842,7 +915,8 @@ static int launch_topk_t(const void* x, int rows, int V, int K, int32_t* tok, fl
     {
         KTimer kt_(KID_TOPK_ROWS, stream);
         e = cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const T*>(x), V, K, jsel, chunk, use_bulk, tok, val,
-                               status, g ? g->E : nullptr, g ? g->H : 0, g ? g->out : nullptr);
+                               status, g ? g->E : nullptr, g ? g->H : 0, g ? g->out : nullptr,
+                               rm ? static_cast<const T*>(rm->target) : nullptr, rm ? rm->keys : nullptr);
     }
     return e == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
@@ -890,16 +964,24 @@ static bool gather_ok(const TopkGather* g, int K) {
 }
 
 int launch_topk(const void* x, int rows, int V, int K, int dtype, int32_t* tok, float* val, int* status,
-                cudaStream_t stream, const TopkGather* g, bool* gathered) {
+                cudaStream_t stream, const TopkGather* g, bool* gathered, const TopkRowmax* rm, bool* rm_done) {
     if (gathered) *gathered = false;
+    if (rm_done) *rm_done = false;
     if (rows == 0) return DARTREE_OK;
-    if (use_stream(x, rows, V, K, dtype == DARTREE_BF16 ? 2 : 4))
+    const int elem = dtype == DARTREE_BF16 ? 2 : 4;
+    if (use_stream(x, rows, V, K, elem))
         return dtype == DARTREE_BF16 ? launch_topk_stream<bf16_t>(x, rows, V, K, tok, val, status, stream)
                                      : launch_topk_stream<float>(x, rows, V, K, tok, val, status, stream);
     const TopkGather* gg = gather_ok(g, K) ? g : nullptr;
-    const int e = dtype == DARTREE_BF16 ? launch_topk_t<bf16_t>(x, rows, V, K, tok, val, status, stream, gg)
-                                        : launch_topk_t<float>(x, rows, V, K, tok, val, status, stream, gg);
+    // the target rows are read with 16-byte vector loads
+    const TopkRowmax* rr = rm && rm->target && rm->keys && reinterpret_cast<uintptr_t>(rm->target) % 16 == 0 &&
+                                   (size_t(V) * elem) % 16 == 0
+                               ? rm
+                               : nullptr;
+    const int e = dtype == DARTREE_BF16 ? launch_topk_t<bf16_t>(x, rows, V, K, tok, val, status, stream, gg, rr)
+                                        : launch_topk_t<float>(x, rows, V, K, tok, val, status, stream, gg, rr);
     if (gathered) *gathered = e == DARTREE_OK && gg != nullptr;
+    if (rm_done) *rm_done = e == DARTREE_OK && rr != nullptr;
     return e;
 }
 
