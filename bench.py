@@ -240,16 +240,18 @@ def measure_e2e(cfg, m, steps, torch, dd):
 # this workload; the C=64 contraction and top-K were captured on fewer requests (8
 # and 20 of them) and scaled by the requests processed (their traffic is per request).
 NCU_TRAFFIC = {
-    ("cfg1_qwen3_4b_c1", "expand_g_kernel"): 15546112,
-    ("cfg1_qwen3_4b_c1", "gemm_bf16_tc_kernel"): 18364928,
+    ("cfg1_qwen3_4b_c1", "expand_g_kernel"): 15546624,
+    ("cfg1_qwen3_4b_c1", "gemm_bf16_tc_kernel"): 18366464,
+    ("cfg1_qwen3_4b_c1", "topk_rows_kernel"): 20144640,
     ("cfg4_c64_stress", "contract_tc_kernel"): 35337472 * 8,   # one launch over all 64 requests
     ("cfg4_c64_stress", "topk_stream_kernel"): int((100288256 + 3384576) * 64 / 20),
 }
 
 
-def kernel_work(cfg, name, accepted_mean, g_path, fused_gather=False):
+def kernel_work(cfg, name, accepted_mean, g_path, fused_gather=False, fused_rowmax=False):
     """Algorithmic work of a kernel family over ONE round: ("hbm", bytes) or ("tensor", flops).
-    fused_gather: the cluster top-K also copied the candidates' rows of E."""
+    fused_gather: the cluster top-K also copied the candidates' rows of E;
+    fused_rowmax: it also read the per-position target rows (their maxima)."""
     eb = 2 if cfg.dtype == "bf16" else 4
     C, L, V, H, K, W, B = cfg.C, cfg.L, cfg.V, cfg.H, cfg.K, cfg.W, cfg.B
     P = [1]
@@ -257,7 +259,8 @@ def kernel_work(cfg, name, accepted_mean, g_path, fused_gather=False):
         P.append(min(W, P[-1] * K))
     if name in ("topk_rows_kernel", "topk_stream_kernel", "rowmax_kernel"):
         gather = 2 * C * L * K * H * 2 if (fused_gather and name == "topk_rows_kernel") else 0
-        return "hbm", C * L * V * eb + gather
+        target = C * L * V * eb if (fused_rowmax and name == "topk_rows_kernel") else 0
+        return "hbm", C * L * V * eb + gather + target
     if name == "gather_rows_kernel":
         return "hbm", 2 * C * L * K * H * eb
     if name == "gemm_bf16_tc_kernel":
@@ -297,7 +300,8 @@ def kernel_roofline(cfg, m, hbm_peak, tf_peak):
     lpr = launches / n
     ms_launch = ms_total / launches
     fused = g_path and "gather_rows_kernel" not in kt
-    bound, work_round = kernel_work(cfg, dom, m["accepted_mean"], g_path, fused)
+    fused_rm = cfg.rows == "position" and "rowmax_kernel" not in kt and "topk_rows_kernel" in kt
+    bound, work_round = kernel_work(cfg, dom, m["accepted_mean"], g_path, fused, fused_rm)
     work = work_round / lpr
     traffic = NCU_TRAFFIC.get((cfg.name, dom))
     split = (not g_path) and cfg.C >= SPLIT_MIN_C and dom in ("contract_tc_kernel", "gemm_bf16_tc_kernel",
