@@ -8,8 +8,8 @@
 // counted against all keys in shared memory (broadcast reads); the nodes of rank
 // below B are chosen and take slots in (depth, rank) order by a block scan. Tree
 // arrays, ancestor table and mask are built in shared memory, and the walk
-// follows the row maxima computed beforehand (on a side stream, overlapping the
-// build), read into shared memory first.
+// follows the row maxima computed beforehand (by the top-K launch, or on a side
+// stream overlapping the build), read into shared memory first.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -65,7 +65,6 @@ __global__ void __launch_bounds__(FN_NT) finish_kernel(int L, int W, int B, cons
     uint64_t* rowk = reinterpret_cast<uint64_t*>(smem + fl.rowk);
     int* next = reinterpret_cast<int*>(smem + fl.next);  // accepted child of every slot, or INT_MAX
     const int r = blockIdx.x, n = L * W, S = B + 1, q = threadIdx.x;
-    const int lane = q & 31, wid = q >> 5;
     const size_t base = size_t(r) * L * W;
 
     // ---- keys of the supertree nodes (0 = no node)

@@ -199,13 +199,19 @@ DARTREE_API int dartree_verify(const dartree_params* p, const dartree_tree* tree
 /* S1-S10 in one call: dartree_build_tree (no supertree or candidate outputs)
  * followed by dartree_verify, with the same results as those two calls.
  * target, rows: as for dartree_verify, with V and dtype of the head. With
- * per-position rows the target-row maxima do not depend on the tree, so they are
- * computed on a library-owned side stream (one per device, created on the first
- * call; make that call before any stream capture) forked from `stream` and
- * joined before the walk; the fork is captured with the rest when `stream` is
- * being captured into a CUDA graph. Calls are serialised on the host while they
- * enqueue. The row maxima go to a workspace region of their own (the workspace of
- * dartree_workspace_bytes suffices). Errors as for the two calls. */
+ * per-position rows the target-row maxima do not depend on the tree: when S1 runs
+ * as one cluster per row (few rows) and the target and logit rows start on 16-byte
+ * boundaries, the S1 launch computes them too; otherwise they are computed on a
+ * library-owned side stream (one per device, created on the first call; make that
+ * call before any stream capture) forked from `stream` after S1 and joined before
+ * the walk; the fork is captured with the rest when `stream` is being captured
+ * into a CUDA graph. Calls are serialised on the host while they enqueue. The row
+ * maxima go to a workspace region of their own (the workspace of
+ * dartree_workspace_bytes suffices). Later kernels of the call may be launched as
+ * programmatic dependents of the one before (each waits for it on the device
+ * before reading its results), so their set-up overlaps its tail; the results and
+ * stream order seen by the caller are those of plain launches. Errors as for the
+ * two calls. */
 DARTREE_API int dartree_round(const dartree_head* head, const dartree_params* p, const void* base_logits,
                               const void* block_hidden, const int32_t* anchor, const void* target, int rows,
                               dartree_tree* tree, int32_t* accepted_len, int32_t* path, int32_t* bonus,
