@@ -1,7 +1,7 @@
 """Benchmark of the DARTree draft-tree build + verify round on one GB300.
 
-One step = dartree_build_tree followed by dartree_verify (S1-S10) over one batch
-of seeded synthetic inputs already resident in HBM. The default workload is the
+One step = one dartree_round call (S1-S10: the draft-tree build and its
+verification) over one batch of seeded synthetic inputs already resident in HBM. The default workload is the
 Qwen3-4B-shaped single-request round (C=1, L=16, V=151936, H=2560, K=64, W=12,
 B=64, bf16); the C=64 stress batch (H=4096, K=512) is measured in the same run
 and reported under "c64". Prints one JSON line on rank 0.
