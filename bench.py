@@ -15,6 +15,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -27,6 +28,7 @@ from dartree_inputs import breadth_first_slot_depth, make_config, make_inputs, m
 MAIN_CFG = "cfg1_qwen3_4b_c1"
 STRESS_CFG = "cfg4_c64_stress"
 L2_BYTES = 129 * 1024 * 1024
+CLOCKS_CSV = None  # where the clock samples of the timed region go (set by --clocks-csv)
 
 
 def _peaks():
@@ -81,9 +83,13 @@ def device_inputs(cfg, torch):
 # --------------------------------------------------------------------------- clocks
 
 class Clocks:
+    """nvidia-smi samples (every 200 ms) of the SM clock and throttle reasons while a
+    measurement runs; the raw samples go to CLOCKS_CSV (--clocks-csv), by default a
+    file in the temporary directory."""
+
     def __init__(self):
         self.p = None
-        self.path = os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
+        self.path = CLOCKS_CSV or os.path.join(tempfile.gettempdir(), f"dartree_bench_clocks_{os.getpid()}.csv")
 
     def start(self):
         try:
@@ -414,7 +420,10 @@ def main():
                     help="profiling mode: run just one entry point on --config and print its timing")
     ap.add_argument("--config", default=None, help="workload name for --only (default: the main workload)")
     ap.add_argument("--C", type=int, default=None, help="--only: override the number of requests (a smaller case)")
+    ap.add_argument("--clocks-csv", default=None, help="file for the raw nvidia-smi clock samples of the timed region")
     args = ap.parse_args()
+    global CLOCKS_CSV
+    CLOCKS_CSV = args.clocks_csv
     if args.only:
         return profile_only(args)
     rank = int(os.environ.get("RANK", "0"))
