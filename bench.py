@@ -170,7 +170,16 @@ def graphed(torch, fn, use_graph=True):
 graphed.keep = []
 
 
-def measure(cfg, steps, warmup, torch, dd, graphs=True):
+def job_rate(ms_sum_local: float, steps: int, world: int, max_over_ranks=None):
+    """Whole-job rounds/s of `world` ranks that each run their own replica of the
+    workload (no exchange between them): the job's time for `steps` rounds is the
+    slowest rank's. Returns (rounds/s over all ranks, ms per step)."""
+    ms_sum = max_over_ranks(ms_sum_local) if max_over_ranks is not None else ms_sum_local
+    ms = ms_sum / steps
+    return world * 1e3 / ms, ms
+
+
+def measure(cfg, steps, warmup, torch, dd, graphs=True, barrier=None):
     inp, x = device_inputs(cfg, torch)
     rows = dd.ROWS_PER_POSITION if cfg.rows == "position" else dd.ROWS_PER_NODE
     rnd = dd.Round(x["E"], x["Wq"], cfg.C, cfg.L, cfg.K, cfg.W, cfg.B, cfg.beta, rows)
@@ -186,7 +195,13 @@ def measure(cfg, steps, warmup, torch, dd, graphs=True):
     run = graphed(torch, step, graphs)
     clocks = Clocks()
     clocks.start()
+    torch.cuda.synchronize()
+    if barrier is not None:  # every rank starts (and ends) the timed steps together
+        barrier()
     t_round = time_steps(torch, run, steps, warmup, flush)
+    torch.cuda.synchronize()
+    if barrier is not None:
+        barrier()
     clk = clocks.stop()
     acc = rnd.out["accepted_len"].float().mean().item()
 
@@ -434,11 +449,11 @@ def main():
         if rank != 0:
             return
         vals = []
-        for _ in range(args.warmup):
-            pass
         t0 = time.time()
         import oracle
         inp = make_inputs(cfg)
+        for _ in range(args.warmup):  # untimed
+            oracle.verify(oracle.build(inp), inp["target"], cfg.dtype, cfg.rows, cfg.L)
         for _ in range(args.steps):
             s = time.time()
             o = oracle.build(inp)
@@ -470,15 +485,18 @@ def main():
     dd.lib()
     hbm_peak, tf_peak, peak_kind = _peaks()
 
-    m = measure(cfg, args.steps, max(3, args.warmup), torch, dd, graphs=not args.no_graph)
-    ms_local = float(np.sum(m["t_round"]))
+    barrier = max_over_ranks = None
     if world > 1:
         import torch.distributed as dist
-        tt = torch.tensor([ms_local], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_local = float(tt.item())
-    ms = ms_local / args.steps
-    value = world * 1e3 / ms
+
+        def max_over_ranks(v):
+            tt = torch.tensor([v], device="cuda")
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            return float(tt.item())
+
+        barrier = dist.barrier
+    m = measure(cfg, args.steps, max(3, args.warmup), torch, dd, graphs=not args.no_graph, barrier=barrier)
+    value, ms = job_rate(float(np.sum(m["t_round"])), args.steps, world, max_over_ranks)
     dom, _, alg, parts = roofline(cfg, m, hbm_peak)
     roof, per_kernel, lpr = kernel_roofline(cfg, m, hbm_peak, tf_peak)
     e2e_ms, h2d, d2h = measure_e2e(cfg, m, min(args.steps, 20), torch, dd)
