@@ -38,11 +38,12 @@ import numpy as np
 
 __all__ = [
     "Config", "CONFIGS", "make_config", "make_inputs", "make_head",
-    "make_target_per_node", "breadth_first_slot_depth", "round_to_bf16_bits",
+    "make_target_per_node", "breadth_first_slot_depth", "make_tie_inputs", "round_to_bf16_bits",
     "bf16_bits_to_f32", "to_f32", "to_f64",
 ]
 
 HEAD_STREAM = 2**31 - 1
+TIE_STREAM = 2**31 - 2
 
 
 @dataclass(frozen=True)
@@ -247,4 +248,51 @@ def make_target_per_node(cfg: Config, inputs: dict, slot_depth: np.ndarray) -> n
                 tok = p if agree else _other_token(rng, cfg.V, p)
                 t[tok] += inputs["boost1"][i, dj]
             out[i, j] = _store(t, cfg.dtype)
+    return out
+
+
+def make_tie_inputs(cfg: Config, requests=None) -> dict:
+    """Inputs on which the tree is decided by exact ties (tie-order checks).
+
+    Starts from make_inputs(cfg, requests) and replaces two things:
+      E = 0, so every parent sees the same corrected logits (the base logits);
+      base row j of request r (stream SeedSequence([seed, r, 2**31-2])): one token
+        U{0..V-1} at 8, n ~ U{0..K} other distinct tokens at 8 - (64 + j mod 16),
+        every other token at 8 - (96 + j mod 16).
+    Every value is an integer, and the gaps below the top token are large enough
+    that the other tokens' exponentials vanish next to it, so the log-softmax of
+    the top candidate is exactly 0 and the others sit at exactly -(64 + j mod 16)
+    or -(96 + j mod 16). Scores are sums of integers and beta*d: with beta = 0 or
+    a short binary fraction they are exact in float32 and float64 alike, and
+    children that tie do so exactly (inside a depth, and, with beta = 0, with
+    their parents across depths). Heavy ties at the K-th candidate exercise the
+    top-K order too. Target rows (per-position layout) are the make_inputs rows
+    with, per position and with probability 0.7, the top base token set to the
+    row maximum + 1, so that verification accepts part of the block.
+    """
+    out = make_inputs(cfg, requests)
+    reqs = out["requests"]
+    out["E"] = np.zeros_like(out["E"])
+    base = np.empty((len(reqs), cfg.L, cfg.V), np.float32)
+    tops = np.empty((len(reqs), cfg.L), np.int64)
+    for i, r in enumerate(reqs):
+        rng = _rng(cfg.seed, int(r), TIE_STREAM)
+        for j in range(cfg.L):
+            row = np.full(cfg.V, np.float32(8 - (96 + j % 16)), np.float32)
+            top = int(rng.integers(0, cfg.V))
+            n2 = int(rng.integers(0, min(cfg.K, cfg.V - 1) + 1))
+            others = rng.choice(cfg.V - 1, size=n2, replace=False)
+            others = others + (others >= top)          # distinct from the top token
+            row[others] = np.float32(8 - (64 + j % 16))
+            row[top] = np.float32(8.0)
+            base[i, j] = row
+            tops[i, j] = top
+        if "target" in out:
+            t = to_f32(out["target"][i], cfg.dtype).copy()
+            for j in range(cfg.L):
+                if rng.random() < 0.7:
+                    t[j, tops[i, j]] = t[j].max() + np.float32(1.0)
+            out["target"][i] = _store(t, cfg.dtype)
+    out["base"] = _store(base, cfg.dtype)
+    out["planted"] = tops.astype(np.int32)
     return out

@@ -127,24 +127,26 @@ def select_top(keys_desc, n: int):
 
 # --------------------------------------------------------------------------- follow mode
 
-def _adopt(own, other, score_of, tol, what, flags, mismatches):
+def _adopt(own, other, score_of, valid, tol, what, flags, mismatches):
     """Compare an alternative ordered selection with the oracle's own.
 
-    The alternative is adopted when, at every rank position, its score and the
-    oracle's score are within `tol` (a near-tie), and flagged; otherwise the
-    oracle keeps its own choice and records a mismatch.
+    The alternative is adopted (and recorded in `flags` with its largest gap) only
+    when it is a list of distinct valid entries of the same length and, at every
+    rank position where the two lists differ, the two scores are unequal but
+    within `tol` of each other: a near-tie that float32 arithmetic may order the
+    other way. An exact tie (equal float64 scores) is not a near-tie: the stated
+    tie order decides it, so a different choice there is a mismatch, like any
+    gap of `tol` or more, a repeated entry or an unknown one. On a mismatch the
+    oracle keeps its own choice.
     """
     if other is None or list(other) == list(own):
         return list(own)
     other = list(other)
-    ok = len(other) == len(own) and len(set(other)) == len(other)
+    ok = len(other) == len(own) and len(set(other)) == len(other) and all(valid(x) for x in other)
+    gaps = []
     if ok:
-        try:
-            gaps = [abs(score_of(a) - score_of(b)) for a, b in zip(own, other)]
-        except (KeyError, IndexError):
-            ok = False
-        else:
-            ok = max(gaps, default=0.0) < tol
+        gaps = [abs(score_of(a) - score_of(b)) for a, b in zip(own, other) if a != b]
+        ok = all(0.0 < g < tol for g in gaps)
     if ok:
         flags.append((what, max(gaps, default=0.0)))
         return other
@@ -215,7 +217,8 @@ def _build_one(inp, i, E, Wq, out, follow, tol):
         n_keep = min(W, P * K)
         own = select_top([depth_key(flat[f], f) for f in range(P * K)], n_keep)
         if follow is not None:
-            own = _adopt(own, follow["depth"](i, d), lambda f: flat[f], tol,
+            own = _adopt(own, follow["depth"](i, d), lambda f: flat[f],
+                         lambda f: isinstance(f, (int, np.integer)) and 0 <= f < P * K, tol,
                          ("depth", i, d), out["flags"], out["mismatches"])
         kept_par = [f // K for f in own]
         kept_c = [f % K for f in own]
@@ -244,8 +247,17 @@ def prune_into(out, i, nodes, B, anchor, follow=None, tol=TIE_TOL):
         if other is not None:
             other = sorted(other, key=lambda dk: (-by_id[dk][0], dk[0], dk[1])) \
                 if all(dk in by_id for dk in other) else list(other)
-        chosen = _adopt(chosen, other, lambda dk: by_id[dk][0], tol,
-                        ("prune", i), out["flags"], out["mismatches"])
+        n_flags = len(out["flags"])
+        kept = _adopt(chosen, other, lambda dk: by_id[dk][0], lambda dk: dk in by_id, tol,
+                      ("prune", i), out["flags"], out["mismatches"])
+        # an adopted set must still be prefix-closed (Lemma 1): every chosen node's
+        # parent is chosen; otherwise it is a mismatch and the oracle's own set stays
+        ks = set(kept)
+        if len(out["flags"]) > n_flags and any(d > 1 and (d - 1, by_id[(d, k)][1]) not in ks for d, k in kept):
+            del out["flags"][n_flags:]
+            out["mismatches"].append(("prune", i))
+        else:
+            chosen = kept
     chosen = sorted(chosen)                       # depth-major, rank within depth
     slot_of = {(0, 0): 0}
     out["tok"][i, 0], out["par"][i, 0], out["depth"][i, 0] = anchor, -1, 0
