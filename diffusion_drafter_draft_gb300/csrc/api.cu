@@ -347,7 +347,7 @@ int dartree_round(const dartree_head* head, const dartree_params* p, const void*
     SideStreams* side = nullptr;
     if (per_pos && !rm_done) {
         lock.lock();
-        side = side_streams();
+        side = side_streams(s);
         if (side) {
             if (cudaEventRecord(side->fork[0], s) != cudaSuccess ||
                 cudaStreamWaitEvent(side->s[0], side->fork[0], 0) != cudaSuccess)
@@ -368,7 +368,7 @@ int dartree_round(const dartree_head* head, const dartree_params* p, const void*
     if (int e = finish_tree(p, &st, anchor, tree, status, s)) return e;
     if (per_pos)
         return launch_walk_position(p->C, p->L, p->B, tree->tok, tree->par, tree->depth, tree->n_nodes, rowkeys,
-                                    accepted_len, path, bonus, s);
+                                    accepted_len, path, bonus, status, s);
     return launch_verify(p->C, p->L, p->B, tree->tok, tree->par, tree->depth, tree->n_nodes, target, rows, head->V,
                          head->dtype, rowkeys, accepted_len, path, bonus, status, s);
 }

@@ -483,8 +483,6 @@ int launch_expand(const ExpandArgs& a, cudaStream_t stream) {
     bool done = false;
     if (int e = try_launch_expand_g(a, stream, &done)) return e;
     if (done) return DARTREE_OK;
-    if (int e = try_launch_expand_small(a, stream, &done)) return e;
-    if (done) return DARTREE_OK;
     auto run = [&](const ExpandArgs& x, cudaStream_t st) {
         return x.dtype == DARTREE_BF16 ? launch_expand_t<bf16_t>(x, st) : launch_expand_t<float>(x, st);
     };
@@ -493,7 +491,7 @@ int launch_expand(const ExpandArgs& a, cudaStream_t stream) {
     // candidate-row contraction (HBM). Requests are independent; every
     // per-request buffer is indexed from the half's first request.
     std::unique_lock<std::recursive_mutex> lock(side_mutex());
-    SideStreams* side = a.C >= kSplitMinC ? side_streams() : nullptr;
+    SideStreams* side = a.C >= kSplitMinC ? side_streams(stream) : nullptr;
     if (!side) return run(a, stream);
     const int c0 = a.C / 2, r0 = c0;
     const size_t eb = a.dtype == DARTREE_BF16 ? 2 : 4;

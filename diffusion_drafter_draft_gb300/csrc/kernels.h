@@ -10,19 +10,26 @@
 namespace dartree {
 
 // Side streams for forks inside one call (0: target-row maxima of a round, 1: the
-// second half of a large batch's expansion). Enqueue under side_mutex().
+// second half of a large batch's expansion), one set per (device, caller stream),
+// so that callers on different streams never wait for each other's forks.
+// Enqueue under side_mutex().
 struct SideStreams {
+    int dev = -1;
+    cudaStream_t caller = nullptr;
     cudaStream_t s[2] = {nullptr, nullptr};
     cudaEvent_t fork[2] = {nullptr, nullptr}, join[2] = {nullptr, nullptr};
     bool ok = false;
 };
-SideStreams* side_streams();  // nullptr when they cannot be created
+// The set of `caller` on the current device (created on its first use); nullptr
+// when it cannot be created or the table of sets is full (the call then runs
+// without forks, on the caller's stream alone).
+SideStreams* side_streams(cudaStream_t caller);
 std::recursive_mutex& side_mutex();
 
 // Kernel ids of the launch timing (dartree_timing): one per kernel family.
 enum KernelId {
     KID_TOPK_ROWS = 0, KID_TOPK_STREAM, KID_GEMM, KID_CONTRACT, KID_EXPAND_G, KID_GATHER, KID_SELECT,
-    KID_STATE, KID_EXPAND_SMALL, KID_FINISH, KID_PRUNE, KID_MASK, KID_ROWMAX, KID_WALK, KID_OTHER,
+    KID_STATE, KID_HEAP, KID_FINISH, KID_PRUNE, KID_MASK, KID_ROWMAX, KID_WALK, KID_OTHER,
     KID_COUNT
 };
 // Brackets the launches of its scope with timing events when timing is enabled.
@@ -113,9 +120,6 @@ int launch_transpose_bf16(const void* src, void* dst, int H, cudaStream_t stream
 bool expand_g_fits(const ExpandArgs& a);
 int try_launch_expand_g(const ExpandArgs& a, cudaStream_t stream, bool* launched);
 
-// Small-batch persistent path; *launched = false when the shape does not fit it.
-int try_launch_expand_small(const ExpandArgs& a, cudaStream_t stream, bool* launched);
-
 // tcgen05 GEMM D[M,N] = A[M,K] . B[N,K]^T (bf16 in, fp32 accumulate).
 // mode 0: fp32 d32 [M,N]; mode 1: bf16 hi/lo pairs into hilo [M/P, 32, N];
 // mode 2: bf16 hi into hilo [M,N] and lo into lo2 [M,N].
@@ -148,9 +152,10 @@ int launch_rowmax_position(int C, int L, int V, int dtype, const void* target, u
                            cudaStream_t stream);
 
 // S10 walk over per-position row maxima computed by launch_rowmax_position.
+// status (may be null): DARTREE_EINTERNAL when the tree is malformed.
 int launch_walk_position(int C, int L, int B, const int32_t* tok, const int32_t* par, const int32_t* depth,
                          const int32_t* n_nodes, const unsigned long long* keys, int32_t* accepted, int32_t* path,
-                         int32_t* bonus, cudaStream_t stream);
+                         int32_t* bonus, int* status, cudaStream_t stream);
 
 // S8-S9 (and S10 with per-position row maxima when rowkeys is not null) for one
 // request per CTA; supertrees of at most 256 nodes (finish_supported).
@@ -161,6 +166,7 @@ int launch_finish(int C, int L, int W, int B, const int32_t* st_tok, const int32
                   int32_t* accepted, int32_t* path, int32_t* bonus, int* status, cudaStream_t stream,
                   bool pdl = false);
 
+// S10 (row maxima + walk); status (may be null): DARTREE_EINTERNAL when the tree is malformed.
 int launch_verify(int C, int L, int B, const int32_t* tok, const int32_t* par, const int32_t* depth,
                   const int32_t* n_nodes, const void* target, int rows_mode, int V, int dtype,
                   unsigned long long* keys, int32_t* accepted, int32_t* path, int32_t* bonus, int* status,

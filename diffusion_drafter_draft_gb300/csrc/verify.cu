@@ -11,6 +11,9 @@
 //  - per-node rows [C, B+1, V]: only the rows on the accepted path are read; one
 //    thread-block cluster per request computes each row's maximum (partials
 //    exchanged through distributed shared memory) and takes the next step.
+// A walk that would take more than L steps can only come from a malformed tree
+// (a parent that is not one depth above its child); it stops there and records
+// DARTREE_EINTERNAL in the status word (when one is given).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -77,7 +80,7 @@ __global__ void __launch_bounds__(RM_NT) rowmax_kernel(const T* __restrict__ x, 
 __global__ void walk_position_kernel(int L, int B, const int32_t* __restrict__ tok, const int32_t* __restrict__ par,
                                      const int32_t* __restrict__ depth, const int32_t* __restrict__ n_nodes,
                                      const unsigned long long* __restrict__ keys, int32_t* __restrict__ accepted,
-                                     int32_t* __restrict__ path, int32_t* __restrict__ bonus) {
+                                     int32_t* __restrict__ path, int32_t* __restrict__ bonus, int* status) {
     const int r = blockIdx.x;
     const int lane = threadIdx.x;
     const int S = B + 1;
@@ -86,7 +89,11 @@ __global__ void walk_position_kernel(int L, int B, const int32_t* __restrict__ t
     const int32_t* pr = par + size_t(r) * S;
     const int32_t* dp = depth + size_t(r) * S;
     int cur = 0, acc = 0, bon = -1;
-    for (int step = 0; step <= L; ++step) {
+    for (int step = 0;; ++step) {
+        if (step > L) {  // more steps than depths: malformed tree
+            if (lane == 0) set_status(status, DARTREE_EINTERNAL);
+            break;
+        }
         const int d = dp[cur];
         if (d < 0 || d >= L) break;
         const int t = int(0xffffffffu - uint32_t(keys[size_t(r) * L + d]));
@@ -116,7 +123,7 @@ __global__ void __launch_bounds__(WK_NT) walk_node_kernel(int L, int B, int V, i
                                                           const int32_t* __restrict__ par,
                                                           const int32_t* __restrict__ n_nodes,
                                                           int32_t* __restrict__ accepted, int32_t* __restrict__ path,
-                                                          int32_t* __restrict__ bonus) {
+                                                          int32_t* __restrict__ bonus, int* status) {
     __shared__ uint64_t part[2][8];
     __shared__ uint64_t red[WK_NT / 32];
     __shared__ int found_s;
@@ -153,7 +160,10 @@ __global__ void __launch_bounds__(WK_NT) walk_node_kernel(int L, int B, int V, i
         if (cr == 0 && threadIdx.x == 0 && acc < L) path[size_t(r) * L + acc] = f;
         ++acc;
         cur = f;
-        if (acc > L) break;
+        if (acc > L) {  // more steps than depths: malformed tree
+            if (cr == 0 && threadIdx.x == 0) set_status(status, DARTREE_EINTERNAL);
+            break;
+        }
     }
     if (cr == 0) {
         for (int q = acc + threadIdx.x; q < L; q += WK_NT) path[size_t(r) * L + q] = -1;
@@ -184,11 +194,12 @@ static int launch_rowmax_t(int rows, int V, const void* target, unsigned long lo
 
 int launch_walk_position(int C, int L, int B, const int32_t* tok, const int32_t* par, const int32_t* depth,
                          const int32_t* n_nodes, const unsigned long long* keys, int32_t* accepted, int32_t* path,
-                         int32_t* bonus, cudaStream_t stream) {
+                         int32_t* bonus, int* status, cudaStream_t stream) {
     if (C == 0) return DARTREE_OK;
     {
         KTimer kt_(KID_WALK, stream);
-        walk_position_kernel<<<C, 32, 0, stream>>>(L, B, tok, par, depth, n_nodes, keys, accepted, path, bonus);
+        walk_position_kernel<<<C, 32, 0, stream>>>(L, B, tok, par, depth, n_nodes, keys, accepted, path, bonus,
+                                                   status);
     }
     return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
@@ -204,13 +215,14 @@ template <typename T>
 static int launch_verify_t(int C, int L, int B, const int32_t* tok, const int32_t* par, const int32_t* depth,
                            const int32_t* n_nodes, const void* target, int rows_mode, int V,
                            unsigned long long* keys, int32_t* accepted, int32_t* path, int32_t* bonus,
-                           cudaStream_t stream) {
+                           int* status, cudaStream_t stream) {
     const T* tg = static_cast<const T*>(target);
     if (rows_mode == DARTREE_ROWS_PER_POSITION) {
         if (int e = launch_rowmax_t<T>(C * L, V, target, keys, stream)) return e;
         {
             KTimer kt_(KID_WALK, stream);
-            walk_position_kernel<<<C, 32, 0, stream>>>(L, B, tok, par, depth, n_nodes, keys, accepted, path, bonus);
+            walk_position_kernel<<<C, 32, 0, stream>>>(L, B, tok, par, depth, n_nodes, keys, accepted, path, bonus,
+                                                       status);
         }
         return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
     }
@@ -232,7 +244,8 @@ static int launch_verify_t(int C, int L, int B, const int32_t* tok, const int32_
     cudaError_t e;
     {
         KTimer kt_(KID_WALK, stream);
-        e = cudaLaunchKernelEx(&cfg, walk_node_kernel<T>, L, B, V, seg, tg, tok, par, n_nodes, accepted, path, bonus);
+        e = cudaLaunchKernelEx(&cfg, walk_node_kernel<T>, L, B, V, seg, tg, tok, par, n_nodes, accepted, path, bonus,
+                               status);
     }
     return e == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
@@ -241,13 +254,12 @@ int launch_verify(int C, int L, int B, const int32_t* tok, const int32_t* par, c
                   const int32_t* n_nodes, const void* target, int rows_mode, int V, int dtype,
                   unsigned long long* keys, int32_t* accepted, int32_t* path, int32_t* bonus, int* status,
                   cudaStream_t stream) {
-    (void)status;
     if (C == 0) return DARTREE_OK;
     if (dtype == DARTREE_BF16)
         return launch_verify_t<bf16_t>(C, L, B, tok, par, depth, n_nodes, target, rows_mode, V, keys, accepted,
-                                       path, bonus, stream);
+                                       path, bonus, status, stream);
     return launch_verify_t<float>(C, L, B, tok, par, depth, n_nodes, target, rows_mode, V, keys, accepted, path,
-                                  bonus, stream);
+                                  bonus, status, stream);
 }
 
 }  // namespace dartree

@@ -4,10 +4,12 @@
 // Some callers cannot allocate device memory where they verify: a serving loop
 // that hands all free HBM to its own caching allocator at start-up, or a plugin
 // reached through a plain C interface that has no allocator handle. For them
-// this entry point takes only inputs and outputs. Its scratch (the status word
-// and one 64-bit row key per target row) lives in g_verify_scratch below, a
-// file-scope device array of kStaticVerifyBytes that every GPU which loads the
-// library keeps until the process exits.
+// this entry point takes only inputs and outputs. Its scratch (one 64-bit row
+// key per target row, after a 256-byte header that is not used) lives in
+// g_verify_scratch below, a file-scope device array of kStaticVerifyBytes that
+// every GPU which loads the library keeps until the process exits. With no
+// status word the caller could read, a malformed tree (which dartree_verify
+// reports as DARTREE_EINTERNAL in its workspace) goes unreported here.
 #include <cuda_runtime.h>
 #include <mutex>
 #include <stdint.h>
@@ -62,10 +64,9 @@ extern "C" int dartree_verify_static(const dartree_params* p, const dartree_tree
     if (int e = scratch_on_current_device(&base)) return e;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* b = static_cast<uint8_t*>(base);
-    // the previous call's contents stay in the array: the status word starts at zero
-    // here, the row keys are cleared by launch_verify before they are used
-    if (cudaMemsetAsync(b, 0, sizeof(int32_t), s) != cudaSuccess) return DARTREE_ECUDA;
+    // the previous call's row keys stay in the array; launch_verify clears the ones
+    // it uses before the row maxima are taken
     return dartree::launch_verify(p->C, p->L, p->B, tree->tok, tree->par, tree->depth, tree->n_nodes, target, rows,
                                   V, dtype, reinterpret_cast<unsigned long long*>(b + kKeysOffset), accepted_len,
-                                  path, bonus, reinterpret_cast<int*>(b), s);
+                                  path, bonus, nullptr, s);
 }

@@ -38,6 +38,15 @@
  *  - Floating point inputs are finite. Equal values are ordered as stated per
  *    step; -0.0 and +0.0 compare equal.
  *  - Calls that share a workspace must not overlap on the device.
+ *  - Process-wide state (no device memory): forks inside a call (the second half
+ *    of a batch of 32 or more requests in S2-S7, the target-row maxima of
+ *    dartree_round) run on library-owned side streams, one pair per (device,
+ *    caller stream), created with their events on the first call that needs them
+ *    on that stream; make that call before capturing the stream into a CUDA graph.
+ *    Callers on different streams use different side streams and do not wait for
+ *    each other; a host mutex is held while a call enqueues its forks. Besides
+ *    these: the device address of the array of dartree_verify_static, and the
+ *    records of dartree_timing.
  */
 #ifndef DARTREE_H
 #define DARTREE_H
@@ -191,7 +200,10 @@ DARTREE_API int dartree_build_tree(const dartree_head* head, const dartree_param
  *   path          [C, L] slot ids of the accepted nodes in depth order, -1 padded
  *   bonus         [C] the target's token after the accepted prefix (argmax of the
  *                 last accepted slot's row), -1 when that row does not exist
- *                 (per-position rows and a fully accepted block) */
+ *                 (per-position rows and a fully accepted block)
+ * A tree whose walk would take more than L steps (a parent that is not one depth
+ * above its child) is malformed: the walk stops and DARTREE_EINTERNAL is recorded
+ * in the status word of ws. */
 DARTREE_API int dartree_verify(const dartree_params* p, const dartree_tree* tree, const void* target,
                    int rows, int V, int dtype, int32_t* accepted_len, int32_t* path,
                    int32_t* bonus, void* ws, size_t ws_bytes, void* stream);
@@ -202,10 +214,9 @@ DARTREE_API int dartree_verify(const dartree_params* p, const dartree_tree* tree
  * per-position rows the target-row maxima do not depend on the tree: when S1 runs
  * as one cluster per row (few rows) and the target and logit rows start on 16-byte
  * boundaries, the S1 launch computes them too; otherwise they are computed on a
- * library-owned side stream (one per device, created on the first call; make that
- * call before any stream capture) forked from `stream` after S1 and joined before
- * the walk; the fork is captured with the rest when `stream` is being captured
- * into a CUDA graph. Calls are serialised on the host while they enqueue. The row
+ * library-owned side stream of `stream` (see the conventions above) forked after
+ * S1 and joined before the walk; the fork is captured with the rest when `stream`
+ * is being captured into a CUDA graph. The row
  * maxima go to a workspace region of their own (the workspace of
  * dartree_workspace_bytes suffices). Later kernels of the call may be launched as
  * programmatic dependents of the one before (each waits for it on the device
@@ -223,15 +234,17 @@ DARTREE_API int dartree_round(const dartree_head* head, const dartree_params* p,
  * paper has no counterpart: this is a deployment variant of dartree_verify with
  * the same arguments, minus the workspace, and the same results.
  * Scratch is one file-scope device array of DARTREE_STATIC_VERIFY_BYTES bytes
- * (status word + 8 bytes per target row key), kept by every GPU that loads the
+ * (a 256-byte header + 8 bytes per target row key), kept by every GPU that loads the
  * library until the process exits. Limit: 256 + 8*C*max(L, B+1) bytes must fit,
  * else DARTREE_EUNSUPPORTED (before anything is enqueued). The first call on a
  * device looks up the array's device address with that device current (a
  * cudaGetSymbolAddress, no allocation); make that first call before any stream
  * capture. All calls share the one array and each starts by clearing what must
  * start at zero: calls that overlap on the GPU (other streams, other threads)
- * race on it and must be serialised by the caller. Allocates nothing: no
- * cudaMalloc, cudaFree or allocating library call. */
+ * race on it and must be serialised by the caller. There is no status word the
+ * caller can read, so a malformed tree (DARTREE_EINTERNAL for dartree_verify)
+ * is not reported by this variant. Allocates nothing: no cudaMalloc, cudaFree
+ * or allocating library call. */
 #define DARTREE_STATIC_VERIFY_BYTES (256u * 1024u)
 DARTREE_API int dartree_verify_static(const dartree_params* p, const dartree_tree* tree, const void* target,
                                       int rows, int V, int dtype, int32_t* accepted_len, int32_t* path,

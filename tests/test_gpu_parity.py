@@ -2,8 +2,10 @@
 
 Node sets, parents, depths, masks, position ids, accepted lengths, paths and bonus
 tokens must be bit-exact; scores agree within 2e-3 absolute. A per-depth or
-global selection that differs from the oracle's only on a score gap below 1e-3 is
-adopted by the oracle (follow mode) and counted, not failed.
+global selection that differs from the oracle's only on a score gap that is not
+zero and below 1e-3 is adopted by the oracle (follow mode) and counted (printed
+at the end of the run), not failed; exact ties must follow the stated order, and
+the tie-recipe cases allow no adopted selection at all.
 """
 import numpy as np
 import pytest
@@ -12,7 +14,7 @@ torch = pytest.importorskip("torch")
 
 import oracle  # noqa: E402
 from dartree_inputs import (breadth_first_slot_depth, make_config, make_inputs,  # noqa: E402
-                            make_target_per_node, round_to_bf16_bits, to_f64)
+                            make_target_per_node, make_tie_inputs, round_to_bf16_bits, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -106,6 +108,32 @@ def test_prune_mask_verify_on_oracle_supertree(name):
     compare_verify(o, gv, inp["target"], cfg, "position")
 
 
+# --------------------------------------------------------------------------- S2-S7 on the oracle's candidates
+
+@pytest.mark.parametrize("C,L,V,H,K,W,B,dtype", [(2, 5, 3001, 512, 64, 12, 30, "bf16"),
+                                                 (3, 4, 1500, 256, 128, 6, 12, "bf16"),
+                                                 (2, 4, 999, 64, 8, 3, 7, "f32")])
+def test_expand_from_oracle_candidates(C, L, V, H, K, W, B, dtype):
+    """dartree_expand fed the oracle's candidate table (kernel-level parity of
+    S2-S7; the supertree is then pruned and masked by dartree_prune and
+    dartree_tree_mask). The first shape takes the candidate-side path with its own
+    gather of the candidates' rows (no top-K launch copies them here), the second
+    the per-depth path, the third the fp32 path."""
+    import diffusion_drafter_draft_gb300 as dd
+    cfg = make_config("cfg1_qwen3_4b_c1").replace(C=C, L=L, V=V, H=H, K=K, W=W, B=B, dtype=dtype,
+                                                   seed=7 * C + K)
+    inp = make_inputs(cfg)
+    o0 = oracle.build(inp)
+    x = upload(inp)
+    ct = torch.from_numpy(o0["cand_tok"].astype(np.int32)).cuda()
+    cv = torch.from_numpy(o0["cand_logit"].astype(np.float32)).cuda()
+    st = dd.expand(x["E"], x["Wq"], x["hidden"], x["anchor"], ct, cv, cfg.W, cfg.beta)
+    tr = dd.prune(st, x["anchor"], cfg.B)
+    dd.tree_mask(tr, cfg.L)
+    g = host(dict(tr, st=st, cand_tok=ct, cand_val=cv))
+    compare_build(inp, g)
+
+
 # --------------------------------------------------------------------------- end to end
 
 @pytest.mark.parametrize("name", ["cfg0_tiny", "cfg1_qwen3_4b_c1", "cfg2_qwen3_8b_fixed", "cfg3_c4_adaptive",
@@ -175,12 +203,14 @@ def test_candidate_side_projection_shapes(C, L, V, H, K, W, B):
 
 def test_stress_batch_sampled_requests():
     """Full C=64, K=512 batch on the GPU; the oracle checks a sample of requests
-    (each request is drawn from its own stream, so a sample is bit-identical)."""
+    (each request is drawn from its own stream, so a sample is bit-identical).
+    The sample holds the first and last request of both halves that the batch is
+    split into (0, 31 | 32, 63) and four more."""
     import diffusion_drafter_draft_gb300 as dd
     cfg = make_config("cfg4_c64_stress")
     full = make_inputs(cfg)
     g, x = run_gpu_build(full)
-    sample = [0, 37, 63]
+    sample = [0, 9, 23, 31, 32, 37, 50, 63]
     small = make_inputs(cfg, requests=sample)
     o = compare_build(small, g, rows=sample)
     # per-node target rows: sampled requests use their true slot depths, the rest a fixed layout
@@ -227,3 +257,42 @@ def test_round_entry_point(name, C, rows):
     compare_build(inp, g)
     for k in ("tok", "par", "depth", "n_nodes", "mask", "pos"):
         np.testing.assert_array_equal(host(ta[k]), g[k], err_msg=k)
+
+
+# --------------------------------------------------------------------------- exact ties
+
+@pytest.mark.parametrize("name,C,L,V,H,K,W,B,beta,dtype", [
+    ("f32 simple path", 2, 5, 30, 8, 4, 5, 9, 0.0, "f32"),
+    ("f32 ragged", 3, 4, 211, 24, 5, 7, 9, 0.0, "f32"),
+    ("bf16 candidate side", 2, 6, 3001, 256, 16, 6, 12, 0.0, "bf16"),
+    ("bf16 candidate side, beta<0", 3, 5, 2000, 512, 64, 12, 30, -0.25, "bf16"),
+    ("bf16 per-depth path", 5, 5, 3001, 256, 200, 12, 30, 0.0, "bf16"),
+    ("qwen3-4b shape", 1, 16, 151936, 2560, 64, 12, 64, 0.0, "bf16"),
+    ("qwen3-4b shape, beta<0", 1, 16, 151936, 2560, 64, 12, 64, -0.25, "bf16"),
+])
+def test_exact_ties_follow_the_stated_order(name, C, L, V, H, K, W, B, beta, dtype):
+    """Tie-recipe inputs (E = 0, integer base logits with q = 1 for the top
+    candidate): every selection is decided by exact ties, which the GPU must break
+    as stated (top-K: lower token id; a depth's top-W: lower flat index p*K + c;
+    the deferred prune: shallower depth, then lower rank). No near-tie adoption
+    is allowed: the tree must equal the oracle's outright."""
+    import diffusion_drafter_draft_gb300 as dd
+    cfg = make_config("cfg1_qwen3_4b_c1").replace(C=C, L=L, V=V, H=H, K=K, W=W, B=B, beta=beta, dtype=dtype,
+                                                   seed=100 + C * L + K)
+    inp = make_tie_inputs(cfg)
+    g, x = run_gpu_build(inp)
+    o = compare_build(inp, g, max_flags=0)
+    # scores are exact here: integers plus beta * depth
+    np.testing.assert_array_equal(g["score"], o["score"].astype(np.float32))
+    tr = {k: torch.from_numpy(v).cuda() for k, v in g.items() if k in ("tok", "par", "depth", "n_nodes")}
+    gv = host(dd.verify(tr, x["target"], dd.ROWS_PER_POSITION, cfg.L))
+    compare_verify(o, gv, inp["target"], cfg, "position")
+    # the one-call round gives the same tree
+    rnd = dd.Round(x["E"], x["Wq"], cfg.C, cfg.L, cfg.K, cfg.W, cfg.B, cfg.beta, dd.ROWS_PER_POSITION)
+    out = {k: v.clone() for k, v in rnd.run(x["base"], x["hidden"], x["anchor"], x["target"]).items()}
+    torch.cuda.synchronize()
+    assert dd.read_status(rnd.ws) == 0
+    for k in ("tok", "par", "depth", "n_nodes", "mask", "pos"):
+        np.testing.assert_array_equal(host(rnd.tree[k]), o[k], err_msg=k)
+    for k in ("accepted_len", "path", "bonus"):
+        np.testing.assert_array_equal(host(out[k]), gv[k], err_msg=k)

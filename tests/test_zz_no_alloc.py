@@ -62,12 +62,53 @@ def test_static_scratch_verify_matches_workspace_verify(dd, rows, dtype):
             np.testing.assert_array_equal(got[k].cpu().numpy(), ref[k].cpu().numpy(), err_msg=k)
 
 
+def _random_trees(rng, C, L, B):
+    """Valid trees (slot 0 = root, parents earlier and one depth up, n_nodes in 1..B+1)."""
+    S = B + 1
+    tok = np.full((C, S), -1, np.int32)
+    par = np.full((C, S), -1, np.int32)
+    depth = np.full((C, S), -1, np.int32)
+    n = rng.integers(1, S + 1, size=C).astype(np.int32)
+    for i in range(C):
+        tok[i, 0], depth[i, 0] = 7, 0
+        for j in range(1, int(n[i])):
+            cand = [q for q in range(j) if depth[i, q] < L]
+            p = int(cand[rng.integers(0, len(cand))])
+            par[i, j], depth[i, j], tok[i, j] = p, depth[i, p] + 1, int(rng.integers(0, 64))
+    return {k: torch.from_numpy(v).cuda() for k, v in dict(tok=tok, par=par, depth=depth, n_nodes=n).items()}
+
+
+@pytest.mark.parametrize("rows", ["position", "node"])
+def test_static_scratch_accepts_its_exact_limit(dd, rows):
+    """C = 503 requests with B + 1 = 65 slots is the largest batch whose row keys
+    fit the array (256 + 8 * 503 * 65 <= 256 KiB): accepted, and equal to the
+    workspace variant on two calls in a row."""
+    C, L, B, V = 503, 16, 64, 64
+    assert 256 + 8 * C * (B + 1) <= 256 * 1024 < 256 + 8 * (C + 1) * (B + 1)
+    rng = np.random.default_rng(5)
+    tree = _random_trees(rng, C, L, B)
+    nrow = L if rows == "position" else B + 1
+    # small integer logits: argmax ties are frequent, the lowest id must win
+    target = torch.from_numpy(rng.integers(-4, 5, size=(C, nrow, V)).astype(np.float32)).cuda().to(torch.bfloat16)
+    mode = dd.ROWS_PER_POSITION if rows == "position" else dd.ROWS_PER_NODE
+    ref = dd.verify(tree, target, mode, L)
+    for _ in range(2):
+        got = dd.verify_static(tree, target, mode, L)
+        torch.cuda.synchronize()
+        for k in ("accepted_len", "path", "bonus"):
+            np.testing.assert_array_equal(got[k].cpu().numpy(), ref[k].cpu().numpy(), err_msg=k)
+
+
 def test_static_scratch_rejects_sizes_beyond_its_array(dd):
+    """One request more than the limit (C = 504 with B + 1 = 65 slots) is rejected
+    on the host, before anything is enqueued (the fake pointers are never used)."""
     L_ = dd.lib()
-    C = 1 + (256 * 1024) // (8 * 65)  # one request too many for B+1 = 65 row keys
-    p = dd.Params(C, 16, 1, 1, 64, 0.0)
+    C = 1 + (256 * 1024 - 256) // (8 * 65)
+    assert C == 504
     fake = ctypes.c_void_p(256)
     tree = dd.Tree(256, 256, 256, 256, 256, None, None)
-    rc = L_.dartree_verify_static(ctypes.byref(p), ctypes.byref(tree), fake, dd.ROWS_PER_NODE, 1000, dd.BF16, fake,
-                                  fake, fake, None)
-    assert rc == dd.EUNSUPPORTED
+    for rows, L in ((dd.ROWS_PER_NODE, 16), (dd.ROWS_PER_POSITION, 16), (dd.ROWS_PER_POSITION, 64)):
+        p = dd.Params(C, L, 1, 1, 64, 0.0)
+        rc = L_.dartree_verify_static(ctypes.byref(p), ctypes.byref(tree), fake, rows, 1000, dd.BF16, fake,
+                                      fake, fake, None)
+        assert rc == dd.EUNSUPPORTED
