@@ -14,15 +14,13 @@ namespace {
 using namespace dartree;
 
 constexpr size_t kAlign = 256;
-constexpr int kMaxClusters = 40;  // 8-CTA clusters: up to 320 SMs
 constexpr int kMaxGRows = 8192;   // candidate rows of the candidate-side projection path
 
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-    size_t status, cand_tok, cand_val, h[2], s[2], U, z, st_tok, st_par, st_s, st_n, keys, zpart, bar, uhl, Eg, Ghi, Glo,
-        total;
-    int zpart_clusters, g_rows;
+    size_t status, cand_tok, cand_val, h[2], s[2], U, z, st_tok, st_par, st_s, st_n, keys, uhl, Eg, Ghi, Glo, total;
+    int g_rows;
 };
 
 Layout layout_of(const dartree_params& p, int H, int dtype) {
@@ -45,10 +43,6 @@ Layout layout_of(const dartree_params& p, int H, int dtype) {
     l.st_s = take(C * L * W * 4);
     l.st_n = take(C * L * 4);
     l.keys = take((C * L > C * (B + 1) ? C * L : C * (B + 1)) * 8);
-    // per-cluster partial logits of the small-batch persistent kernel (C*W <= 48)
-    l.zpart_clusters = (C * W <= 48) ? kMaxClusters : 0;
-    l.zpart = take(size_t(l.zpart_clusters) * C * W * K * 4);
-    l.bar = take(4);
     // bf16 hi/lo projection rows for the tensor-core contraction, [C, 32, H]
     l.uhl = take(dtype == DARTREE_BF16 ? C * 32 * size_t(H) * 2 : 0);
     // candidate-side projection path (prepared bf16 heads, small batches): gathered
@@ -215,9 +209,6 @@ static ExpandArgs expand_args(const dartree_head* head, const dartree_params* p,
     a.sbuf[1] = at<float>(ws, l.s[1]);
     a.U = at<float>(ws, l.U);
     a.z = at<float>(ws, l.z);
-    a.zpart = l.zpart_clusters ? at<float>(ws, l.zpart) : nullptr;
-    a.zpart_clusters = l.zpart_clusters;
-    a.bar = at<unsigned>(ws, l.bar);
     a.uhl = head->dtype == DARTREE_BF16 ? at<uint16_t>(ws, l.uhl) : nullptr;
     a.WqT = head->WqT;
     a.g_rows = l.g_rows;
@@ -309,7 +300,15 @@ int dartree_build_tree(const dartree_head* head, const dartree_params* p, const 
     int* status = at<int>(ws, l.status);
     ExpandArgs a = expand_args(head, p, block_hidden, anchor, ct, cv, sp, ws, l);
     if (int e = topk_for_expand(head, p, base_logits, ct, cv, status, a, s)) return e;
+    // S8-S9 inside the expansion launch when its path can take them
+    const FinishOut fo{tree->tok, tree->par, tree->depth, tree->score, tree->n_nodes, tree->mask, tree->pos,
+                       nullptr, nullptr, nullptr, nullptr};
+    bool fin_done = false;
+    a.B = p->B;
+    a.fin = &fo;
+    a.fin_done = &fin_done;
     if (int e = launch_expand(a, s)) return e;
+    if (fin_done) return DARTREE_OK;
     return finish_tree(p, sp, anchor, tree, status, s);
 }
 
@@ -339,10 +338,20 @@ int dartree_round(const dartree_head* head, const dartree_params* p, const void*
     // after S1, overlapping the expansion, which leaves most SMs idle for small
     // batches (forked before S1 they would compete with it for HBM)
     ExpandArgs a = expand_args(head, p, block_hidden, anchor, ct, cv, &st, ws, l);
-    const TopkRowmax rm{target, rowkeys};
+    // on the candidate-side path the projection GEMM's idle warps take the bf16 row
+    // maxima (the top-K launch only clears their keys)
+    const bool gemm_rm = per_pos && head->dtype == DARTREE_BF16 && expand_g_fits(a) &&
+                         reinterpret_cast<uintptr_t>(target) % 16 == 0 && (size_t(head->V) * 2) % 16 == 0;
+    const TopkRowmax rm{target, rowkeys, gemm_rm};
     bool rm_done = false;
     if (int e = topk_for_expand(head, p, base_logits, ct, cv, status, a, s, per_pos ? &rm : nullptr, &rm_done))
         return e;
+    if (gemm_rm && rm_done) {
+        a.rm_target = target;
+        a.rm_keys = rowkeys;
+    } else if (gemm_rm) {
+        rm_done = false;  // keys not cleared: the maxima are taken below instead
+    }
     std::unique_lock<std::recursive_mutex> lock(side_mutex(), std::defer_lock);
     SideStreams* side = nullptr;
     if (per_pos && !rm_done) {
@@ -359,8 +368,22 @@ int dartree_round(const dartree_head* head, const dartree_params* p, const void*
             if (int e = launch_rowmax_position(p->C, p->L, head->V, head->dtype, target, rowkeys, s)) return e;
         }
     }
+    // S8-S10 inside the expansion launch when its path can take them and the row
+    // maxima are complete before it starts (not on a side stream)
+    const FinishOut fo{tree->tok, tree->par, tree->depth, tree->score, tree->n_nodes, tree->mask, tree->pos,
+                       per_pos ? rowkeys : nullptr, accepted_len, path, bonus};
+    bool fin_done = false;
+    if (!side) {
+        a.B = p->B;
+        a.fin = &fo;
+        a.fin_done = &fin_done;
+    }
     if (int e = launch_expand(a, s)) return e;
     if (side && cudaStreamWaitEvent(s, side->join[0], 0) != cudaSuccess) return DARTREE_ECUDA;
+    if (fin_done)
+        return per_pos ? DARTREE_OK
+                       : launch_verify(p->C, p->L, p->B, tree->tok, tree->par, tree->depth, tree->n_nodes, target,
+                                       rows, head->V, head->dtype, rowkeys, accepted_len, path, bonus, status, s);
     if (per_pos && finish_supported(p->L, p->W))  // (set-up overlapping the expansion's tail)
         return launch_finish(p->C, p->L, p->W, p->B, st.tok, st.par, st.score, st.n, anchor, tree->tok, tree->par,
                              tree->depth, tree->score, tree->n_nodes, tree->mask, tree->pos, rowkeys, accepted_len,

@@ -80,6 +80,11 @@ __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
     hi = __shfl_xor_sync(0xffffffffu, hi, m);
     return (uint64_t(hi) << 32) | lo;
 }
+__device__ __forceinline__ uint64_t shfl_idx_u64(uint64_t v, int src) {
+    const uint32_t lo = __shfl_sync(0xffffffffu, uint32_t(v), src);
+    const uint32_t hi = __shfl_sync(0xffffffffu, uint32_t(v >> 32), src);
+    return (uint64_t(hi) << 32) | lo;
+}
 __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
     for (int m = 16; m; m >>= 1) { uint64_t o = shfl_xor_u64(v, m); v = o > v ? o : v; }
     return v;

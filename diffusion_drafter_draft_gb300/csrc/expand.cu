@@ -496,6 +496,7 @@ int launch_expand(const ExpandArgs& a, cudaStream_t stream) {
     const int c0 = a.C / 2, r0 = c0;
     const size_t eb = a.dtype == DARTREE_BF16 ? 2 : 4;
     ExpandArgs h0 = a, h1 = a;
+    h0.fin = h1.fin = nullptr;  // the per-depth path leaves S8-S10 to the caller
     h0.C = c0;
     h1.C = a.C - c0;
     h1.hidden = static_cast<const uint8_t*>(a.hidden) + size_t(r0) * a.L * a.H * eb;

@@ -38,6 +38,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "finish.cuh"
 #include "kernels.h"
 #include "tc.cuh"
 
@@ -51,13 +52,15 @@ constexpr int XG_MAXW = 16;   // parents per depth: one 16-row mma tile
 __host__ __device__ constexpr size_t xg_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct XgLayout {
-    size_t gs, hs, es, hds, ctok, cval, zred, rkeys, lists, mrg, ssq, sel, spar, stout, mbar, total;
+    size_t gs, hs, es, hds, ctok, cval, zred, rkeys, lists, mrg, ssq, sel, spar, stout, fgk, ftree, fnext, frow,
+        fcnt, floc, fbits, mbar, total;
 };
 
 constexpr int XG_GB = 32;  // columns of one swizzled G tile (64 bytes)
 
-// fs: features per CTA (a multiple of 32, at most 256), cs: cluster size
-__host__ __device__ inline XgLayout xg_layout(int fs, int K, int cs, int L) {
+// fs: features per CTA (a multiple of 32, at most 256), cs: cluster size, B: node
+// budget of the S8-S10 run after the last depth (0: none)
+__host__ __device__ inline XgLayout xg_layout(int fs, int K, int cs, int L, int B) {
     const size_t fp = size_t(fs) + 8;
     const size_t rpo = XG_MAXW / cs;  // parent rows per owner
     XgLayout l{};
@@ -77,7 +80,16 @@ __host__ __device__ inline XgLayout xg_layout(int fs, int K, int cs, int L) {
     l.sel = take(size_t(XG_MAXW) * 8 + 2 * XG_MAXW * 4, 16);
     l.spar = take(size_t(XG_MAXW) * 4, 16);
     l.stout = take(size_t(L) * XG_MAXW * 8 + size_t(L) * 4, 16);  // supertree of the request, written at the end
-    l.mbar = take(4 * 8, 8);                         // prefetch barrier; exchanges A, B, C
+    // S8-S10 after the last depth (B + 1 slots)
+    const size_t S = size_t(B) + 1;
+    l.fgk = take(size_t(L) * XG_MAXW * 8, 16);       // keys in the global order [L][16]
+    l.ftree = take(4 * S * 4, 16);                   // slot arrays: token, parent, depth, score
+    l.fnext = take(S * 4, 16);                       // accepted child of every slot
+    l.frow = take(size_t(L) * 8, 16);                // per-position target row maxima
+    l.fcnt = take(2 * size_t(L) * 4, 16);            // chosen per depth (received), first slot per depth
+    l.floc = take(64 * 4, 16);                       // chosen per local depth; totals
+    l.fbits = take(size_t(XG_NW) * 32 * 4, 16);      // one ancestor bitset per warp (S <= 1024)
+    l.mbar = take(5 * 8, 8);                         // prefetch barrier; exchanges A, B, C; chosen counts F
     l.total = o;
     return l;
 }
@@ -95,6 +107,9 @@ struct XgArgs {
     float* st_s;
     int32_t* st_n;
     int* status;
+    int fin;       // run S8-S10 (and the walk when fo.rowkeys is set) after the last depth
+    int B;
+    FinishOut fo;
 };
 
 __device__ __forceinline__ void xg_ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
@@ -118,6 +133,10 @@ __device__ __forceinline__ void st_async_v2f32(uint32_t addr, float x, float y, 
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
                  :: "r"(addr), "f"(x), "f"(y), "r"(bar) : "memory");
 }
+__device__ __forceinline__ void st_async_u32(uint32_t addr, uint32_t v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+                 :: "r"(addr), "r"(v), "r"(bar) : "memory");
+}
 __device__ __forceinline__ void st_async_b64(uint32_t addr, uint64_t v, uint32_t bar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];"
                  :: "r"(addr), "l"(v), "r"(bar) : "memory");
@@ -130,6 +149,186 @@ __device__ __forceinline__ float half_sum(float v) {
     return v;
 }
 
+// S8-S10 of request r after the last depth, by the whole cluster (DARTree blog
+// post, 3.1: deferred pruning, one global top-B over the supertree, prefix-closed
+// for beta <= 0 (Lemma 1); 3.2: tree-attention mask, position ids, greedy longest
+// accepted prefix). Every CTA holds the same supertree: the kept keys of every
+// depth, sorted. In the global order (score desc, depth asc, rank asc) the
+// chosen set is the top min(B, nodes), and within a depth it is a prefix of the
+// sorted keys, so a depth's choice is one number: CTA q ranks the keys of depths
+// q, q + CS, ... against all keys (a warp per key), and sends each such depth's
+// chosen count to every CTA (st.async counted on barrier F). With all counts,
+// every CTA lays out the slots (depth-major, rank within a depth) and the parents'
+// slots itself. CTA 0 writes the tree arrays, CTA q the mask rows i = q mod CS,
+// and CTA 1 (CTA 0 for a cluster of one) follows the greedy walk over the
+// per-position target row maxima. Remote stores into this CTA all completed before
+// the last depth's list barrier, and no copy is in flight.
+template <int CS>
+__device__ void xg_finish(const XgArgs& a, uint8_t* smem, const XgLayout& lay, int r, uint32_t cr,
+                          const uint64_t* stkey, const int* stn, const int32_t* ctok) {
+    const int L = a.L, K = a.K, S = a.B + 1;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    uint64_t* fgk = reinterpret_cast<uint64_t*>(smem + lay.fgk);
+    int* ttok = reinterpret_cast<int*>(smem + lay.ftree);
+    int* tpar = ttok + S;
+    int* tdep = ttok + 2 * S;
+    float* tsc = reinterpret_cast<float*>(ttok + 3 * S);
+    int* fnext = reinterpret_cast<int*>(smem + lay.fnext);
+    uint64_t* frow = reinterpret_cast<uint64_t*>(smem + lay.frow);
+    int* fcnt = reinterpret_cast<int*>(smem + lay.fcnt);  // [L] chosen per depth
+    int* foff = fcnt + L;                                 // [L] first slot of every depth
+    int* floc = reinterpret_cast<int*>(smem + lay.floc);  // [0..8) chosen per local depth, [32] total
+    uint32_t* fbits = reinterpret_cast<uint32_t*>(smem + lay.fbits);
+    uint64_t* mbF = reinterpret_cast<uint64_t*>(smem + lay.mbar) + 4;
+    const uint32_t walker = CS > 1 ? 1u : 0u;
+    const bool walk = a.fo.rowkeys != nullptr && cr == walker;
+    const int nd = L * XG_MAXW;
+    if (walk)  // (the global loads overlap the ranking)
+        for (int d = threadIdx.x; d < L; d += XG_NT) frow[d] = a.fo.rowkeys[size_t(r) * L + d];
+    for (int i = threadIdx.x; i < nd; i += XG_NT) {
+        const int dm1 = i / XG_MAXW, k = i % XG_MAXW;
+        fgk[i] = k < stn[dm1] ? finish_key(uint32_t(stkey[i] >> 32), dm1, k) : 0ull;
+    }
+    if (threadIdx.x < 64) floc[threadIdx.x] = 0;
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(mbF, uint32_t(L * 4));
+    __syncthreads();
+    int nv = 0;
+    for (int d = 0; d < L; ++d) nv += stn[d];
+    const int N = min(a.B, nv);
+    // ranks of the keys of depths cr, cr + CS, ...: a warp per key, lanes over all keys
+    const int nloc = (L - int(cr) + CS - 1) / CS;
+    for (int i = wid; i < nloc * XG_MAXW; i += XG_NW) {
+        const int dl = i / XG_MAXW, k = i % XG_MAXW, dm1 = int(cr) + dl * CS;
+        if (k >= stn[dm1]) continue;  // uniform across the warp
+        const uint64_t x = fgk[dm1 * XG_MAXW + k];
+        int c = 0;
+        for (int j = lane; j < nd; j += 32) c += fgk[j] > x;
+        c = __reduce_add_sync(0xffffffffu, c);
+        if (lane == 0 && c < N) atomicAdd(&floc[dl], 1);
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < nloc * CS; t += XG_NT) {
+        const int dl = t / CS, q = t % CS, dm1 = int(cr) + dl * CS;
+        st_async_u32(mapa_u32(smem_u32(fcnt + dm1), uint32_t(q)), uint32_t(floc[dl]),
+                     mapa_u32(smem_u32(mbF), uint32_t(q)));
+    }
+    mbar_wait_bounded(mbF, 0, a.status);  // every depth's chosen count
+    // first slot of every depth: 1 + chosen counts of the depths above (L <= 64)
+    if (wid == 0) {
+        const int v0 = lane < L ? fcnt[lane] : 0, v1 = lane + 32 < L ? fcnt[lane + 32] : 0;
+        int s0 = v0, s1 = v1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y0 = __shfl_up_sync(0xffffffffu, s0, o), y1 = __shfl_up_sync(0xffffffffu, s1, o);
+            if (lane >= o) { s0 += y0; s1 += y1; }
+        }
+        const int t0 = __shfl_sync(0xffffffffu, s0, 31);
+        if (lane < L) foff[lane] = 1 + s0 - v0;
+        if (lane + 32 < L) foff[lane + 32] = 1 + t0 + s1 - v1;
+        if (lane == 31) floc[32] = t0 + s1;
+    }
+    __syncthreads();
+    const int chosen = floc[32], nn = min(S, 1 + chosen);
+    if (cr == 0 && threadIdx.x == 0 && chosen != N) set_status(a.status, DARTREE_EINTERNAL);
+    // slot arrays (parents as slots: a chosen node's parent must be chosen)
+    for (int i = threadIdx.x; i < nd; i += XG_NT) {
+        const int dm1 = i / XG_MAXW, k = i % XG_MAXW;
+        if (k < fcnt[dm1]) {
+            const int j = foff[dm1] + k;
+            const uint64_t sk = stkey[i];
+            const uint32_t f = 0xffffffffu - uint32_t(sk);
+            const int pr = int(f) / K;
+            int ps = 0;
+            if (dm1 > 0) {
+                ps = pr < fcnt[dm1 - 1] ? foff[dm1 - 1] + pr : -1;
+                if (ps < 0 && cr == 0) set_status(a.status, DARTREE_EINTERNAL);  // not prefix-closed
+            }
+            if (j < S) {
+                ttok[j] = ctok[dm1 * K + int(f) % K];
+                tpar[j] = ps;
+                tdep[j] = dm1 + 1;
+                tsc[j] = f32_from_ord(uint32_t(sk >> 32));
+            }
+        }
+    }
+    for (int j = threadIdx.x; j < S; j += XG_NT) {
+        if (j == 0) {
+            ttok[0] = a.anchor[r];
+            tpar[0] = -1;
+            tdep[0] = 0;
+            tsc[0] = 0.f;
+        } else if (j >= nn) {
+            ttok[j] = tpar[j] = tdep[j] = -1;
+            tsc[j] = 0.f;
+        }
+    }
+    __syncthreads();
+    if (cr == 0) {
+        for (int j = threadIdx.x; j < S; j += XG_NT) {
+            const size_t o = size_t(r) * S + j;
+            a.fo.tok[o] = ttok[j];
+            a.fo.par[o] = tpar[j];
+            a.fo.depth[o] = tdep[j];
+            a.fo.score[o] = tsc[j];
+            if (a.fo.pos) a.fo.pos[o] = tdep[j];
+        }
+        if (threadIdx.x == 0) a.fo.n_nodes[r] = 1 + chosen;
+    }
+    // S9: mask rows i = cr (mod CS), a warp per row: the ancestor-or-self bitset of
+    // slot i (a walk up its parents), then one byte per column
+    if (a.fo.mask) {
+        uint32_t* bits = fbits + wid * 32;
+        const int nw = (S + 31) / 32;
+        for (int i = int(cr) + wid * CS; i < S; i += CS * XG_NW) {
+            if (lane < nw) bits[lane] = 0u;
+            __syncwarp();
+            if (lane == 0 && i < nn) {
+                int b = i;
+                for (int g = 0; g <= L && b >= 0 && b < S; ++g) {
+                    bits[b >> 5] |= 1u << (b & 31);
+                    b = tpar[b];
+                }
+            }
+            __syncwarp();
+            uint8_t* row = a.fo.mask + (size_t(r) * S + i) * S;
+            for (int j = lane; j < S; j += 32) row[j] = uint8_t((bits[j >> 5] >> (j & 31)) & 1u);
+            __syncwarp();
+        }
+    }
+    // S10 with per-position row maxima: every slot's accepted child (the lowest slot
+    // under it whose token is the argmax of its row), then one thread follows them
+    if (walk) {
+        for (int j = threadIdx.x; j < S; j += XG_NT) fnext[j] = 0x7fffffff;
+        __syncthreads();
+        for (int j = 1 + threadIdx.x; j < nn; j += XG_NT) {
+            const int p = tpar[j];
+            const int dp = (p >= 0 && p < nn) ? tdep[p] : -1;
+            if (dp >= 0 && dp < L && ttok[j] == int(0xffffffffu - uint32_t(frow[dp]))) atomicMin(&fnext[p], j);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int cur = 0, acc = 0, bon = -1;
+            for (int step = 0; step <= L; ++step) {
+                const int d = tdep[cur];
+                if (d < 0 || d >= L) break;
+                const int f = fnext[cur];
+                if (f == 0x7fffffff) {
+                    bon = int(0xffffffffu - uint32_t(frow[d]));
+                    break;
+                }
+                if (acc < L) a.fo.path[size_t(r) * L + acc] = f;
+                ++acc;
+                cur = f;
+            }
+            a.fo.accepted[r] = acc;
+            a.fo.bonus[r] = bon;
+            floc[33] = acc;
+        }
+        __syncthreads();
+        for (int u = floc[33] + threadIdx.x; u < L; u += XG_NT) a.fo.path[size_t(r) * L + u] = -1;
+    }
+}
+
 template <int CS>
 __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __grid_constant__ CUtensorMap tm_ghi,
                                                              const __grid_constant__ CUtensorMap tm_glo,
@@ -138,7 +337,7 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
     extern __shared__ __align__(1024) uint8_t smem[];
     const int H = a.H, L = a.L, K = a.K, W = a.W;
     const int fs = H / CS, fp = fs + 8, cpr = fs / 8, nb = fs / XG_GB;
-    const XgLayout lay = xg_layout(fs, K, CS, L);
+    const XgLayout lay = xg_layout(fs, K, CS, L, a.fin ? a.B : 0);
     uint8_t* gs = smem + lay.gs;
     uint16_t* hs = reinterpret_cast<uint16_t*>(smem + lay.hs);
     uint16_t* es = reinterpret_cast<uint16_t*>(smem + lay.es);
@@ -156,7 +355,7 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
     uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + lay.mbar);  // prefetch
     uint64_t* mbA = mbar + 1;  // partial logits of the owned rows
     uint64_t* mbB = mbar + 2;  // row lists
-    uint64_t* mbC = mbar + 3;  // partial sums of squares
+    uint64_t* mbC = mbar + 3;  // partial sums of squares (mbar + 4: chosen counts of S8, in xg_finish)
     uint64_t* stkey = reinterpret_cast<uint64_t*>(smem + lay.stout);  // [L][16] kept keys (0 = none)
     int* stn = reinterpret_cast<int*>(stkey + size_t(L) * XG_MAXW);    // [L] kept per depth
 
@@ -181,7 +380,7 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
 
     griddep_launch_dependents();
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(&mbar[i], 1);
+        for (int i = 0; i < 5; ++i) mbar_init(&mbar[i], 1);
         fence_mbar_init();
     }
     // root: h = E[anchor] (this CTA's slice), s = 0
@@ -413,10 +612,13 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
         }
         mbar_wait_bounded(mbC, par, a.status);  // every partial sum of squares
         if (row_ok) {
-            float tot = 0.f;
+            // the CS partial sums in four fixed chains; reciprocal square root in
+            // one instruction (its error is far below the bf16 rounding of h)
+            float t4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int q = 0; q < CS; ++q) tot += ssq[q * XG_MAXW + k];
-            const float inv = 1.0f / sqrtf(tot / float(H) + 1e-6f);
+            for (int q = 0; q < CS; ++q) t4[q & 3] += ssq[q * XG_MAXW + k];
+            const float tot = (t4[0] + t4[1]) + (t4[2] + t4[3]);
+            const float inv = rsqrtf(tot / float(H) + 1e-6f);
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int j = hl + 16 * cc;
@@ -456,6 +658,7 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
     }
     // a prefetch still in flight (only after a timed-out wait) lands before the CTA leaves
     if (!pf_ok) mbar_wait_bounded(mbar, uint32_t(waited) & 1u, a.status);
+    if (a.fin) xg_finish<CS>(a, smem, lay, r, cr, stkey, stn, ctok);
 }
 
 // --------------------------------------------------------------------------- gathers, transpose
@@ -568,17 +771,24 @@ static bool xg_fs_ok(int H, int cs) { return H % (cs * XG_GB) == 0 && H / cs <= 
 
 // Cluster size of the path for these arguments (0: it does not apply) and its
 // shared memory.
+// Whether the launch also runs S8-S10 (a.fin given and the supertree small enough).
+static bool xg_fin(const ExpandArgs& a) {
+    return a.fin && a.fin_done && a.B >= 1 && a.B + 1 <= 1024 && a.L * XG_MAXW <= 4096;
+}
+
 static int xg_plan(const ExpandArgs& a, size_t* smem) {
     if (a.dtype != DARTREE_BF16 || !a.WqT || !a.Eg || !a.Ghi || !a.Glo) return 0;
     const int M = a.C * a.L * a.K;
     if (M > a.g_rows || a.K > XG_MAXK || a.K % 8 != 0 || a.W > XG_MAXW) return 0;
     if (!gemm_tc_supported(M, a.H, a.H) || a.H / 8 > GR_MAXV * GR_NT) return 0;
+    const int fin_b = xg_fin(a) ? a.B : 0;
+    auto need = [&](int cs) { return xg_layout(a.H / cs, a.K, cs, a.L, fin_b).total; };
     if (xg_fs_ok(a.H, 16)) {
-        const size_t sm = xg_layout(a.H / 16, a.K, 16, a.L).total;
+        const size_t sm = need(16);
         if (sm <= 227 * 1024 && xg_cluster_ok<16>(sm)) { *smem = sm; return 16; }
     }
     if (xg_fs_ok(a.H, 8)) {
-        const size_t sm = xg_layout(a.H / 8, a.K, 8, a.L).total;
+        const size_t sm = need(8);
         if (sm <= 227 * 1024 && xg_cluster_ok<8>(sm)) { *smem = sm; return 8; }
     }
     return 0;
@@ -605,7 +815,9 @@ int try_launch_expand_g(const ExpandArgs& a, cudaStream_t stream, bool* launched
         if (cudaGetLastError() != cudaSuccess) return DARTREE_ECUDA;
     }
     // the GEMM's W_q^T tiles and set-up overlap the previous kernel's tail
-    if (int e = launch_gemm_bf16_tc(a.Eg, a.WqT, M, a.H, a.H, 2, nullptr, a.Ghi, 1, a.status, stream, a.Glo, true))
+    const GemmRowmax grm{static_cast<const uint16_t*>(a.rm_target), a.C * a.L, a.V, a.rm_keys};
+    if (int e = launch_gemm_bf16_tc(a.Eg, a.WqT, M, a.H, a.H, 2, nullptr, a.Ghi, 1, a.status, stream, a.Glo, true,
+                                    a.rm_target ? &grm : nullptr))
         return e;
     const int fs = a.H / cs;
     CUtensorMap ghi, glo, eg;
@@ -630,6 +842,12 @@ int try_launch_expand_g(const ExpandArgs& a, cudaStream_t stream, bool* launched
     x.st_s = a.st_s;
     x.st_n = a.st_n;
     x.status = a.status;
+    if (xg_fin(a)) {
+        x.fin = 1;
+        x.B = a.B;
+        x.fo = *a.fin;
+        *a.fin_done = true;
+    }
     return cs == 16 ? xg_launch<16>(x, ghi, glo, eg, a.C, smem, stream) : xg_launch<8>(x, ghi, glo, eg, a.C, smem, stream);
 }
 

@@ -1,72 +1,22 @@
-// S8-S10 for one request per CTA when the supertree holds at most 256 nodes:
-// deferred pruning (DARTree blog post, 3.1 "Basic flow", Lemma 1: one global
-// top-B over the supertree, prefix-closed for beta <= 0), the tree-attention mask
-// and position ids (3.2), and, with per-position target rows, the greedy
-// longest accepted prefix (3.2).
-//
-// Every supertree node's global rank under (score desc, depth asc, rank asc) is
-// counted against all keys in shared memory (broadcast reads); the nodes of rank
-// below B are chosen and take slots in (depth, rank) order by a block scan. Tree
-// arrays, ancestor table and mask are built in shared memory, and the walk
-// follows the row maxima computed beforehand (by the top-K launch, or on a side
-// stream overlapping the build), read into shared memory first.
+// S8-S10 for one request per CTA when the supertree holds at most 256 nodes
+// (finish.cuh): the supertree is read from global memory.
 #include "common.cuh"
+#include "finish.cuh"
 #include "kernels.h"
 
 namespace dartree {
-
-constexpr int FN_NT = 256;  // one supertree node per thread
-
-struct FnSmem {
-    size_t keys, slot, ttok, tpar, tdep, anc, rowk, next, wtot, misc, bytes;
-};
-__host__ __device__ inline FnSmem fn_smem(int L, int B) {
-    const size_t S = size_t(B) + 1;
-    FnSmem f{};
-    size_t o = 0;
-    auto take = [&](size_t b) { size_t at = o; o = (o + b + 15) / 16 * 16; return at; };
-    f.keys = take(FN_NT * 8);
-    f.slot = take(FN_NT * 4);
-    f.ttok = take(S * 4);
-    f.tpar = take(S * 4);
-    f.tdep = take(S * 4);
-    f.anc = take(S * (size_t(L) + 1) * 2);
-    f.rowk = take(size_t(L) * 8);
-    f.next = take(S * 4);
-    f.wtot = take(32 * 4);
-    f.misc = take(16);
-    f.bytes = o;
-    return f;
-}
 
 template <bool WALK>
 __global__ void __launch_bounds__(FN_NT) finish_kernel(int L, int W, int B, const int32_t* __restrict__ st_tok,
                                                        const int32_t* __restrict__ st_par,
                                                        const float* __restrict__ st_s,
                                                        const int32_t* __restrict__ st_n,
-                                                       const int32_t* __restrict__ anchor, int32_t* __restrict__ tok,
-                                                       int32_t* __restrict__ par, int32_t* __restrict__ depth,
-                                                       float* __restrict__ score, int32_t* __restrict__ n_nodes,
-                                                       uint8_t* __restrict__ mask, int32_t* __restrict__ pos,
-                                                       const unsigned long long* __restrict__ rowkeys,
-                                                       int32_t* __restrict__ accepted, int32_t* __restrict__ path,
-                                                       int32_t* __restrict__ bonus, int* status) {
+                                                       const int32_t* __restrict__ anchor, FinishOut o,
+                                                       int* status) {
     extern __shared__ __align__(16) uint8_t smem[];
     griddep_wait();  // the supertree comes from the kernel before this one
-    const FnSmem fl = fn_smem(L, B);
-    uint64_t* keys = reinterpret_cast<uint64_t*>(smem + fl.keys);
-    int* slot = reinterpret_cast<int*>(smem + fl.slot);
-    int* ttok = reinterpret_cast<int*>(smem + fl.ttok);
-    int* tpar = reinterpret_cast<int*>(smem + fl.tpar);
-    int* tdep = reinterpret_cast<int*>(smem + fl.tdep);
-    int16_t* anc = reinterpret_cast<int16_t*>(smem + fl.anc);
-    int* wtot = reinterpret_cast<int*>(smem + fl.wtot);
-    int* misc = reinterpret_cast<int*>(smem + fl.misc);  // [0] scan total
-    uint64_t* rowk = reinterpret_cast<uint64_t*>(smem + fl.rowk);
-    int* next = reinterpret_cast<int*>(smem + fl.next);  // accepted child of every slot, or INT_MAX
-    const int r = blockIdx.x, n = L * W, S = B + 1, q = threadIdx.x;
+    const int r = blockIdx.x, n = L * W, q = threadIdx.x;
     const size_t base = size_t(r) * L * W;
-
     // ---- keys of the supertree nodes (0 = no node)
     uint64_t key = 0;
     int s_tok = -1, s_par = -1, dm1 = 0;
@@ -78,135 +28,10 @@ __global__ void __launch_bounds__(FN_NT) finish_kernel(int L, int W, int B, cons
             s_sc = st_s[base + q];
             s_tok = st_tok[base + q];
             s_par = st_par[base + q];
-            const float sv = s_sc + 0.f;
-            key = (uint64_t(ord_f32(sv)) << 32) | (uint64_t(0xffffu - uint32_t(dm1 + 1)) << 16) | (0xffffu - uint32_t(k));
+            key = finish_key(ord_f32(s_sc + 0.f), dm1, k);
         }
     }
-    keys[q] = key;
-    if (WALK)
-        for (int d = q; d < L; d += FN_NT) rowk[d] = rowkeys[size_t(r) * L + d];
-    const int nv = __syncthreads_count(key != 0);
-    const int N = min(B, nv);
-    // ---- global rank: keys above this one (all threads read the same pair at once)
-    int above = 0;
-    {
-        const ulonglong2* k2 = reinterpret_cast<const ulonglong2*>(keys);
-        const int n2 = (n + 1) / 2;
-#pragma unroll 4
-        for (int i = 0; i < n2; ++i) {
-            const ulonglong2 v = k2[i];
-            above += (v.x > key) + (v.y > key);
-        }
-    }
-    const bool ch = key != 0 && above < N;
-    // ---- slots in (depth, rank) order
-    const int ex = block_exclusive_scan<FN_NT>(ch ? 1 : 0, wtot, misc);
-    const int chosen = misc[0];
-    slot[q] = ch ? 1 + ex : -1;
-    for (int j = q; j < S; j += FN_NT) {
-        if (j == 0) { ttok[0] = anchor[r]; tpar[0] = -1; tdep[0] = 0; }
-        else if (j > chosen) { ttok[j] = -1; tpar[j] = -1; tdep[j] = -1; }
-    }
-    __syncthreads();
-    int32_t* t_tok = tok + size_t(r) * S;
-    int32_t* t_par = par + size_t(r) * S;
-    int32_t* t_dep = depth + size_t(r) * S;
-    float* t_sc = score + size_t(r) * S;
-    if (ch) {
-        const int j = 1 + ex;
-        int ps = 0;
-        if (dm1 > 0) {
-            ps = (s_par >= 0 && s_par < W) ? slot[(dm1 - 1) * W + s_par] : -1;
-            if (ps < 0) set_status(status, DARTREE_EINTERNAL);  // the chosen set is not prefix-closed
-        }
-        if (j < S) {
-            ttok[j] = s_tok;
-            tpar[j] = ps;
-            tdep[j] = dm1 + 1;
-        }
-    }
-    __syncthreads();
-    for (int j = q; j < S; j += FN_NT) {
-        t_tok[j] = ttok[j];
-        t_par[j] = tpar[j];
-        t_dep[j] = tdep[j];
-    }
-    if (ch && 1 + ex < S) t_sc[1 + ex] = s_sc;
-    for (int j = q; j < S; j += FN_NT)
-        if (j == 0 || j > chosen) t_sc[j] = 0.f;
-    if (q == 0) {
-        n_nodes[r] = 1 + chosen;
-        if (chosen != N) set_status(status, DARTREE_EINTERNAL);
-    }
-    const int nn = min(S, 1 + chosen);
-    // ---- mask and position ids: anc[i][delta] = ancestor of slot i at depth delta
-    if (mask) {
-        for (int i = q; i < S; i += FN_NT) {
-            const int di = i < nn ? min(max(tdep[i], 0), L) : -1;
-            if (di >= 0) {
-                int b = i;
-                for (int dd = di; dd >= 0; --dd) {
-                    anc[size_t(i) * (L + 1) + dd] = int16_t(b);
-                    b = (b >= 0 && b < S) ? tpar[b] : -1;
-                }
-            }
-            pos[size_t(r) * S + i] = di;
-        }
-        __syncthreads();
-        uint8_t* m = mask + size_t(r) * S * S;
-        const int total = S * S;
-        for (int e = q * 4; e < total; e += FN_NT * 4) {
-            uint32_t word = 0;
-            const int i0 = e / S;
-            int i = i0, j = e - i0 * S;  // (row, column) of byte e, then stepped
-            const int di = i < nn ? tdep[i] : -1;
-            const int di2 = i + 1 < nn ? tdep[i + 1] : -1;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (e + u >= total) break;
-                const int dii = i == i0 ? di : di2;
-                const int dj = j < nn ? tdep[j] : -1;
-                const bool on = dii >= 0 && dj >= 0 && dj <= dii && anc[size_t(i) * (L + 1) + dj] == j;
-                word |= uint32_t(on) << (8 * u);
-                if (++j == S) { j = 0; ++i; }
-            }
-            if (e + 4 <= total && (reinterpret_cast<uintptr_t>(m + e) & 3) == 0) {
-                *reinterpret_cast<uint32_t*>(m + e) = word;
-            } else {
-                for (int u = 0; u < 4 && e + u < total; ++u) m[e + u] = uint8_t(word >> (8 * u));
-            }
-        }
-    }
-    // ---- greedy walk with per-position row maxima: every slot's accepted child
-    //      (the lowest slot whose parent it is and whose token is the argmax of
-    //      the parent's row) in parallel, then one thread follows the chain
-    if (WALK) {
-        for (int j = q; j < S; j += FN_NT) next[j] = 0x7fffffff;
-        __syncthreads();
-        for (int j = 1 + q; j < nn; j += FN_NT) {
-            const int p = tpar[j];
-            const int dp = (p >= 0 && p < nn) ? tdep[p] : -1;
-            if (dp >= 0 && dp < L && ttok[j] == int(0xffffffffu - uint32_t(rowk[dp]))) atomicMin(&next[p], j);
-        }
-        __syncthreads();
-        if (q == 0) {
-            int cur = 0, acc = 0, bon = -1;
-            for (int step = 0; step <= L; ++step) {
-                const int d = tdep[cur];
-                if (d < 0 || d >= L) break;
-                const int f = next[cur];
-                if (f == 0x7fffffff) { bon = int(0xffffffffu - uint32_t(rowk[d])); break; }
-                if (acc < L) path[size_t(r) * L + acc] = f;
-                ++acc;
-                cur = f;
-            }
-            accepted[r] = acc;
-            bonus[r] = bon;
-            misc[1] = acc;
-        }
-        __syncthreads();
-        for (int u = misc[1] + q; u < L; u += FN_NT) path[size_t(r) * L + u] = -1;
-    }
+    finish_request<WALK>(r, L, W, B, smem, key, s_tok, s_par, s_sc, dm1, anchor[r], o, status);
 }
 
 bool finish_supported(int L, int W) { return L * W <= FN_NT; }
@@ -230,11 +55,11 @@ int launch_finish(int C, int L, int W, int B, const int32_t* st_tok, const int32
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+    const FinishOut o{tok, par, depth, score, n_nodes, mask, pos, rowkeys, accepted, path, bonus};
     cudaError_t e;
     {
         KTimer kt_(KID_FINISH, stream);
-        e = cudaLaunchKernelEx(&cfg, kern, L, W, B, st_tok, st_par, st_s, st_n, anchor, tok, par, depth, score,
-                               n_nodes, mask, pos, rowkeys, accepted, path, bonus, status);
+        e = cudaLaunchKernelEx(&cfg, kern, L, W, B, st_tok, st_par, st_s, st_n, anchor, o, status);
     }
     return e == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }

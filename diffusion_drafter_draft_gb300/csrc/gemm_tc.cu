@@ -13,7 +13,10 @@
 //   mode 0: fp32 D (row-major, ld = N);
 //   mode 1: the contraction's operand, U split into a bf16 pair (hi = bf16(u),
 //           lo = bf16(u - hi)), row m = r*P + p going to rows r*32 + p and
-//           r*32 + 16 + p of a [requests, 32, N] buffer.
+//           r*32 + 16 + p of a [requests, 32, N] buffer;
+//   mode 2: the same pair into two [M, N] buffers.
+// The bf16 pairs are staged in shared memory (the drained operand ring) and
+// written row by row, so that consecutive lanes store consecutive 16 bytes.
 // Every mbarrier wait is bounded; a wait that runs out records DARTREE_ETIMEOUT.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -33,7 +36,68 @@ struct GemmOut {
     uint16_t* hilo;
     uint16_t* lo2;     // mode 2: [M, N]
     int P;             // mode 1: rows per request (<= 16)
+    GemmRowmax rm;     // rm.target null: none
 };
+
+// Maxima keys (ord(value) << 32 | ~token) of bf16 rows: warps 2 and 3 of every CTA
+// (idle while the ring streams) take segments of the rows, spread over the grid,
+// and merge them with one 64-bit atomic max per warp and segment. The keys were
+// cleared by the launch before this one, whose completion griddep_wait ensures.
+struct RowmaxSeg {
+    int spr, per, nvr, nb, b;
+};
+__device__ __forceinline__ RowmaxSeg rowmax_seg(const GemmRowmax& rm) {
+    RowmaxSeg g;
+    g.nb = int(gridDim.x * gridDim.y);
+    g.b = int(blockIdx.y * gridDim.x + blockIdx.x);
+    g.spr = (g.nb + rm.rows - 1) / rm.rows;  // segments per row
+    g.nvr = rm.V / 8;                        // 16-byte vectors per row
+    g.per = (g.nvr + g.spr - 1) / g.spr;
+    return g;
+}
+// Before the dependency wait (the rows are inputs, not written by the launch before):
+// this CTA's segments into L2, one bulk prefetch per 16 KB.
+__device__ void gemm_rowmax_prefetch(const GemmRowmax& rm) {
+    const RowmaxSeg g = rowmax_seg(rm);
+    for (int item = g.b; item < rm.rows * g.spr; item += g.nb) {
+        const int row = item / g.spr, seg = item - row * g.spr;
+        const int v0 = seg * g.per, v1 = min(g.nvr, v0 + g.per);
+        const uint4* src = reinterpret_cast<const uint4*>(rm.target + size_t(row) * rm.V);
+        for (int v = v0 + (threadIdx.x - 64) * 1024; v < v1; v += 64 * 1024)
+            prefetch_l2_bulk(src + v, uint32_t(min(1024, v1 - v)) * 16u);
+    }
+}
+__device__ void gemm_rowmax(const GemmRowmax& rm) {
+    const int lane = threadIdx.x & 31, t = threadIdx.x - 64;  // 0..63
+    const RowmaxSeg g = rowmax_seg(rm);
+    constexpr int U = 8;  // loads in flight per thread
+    for (int item = g.b; item < rm.rows * g.spr; item += g.nb) {
+        const int row = item / g.spr, seg = item - row * g.spr;
+        const int v0 = seg * g.per, v1 = min(g.nvr, v0 + g.per);
+        const uint4* src = reinterpret_cast<const uint4*>(rm.target + size_t(row) * rm.V);
+        uint64_t best = 0;
+        for (int vb = v0 + t; vb < v1; vb += 64 * U) {
+            uint4 w[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (vb + u * 64 < v1) w[u] = __ldg(src + vb + u * 64);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = vb + u * 64;
+                if (v >= v1) break;
+                const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t o = ord_bf16((ws[e >> 1] >> ((e & 1) * 16)) & 0xffffu);
+                    const uint64_t k = (uint64_t(o) << 32) | (0xffffffffu - uint32_t(v * 8 + e));
+                    best = k > best ? k : best;
+                }
+            }
+        }
+        best = warp_max_u64(best);
+        if (lane == 0 && best) atomicMax(rm.keys + row, (unsigned long long)best);
+    }
+}
 
 template <int BN>
 struct GtSmem {
@@ -46,6 +110,10 @@ struct GtSmem {
     static constexpr size_t SLOT = BAR + 8 * (2 * STAGES + 1);
     static constexpr size_t TOTAL = SLOT + 16 + 1024;      // + alignment slack
     static constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+    // epilogue staging of the bf16 pair in the drained ring: rows padded by 16
+    // bytes, so a warp's 16-byte row stores fall on all 32 banks
+    static constexpr int EPI_PITCH = BN * 2 + 16;
+    static_assert(size_t(2) * GT_BM * EPI_PITCH <= BAR, "epilogue staging fits in the operand ring");
 };
 
 __device__ __forceinline__ uint16_t bf16_rn_bits(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
@@ -77,6 +145,7 @@ __global__ void __launch_bounds__(GT_NT, 1) gemm_bf16_tc_kernel(const __grid_con
     const uint32_t tmem = *slot;
 
     griddep_launch_dependents();
+    if (warp >= 2 && out.rm.target) gemm_rowmax_prefetch(out.rm);
     if (warp == 0 && lane == 0) {
         // producer: TMA ring. B is not written by the previous kernel of the stream:
         // the first stages' B tiles load before the dependency wait, A after it.
@@ -119,25 +188,37 @@ __global__ void __launch_bounds__(GT_NT, 1) gemm_bf16_tc_kernel(const __grid_con
     }
     __syncwarp();
     griddep_wait();  // (the producer's wait already covers the operands; this orders the stores)
+    if (warp >= 2 && out.rm.target) gemm_rowmax(out.rm);
 
     // epilogue: TMEM -> registers -> global
-    const bool have = mbar_wait_bounded(accum, 0, status);
+    const bool have = __syncthreads_and(mbar_wait_bounded(accum, 0, status) ? 1 : 0) != 0;
     tc::fence_after_sync();
     const int m = m0 + warp * 32 + lane;
     const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t r[32];
-        tc::tmem_ld32(trow + uint32_t(c0), r);
-        const int n = n0 + c0;
-        if (!have || m >= M || n >= N) continue;
-        if (out.mode == 0) {
+    if (out.mode == 0) {
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t r[32];
+            tc::tmem_ld32(trow + uint32_t(c0), r);
+            const int n = n0 + c0;
+            if (!have || m >= M || n >= N) continue;
             float4* dst = reinterpret_cast<float4*>(out.d32 + size_t(m) * N + n);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
                 dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                                      __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-        } else {
-            const int rq = out.mode == 1 ? m / out.P : 0, p = out.mode == 1 ? m % out.P : 0;
+        }
+    } else if (have) {
+        // bf16 pair: every thread splits its row into shared memory (the operand
+        // ring is drained: every stage was consumed by the MMAs that completed),
+        // then the tile is written row by row, consecutive lanes on consecutive
+        // 16-byte chunks of a row
+        constexpr int PITCH = L::EPI_PITCH;
+        uint8_t* sh = smem;
+        uint8_t* sl = smem + GT_BM * PITCH;
+        const int rl = warp * 32 + lane;
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t r[32];
+            tc::tmem_ld32(trow + uint32_t(c0), r);
             uint32_t hi[16], lo[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -148,15 +229,33 @@ __global__ void __launch_bounds__(GT_NT, 1) gemm_bf16_tc_kernel(const __grid_con
                 hi[j] = uint32_t(h0) | (uint32_t(h1) << 16);
                 lo[j] = uint32_t(l0) | (uint32_t(l1) << 16);
             }
-            uint4* dh = out.mode == 2 ? reinterpret_cast<uint4*>(out.hilo + size_t(m) * N + n)
-                                      : reinterpret_cast<uint4*>(out.hilo + (size_t(rq) * 32 + p) * N + n);
-            uint4* dl = out.mode == 2 ? reinterpret_cast<uint4*>(out.lo2 + size_t(m) * N + n)
-                                      : reinterpret_cast<uint4*>(out.hilo + (size_t(rq) * 32 + 16 + p) * N + n);
+            uint4* dh = reinterpret_cast<uint4*>(sh + size_t(rl) * PITCH + size_t(c0) * 2);
+            uint4* dl = reinterpret_cast<uint4*>(sl + size_t(rl) * PITCH + size_t(c0) * 2);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 dh[j] = make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
                 dl[j] = make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
             }
+        }
+        __syncthreads();
+        constexpr int CPR = BN / 8;  // 16-byte chunks per row
+        for (int i = threadIdx.x; i < GT_BM * CPR; i += GT_NT) {
+            const int rr = i / CPR, cc = i - rr * CPR, mm = m0 + rr;
+            if (mm >= M || n0 >= N) continue;
+            const uint4 vh = *reinterpret_cast<const uint4*>(sh + size_t(rr) * PITCH + cc * 16);
+            const uint4 vl = *reinterpret_cast<const uint4*>(sl + size_t(rr) * PITCH + cc * 16);
+            uint16_t* gh;
+            uint16_t* gl;
+            if (out.mode == 2) {
+                gh = out.hilo + size_t(mm) * N + n0;
+                gl = out.lo2 + size_t(mm) * N + n0;
+            } else {
+                const int rq = mm / out.P, p = mm % out.P;
+                gh = out.hilo + (size_t(rq) * 32 + p) * N + n0;
+                gl = out.hilo + (size_t(rq) * 32 + 16 + p) * N + n0;
+            }
+            reinterpret_cast<uint4*>(gh)[cc] = vh;
+            reinterpret_cast<uint4*>(gl)[cc] = vl;
         }
     }
     tc::fence_before_sync();
@@ -233,13 +332,16 @@ static int launch_gemm_bn(const void* A, const void* B, int M, int N, int K, con
 }
 
 int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int mode, float* d32, uint16_t* hilo,
-                        int P, int* status, cudaStream_t stream, uint16_t* lo2, bool pdl) {
+                        int P, int* status, cudaStream_t stream, uint16_t* lo2, bool pdl, const GemmRowmax* rm) {
     if (!gemm_tc_supported(M, N, K)) return DARTREE_EUNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) % 16) return DARTREE_EINVAL;
     if (mode == 1 && (P < 1 || P > 16 || !hilo)) return DARTREE_EINVAL;
     if (mode == 0 && !d32) return DARTREE_EINVAL;
     if (mode == 2 && (!hilo || !lo2)) return DARTREE_EINVAL;
-    GemmOut o{mode, d32, hilo, lo2, P};
+    if (rm && (!rm->target || !rm->keys || rm->rows < 1 || rm->V % 8 != 0 ||
+               reinterpret_cast<uintptr_t>(rm->target) % 16 != 0))
+        return DARTREE_EINVAL;
+    GemmOut o{mode, d32, hilo, lo2, P, rm ? *rm : GemmRowmax{nullptr, 0, 0, nullptr}};
     // Tile width: the operand bytes a CTA streams per k block (its ingest time)
     // times the number of waves of CTAs over the SMs, smallest wins.
     const int mt = (M + GT_BM - 1) / GT_BM, sms = num_sms();

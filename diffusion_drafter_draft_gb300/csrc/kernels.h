@@ -64,10 +64,20 @@ struct TopkGather {
 };
 
 // Maxima keys (ord(value) << 32 | ~index) of per-position target rows [rows, V],
-// the same dtype as the top-K rows, computed by the top-K launch itself.
+// the same dtype as the top-K rows, computed by the top-K launch itself; with
+// zero_only the launch only clears keys (a later launch takes the maxima).
 struct TopkRowmax {
     const void* target;
     unsigned long long* keys;  // [rows]
+    bool zero_only;
+};
+
+// Per-position target row maxima taken by the otherwise idle warps of the
+// candidate-side projection GEMM (bf16 rows [rows, V], keys cleared beforehand).
+struct GemmRowmax {
+    const uint16_t* target;
+    int rows, V;
+    unsigned long long* keys;
 };
 
 // S1: top-K of `rows` rows of V values. With g, *gathered tells whether the rows of
@@ -76,6 +86,21 @@ struct TopkRowmax {
 int launch_topk(const void* x, int rows, int V, int K, int dtype, int32_t* tok, float* val, int* status,
                 cudaStream_t stream, const TopkGather* g = nullptr, bool* gathered = nullptr,
                 const TopkRowmax* rm = nullptr, bool* rm_done = nullptr);
+
+// Outputs of S8-S10 (the tree arrays of dartree_tree; mask/pos and the walk are optional).
+struct FinishOut {
+    int32_t* tok;
+    int32_t* par;
+    int32_t* depth;
+    float* score;
+    int32_t* n_nodes;
+    uint8_t* mask;                      // null: no mask and position ids
+    int32_t* pos;
+    const unsigned long long* rowkeys;  // [C, L] per-position target row maxima; null: no walk
+    int32_t* accepted;
+    int32_t* path;
+    int32_t* bonus;
+};
 
 struct ExpandArgs {
     const void* E;
@@ -102,10 +127,16 @@ struct ExpandArgs {
     uint16_t* Ghi;            // [C*L*K, H] G = E[cand] W_q, bf16 high part
     uint16_t* Glo;            // [C*L*K, H] low part
     int g_rows;               // rows the Eg/G buffers hold (0: path unavailable)
-    float* zpart;             // [zpart_clusters, C*W*K] per-cluster partial logits (small-batch path)
-    int zpart_clusters;       // 0: small-batch path unavailable
-    unsigned* bar;            // grid barrier counter (small-batch path)
     int* status;
+    // Optional per-position target row maxima (bf16 rows [C*L, V]) taken inside the
+    // candidate-side path's GEMM launch (keys cleared by the top-K launch)
+    const void* rm_target;
+    unsigned long long* rm_keys;
+    // Optional S8-S10 in the same launch (candidate-side path, L*W <= 256): the
+    // path that takes it sets *fin_done; otherwise the caller runs them.
+    int B;
+    const FinishOut* fin;
+    bool* fin_done;
 };
 
 // 2-D bf16 TMA descriptor of a row-major [rows, cols] tensor, box box_cols x box_rows,
@@ -127,7 +158,8 @@ int try_launch_expand_g(const ExpandArgs& a, cudaStream_t stream, bool* launched
 // the outputs are not touched by it).
 bool gemm_tc_supported(int M, int N, int K);
 int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int mode, float* d32, uint16_t* hilo,
-                        int P, int* status, cudaStream_t stream, uint16_t* lo2 = nullptr, bool pdl = false);
+                        int P, int* status, cudaStream_t stream, uint16_t* lo2 = nullptr, bool pdl = false,
+                        const GemmRowmax* rm = nullptr);
 
 // tcgen05 contraction of one depth: z[r,p,c] from gathered candidate rows and uhl.
 bool contract_tc_supported(int P, int H);

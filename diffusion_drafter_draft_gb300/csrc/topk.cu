@@ -299,6 +299,7 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
     const int npieces = use_bulk ? int((bytes + TK_PIECE - 1) / TK_PIECE) : 0;
 
     // misc: [2] CTA min, [3] leader min, [4] leader count, [8..] scans
+    if (tkeys && !tgt && cr == 0 && threadIdx.x == 0) tkeys[row] = 0ull;  // the maxima come later
     if (threadIdx.x < 64) misc[threadIdx.x] = (threadIdx.x == 2 || threadIdx.x == 3) ? 0xffffffffu : 0u;
     if (use_bulk) {
         if (threadIdx.x == 0) {
@@ -470,12 +471,19 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
         }
         tkeys[row] = m;
     }
-    uint32_t base = 0, total = 0, anyover = 0;
-    for (uint32_t q = 0; q < S; ++q) {
-        const uint32_t tq = ld_dsmem_u32(dsmem_addr(&misc[8], q));
-        anyover |= ld_dsmem_u32(dsmem_addr(&misc[9], q));
-        base += q < cr ? tq : 0u;
-        total += tq;
+    // every CTA's candidate count and overflow flag: lane q reads CTA q's (one
+    // remote load each, all in flight together), then the warp sums them
+    uint32_t base, total, anyover;
+    {
+        const uint32_t lane = threadIdx.x & 31u;
+        uint32_t tq = 0, oq = 0;
+        if (lane < S) {
+            tq = ld_dsmem_u32(dsmem_addr(&misc[8], lane));
+            oq = ld_dsmem_u32(dsmem_addr(&misc[9], lane));
+        }
+        base = __reduce_add_sync(0xffffffffu, lane < cr ? tq : 0u);
+        total = __reduce_add_sync(0xffffffffu, tq);
+        anyover = __reduce_or_sync(0xffffffffu, oq);
     }
     // the same decision in every CTA: the totals and flags are shared
     const bool fits = total >= uint32_t(K) && total <= uint32_t(L.cap) && !anyover;
@@ -916,7 +924,8 @@ static int launch_topk_t(const void* x, int rows, int V, int K, int32_t* tok, fl
         KTimer kt_(KID_TOPK_ROWS, stream);
         e = cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const T*>(x), V, K, jsel, chunk, use_bulk, tok, val,
                                status, g ? g->E : nullptr, g ? g->H : 0, g ? g->out : nullptr,
-                               rm ? static_cast<const T*>(rm->target) : nullptr, rm ? rm->keys : nullptr);
+                               rm && !rm->zero_only ? static_cast<const T*>(rm->target) : nullptr,
+                               rm ? rm->keys : nullptr);
     }
     return e == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
@@ -974,8 +983,9 @@ int launch_topk(const void* x, int rows, int V, int K, int dtype, int32_t* tok, 
                                      : launch_topk_stream<float>(x, rows, V, K, tok, val, status, stream);
     const TopkGather* gg = gather_ok(g, K) ? g : nullptr;
     // the target rows are read with 16-byte vector loads
-    const TopkRowmax* rr = rm && rm->target && rm->keys && reinterpret_cast<uintptr_t>(rm->target) % 16 == 0 &&
-                                   (size_t(V) * elem) % 16 == 0
+    const TopkRowmax* rr = rm && rm->keys &&
+                                   (rm->zero_only || (rm->target && reinterpret_cast<uintptr_t>(rm->target) % 16 == 0 &&
+                                                      (size_t(V) * elem) % 16 == 0))
                                ? rm
                                : nullptr;
     const int e = dtype == DARTREE_BF16 ? launch_topk_t<bf16_t>(x, rows, V, K, tok, val, status, stream, gg, rr)
