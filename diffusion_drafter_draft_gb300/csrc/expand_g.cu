@@ -193,6 +193,8 @@ __device__ void xg_finish(const XgArgs& a, uint8_t* smem, const XgLayout& lay, i
     if (threadIdx.x == 0) mbar_arrive_expect_tx(mbF, uint32_t(L * 4));
     __syncthreads();
     int nv = 0;
+    // (loops over shared memory are unrolled so that their loads are in flight together)
+#pragma unroll 16
     for (int d = 0; d < L; ++d) nv += stn[d];
     const int N = min(a.B, nv);
     // ranks of the keys of depths cr, cr + CS, ...: a warp per key, lanes over all keys
@@ -202,7 +204,13 @@ __device__ void xg_finish(const XgArgs& a, uint8_t* smem, const XgLayout& lay, i
         if (k >= stn[dm1]) continue;  // uniform across the warp
         const uint64_t x = fgk[dm1 * XG_MAXW + k];
         int c = 0;
-        for (int j = lane; j < nd; j += 32) c += fgk[j] > x;
+        for (int j0 = lane; j0 < nd; j0 += 32 * 8) {  // 8 unconditional loads in flight
+            uint64_t y[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) y[u] = fgk[min(j0 + 32 * u, nd - 1)];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) c += (j0 + 32 * u < nd && y[u] > x) ? 1 : 0;
+        }
         c = __reduce_add_sync(0xffffffffu, c);
         if (lane == 0 && c < N) atomicAdd(&floc[dl], 1);
     }
@@ -521,7 +529,13 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
             uint64_t x = 0;
             if (live) {
                 x = rkeys[slot * K + i];
-                for (int j = qd; j < K; j += 4) cnt += rkeys[slot * K + j] > x;
+                // K <= 64: the 16 loads are unconditional (clamped index), so they are
+                // all in flight together
+                uint64_t y[XG_MAXK / 4];
+#pragma unroll
+                for (int jj = 0; jj < XG_MAXK / 4; ++jj) y[jj] = rkeys[slot * K + min(qd + 4 * jj, K - 1)];
+#pragma unroll
+                for (int jj = 0; jj < XG_MAXK / 4; ++jj) cnt += (qd + 4 * jj < K && y[jj] > x) ? 1 : 0;
             }
             cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
             cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);

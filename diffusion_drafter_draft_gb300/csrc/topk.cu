@@ -465,6 +465,7 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
     cluster_sync();  // CTA totals visible
     if (tgt && cr == 0 && threadIdx.x == 0) {
         uint64_t m = 0;
+#pragma unroll 16
         for (uint32_t q = 0; q < S; ++q) {
             const uint64_t x = *reinterpret_cast<const uint64_t*>(&misc[32 + 2 * q]);
             m = x > m ? x : m;
@@ -520,7 +521,13 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
         int32_t* ranked = reinterpret_cast<int32_t*>(fb);  // token of each rank < K
         if (int(threadIdx.x) < n) {
             int larger = 0;
-            for (int j = 0; j < n; ++j) larger += cand[j] > key ? 1 : 0;
+            for (int j0 = 0; j0 < n; j0 += 8) {  // 8 unconditional loads in flight
+                uint64_t y[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) y[u] = cand[min(j0 + u, n - 1)];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) larger += (j0 + u < n && y[u] > key) ? 1 : 0;
+            }
             if (larger < K) {
                 const int32_t t = int32_t(0xffffffffu - uint32_t(key));
                 if (cr == 0) {
