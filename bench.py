@@ -41,23 +41,40 @@ def _peaks():
 
 
 # --------------------------------------------------------------------------- algorithmic work (per round)
+#
+# The roofline numerator is the METHOD's work (the steps of one round as the method
+# states them): base logits read once (S1), the stand-in head's weights and the
+# candidates' embedding rows and block hidden rows (S2-S7), the projection flops of
+# S3 (2 * C * sum_d P_d * H^2) and the contraction flops of S4, the target rows the
+# walk reads (S10). W_q is counted once per round: it is the compulsory traffic of
+# the per-depth projection (33.5 MB at H = 4096 stays in the 129 MB L2 between
+# depths); the variant that re-reads it at every depth is reported beside it.
+# What the implementation adds on top (the candidate rows copied for the G GEMM,
+# the G or u bf16 pairs, the logits, the reassociated GEMM's extra flops) is
+# reported separately as intermediate bytes and extra flops.
+
+def parents(cfg):
+    P = [1]
+    for _ in range(cfg.L - 1):
+        P.append(min(cfg.W, P[-1] * cfg.K))
+    return P
+
 
 def algorithmic(cfg, accepted_mean: float) -> dict:
     """Bytes and flops the method must touch once per round (roofline numerator)."""
     eb = 2 if cfg.dtype == "bf16" else 4
-    C, L, V, H, K, W = cfg.C, cfg.L, cfg.V, cfg.H, cfg.K, cfg.W
-    P = [1]
-    for _ in range(L - 1):
-        P.append(min(W, P[-1] * K))
+    C, L, V, H, K = cfg.C, cfg.L, cfg.V, cfg.H, cfg.K
+    P = parents(cfg)
     topk_bytes = C * L * V * eb
-    expand_bytes = (H * H * eb                # W_q once (it fits in L2)
+    expand_bytes = (H * H * eb                # W_q once (compulsory)
                     + C * L * K * H * eb      # candidate embedding rows
                     + C * L * H * eb)         # block hidden rows
     rows_walked = (accepted_mean + 1) if cfg.rows == "node" else L
     verify_bytes = C * rows_walked * V * eb
     flops = 2 * C * H * H * sum(P) + 2 * C * K * H * sum(P)
     return dict(topk=topk_bytes, expand=expand_bytes, verify=verify_bytes, flops=flops,
-                total=topk_bytes + expand_bytes + verify_bytes)
+                total=topk_bytes + expand_bytes + verify_bytes,
+                total_wq_per_depth=topk_bytes + expand_bytes + (L - 1) * H * H * eb + verify_bytes)
 
 
 # --------------------------------------------------------------------------- inputs
@@ -260,48 +277,51 @@ def measure_e2e(cfg, m, steps, torch, dd):
 # DRAM bytes per launch (read + write) from one ncu capture of the current kernel on
 # this workload; the C=64 contraction and top-K were captured on fewer requests (8
 # and 20 of them) and scaled by the requests processed (their traffic is per request).
+# A kernel changed since its capture has no entry (traffic null).
 NCU_TRAFFIC = {
-    ("cfg1_qwen3_4b_c1", "expand_g_kernel"): 15546624,
-    ("cfg1_qwen3_4b_c1", "gemm_bf16_tc_kernel"): 18366464,
-    ("cfg1_qwen3_4b_c1", "topk_rows_kernel"): 20144640,
     ("cfg4_c64_stress", "contract_tc_kernel"): 35337472 * 8,   # one launch over all 64 requests
     ("cfg4_c64_stress", "topk_stream_kernel"): int((100288256 + 3384576) * 64 / 20),
 }
 
 
-def kernel_work(cfg, name, accepted_mean, g_path, fused_gather=False, fused_rowmax=False):
-    """Algorithmic work of a kernel family over ONE round: ("hbm", bytes) or ("tensor", flops).
-    fused_gather: the cluster top-K also copied the candidates' rows of E;
-    fused_rowmax: it also read the per-position target rows (their maxima)."""
+def kernel_work(cfg, name, accepted_mean, g_path, fused_gather=False):
+    """Work of a kernel family over ONE round: (bound, method work, intermediate
+    bytes, extra flops). The method work is bytes ("hbm") or flops ("tensor") of the
+    method's own steps that the family performs; the intermediates are what the
+    implementation writes and reads back in between; extra flops are the flops the
+    implementation does beyond the method's (the candidate-side G GEMM).
+    fused_gather: the cluster top-K also copied the candidates' rows of E."""
     eb = 2 if cfg.dtype == "bf16" else 4
     C, L, V, H, K, W, B = cfg.C, cfg.L, cfg.V, cfg.H, cfg.K, cfg.W, cfg.B
-    P = [1]
-    for _ in range(L - 1):
-        P.append(min(W, P[-1] * K))
-    if name in ("topk_rows_kernel", "topk_stream_kernel", "rowmax_kernel"):
-        gather = 2 * C * L * K * H * 2 if (fused_gather and name == "topk_rows_kernel") else 0
-        target = C * L * V * eb if (fused_rowmax and name == "topk_rows_kernel") else 0
-        return "hbm", C * L * V * eb + gather + target
+    P = parents(cfg)
+    proj_flops = 2 * C * sum(P) * H * H
+    logits = sum(C * p * K * 4 for p in P)
+    rows_walked = (accepted_mean + 1) if cfg.rows == "node" else L
+    if name in ("topk_rows_kernel", "topk_stream_kernel"):
+        copy = 2 * C * L * K * H * 2 if (fused_gather and name == "topk_rows_kernel") else 0
+        return "hbm", C * L * V * eb, copy, 0
     if name == "gather_rows_kernel":
-        return "hbm", 2 * C * L * K * H * eb
+        return "hbm", 0, 2 * C * L * K * H * eb, 0
+    if name == "rowmax_kernel":
+        return "hbm", C * L * V * eb, 0, 0
     if name == "gemm_bf16_tc_kernel":
-        if g_path:
-            return "tensor", 2 * (C * L * K) * H * H
-        return "tensor", sum(2 * C * p * H * H for p in P)
-    if name == "contract_tc_kernel":
-        return "hbm", L * (C * K * H * eb + C * 32 * H * 2)
-    if name == "expand_g_kernel":
-        return "hbm", 3 * C * L * K * H * 2 + C * L * H * 2
+        if g_path:  # G = E[cand] W_q for all C*L*K candidates; S3's flops are the method's part
+            g_flops = 2 * C * L * K * H * H
+            return "tensor", proj_flops, C * L * K * H * 2 + 2 * C * L * K * H * 2, g_flops - proj_flops
+        return "tensor", proj_flops, sum(2 * C * p * H * 2 for p in P), 0
+    if name == "expand_g_kernel":  # S2, S4-S7 (and S8-S10 after the last depth) over G
+        return "hbm", C * L * K * H * eb + C * L * H * eb, 2 * C * L * K * H * 2 + logits, 0
+    if name == "contract_tc_kernel":  # S4: every depth's candidate rows against the u pair
+        return "hbm", L * C * K * H * eb, L * C * 32 * H * 2 + logits, 0
     if name == "select_kernel":
-        return "hbm", sum(C * p * K * 4 for p in P)
-    if name == "state_kernel":
-        return "hbm", (L - 1) * 4 * C * W * H * eb
+        return "hbm", 0, logits, 0
+    if name == "state_kernel":  # S7: the kept children's rows of E and H_d
+        return "hbm", (L - 1) * C * (W + 1) * H * eb, (L - 1) * 2 * C * W * H * eb, 0
     if name == "walk_kernel":
-        rows_walked = (accepted_mean + 1) if cfg.rows == "node" else L
-        return "hbm", C * rows_walked * V * eb
+        return "hbm", C * rows_walked * V * eb, 0, 0
     if name == "finish_kernel":
-        return "hbm", C * (L * W * 16 + (B + 1) * (B + 1) + (B + 1) * 20)
-    return "hbm", 0
+        return "hbm", 0, C * (L * W * 16 + (B + 1) * (B + 1) + (B + 1) * 20), 0
+    return "hbm", 0, 0, 0
 
 
 # Batches of at least this many requests expand as two halves on two streams.
@@ -310,8 +330,8 @@ SPLIT_MIN_C = 32
 
 def kernel_roofline(cfg, m, hbm_peak, tf_peak):
     """Roofline of the kernel family with the largest device time per round:
-    algorithmic work of one launch (the round's work / launches per round) over the
-    average launch time. When the batch expands as two halves on two streams
+    the method's work of one launch (the round's work / launches per round) over
+    the average launch time. When the batch expands as two halves on two streams
     ("concurrent_halves": 2), a launch covers half of the requests and shares the
     GPU with its sibling, so its own rate understates the pair's."""
     kt, n = m["kernel_times"], m["n_prof"]
@@ -321,9 +341,8 @@ def kernel_roofline(cfg, m, hbm_peak, tf_peak):
     lpr = launches / n
     ms_launch = ms_total / launches
     fused = g_path and "gather_rows_kernel" not in kt
-    fused_rm = cfg.rows == "position" and "rowmax_kernel" not in kt and "topk_rows_kernel" in kt
-    bound, work_round = kernel_work(cfg, dom, m["accepted_mean"], g_path, fused, fused_rm)
-    work = work_round / lpr
+    bound, work_round, inter_round, extra_round = kernel_work(cfg, dom, m["accepted_mean"], g_path, fused)
+    work, inter, extra = work_round / lpr, inter_round / lpr, extra_round / lpr
     traffic = NCU_TRAFFIC.get((cfg.name, dom))
     split = (not g_path) and cfg.C >= SPLIT_MIN_C and dom in ("contract_tc_kernel", "gemm_bf16_tc_kernel",
                                                                "select_kernel", "state_kernel")
@@ -337,7 +356,8 @@ def kernel_roofline(cfg, m, hbm_peak, tf_peak):
         achieved = work / (ms_launch * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "traffic": traffic, "bytes_per_launch": int(work)}
-    roof.update({"kernel": dom, "ms_per_launch": round(ms_launch, 5), "launches_per_round": lpr,
+    roof.update({"intermediate_bytes_per_launch": int(inter), "extra_flops_per_launch": int(extra),
+                 "kernel": dom, "ms_per_launch": round(ms_launch, 5), "launches_per_round": lpr,
                  "share_of_kernel_time": round(ms_total / sum(v[1] for v in kt.values()), 4)})
     if split:
         roof["concurrent_halves"] = 2
@@ -364,7 +384,31 @@ def roofline(cfg, m, hbm_peak):
 
 # --------------------------------------------------------------------------- CPU oracle leg
 
-def cpu_baseline(cfg, budget_s=10.0):
+def cpu_model() -> str:
+    """The host CPU's name from /proc/cpuinfo (x86 'model name', else the Arm part
+    numbers), or the platform's machine name."""
+    import platform
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        info = []
+    for key in ("model name", "Model name"):
+        for line in info:
+            if line.startswith(key):
+                return line.split(":", 1)[1].strip()
+    parts = {}
+    for line in info:
+        if ":" in line:
+            k, v = (x.strip() for x in line.split(":", 1))
+            if k in ("CPU implementer", "CPU part") and k not in parts:
+                parts[k] = v
+    if parts:
+        return f"{platform.machine()} implementer {parts.get('CPU implementer', '?')} part {parts.get('CPU part', '?')}"
+    return platform.machine()
+
+
+def _oracle_rate(cfg, budget_s):
+    """(rounds, seconds) of full oracle rounds (build + verify) within budget_s."""
     import oracle
     inp = make_inputs(cfg)
     t0 = time.time()
@@ -376,10 +420,34 @@ def cpu_baseline(cfg, budget_s=10.0):
         n += 1
         if time.time() - t0 > budget_s:
             break
-    dt = time.time() - t0
-    return {"value": round(n / dt, 4), "unit": "rounds/s", "cores": len(os.sched_getaffinity(0)),
-            "kind": "oracle",
-            "sample": f"{n} full oracle round(s) of {cfg.name} (build+verify, float64 numpy), {dt:.1f} s"}
+    return n, time.time() - t0
+
+
+def _oracle_rate_one_thread(cfg_name, budget_s):
+    """The same in a child process whose BLAS and OpenMP pools have one thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1")
+    code = ("import sys, json; sys.path.insert(0, %r); import bench; from dartree_inputs import make_config; "
+            "n, dt = bench._oracle_rate(make_config(%r), %r); print(json.dumps([n, dt]))" % (ROOT, cfg_name, budget_s))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=budget_s * 10 + 120)
+        n, dt = json.loads(r.stdout.strip().splitlines()[-1])
+        return n, dt
+    except Exception:
+        return None
+
+
+def cpu_baseline(cfg, budget_s=10.0, one_thread_s=5.0):
+    n, dt = _oracle_rate(cfg, budget_s)
+    out = {"value": round(n / dt, 4), "unit": "rounds/s", "cores": len(os.sched_getaffinity(0)),
+           "kind": "oracle", "cpu": cpu_model(),
+           "sample": f"{n} full oracle round(s) of {cfg.name} (build+verify, float64 numpy), {dt:.1f} s"}
+    one = _oracle_rate_one_thread(cfg.name, one_thread_s)
+    if one:
+        out["value_one_thread"] = round(one[0] / one[1], 4)
+        out["sample_one_thread"] = f"{one[0]} round(s) in {one[1]:.1f} s with one BLAS/OpenMP thread"
+    return out
 
 
 def cpu_baseline_stress(cfg, budget_requests=1):
@@ -393,6 +461,13 @@ def cpu_baseline_stress(cfg, budget_requests=1):
     return {"value": round(1.0 / per_round, 6), "unit": "rounds/s", "cores": len(os.sched_getaffinity(0)),
             "kind": "oracle",
             "sample": f"oracle build of {budget_requests} of {cfg.C} requests ({dt:.1f} s), scaled to the batch"}
+
+
+def workload_config(cfg, graphs: bool, world: int) -> dict:
+    """The `config` object of the JSON line, the same for both arms."""
+    return {"workload": cfg.name, "C": cfg.C, "L": cfg.L, "V": cfg.V, "H": cfg.H, "K": cfg.K, "W": cfg.W,
+            "B": cfg.B, "beta": cfg.beta, "l2": "flushed between timed steps (2x L2 write)",
+            "cuda_graph": graphs, "parallelism": "replicas" if world > 1 else "single"}
 
 
 # --------------------------------------------------------------------------- profiling mode
@@ -466,10 +541,10 @@ def main():
             "unit": "rounds/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg.name, "C": cfg.C, "L": cfg.L, "V": cfg.V, "H": cfg.H, "K": cfg.K,
-                       "W": cfg.W, "B": cfg.B, "beta": cfg.beta},
+            "config": workload_config(cfg, not args.no_graph, world),
             "cpu_baseline": {"value": round(v, 4), "unit": "rounds/s", "cores": len(os.sched_getaffinity(0)),
-                             "kind": "oracle", "sample": f"{args.steps} full rounds of {cfg.name}"},
+                             "kind": "oracle", "cpu": cpu_model(),
+                             "sample": f"{args.steps} full rounds of {cfg.name}"},
             "e2e": {"value": round(v, 4), "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": round(time.time() - t0, 1)}))
         return
@@ -507,10 +582,10 @@ def main():
         "us_per_round_p90": round(float(np.percentile(m["t_round"], 90)) * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
         "data": "synthetic",
-        "config": {"workload": cfg.name, "C": cfg.C, "L": cfg.L, "V": cfg.V, "H": cfg.H, "K": cfg.K, "W": cfg.W,
-                   "B": cfg.B, "beta": cfg.beta, "l2": "flushed between timed steps (2x L2 write)",
-                   "cuda_graph": not args.no_graph, "parallelism": "replicas" if world > 1 else "single"},
+        "config": workload_config(cfg, not args.no_graph, world),
         "roofline": dict(roof, peak_kind=peak_kind),
+        "round_hbm_frac": round(alg["total"] / (float(np.median(m["t_round"])) * 1e-3) / 1e9 / hbm_peak, 4),
+        "round_tensor_frac": round(alg["flops"] / (float(np.median(m["t_round"])) * 1e-3) / 1e12 / tf_peak, 4),
         "breakdown_ms": {k: round(v[1], 4) for k, v in parts.items()},
         "kernels": per_kernel,
         "accepted_mean": m["accepted_mean"],
@@ -531,6 +606,8 @@ def main():
                        "request_rounds_per_s": round(scfg.C * 1e3 / sms, 1), "us_per_round_p50": round(sms * 1e3, 1),
                        "roofline": dict(sroof, peak_kind=peak_kind),
                        "round_hbm_frac": round(salg["total"] / (sms * 1e-3) / 1e9 / hbm_peak, 4),
+                       "round_hbm_frac_wq_per_depth": round(salg["total_wq_per_depth"] / (sms * 1e-3) / 1e9
+                                                            / hbm_peak, 4),
                        "round_tensor_frac": round(salg["flops"] / (sms * 1e-3) / 1e12 / tf_peak, 4),
                        "breakdown_ms": {k: round(v[1], 4) for k, v in sparts.items()},
                        "kernels": sper_kernel,
