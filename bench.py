@@ -274,6 +274,20 @@ def measure_e2e(cfg, m, steps, torch, dd):
     return ms, h2d, d2h
 
 
+def measure_heap(cfg, m, steps, warmup, torch, dd, graphs=True):
+    """The node-by-node heap -> correction baseline (one head evaluation per popped
+    node, the same S1 and G projection) on the same inputs: us per build, and the
+    ratio to the deferred round's p50 (build + verify)."""
+    x = m["x"]
+    h = dd.HeapRound(x["E"], x["Wq"], cfg.C, cfg.L, cfg.K, cfg.B, cfg.beta)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    t = time_steps(torch, graphed(torch, lambda: h.run(x["base"], x["hidden"], x["anchor"]), graphs), steps, warmup,
+                   flush)
+    us = float(np.median(t)) * 1e3
+    return {"heap_baseline_us": round(us, 2), "deferred_round_us": round(float(np.median(m["t_round"])) * 1e3, 2),
+            "heap_over_deferred": round(us / (float(np.median(m["t_round"])) * 1e3), 3)}
+
+
 # DRAM bytes per launch (read + write) from one ncu capture of the current kernel on
 # this workload; the C=64 contraction and top-K were captured on fewer requests (8
 # and 20 of them) and scaled by the requests processed (their traffic is per request).
@@ -575,6 +589,7 @@ def main():
     dom, _, alg, parts = roofline(cfg, m, hbm_peak)
     roof, per_kernel, lpr = kernel_roofline(cfg, m, hbm_peak, tf_peak)
     e2e_ms, h2d, d2h = measure_e2e(cfg, m, min(args.steps, 20), torch, dd)
+    heap = measure_heap(cfg, m, args.steps, max(3, args.warmup), torch, dd, graphs=not args.no_graph)
     line = {
         "metric": "draft-tree rounds/sec (build+verify)", "value": round(value, 3), "unit": "rounds/s",
         "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5),
@@ -593,6 +608,7 @@ def main():
         "e2e": {"value": round(1e3 / e2e_ms, 3), "unit": "rounds/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "clocks": m["clocks"],
+        "heap_baseline": heap,
     }
     del m
     torch.cuda.empty_cache()

@@ -15,7 +15,7 @@ import torch
 __all__ = [
     "DartreeError", "lib", "library_path", "F32", "BF16", "ROWS_PER_POSITION", "ROWS_PER_NODE",
     "workspace_bytes", "new_workspace", "topk", "expand", "prune", "tree_mask", "build_tree",
-    "verify", "read_status", "clear_status", "Round", "EXPORTS",
+    "verify", "read_status", "clear_status", "Round", "EXPORTS", "heap_build", "HeapRound",
 ]
 
 F32, BF16 = 0, 1
@@ -26,7 +26,7 @@ EXPORTS = ("dartree_head_init", "dartree_workspace_bytes", "dartree_topk", "dart
            "dartree_tree_mask", "dartree_build_tree", "dartree_verify", "dartree_read_status",
            "dartree_clear_status", "dartree_status_string", "dartree_verify_static", "dartree_gemm_bf16",
            "dartree_head_prepare", "dartree_round", "dartree_selftest_wait", "dartree_timing",
-           "dartree_timing_read", "dartree_kernel_name")
+           "dartree_timing_read", "dartree_kernel_name", "dartree_heap_workspace_bytes", "dartree_heap_build")
 
 
 class DartreeError(RuntimeError):
@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
         "dartree_timing_read": (i, [i, P(ctypes.c_int), P(ctypes.c_double)]),
         "dartree_kernel_name": (ctypes.c_char_p, [i]),
         "dartree_head_prepare": (i, [P(Head), vp, vp]),
+        "dartree_heap_workspace_bytes": (sz, [P(Params), i, i, i]),
+        "dartree_heap_build": (i, [P(Head), P(Params), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "dartree_workspace_bytes": (sz, [P(Params), i, i, i]),
         "dartree_topk": (i, [vp, i, i, i, i, vp, vp, vp, sz, vp]),
         "dartree_expand": (i, [P(Head), P(Params), vp, vp, P(Candidates), P(Supertree), vp, sz, vp]),
@@ -446,3 +448,43 @@ class Round:
               ctypes.c_void_p(self.out["path"].data_ptr()), ctypes.c_void_p(self.out["bonus"].data_ptr()),
               ctypes.c_void_p(self.ws.data_ptr()), self.ws.numel(), s)
         return self.out
+
+
+class HeapRound:
+    """Node-by-node best-first drafting (one head evaluation per popped node), the
+    baseline the deferred search replaces; every buffer allocated once, run()
+    allocates nothing (it can be timed or captured in a CUDA graph)."""
+
+    def __init__(self, E, Wq, C, L, K, B, beta, device=None):
+        self.V, self.H = E.shape
+        self.C, self.L, self.K, self.B, self.beta = C, L, K, B, beta
+        dev = device or E.device
+        self.head, self.wqt = _head(E, Wq, prepare=True)
+        self.p = _params(C, L, K, 1, B, beta)
+        n = lib().dartree_heap_workspace_bytes(ctypes.byref(self.p), int(self.V), int(self.H), int(self.head.dtype))
+        if n == 0:
+            raise DartreeError(EUNSUPPORTED, "dartree_heap_workspace_bytes")
+        self.ws = new_workspace(n, dev)
+        self.out = dict(tok=torch.empty((C, B), dtype=torch.int32, device=dev),
+                        parent=torch.empty((C, B), dtype=torch.int32, device=dev),
+                        depth=torch.empty((C, B), dtype=torch.int32, device=dev),
+                        score=torch.empty((C, B), dtype=torch.float32, device=dev))
+
+    def run(self, base, hidden, anchor, stream=None):
+        o = self.out
+        _call("dartree_heap_build", ctypes.byref(self.head), ctypes.byref(self.p), ctypes.c_void_p(base.data_ptr()),
+              ctypes.c_void_p(hidden.data_ptr()), ctypes.c_void_p(anchor.data_ptr()),
+              ctypes.c_void_p(o["tok"].data_ptr()), ctypes.c_void_p(o["parent"].data_ptr()),
+              ctypes.c_void_p(o["depth"].data_ptr()), ctypes.c_void_p(o["score"].data_ptr()),
+              ctypes.c_void_p(self.ws.data_ptr()), self.ws.numel(), _stream(stream))
+        return o
+
+
+def heap_build(E, Wq, base, hidden, anchor, K, B, beta, stream=None):
+    """dartree_heap_build on fresh buffers -> dict(tok, parent, depth, score) [C, B] in pop order."""
+    C, L, _ = base.shape
+    h = HeapRound(E, Wq, C, L, K, B, beta, device=base.device)
+    out = h.run(base, hidden, anchor, stream)
+    _keep(stream, h.ws, h.wqt)
+    out["_keep"] = (h.ws, h.wqt)
+    return out

@@ -98,9 +98,80 @@ int finish_tree(const dartree_params* p, const dartree_supertree* sp, const int3
     return DARTREE_OK;
 }
 
+// Workspace of the node-by-node heap search: status, candidate table, gathered
+// candidate rows and the G pair, and the popped nodes' states.
+struct HeapLayout {
+    size_t status, cand_tok, cand_val, Eg, Ghi, Glo, hws, total;
+};
+HeapLayout heap_layout(const dartree_params& p, int H) {
+    const size_t C = size_t(p.C), L = size_t(p.L), K = size_t(p.K), B = size_t(p.B), g = C * L * K;
+    HeapLayout l{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o += up(bytes); return at; };
+    l.status = take(4);
+    l.cand_tok = take(g * 4);
+    l.cand_val = take(g * 4);
+    l.Eg = take(g * size_t(H) * 2);
+    l.Ghi = take(g * size_t(H) * 2);
+    l.Glo = take(g * size_t(H) * 2);
+    l.hws = take(C * B * size_t(H) * 2);
+    l.total = o;
+    return l;
+}
+
+int check_heap(const dartree_head* head, const dartree_params* p) {
+    if (!head || !p) return DARTREE_EINVAL;
+    if (head->dtype != DARTREE_BF16) return DARTREE_EUNSUPPORTED;
+    if (p->C < 0 || p->L < 1 || p->K < 1 || p->B < 1 || p->K > head->V) return DARTREE_EINVAL;
+    if (!(p->beta <= 0.0f)) return DARTREE_EINVAL;
+    // (the G GEMM's shape rule: N = H a multiple of 128; the row gather: H <= 6144)
+    if (p->L > DARTREE_MAX_L || !heap_supported(head->H, p->K, p->B) || head->H % 128 != 0 || head->H / 8 > 768)
+        return DARTREE_EUNSUPPORTED;
+    return DARTREE_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t dartree_heap_workspace_bytes(const dartree_params* p, int V, int H, int dtype) {
+    dartree_head h{};
+    h.V = V;
+    h.H = H;
+    h.dtype = dtype;
+    if (H < 8 || H % 8 != 0 || check_heap(&h, p) != DARTREE_OK) return 0;
+    return heap_layout(*p, H).total;
+}
+
+int dartree_heap_build(const dartree_head* head, const dartree_params* p, const void* base_logits,
+                       const void* block_hidden, const int32_t* anchor, int32_t* tok, int32_t* parent, int32_t* depth,
+                       float* score, void* ws, size_t ws_bytes, void* stream) {
+    if (int e = check_heap(head, p)) return e;
+    if (p->C == 0) return DARTREE_OK;
+    if (!head->E || !head->WqT || !base_logits || !block_hidden || !anchor || !tok || !parent || !depth || !score)
+        return DARTREE_EINVAL;
+    const HeapLayout l = heap_layout(*p, head->H);
+    if (int e = check_ws(ws, ws_bytes, l.total)) return e;
+    cudaStream_t s = as_stream(stream);
+    int* status = at<int>(ws, l.status);
+    int32_t* ct = at<int32_t>(ws, l.cand_tok);
+    float* cv = at<float>(ws, l.cand_val);
+    uint16_t* Eg = at<uint16_t>(ws, l.Eg);
+    const int M = p->C * p->L * p->K;
+    // S1 (the same launch copies the candidates' rows when it can), then G = E[cand] W_q
+    const TopkGather g{static_cast<const uint16_t*>(head->E), head->H, Eg};
+    bool gathered = false;
+    if (int e = launch_topk(base_logits, p->C * p->L, head->V, p->K, head->dtype, ct, cv, status, s, &g, &gathered))
+        return e;
+    if (!gathered)
+        if (int e = launch_gather_rows(static_cast<const uint16_t*>(head->E), ct, head->H, M, Eg, s)) return e;
+    if (int e = launch_gemm_bf16_tc(Eg, head->WqT, M, head->H, head->H, 2, nullptr, at<uint16_t>(ws, l.Ghi), 1,
+                                    status, s, at<uint16_t>(ws, l.Glo), true))
+        return e;
+    return launch_heap_search(head->E, block_hidden, anchor, ct, cv, at<uint16_t>(ws, l.Ghi), at<uint16_t>(ws, l.Glo),
+                              p->C, head->H, p->L, p->K, p->B, p->beta, at<uint16_t>(ws, l.hws), tok, parent, depth,
+                              score, status, s);
+}
 
 const char* dartree_status_string(int s) {
     switch (s) {

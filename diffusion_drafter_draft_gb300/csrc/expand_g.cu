@@ -721,6 +721,16 @@ __global__ void transpose_bf16_kernel(const uint16_t* __restrict__ src, uint16_t
     }
 }
 
+int launch_gather_rows(const uint16_t* E, const int32_t* idx, int H, int M, uint16_t* out, cudaStream_t stream) {
+    if (M == 0) return DARTREE_OK;
+    if (H % 8 != 0 || H / 8 > GR_MAXV * GR_NT) return DARTREE_EUNSUPPORTED;
+    {
+        KTimer kt_(KID_GATHER, stream);
+        gather_rows_kernel<<<(M + GR_ROWS - 1) / GR_ROWS, GR_NT, 0, stream>>>(E, idx, H, M, out);
+    }
+    return cudaGetLastError() == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
+}
+
 int launch_transpose_bf16(const void* src, void* dst, int H, cudaStream_t stream) {
     dim3 grid((H + 31) / 32, (H + 31) / 32), block(32, 8);
     {

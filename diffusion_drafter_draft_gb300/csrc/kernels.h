@@ -143,6 +143,17 @@ struct ExpandArgs {
 // swizzle 0 (none), 32, 64 or 128 bytes. False when the driver refuses it.
 bool make_tensor_map_bf16(CUtensorMap* map, const void* base, int rows, int cols, int box_cols, int box_rows,
                           int swizzle_bytes);
+// out[m] = E[idx[m]] for m < M (rows of H bf16, H / 8 <= 768).
+int launch_gather_rows(const uint16_t* E, const int32_t* idx, int H, int M, uint16_t* out, cudaStream_t stream);
+
+// Node-by-node best-first search (one head evaluation per popped node) over the
+// candidates of S1 and the candidate-side G pair; outputs [C, B] in pop order.
+bool heap_supported(int H, int K, int B);
+int launch_heap_search(const void* E, const void* hidden, const int32_t* anchor, const int32_t* cand_tok,
+                       const float* cand_val, const uint16_t* Ghi, const uint16_t* Glo, int C, int H, int L, int K,
+                       int B, float beta, uint16_t* hws, int32_t* tok, int32_t* par, int32_t* depth, float* score,
+                       int* status, cudaStream_t stream);
+
 // Transpose of an H x H bf16 matrix (head preparation).
 int launch_transpose_bf16(const void* src, void* dst, int H, cudaStream_t stream);
 

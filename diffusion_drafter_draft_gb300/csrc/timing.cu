@@ -44,7 +44,7 @@ void release_all() {
 const char* const kNames[KID_COUNT] = {
     "topk_rows_kernel",  "topk_stream_kernel", "gemm_bf16_tc_kernel", "contract_tc_kernel",
     "expand_g_kernel",   "gather_rows_kernel", "select_kernel",       "state_kernel",
-    "heap_expand_kernel",  "finish_kernel",    "prune_kernel",        "mask_kernel",
+    "heap_search_kernel",  "finish_kernel",    "prune_kernel",        "mask_kernel",
     "rowmax_kernel",     "walk_kernel",        "other"};
 }  // namespace
 

@@ -228,6 +228,28 @@ DARTREE_API int dartree_round(const dartree_head* head, const dartree_params* p,
                               dartree_tree* tree, int32_t* accepted_len, int32_t* path, int32_t* bonus,
                               void* ws, size_t ws_bytes, void* stream);
 
+/* Baseline of the deferred search: node-by-node best-first drafting with one
+ * correction-head evaluation per popped node ("heap pop -> correction"; DARTree
+ * blog post, section 2, latency breakdown, and section 4.3, Table 2). After S1 and
+ * the candidate-side projection (the same launches as dartree_build_tree), one CTA
+ * per request pops B nodes one at a time from all children pushed so far, largest
+ * score first (ties: shallower depth, then earlier push; a node's K children are
+ * pushed in candidate order when it is popped), computes the popped node's state
+ * and, below depth L, its K children's scores with the stand-in head. The root is
+ * expanded first and is not counted. With W >= B the deferred tree holds the same
+ * nodes (its per-depth top-W never drops a node the heap pops).
+ *   p            C, L, K (<= 64), B (<= 256) and beta; W is not used
+ *   head         bf16, prepared with dartree_head_prepare (W_q^T), H a multiple of
+ *                128 and at most 6144
+ *   tok, parent, depth, score  [C, B] in pop order: token, pop index of the parent
+ *                (-1 = the root), depth (1..L), score s_beta
+ *   ws           dartree_heap_workspace_bytes() bytes, 256-byte aligned
+ * Returns DARTREE_EUNSUPPORTED outside these limits (nothing enqueued). */
+DARTREE_API size_t dartree_heap_workspace_bytes(const dartree_params* p, int V, int H, int dtype);
+DARTREE_API int dartree_heap_build(const dartree_head* head, const dartree_params* p, const void* base_logits,
+                                   const void* block_hidden, const int32_t* anchor, int32_t* tok, int32_t* parent,
+                                   int32_t* depth, float* score, void* ws, size_t ws_bytes, void* stream);
+
 /* S10 without a workspace, for callers that cannot allocate device memory where
  * they verify (for example a serving loop whose caching allocator holds all free
  * HBM, or a plugin behind a plain C interface with no allocator handle). The

@@ -73,3 +73,22 @@ def test_argument_errors_are_reported_on_the_host(L):
                            fake, fake, ws_ok, need, None) == dd.EDTYPE
     assert L.dartree_round(ctypes.byref(h), ctypes.byref(p), fake, fake, fake, fake, 0, ctypes.byref(tree), fake,
                            fake, fake, ws_ok, need - 256, None) == dd.EWORKSPACE
+
+
+def test_heap_search_limits_are_checked_on_the_host(L):
+    import diffusion_drafter_draft_gb300 as dd
+    P = dd.Params
+    ok = P(2, 4, 16, 1, 12, -0.1)
+    assert L.dartree_heap_workspace_bytes(ctypes.byref(ok), 3001, 256, dd.BF16) > 0
+    assert L.dartree_heap_workspace_bytes(ctypes.byref(ok), 3001, 256, dd.F32) == 0                 # bf16 only
+    assert L.dartree_heap_workspace_bytes(ctypes.byref(P(2, 4, 65, 1, 12, -0.1)), 3001, 256, dd.BF16) == 0  # K
+    assert L.dartree_heap_workspace_bytes(ctypes.byref(P(2, 4, 16, 1, 257, -0.1)), 3001, 256, dd.BF16) == 0  # B
+    assert L.dartree_heap_workspace_bytes(ctypes.byref(P(2, 4, 16, 1, 12, 0.5)), 3001, 256, dd.BF16) == 0  # beta
+    assert L.dartree_heap_workspace_bytes(ctypes.byref(ok), 3001, 200, dd.BF16) == 0                  # H % 128
+    fake = ctypes.c_void_p(256)
+    head = dd.Head(256, 256, 3001, 256, dd.F32, None)
+    assert L.dartree_heap_build(ctypes.byref(head), ctypes.byref(ok), fake, fake, fake, fake, fake, fake, fake,
+                                fake, 1 << 20, None) == dd.EUNSUPPORTED
+    head = dd.Head(256, 256, 3001, 256, dd.BF16, None)   # not prepared (no W_q^T)
+    assert L.dartree_heap_build(ctypes.byref(head), ctypes.byref(ok), fake, fake, fake, fake, fake, fake, fake,
+                                fake, 1 << 20, None) == dd.EINVAL
