@@ -293,6 +293,9 @@ def measure_heap(cfg, m, steps, warmup, torch, dd, graphs=True):
 # and 20 of them) and scaled by the requests processed (their traffic is per request).
 # A kernel changed since its capture has no entry (traffic null).
 NCU_TRAFFIC = {
+    ("cfg1_qwen3_4b_c1", "expand_g_kernel"): 15566336,      # one launch = one round, full size
+    ("cfg1_qwen3_4b_c1", "gemm_bf16_tc_kernel"): 23248384,
+    ("cfg1_qwen3_4b_c1", "topk_rows_kernel"): 15284736,
     ("cfg4_c64_stress", "contract_tc_kernel"): 35337472 * 8,   # one launch over all 64 requests
     ("cfg4_c64_stress", "topk_stream_kernel"): int((100288256 + 3384576) * 64 / 20),
 }
@@ -502,6 +505,9 @@ def profile_only(args):
         ws = dd.new_workspace(256)
         base2 = x["base"].view(cfg.C * cfg.L, V)
         fn = lambda: dd.topk(base2, cfg.K, ws=ws)  # noqa: E731
+    elif args.only == "heap":
+        h = dd.HeapRound(x["E"], x["Wq"], cfg.C, cfg.L, cfg.K, cfg.B, cfg.beta)
+        fn = lambda: h.run(x["base"], x["hidden"], x["anchor"])  # noqa: E731
     else:
         rnd = dd.Round(x["E"], x["Wq"], cfg.C, cfg.L, cfg.K, cfg.W, cfg.B, cfg.beta, rows)
         fn = lambda: rnd.run(x["base"], x["hidden"], x["anchor"], x["target"])  # noqa: E731
@@ -520,7 +526,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-stress", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
-    ap.add_argument("--only", choices=["topk", "round"], default=None,
+    ap.add_argument("--only", choices=["topk", "round", "heap"], default=None,
                     help="profiling mode: run just one entry point on --config and print its timing")
     ap.add_argument("--config", default=None, help="workload name for --only (default: the main workload)")
     ap.add_argument("--C", type=int, default=None, help="--only: override the number of requests (a smaller case)")
