@@ -8,3 +8,4 @@ from .dartree import (  # noqa: F401
     logsumexp, mask_pos, prune_into, rmsnorm, round_bf16, round_state, topk_candidates,
     tree_paths, verify,
 )
+from . import sampling  # noqa: F401,E402  (temperature-T verification, adaptive budget)
