@@ -288,6 +288,27 @@ def measure_heap(cfg, m, steps, warmup, torch, dd, graphs=True):
             "heap_over_deferred": round(us / (float(np.median(m["t_round"])) * 1e3), 3)}
 
 
+def measure_sample(cfg, m, steps, warmup, torch, dd, hbm_peak, graphs=True, temperature=1.0, seed=2026):
+    """Verification at temperature T (dartree_verify_sample) on the round's tree and
+    target rows, beside greedy verification on the same inputs: us per call and the
+    target bytes the draw reads (per-position rows: all C*L rows; per-node rows: the
+    rows on the walked paths)."""
+    x, rnd, rows = m["x"], m["rnd"], m["rows"]
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    fn = lambda: dd.verify_sample(rnd.tree, x["target"], rows, cfg.L, temperature, seed, ws=rnd.ws)  # noqa: E731
+    out = fn()
+    torch.cuda.synchronize()
+    walked = float(out["accepted_len"].float().mean().item()) + 1.0
+    t = time_steps(torch, graphed(torch, fn, graphs), steps, warmup, flush)
+    us = float(np.median(t)) * 1e3
+    eb = 2 if cfg.dtype == "bf16" else 4
+    nbytes = cfg.C * (cfg.L if cfg.rows == "position" else walked) * cfg.V * eb
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us": round(us, 2), "greedy_verify_us": round(float(np.median(m["t_verify"])) * 1e3, 2),
+            "temperature": temperature, "rows": cfg.rows, "accepted_mean": round(walked - 1.0, 3),
+            "target_bytes": int(nbytes), "achieved_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4)}
+
+
 # DRAM bytes per launch (read + write) from one ncu capture of the current kernel on
 # this workload; the C=64 contraction and top-K were captured on fewer requests (8
 # and 20 of them) and scaled by the requests processed (their traffic is per request).
@@ -596,6 +617,7 @@ def main():
     roof, per_kernel, lpr = kernel_roofline(cfg, m, hbm_peak, tf_peak)
     e2e_ms, h2d, d2h = measure_e2e(cfg, m, min(args.steps, 20), torch, dd)
     heap = measure_heap(cfg, m, args.steps, max(3, args.warmup), torch, dd, graphs=not args.no_graph)
+    sample = measure_sample(cfg, m, args.steps, max(3, args.warmup), torch, dd, hbm_peak, graphs=not args.no_graph)
     line = {
         "metric": "draft-tree rounds/sec (build+verify)", "value": round(value, 3), "unit": "rounds/s",
         "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5),
@@ -615,6 +637,7 @@ def main():
                 "d2h_bytes_per_step": int(d2h)},
         "clocks": m["clocks"],
         "heap_baseline": heap,
+        "verify_sample": sample,
     }
     del m
     torch.cuda.empty_cache()
@@ -633,7 +656,9 @@ def main():
                        "round_tensor_frac": round(salg["flops"] / (sms * 1e-3) / 1e12 / tf_peak, 4),
                        "breakdown_ms": {k: round(v[1], 4) for k, v in sparts.items()},
                        "kernels": sper_kernel,
-                       "accepted_mean": sm["accepted_mean"], "clocks": sm["clocks"]}
+                       "accepted_mean": sm["accepted_mean"], "clocks": sm["clocks"],
+                       "verify_sample": measure_sample(scfg, sm, max(5, min(args.steps, 20)), 3, torch, dd,
+                                                       hbm_peak, graphs=not args.no_graph)}
         del sm
         torch.cuda.empty_cache()
     if rank == 0:

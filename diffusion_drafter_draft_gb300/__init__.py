@@ -16,6 +16,7 @@ __all__ = [
     "DartreeError", "lib", "library_path", "F32", "BF16", "ROWS_PER_POSITION", "ROWS_PER_NODE",
     "workspace_bytes", "new_workspace", "topk", "expand", "prune", "tree_mask", "build_tree",
     "verify", "read_status", "clear_status", "Round", "EXPORTS", "heap_build", "HeapRound",
+    "verify_sample", "adaptive_budget",
 ]
 
 F32, BF16 = 0, 1
@@ -26,7 +27,8 @@ EXPORTS = ("dartree_head_init", "dartree_workspace_bytes", "dartree_topk", "dart
            "dartree_tree_mask", "dartree_build_tree", "dartree_verify", "dartree_read_status",
            "dartree_clear_status", "dartree_status_string", "dartree_verify_static", "dartree_gemm_bf16",
            "dartree_head_prepare", "dartree_round", "dartree_selftest_wait", "dartree_timing",
-           "dartree_timing_read", "dartree_kernel_name", "dartree_heap_workspace_bytes", "dartree_heap_build")
+           "dartree_timing_read", "dartree_kernel_name", "dartree_heap_workspace_bytes", "dartree_heap_build",
+           "dartree_verify_sample", "dartree_adaptive_budget")
 
 
 class DartreeError(RuntimeError):
@@ -97,6 +99,9 @@ def lib() -> ctypes.CDLL:
                                    vp]),
         "dartree_verify": (i, [P(Params), P(Tree), vp, i, i, i, vp, vp, vp, vp, sz, vp]),
         "dartree_verify_static": (i, [P(Params), P(Tree), vp, i, i, i, vp, vp, vp, vp]),
+        "dartree_verify_sample": (i, [P(Params), P(Tree), vp, i, i, i, ctypes.c_float, ctypes.c_uint64, vp, vp, vp,
+                                      vp, sz, vp]),
+        "dartree_adaptive_budget": (i, [i, P(ctypes.c_int), P(ctypes.c_int)]),
         "dartree_gemm_bf16": (i, [vp, vp, vp, i, i, i, vp, vp]),
         "dartree_read_status": (i, [vp, P(ctypes.c_int32), vp]),
         "dartree_clear_status": (i, [vp, vp]),
@@ -345,6 +350,34 @@ def verify(tree, target, rows: int, L: int, ws=None, stream=None):
           _dtype_code(target), ctypes.c_void_p(out["accepted_len"].data_ptr()), ctypes.c_void_p(out["path"].data_ptr()),
           ctypes.c_void_p(out["bonus"].data_ptr()), ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
     return out
+
+
+def verify_sample(tree, target, rows: int, L: int, temperature: float, seed: int, ws=None, stream=None):
+    """S10 at temperature T > 0 (Gumbel-max draws, Philox4x32-10 noise keyed by seed)
+    -> dict(accepted_len, path, bonus)."""
+    C, S = tree["tok"].shape
+    V = target.shape[-1]
+    _need(target, "target", None, (C, L, V) if rows == ROWS_PER_POSITION else (C, S, V))
+    dev = target.device
+    out = dict(accepted_len=torch.empty((C,), dtype=torch.int32, device=dev),
+               path=torch.empty((C, L), dtype=torch.int32, device=dev),
+               bonus=torch.empty((C,), dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = new_workspace(256 + 8 * C * max(L, S), dev)
+    p = _params(C, L, 1, 1, S - 1, 0.0)
+    ts = _tree_struct(tree)
+    _call("dartree_verify_sample", ctypes.byref(p), ctypes.byref(ts), ctypes.c_void_p(target.data_ptr()), int(rows),
+          int(V), _dtype_code(target), float(temperature), int(seed) & 0xFFFFFFFFFFFFFFFF,
+          ctypes.c_void_p(out["accepted_len"].data_ptr()), ctypes.c_void_p(out["path"].data_ptr()),
+          ctypes.c_void_p(out["bonus"].data_ptr()), ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
+    return out
+
+
+def adaptive_budget(C: int) -> tuple[int, int]:
+    """(B, W) for C concurrent requests (dartree_adaptive_budget)."""
+    B, W = ctypes.c_int(), ctypes.c_int()
+    _call("dartree_adaptive_budget", int(C), ctypes.byref(B), ctypes.byref(W))
+    return B.value, W.value
 
 
 def verify_static(tree, target, rows: int, L: int, stream=None):

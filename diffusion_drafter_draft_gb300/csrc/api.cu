@@ -1,6 +1,7 @@
 // C ABI of the DARTree draft-tree build and verify step: argument checks,
 // workspace carving and kernel launches on the caller's stream.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -484,6 +485,33 @@ int dartree_verify(const dartree_params* p, const dartree_tree* tree, const void
     return launch_verify(p->C, p->L, p->B, tree->tok, tree->par, tree->depth, tree->n_nodes, target, rows, V, dtype,
                          at<unsigned long long>(ws, keys_off), accepted_len, path, bonus, at<int>(ws, 0),
                          as_stream(stream));
+}
+
+int dartree_verify_sample(const dartree_params* p, const dartree_tree* tree, const void* target, int rows, int V,
+                          int dtype, float temperature, uint64_t seed, int32_t* accepted_len, int32_t* path,
+                          int32_t* bonus, void* ws, size_t ws_bytes, void* stream) {
+    if (!p || p->C < 0 || p->L < 1 || p->B < 1 || V < 1) return DARTREE_EINVAL;
+    if (!(temperature > 0.0f) || !isfinite(temperature)) return DARTREE_EINVAL;
+    if (!dtype_ok(dtype) || (rows != DARTREE_ROWS_PER_POSITION && rows != DARTREE_ROWS_PER_NODE))
+        return DARTREE_EDTYPE;
+    if (p->L > DARTREE_MAX_L || p->B + 1 > DARTREE_MAX_SLOTS) return DARTREE_EUNSUPPORTED;
+    if (p->C == 0) return DARTREE_OK;
+    if (!tree || !tree->tok || !tree->par || !tree->depth || !tree->n_nodes || !target || !accepted_len || !path ||
+        !bonus)
+        return DARTREE_EINVAL;
+    const size_t keys_bytes = size_t(p->C) * (p->L > p->B + 1 ? p->L : p->B + 1) * 8;
+    if (int e = check_ws(ws, ws_bytes, kAlign + keys_bytes)) return e;
+    return launch_verify_sample(p->C, p->L, p->B, tree->tok, tree->par, tree->depth, tree->n_nodes, target, rows, V,
+                                dtype, temperature, seed, at<unsigned long long>(ws, kAlign), accepted_len, path,
+                                bonus, at<int>(ws, 0), as_stream(stream));
+}
+
+int dartree_adaptive_budget(int C, int* B, int* W) {
+    if (C < 1 || !B || !W) return DARTREE_EINVAL;
+    const bool reduced = C >= DARTREE_REDUCED_BUDGET_FROM_C;
+    *B = reduced ? 32 : 64;
+    *W = reduced ? 3 : 12;
+    return DARTREE_OK;
 }
 
 }  // extern "C"

@@ -208,6 +208,35 @@ DARTREE_API int dartree_verify(const dartree_params* p, const dartree_tree* tree
                    int rows, int V, int dtype, int32_t* accepted_len, int32_t* path,
                    int32_t* bonus, void* ws, size_t ws_bytes, void* stream);
 
+/* S10 when the target samples at a temperature T > 0 (DARTree blog post, section 4
+ * and Table 1: results at temperatures 0 and 1, speed-ups called lossless; the pages
+ * print no acceptance rule for T > 0). The same walk as dartree_verify, on a drawn
+ * token instead of the row's maximum: t = argmax_v (x_v / T + G_v), lowest token id
+ * among equal values, G_v = -log(-log U_v), a Gumbel-max draw from softmax(row / T).
+ * Every emitted token (accepted drafts and the bonus) is a draw of the target at T,
+ * so the output distribution is the target's own. U_v comes from Philox4x32-10
+ * (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC
+ * 2011) with key (seed & 0xffffffff, seed >> 32), counter (v / 4, row, request, 0)
+ * and output word v % 4, U_v = (2 (word >> 9) + 1) 2^-24; row is the slot's depth
+ * for per-position rows and the slot index for per-node rows. x_v / T, the sum and
+ * the logarithms are float32.
+ *   temperature  T, positive and finite (DARTREE_EINVAL otherwise)
+ *   seed         64-bit generator key; equal seeds give equal draws
+ *   other arguments, outputs, workspace and errors as for dartree_verify. */
+DARTREE_API int dartree_verify_sample(const dartree_params* p, const dartree_tree* tree, const void* target,
+                                      int rows, int V, int dtype, float temperature, uint64_t seed,
+                                      int32_t* accepted_len, int32_t* path, int32_t* bonus, void* ws,
+                                      size_t ws_bytes, void* stream);
+
+/* Node budget and width for a batch of C concurrent requests (DARTree blog post,
+ * section 4.4: at concurrency 4 the budget B shrinks from 64 to 32 and the width W
+ * from 12 to 3; at concurrency 1 and 2 the defaults run). Reading: the reduced pair
+ * applies from C = DARTREE_REDUCED_BUDGET_FROM_C on. Host only, no GPU work.
+ *   C     requests in the batch, >= 1 (DARTREE_EINVAL otherwise)
+ *   B, W  outputs: (64, 12) below the threshold, (32, 3) from it */
+#define DARTREE_REDUCED_BUDGET_FROM_C 4
+DARTREE_API int dartree_adaptive_budget(int C, int* B, int* W);
+
 /* S1-S10 in one call: dartree_build_tree (no supertree or candidate outputs)
  * followed by dartree_verify, with the same results as those two calls.
  * target, rows: as for dartree_verify, with V and dtype of the head. With

@@ -100,16 +100,20 @@ def sample_token(row_f32: np.ndarray, T: float, seed: int, request: int, row: in
     return t, float(y[t]) - float(rest.max())
 
 
-def verify_sample(tree: dict, target: np.ndarray, dtype: str, rows: str, L: int, T: float, seed: int) -> dict:
+def verify_sample(tree: dict, target: np.ndarray, dtype: str, rows: str, L: int, T: float, seed: int,
+                  requests=None) -> dict:
     """Longest accepted prefix when the target samples at temperature T (rule above).
 
     Same walk and outputs as verify(); per-position rows: the slot at depth delta uses
     row delta (no row at depth L: bonus -1); per-node rows: slot j uses row j. Also
-    returns the smallest decision margin met on the walks.
+    returns the smallest decision margin met on the walks. requests: the request
+    index of each entry in the counter (default 0, 1, ...), so that a sample of a
+    batch can be checked on its own.
     """
     if not (T > 0 and np.isfinite(T)):
         raise ValueError("temperature must be positive and finite")
     n = len(tree["n_nodes"])
+    req = np.arange(n) if requests is None else np.asarray(requests)
     acc = np.zeros(n, np.int64)
     path = np.full((n, L), -1, np.int64)
     bonus = np.full(n, -1, np.int64)
@@ -125,7 +129,7 @@ def verify_sample(tree: dict, target: np.ndarray, dtype: str, rows: str, L: int,
                 rid, row = d, to_f32(target[i, d], dtype)
             else:
                 rid, row = cur, to_f32(target[i, cur], dtype)
-            t, margin = sample_token(row, T, seed, i, rid)
+            t, margin = sample_token(row, T, seed, int(req[i]), rid)
             min_margin = min(min_margin, margin)
             nxt = [j for j in range(1, nn) if tree["par"][i, j] == cur and tree["tok"][i, j] == t]
             if not nxt:

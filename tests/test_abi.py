@@ -92,3 +92,30 @@ def test_heap_search_limits_are_checked_on_the_host(L):
     head = dd.Head(256, 256, 3001, 256, dd.BF16, None)   # not prepared (no W_q^T)
     assert L.dartree_heap_build(ctypes.byref(head), ctypes.byref(ok), fake, fake, fake, fake, fake, fake, fake,
                                 fake, 1 << 20, None) == dd.EINVAL
+
+
+def test_sampled_verify_arguments_are_checked_on_the_host(L):
+    import diffusion_drafter_draft_gb300 as dd
+    p = dd.Params(1, 4, 8, 2, 8, -0.1)
+    fake = ctypes.c_void_p(256)
+    ws_ok = ctypes.c_void_p(1 << 20)
+    tree = dd.Tree(256, 256, 256, 256, 256, None, None)
+    f = L.dartree_verify_sample
+    for T in (0.0, -1.0, float("inf"), float("nan")):
+        assert f(ctypes.byref(p), ctypes.byref(tree), fake, 0, 100, dd.F32, T, 1, fake, fake, fake, ws_ok, 4096,
+                 None) == dd.EINVAL
+    assert f(ctypes.byref(p), ctypes.byref(tree), fake, 5, 100, dd.F32, 1.0, 1, fake, fake, fake, ws_ok, 4096,
+             None) == dd.EDTYPE
+    assert f(ctypes.byref(p), ctypes.byref(tree), fake, 0, 100, dd.F32, 1.0, 1, fake, fake, fake, ws_ok, 64,
+             None) == dd.EWORKSPACE
+    assert f(ctypes.byref(dd.Params(0, 4, 8, 2, 8, -0.1)), ctypes.byref(tree), fake, 0, 100, dd.F32, 1.0, 1, fake,
+             fake, fake, ws_ok, 64, None) == dd.OK   # an empty batch launches nothing
+
+
+def test_adaptive_budget_matches_the_oracle_policy(L):
+    import diffusion_drafter_draft_gb300 as dd
+    from oracle.sampling import adaptive_budget
+    for C in (1, 2, 3, 4, 5, 8, 64, 1000):
+        assert dd.adaptive_budget(C) == adaptive_budget(C)
+    with pytest.raises(dd.DartreeError):
+        dd.adaptive_budget(0)

@@ -139,3 +139,18 @@ def test_adaptive_budget_values():
     assert [osm.adaptive_budget(C) for C in (4, 5, 16, 64)] == [(32, 3)] * 4
     with pytest.raises(ValueError):
         osm.adaptive_budget(0)
+
+
+def test_request_ids_key_the_draws():
+    """Checking request i of a batch on its own (requests=[i]) draws what the batch
+    call draws for entry i."""
+    n = 5
+    tree = _tree(n, tok=[7, 0, 2, 1], par=[-1, 0, 0, 1], depth=[0, 1, 1, 2])
+    rng = np.random.default_rng(0)
+    target = rng.standard_normal((n, 2, 4)).astype(np.float32)
+    full = osm.verify_sample(tree, target, "f32", "position", 2, 1.0, seed=3)
+    for i in range(n):
+        sub = {k: v[i:i + 1] for k, v in tree.items()}
+        one = osm.verify_sample(sub, target[i:i + 1], "f32", "position", 2, 1.0, seed=3, requests=[i])
+        for k in ("accepted_len", "path", "bonus"):
+            np.testing.assert_array_equal(one[k][0], full[k][i])
