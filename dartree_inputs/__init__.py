@@ -39,11 +39,12 @@ import numpy as np
 __all__ = [
     "Config", "CONFIGS", "make_config", "make_inputs", "make_head",
     "make_target_per_node", "breadth_first_slot_depth", "make_tie_inputs", "round_to_bf16_bits",
-    "bf16_bits_to_f32", "to_f32", "to_f64",
+    "bf16_bits_to_f32", "to_f32", "to_f64", "make_lm_head",
 ]
 
 HEAD_STREAM = 2**31 - 1
 TIE_STREAM = 2**31 - 2
+LM_HEAD_STREAM = 2**31 - 3
 
 
 @dataclass(frozen=True)
@@ -142,6 +143,20 @@ def make_head(cfg: Config) -> tuple[np.ndarray, np.ndarray]:
         E[r0:r1] = _store(rng.standard_normal((r1 - r0, cfg.H), dtype=np.float32) * scale, cfg.dtype)
     Wq = _store(rng.standard_normal((cfg.H, cfg.H), dtype=np.float32) * scale, cfg.dtype)
     return E, Wq
+
+
+def make_lm_head(cfg: Config) -> np.ndarray:
+    """Stand-in LM-head weights W_lm [V, H] of the block drafter in storage form,
+    N(0, sigma^2 / H), so that the logits of the N(0, 1) block hidden states have the
+    spread (sigma) of the configuration's base-logit noise."""
+    rng = _rng(cfg.seed, LM_HEAD_STREAM)
+    scale = np.float32(cfg.sigma / np.sqrt(cfg.H))
+    W = np.empty((cfg.V, cfg.H), dtype=np.uint16 if cfg.dtype == "bf16" else np.float32)
+    step = max(1, (1 << 24) // cfg.H)
+    for r0 in range(0, cfg.V, step):
+        r1 = min(cfg.V, r0 + step)
+        W[r0:r1] = _store(rng.standard_normal((r1 - r0, cfg.H), dtype=np.float32) * scale, cfg.dtype)
+    return W
 
 
 def _other_token(rng: np.random.Generator, V: int, avoid: int) -> int:

@@ -9,3 +9,4 @@ from .dartree import (  # noqa: F401
     tree_paths, verify,
 )
 from . import sampling  # noqa: F401,E402  (temperature-T verification, adaptive budget)
+from . import lm_head  # noqa: F401,E402  (stand-in LM head followed by S1)
