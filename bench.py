@@ -23,7 +23,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from dartree_inputs import breadth_first_slot_depth, make_config, make_inputs, make_target_per_node  # noqa: E402
+from dartree_inputs import (breadth_first_slot_depth, make_config, make_inputs, make_lm_head,  # noqa: E402
+                            make_target_per_node)
 
 MAIN_CFG = "cfg1_qwen3_4b_c1"
 STRESS_CFG = "cfg4_c64_stress"
@@ -309,6 +310,32 @@ def measure_sample(cfg, m, steps, warmup, torch, dd, hbm_peak, graphs=True, temp
             "target_bytes": int(nbytes), "achieved_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4)}
 
 
+def measure_lm_head(cfg, m, steps, warmup, torch, dd, hbm_peak, graphs=True):
+    """The drafter's LM head fused with S1 (dartree_lm_head_topk) on the round's block
+    hidden states and a stand-in W_lm [V, H]: us per call and the fraction of the
+    measured copy bandwidth its bytes (W_lm once, the hidden rows) reach. Beside it,
+    for context only, the unfused library path (torch matmul writing the logits,
+    then torch.topk) on the same operands."""
+    if cfg.dtype != "bf16":
+        return None
+    x = m["x"]
+    R = cfg.C * cfg.L
+    h = x["hidden"].view(R, cfg.H)
+    W = torch.from_numpy(make_lm_head(cfg).view(np.int16)).cuda().view(torch.bfloat16)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    ws = dd.new_workspace(dd.lib().dartree_lm_head_workspace_bytes(R, cfg.V, cfg.H, cfg.K))
+    t = time_steps(torch, graphed(torch, lambda: dd.lm_head_topk(h, W, cfg.K, ws=ws), graphs), steps, warmup, flush)
+    us = float(np.median(t)) * 1e3
+    nbytes = cfg.V * cfg.H * 2 + R * cfg.H * 2
+    t_lib = time_steps(torch, graphed(torch, lambda: torch.topk((h @ W.t()).float(), cfg.K, dim=1), graphs), steps,
+                       warmup, flush)
+    del W
+    return {"us": round(us, 2), "rows": R, "V": cfg.V, "H": cfg.H, "K": cfg.K, "bytes": int(nbytes),
+            "achieved_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+            "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 4),
+            "unfused_torch_us": round(float(np.median(t_lib)) * 1e3, 2)}
+
+
 # DRAM bytes per launch (read + write) from one ncu capture of the current kernel on
 # this workload; the C=64 contraction and top-K were captured on fewer requests (8
 # and 20 of them) and scaled by the requests processed (their traffic is per request).
@@ -526,6 +553,12 @@ def profile_only(args):
         ws = dd.new_workspace(256)
         base2 = x["base"].view(cfg.C * cfg.L, V)
         fn = lambda: dd.topk(base2, cfg.K, ws=ws)  # noqa: E731
+    elif args.only == "lmhead":
+        R = cfg.C * cfg.L
+        W = torch.from_numpy(make_lm_head(cfg).view(np.int16)).cuda().view(torch.bfloat16)
+        h = x["hidden"].view(R, cfg.H)
+        ws = dd.new_workspace(dd.lib().dartree_lm_head_workspace_bytes(R, cfg.V, cfg.H, cfg.K))
+        fn = lambda: dd.lm_head_topk(h, W, cfg.K, ws=ws)  # noqa: E731
     elif args.only == "heap":
         h = dd.HeapRound(x["E"], x["Wq"], cfg.C, cfg.L, cfg.K, cfg.B, cfg.beta)
         fn = lambda: h.run(x["base"], x["hidden"], x["anchor"])  # noqa: E731
@@ -547,7 +580,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-stress", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
-    ap.add_argument("--only", choices=["topk", "round", "heap"], default=None,
+    ap.add_argument("--only", choices=["topk", "round", "heap", "lmhead"], default=None,
                     help="profiling mode: run just one entry point on --config and print its timing")
     ap.add_argument("--config", default=None, help="workload name for --only (default: the main workload)")
     ap.add_argument("--C", type=int, default=None, help="--only: override the number of requests (a smaller case)")
@@ -618,6 +651,7 @@ def main():
     e2e_ms, h2d, d2h = measure_e2e(cfg, m, min(args.steps, 20), torch, dd)
     heap = measure_heap(cfg, m, args.steps, max(3, args.warmup), torch, dd, graphs=not args.no_graph)
     sample = measure_sample(cfg, m, args.steps, max(3, args.warmup), torch, dd, hbm_peak, graphs=not args.no_graph)
+    lmh = measure_lm_head(cfg, m, args.steps, max(3, args.warmup), torch, dd, hbm_peak, graphs=not args.no_graph)
     line = {
         "metric": "draft-tree rounds/sec (build+verify)", "value": round(value, 3), "unit": "rounds/s",
         "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5),
@@ -638,6 +672,7 @@ def main():
         "clocks": m["clocks"],
         "heap_baseline": heap,
         "verify_sample": sample,
+        "lm_head_topk": lmh,
     }
     del m
     torch.cuda.empty_cache()

@@ -16,7 +16,7 @@ __all__ = [
     "DartreeError", "lib", "library_path", "F32", "BF16", "ROWS_PER_POSITION", "ROWS_PER_NODE",
     "workspace_bytes", "new_workspace", "topk", "expand", "prune", "tree_mask", "build_tree",
     "verify", "read_status", "clear_status", "Round", "EXPORTS", "heap_build", "HeapRound",
-    "verify_sample", "adaptive_budget",
+    "verify_sample", "adaptive_budget", "lm_head_topk",
 ]
 
 F32, BF16 = 0, 1
@@ -28,7 +28,8 @@ EXPORTS = ("dartree_head_init", "dartree_workspace_bytes", "dartree_topk", "dart
            "dartree_clear_status", "dartree_status_string", "dartree_verify_static", "dartree_gemm_bf16",
            "dartree_head_prepare", "dartree_round", "dartree_selftest_wait", "dartree_timing",
            "dartree_timing_read", "dartree_kernel_name", "dartree_heap_workspace_bytes", "dartree_heap_build",
-           "dartree_verify_sample", "dartree_adaptive_budget")
+           "dartree_verify_sample", "dartree_adaptive_budget", "dartree_lm_head_workspace_bytes",
+           "dartree_lm_head_topk")
 
 
 class DartreeError(RuntimeError):
@@ -102,6 +103,8 @@ def lib() -> ctypes.CDLL:
         "dartree_verify_sample": (i, [P(Params), P(Tree), vp, i, i, i, ctypes.c_float, ctypes.c_uint64, vp, vp, vp,
                                       vp, sz, vp]),
         "dartree_adaptive_budget": (i, [i, P(ctypes.c_int), P(ctypes.c_int)]),
+        "dartree_lm_head_workspace_bytes": (sz, [i, i, i, i]),
+        "dartree_lm_head_topk": (i, [vp, vp, i, i, i, i, i, vp, vp, vp, sz, vp]),
         "dartree_gemm_bf16": (i, [vp, vp, vp, i, i, i, vp, vp]),
         "dartree_read_status": (i, [vp, P(ctypes.c_int32), vp]),
         "dartree_clear_status": (i, [vp, vp]),
@@ -378,6 +381,27 @@ def adaptive_budget(C: int) -> tuple[int, int]:
     B, W = ctypes.c_int(), ctypes.c_int()
     _call("dartree_adaptive_budget", int(C), ctypes.byref(B), ctypes.byref(W))
     return B.value, W.value
+
+
+def lm_head_topk(hidden, W_lm, K: int, ws=None, stream=None):
+    """The drafter's LM head fused with S1: hidden [R, H] x W_lm[V, H]^T -> per-row
+    top-K (tok [R, K] int32, val [R, K] fp32), logits never written."""
+    R, H = hidden.shape
+    V = W_lm.shape[0]
+    _need(hidden, "hidden", torch.bfloat16, (R, H))
+    _need(W_lm, "W_lm", torch.bfloat16, (V, H))
+    dev = hidden.device
+    tok = torch.empty((R, K), dtype=torch.int32, device=dev)
+    val = torch.empty((R, K), dtype=torch.float32, device=dev)
+    need = lib().dartree_lm_head_workspace_bytes(R, V, H, K)
+    if need == 0:
+        raise DartreeError(EUNSUPPORTED, "dartree_lm_head_workspace_bytes")
+    if ws is None:
+        ws = new_workspace(need, dev)
+    _call("dartree_lm_head_topk", ctypes.c_void_p(hidden.data_ptr()), ctypes.c_void_p(W_lm.data_ptr()), R, V, H,
+          int(K), BF16, ctypes.c_void_p(tok.data_ptr()), ctypes.c_void_p(val.data_ptr()),
+          ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
+    return tok, val
 
 
 def verify_static(tree, target, rows: int, L: int, stream=None):

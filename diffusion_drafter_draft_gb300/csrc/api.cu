@@ -506,6 +506,26 @@ int dartree_verify_sample(const dartree_params* p, const dartree_tree* tree, con
                                 bonus, at<int>(ws, 0), as_stream(stream));
 }
 
+size_t dartree_lm_head_workspace_bytes(int R, int V, int H, int K) {
+    if (!lmhead_supported(R, V, H, K)) return 0;
+    return kAlign + up(lmhead_part_bytes(R < 64 ? R : 64, V, K));
+}
+
+int dartree_lm_head_topk(const void* hidden, const void* W_lm, int R, int V, int H, int K, int dtype, int32_t* tok,
+                         float* val, void* ws, size_t ws_bytes, void* stream) {
+    if (R < 0 || V < 1 || H < 1 || K < 1 || K > V) return DARTREE_EINVAL;
+    if (!dtype_ok(dtype)) return DARTREE_EDTYPE;
+    if (dtype != DARTREE_BF16) return DARTREE_EUNSUPPORTED;  // bf16 tensor-core operands
+    if (R == 0) return DARTREE_OK;
+    if (!lmhead_supported(R, V, H, K)) return DARTREE_EUNSUPPORTED;
+    if (!hidden || !W_lm || !tok || !val || reinterpret_cast<uintptr_t>(hidden) % 16 != 0 ||
+        reinterpret_cast<uintptr_t>(W_lm) % 16 != 0)
+        return DARTREE_EINVAL;
+    if (int e = check_ws(ws, ws_bytes, dartree_lm_head_workspace_bytes(R, V, H, K))) return e;
+    return launch_lmhead_topk(hidden, W_lm, R, V, H, K, tok, val, at<unsigned long long>(ws, kAlign),
+                              at<int>(ws, 0), as_stream(stream));
+}
+
 int dartree_adaptive_budget(int C, int* B, int* W) {
     if (C < 1 || !B || !W) return DARTREE_EINVAL;
     const bool reduced = C >= DARTREE_REDUCED_BUDGET_FROM_C;

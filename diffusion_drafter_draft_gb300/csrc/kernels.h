@@ -29,7 +29,8 @@ std::recursive_mutex& side_mutex();
 // Kernel ids of the launch timing (dartree_timing): one per kernel family.
 enum KernelId {
     KID_TOPK_ROWS = 0, KID_TOPK_STREAM, KID_GEMM, KID_CONTRACT, KID_EXPAND_G, KID_GATHER, KID_SELECT,
-    KID_STATE, KID_HEAP, KID_FINISH, KID_PRUNE, KID_MASK, KID_ROWMAX, KID_WALK, KID_ROWSAMPLE, KID_OTHER,
+    KID_STATE, KID_HEAP, KID_FINISH, KID_PRUNE, KID_MASK, KID_ROWMAX, KID_WALK, KID_ROWSAMPLE, KID_LMHEAD,
+    KID_LMMERGE, KID_OTHER,
     KID_COUNT
 };
 // Brackets the launches of its scope with timing events when timing is enabled.
@@ -220,6 +221,13 @@ int launch_verify_sample(int C, int L, int B, const int32_t* tok, const int32_t*
                          const int32_t* n_nodes, const void* target, int rows_mode, int V, int dtype, float temp,
                          uint64_t seed, unsigned long long* keys, int32_t* accepted, int32_t* path, int32_t* bonus,
                          int* status, cudaStream_t stream);
+
+// The LM head fused with S1: tok/val [R, K] = top-K of hidden [R, H] x W[V, H]^T per
+// row (bf16 operands, fp32 logits); part: lmhead_part_bytes of scratch.
+bool lmhead_supported(int R, int V, int H, int K);
+size_t lmhead_part_bytes(int R, int V, int K);
+int launch_lmhead_topk(const void* hidden, const void* W, int R, int V, int H, int K, int32_t* tok, float* val,
+                       unsigned long long* part, int* status, cudaStream_t stream);
 
 // Bounded-wait self-test (which = 0: mbarrier, 1: grid barrier on ctr).
 int launch_selftest_wait(int which, unsigned* ctr, int* status, uint64_t limit_ns, cudaStream_t stream);

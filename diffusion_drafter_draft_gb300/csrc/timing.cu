@@ -45,7 +45,8 @@ const char* const kNames[KID_COUNT] = {
     "topk_rows_kernel",  "topk_stream_kernel", "gemm_bf16_tc_kernel", "contract_tc_kernel",
     "expand_g_kernel",   "gather_rows_kernel", "select_kernel",       "state_kernel",
     "heap_search_kernel",  "finish_kernel",    "prune_kernel",        "mask_kernel",
-    "rowmax_kernel",     "walk_kernel",        "rowsample_kernel",    "other"};
+    "rowmax_kernel",     "walk_kernel",        "rowsample_kernel",    "lmhead_topk_kernel",
+    "lmhead_merge_kernel", "other"};
 }  // namespace
 
 KTimer::KTimer(int id, cudaStream_t s) : id_(id), s_(s), b_(nullptr) {

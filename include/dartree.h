@@ -228,6 +228,26 @@ DARTREE_API int dartree_verify_sample(const dartree_params* p, const dartree_tre
                                       int32_t* accepted_len, int32_t* path, int32_t* bonus, void* ws,
                                       size_t ws_bytes, void* stream);
 
+/* The block drafter's LM head fused with S1 (DARTree blog post, "3.1 Basic flow",
+ * candidate generation: the top-K tokens of every block position's base logits).
+ * The base logits L[r, v] = <hidden[r], W_lm[v]> (a linear head without bias; the
+ * pages do not print the drafter's head) are accumulated in fp32 on the tensor
+ * cores and reduced to candidates on chip: they are never written to memory.
+ *   hidden    [R, H] bf16, one row per (request, block position): R = C * L
+ *   W_lm      [V, H] bf16, one row per vocabulary token (row-major)
+ *   K         candidates per row, 1..128, K <= V
+ *   tok, val  [R, K] outputs: tokens ordered by (logit desc, token id asc) and
+ *             their fp32 logits; the same layout as dartree_candidates, so the
+ *             result can be handed to dartree_expand
+ * H must be a multiple of 64; hidden and W_lm start on 16-byte boundaries. Rows
+ * are processed 64 at a time (each group of 64 rows streams W_lm once). fp32
+ * operands: DARTREE_EUNSUPPORTED. Workspace: dartree_lm_head_workspace_bytes
+ * (status word + one K-key list per row and SM). */
+DARTREE_API size_t dartree_lm_head_workspace_bytes(int R, int V, int H, int K);
+DARTREE_API int dartree_lm_head_topk(const void* hidden, const void* W_lm, int R, int V, int H, int K,
+                                     int dtype, int32_t* tok, float* val, void* ws, size_t ws_bytes,
+                                     void* stream);
+
 /* Node budget and width for a batch of C concurrent requests (DARTree blog post,
  * section 4.4: at concurrency 4 the budget B shrinks from 64 to 32 and the width W
  * from 12 to 3; at concurrency 1 and 2 the defaults run). Reading: the reduced pair

@@ -119,3 +119,24 @@ def test_adaptive_budget_matches_the_oracle_policy(L):
         assert dd.adaptive_budget(C) == adaptive_budget(C)
     with pytest.raises(dd.DartreeError):
         dd.adaptive_budget(0)
+
+
+def test_lm_head_arguments_are_checked_on_the_host(L):
+    import diffusion_drafter_draft_gb300 as dd
+    fake = ctypes.c_void_p(256)
+    ws_ok = ctypes.c_void_p(1 << 20)
+    need = L.dartree_lm_head_workspace_bytes(16, 151936, 2560, 64)
+    assert need >= 256 + 16 * 64 * 8    # status word + one K-key list per row and SM
+    assert L.dartree_lm_head_workspace_bytes(16, 1000, 100, 8) == 0      # H % 64
+    assert L.dartree_lm_head_workspace_bytes(16, 1000, 128, 129) == 0    # K > 128
+    assert L.dartree_lm_head_workspace_bytes(16, 10, 128, 11) == 0       # K > V
+    f = L.dartree_lm_head_topk
+    assert f(fake, fake, 16, 1000, 128, 8, dd.F32, fake, fake, ws_ok, need, None) == dd.EUNSUPPORTED
+    assert f(fake, fake, 16, 1000, 128, 8, 9, fake, fake, ws_ok, need, None) == dd.EDTYPE
+    assert f(fake, fake, 16, 1000, 128, 2000, dd.BF16, fake, fake, ws_ok, need, None) == dd.EINVAL
+    assert f(fake, fake, 16, 1000, 100, 8, dd.BF16, fake, fake, ws_ok, need, None) == dd.EUNSUPPORTED
+    assert f(ctypes.c_void_p(258), fake, 16, 1000, 128, 8, dd.BF16, fake, fake, ws_ok, 1 << 24, None) \
+        == dd.EINVAL                                                     # hidden not 16-byte aligned
+    small = L.dartree_lm_head_workspace_bytes(16, 1000, 128, 8)
+    assert f(fake, fake, 16, 1000, 128, 8, dd.BF16, fake, fake, ws_ok, small - 8, None) == dd.EWORKSPACE
+    assert f(fake, fake, 0, 1000, 128, 8, dd.BF16, fake, fake, ws_ok, 0, None) == dd.OK
