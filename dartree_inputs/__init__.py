@@ -39,12 +39,13 @@ import numpy as np
 __all__ = [
     "Config", "CONFIGS", "make_config", "make_inputs", "make_head",
     "make_target_per_node", "breadth_first_slot_depth", "make_tie_inputs", "round_to_bf16_bits",
-    "bf16_bits_to_f32", "to_f32", "to_f64", "make_lm_head",
+    "bf16_bits_to_f32", "to_f32", "to_f64", "make_lm_head", "make_attention_inputs",
 ]
 
 HEAD_STREAM = 2**31 - 1
 TIE_STREAM = 2**31 - 2
 LM_HEAD_STREAM = 2**31 - 3
+ATTN_STREAM = 2**31 - 4
 
 
 @dataclass(frozen=True)
@@ -157,6 +158,26 @@ def make_lm_head(cfg: Config) -> np.ndarray:
         r1 = min(cfg.V, r0 + step)
         W[r0:r1] = _store(rng.standard_normal((r1 - r0, cfg.H), dtype=np.float32) * scale, cfg.dtype)
     return W
+
+
+def make_attention_inputs(C: int, S: int, Hq: int, Hkv: int, D: int, N: int, seed: int, n_ctx=None,
+                          dtype: str = "bf16") -> dict:
+    """One target attention layer's operands for the tree of each request, N(0, 1):
+    tree queries q [C, S, Hq, D], tree keys/values k_tree, v_tree [C, S, Hkv, D]
+    (queries and keys unrotated), and the cached prefix k_cache, v_cache
+    [C, Hkv, N, D] (keys stored rotated); n_ctx [C] cached lengths (default N). Each
+    request draws from its own stream, so a sample of a batch is bit-identical."""
+    sdt = np.uint16 if dtype == "bf16" else np.float32
+    out = dict(q=np.empty((C, S, Hq, D), sdt), k_tree=np.empty((C, S, Hkv, D), sdt),
+               v_tree=np.empty((C, S, Hkv, D), sdt), k_cache=np.empty((C, Hkv, N, D), sdt),
+               v_cache=np.empty((C, Hkv, N, D), sdt),
+               n_ctx=np.full(C, N, np.int32) if n_ctx is None else np.asarray(n_ctx, np.int32))
+    for r in range(C):
+        rng = _rng(seed, ATTN_STREAM, r)
+        for k, shape in (("q", (S, Hq, D)), ("k_tree", (S, Hkv, D)), ("v_tree", (S, Hkv, D)),
+                         ("k_cache", (Hkv, N, D)), ("v_cache", (Hkv, N, D))):
+            out[k][r] = _store(rng.standard_normal(shape, dtype=np.float32), dtype)
+    return out
 
 
 def _other_token(rng: np.random.Generator, V: int, avoid: int) -> int:

@@ -10,3 +10,4 @@ from .dartree import (  # noqa: F401
 )
 from . import sampling  # noqa: F401,E402  (temperature-T verification, adaptive budget)
 from . import lm_head  # noqa: F401,E402  (stand-in LM head followed by S1)
+from . import tree_attention  # noqa: F401,E402  (the verification pass's tree attention)
