@@ -336,6 +336,40 @@ def measure_lm_head(cfg, m, steps, warmup, torch, dd, hbm_peak, graphs=True):
             "unfused_torch_us": round(float(np.median(t_lib)) * 1e3, 2)}
 
 
+ATTN_SHAPE = dict(Hq=32, Hkv=8, D=128, N=2048, theta=1.0e6)   # a Qwen3-4B/8B attention layer, 2048 cached
+
+
+def measure_attention(cfg, m, steps, warmup, torch, dd, hbm_peak, tf_peak, graphs=True):
+    """One tree-attention layer of the verification pass (dartree_tree_attention) on the
+    round's tree (S9's mask and positions) over a full 2048-token cache per request:
+    us per call, the cache bytes it streams against the measured copy bandwidth, and
+    its score + value flops (over every cached key and the tree) against bf16 peak."""
+    tr = m["rnd"].tree
+    C, S = tr["mask"].shape[0], tr["mask"].shape[1]
+    Hq, Hkv, D, N = ATTN_SHAPE["Hq"], ATTN_SHAPE["Hkv"], ATTN_SHAPE["D"], ATTN_SHAPE["N"]
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(2026)
+    r = lambda *shape: torch.randn(*shape, generator=gen, device="cuda").to(torch.bfloat16)  # noqa: E731
+    q, kt, vt = r(C, S, Hq, D), r(C, S, Hkv, D), r(C, S, Hkv, D)
+    kc, vtc = r(C, Hkv, N, D), r(C, Hkv, D, N)
+    n_ctx = torch.full((C,), N, dtype=torch.int32, device="cuda")
+    p = dd.AttnParams(C, S, Hq, Hkv, D, N, ATTN_SHAPE["theta"])
+    import ctypes
+    ws = dd.new_workspace(dd.lib().dartree_tree_attention_workspace_bytes(ctypes.byref(p)))
+    fn = lambda: dd.tree_attention(q, kt, vt, kc, vtc, n_ctx, tr, ATTN_SHAPE["theta"], ws=ws)  # noqa: E731
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    t = time_steps(torch, graphed(torch, fn, graphs), steps, warmup, flush)
+    us = float(np.median(t)) * 1e3
+    nbytes = C * Hkv * N * D * 2 * 2 + C * S * (Hq + 2 * Hkv) * D * 2 + C * S * Hq * D * 2
+    flops = 2 * 2 * C * Hq * S * (N + S) * D
+    del q, kt, vt, kc, vtc
+    return {"us": round(us, 2), "C": C, "S": S, "Hq": Hq, "Hkv": Hkv, "D": D, "n_ctx": N, "bytes": int(nbytes),
+            "achieved_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+            "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 4),
+            "tflops": round(flops / (us * 1e-6) / 1e12, 1),
+            "tensor_frac": round(flops / (us * 1e-6) / 1e12 / tf_peak, 4)}
+
+
 # DRAM bytes per launch (read + write) from one ncu capture of the current kernel on
 # this workload; the C=64 contraction and top-K were captured on fewer requests (8
 # and 20 of them) and scaled by the requests processed (their traffic is per request).
@@ -559,6 +593,19 @@ def profile_only(args):
         h = x["hidden"].view(R, cfg.H)
         ws = dd.new_workspace(dd.lib().dartree_lm_head_workspace_bytes(R, cfg.V, cfg.H, cfg.K))
         fn = lambda: dd.lm_head_topk(h, W, cfg.K, ws=ws)  # noqa: E731
+    elif args.only == "attn":
+        import ctypes
+        rnd0 = dd.Round(x["E"], x["Wq"], cfg.C, cfg.L, cfg.K, cfg.W, cfg.B, cfg.beta, rows)
+        rnd0.run(x["base"], x["hidden"], x["anchor"], x["target"])
+        tr = rnd0.tree
+        C, S = cfg.C, cfg.B + 1
+        Hq, Hkv, D, N = ATTN_SHAPE["Hq"], ATTN_SHAPE["Hkv"], ATTN_SHAPE["D"], ATTN_SHAPE["N"]
+        r_ = lambda *shape: torch.randn(*shape, device="cuda").to(torch.bfloat16)  # noqa: E731
+        aq, akt, avt, akc, avc = r_(C, S, Hq, D), r_(C, S, Hkv, D), r_(C, S, Hkv, D), r_(C, Hkv, N, D), r_(C, Hkv, D, N)
+        n_ctx = torch.full((C,), N, dtype=torch.int32, device="cuda")
+        ap = dd.AttnParams(C, S, Hq, Hkv, D, N, ATTN_SHAPE["theta"])
+        aws = dd.new_workspace(dd.lib().dartree_tree_attention_workspace_bytes(ctypes.byref(ap)))
+        fn = lambda: dd.tree_attention(aq, akt, avt, akc, avc, n_ctx, tr, ATTN_SHAPE["theta"], ws=aws)  # noqa: E731
     elif args.only == "heap":
         h = dd.HeapRound(x["E"], x["Wq"], cfg.C, cfg.L, cfg.K, cfg.B, cfg.beta)
         fn = lambda: h.run(x["base"], x["hidden"], x["anchor"])  # noqa: E731
@@ -580,7 +627,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-stress", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
-    ap.add_argument("--only", choices=["topk", "round", "heap", "lmhead"], default=None,
+    ap.add_argument("--only", choices=["topk", "round", "heap", "lmhead", "attn"], default=None,
                     help="profiling mode: run just one entry point on --config and print its timing")
     ap.add_argument("--config", default=None, help="workload name for --only (default: the main workload)")
     ap.add_argument("--C", type=int, default=None, help="--only: override the number of requests (a smaller case)")
@@ -652,6 +699,8 @@ def main():
     heap = measure_heap(cfg, m, args.steps, max(3, args.warmup), torch, dd, graphs=not args.no_graph)
     sample = measure_sample(cfg, m, args.steps, max(3, args.warmup), torch, dd, hbm_peak, graphs=not args.no_graph)
     lmh = measure_lm_head(cfg, m, args.steps, max(3, args.warmup), torch, dd, hbm_peak, graphs=not args.no_graph)
+    attn = measure_attention(cfg, m, args.steps, max(3, args.warmup), torch, dd, hbm_peak, tf_peak,
+                             graphs=not args.no_graph)
     line = {
         "metric": "draft-tree rounds/sec (build+verify)", "value": round(value, 3), "unit": "rounds/s",
         "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5),
@@ -673,6 +722,7 @@ def main():
         "heap_baseline": heap,
         "verify_sample": sample,
         "lm_head_topk": lmh,
+        "tree_attention": attn,
     }
     del m
     torch.cuda.empty_cache()
@@ -693,7 +743,9 @@ def main():
                        "kernels": sper_kernel,
                        "accepted_mean": sm["accepted_mean"], "clocks": sm["clocks"],
                        "verify_sample": measure_sample(scfg, sm, max(5, min(args.steps, 20)), 3, torch, dd,
-                                                       hbm_peak, graphs=not args.no_graph)}
+                                                       hbm_peak, graphs=not args.no_graph),
+                       "tree_attention": measure_attention(scfg, sm, max(5, min(args.steps, 20)), 3, torch, dd,
+                                                           hbm_peak, tf_peak, graphs=not args.no_graph)}
         del sm
         torch.cuda.empty_cache()
     if rank == 0:

@@ -16,7 +16,7 @@ __all__ = [
     "DartreeError", "lib", "library_path", "F32", "BF16", "ROWS_PER_POSITION", "ROWS_PER_NODE",
     "workspace_bytes", "new_workspace", "topk", "expand", "prune", "tree_mask", "build_tree",
     "verify", "read_status", "clear_status", "Round", "EXPORTS", "heap_build", "HeapRound",
-    "verify_sample", "adaptive_budget", "lm_head_topk",
+    "verify_sample", "adaptive_budget", "lm_head_topk", "tree_attention", "AttnParams",
 ]
 
 F32, BF16 = 0, 1
@@ -29,7 +29,7 @@ EXPORTS = ("dartree_head_init", "dartree_workspace_bytes", "dartree_topk", "dart
            "dartree_head_prepare", "dartree_round", "dartree_selftest_wait", "dartree_timing",
            "dartree_timing_read", "dartree_kernel_name", "dartree_heap_workspace_bytes", "dartree_heap_build",
            "dartree_verify_sample", "dartree_adaptive_budget", "dartree_lm_head_workspace_bytes",
-           "dartree_lm_head_topk")
+           "dartree_lm_head_topk", "dartree_tree_attention_workspace_bytes", "dartree_tree_attention")
 
 
 class DartreeError(RuntimeError):
@@ -55,6 +55,11 @@ class Candidates(ctypes.Structure):
 class Supertree(ctypes.Structure):
     _fields_ = [("tok", ctypes.c_void_p), ("par", ctypes.c_void_p), ("score", ctypes.c_void_p),
                 ("n", ctypes.c_void_p)]
+
+
+class AttnParams(ctypes.Structure):
+    _fields_ = [("C", ctypes.c_int), ("S", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
+                ("D", ctypes.c_int), ("N", ctypes.c_int), ("theta", ctypes.c_float)]
 
 
 class Tree(ctypes.Structure):
@@ -104,6 +109,8 @@ def lib() -> ctypes.CDLL:
                                       vp, sz, vp]),
         "dartree_adaptive_budget": (i, [i, P(ctypes.c_int), P(ctypes.c_int)]),
         "dartree_lm_head_workspace_bytes": (sz, [i, i, i, i]),
+        "dartree_tree_attention_workspace_bytes": (sz, [P(AttnParams)]),
+        "dartree_tree_attention": (i, [P(AttnParams), vp, vp, vp, vp, vp, vp, P(Tree), vp, vp, sz, vp]),
         "dartree_lm_head_topk": (i, [vp, vp, i, i, i, i, i, vp, vp, vp, sz, vp]),
         "dartree_gemm_bf16": (i, [vp, vp, vp, i, i, i, vp, vp]),
         "dartree_read_status": (i, [vp, P(ctypes.c_int32), vp]),
@@ -402,6 +409,37 @@ def lm_head_topk(hidden, W_lm, K: int, ws=None, stream=None):
           int(K), BF16, ctypes.c_void_p(tok.data_ptr()), ctypes.c_void_p(val.data_ptr()),
           ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
     return tok, val
+
+
+def tree_attention(q, k_tree, v_tree, k_cache, vt_cache, n_ctx, tree, theta: float = 1.0e6, ws=None,
+                   stream=None):
+    """One attention layer of the verification pass over the tree (dartree_tree_attention):
+    q [C, S, Hq, D], k_tree/v_tree [C, S, Hkv, D], k_cache [C, Hkv, N, D], vt_cache
+    [C, Hkv, D, N] (bf16), n_ctx [C] int32, tree with mask/pos/n_nodes -> out [C, S, Hq, D]."""
+    C, S, Hq, D = q.shape
+    Hkv = k_tree.shape[2]
+    N = k_cache.shape[2]
+    for name, x, shp in (("q", q, (C, S, Hq, D)), ("k_tree", k_tree, (C, S, Hkv, D)),
+                         ("v_tree", v_tree, (C, S, Hkv, D)), ("k_cache", k_cache, (C, Hkv, N, D)),
+                         ("vt_cache", vt_cache, (C, Hkv, D, N))):
+        _need(x, name, torch.bfloat16, shp)
+    _need(n_ctx, "n_ctx", torch.int32, (C,))
+    _need(tree["mask"], "mask", torch.uint8, (C, S, S))
+    _need(tree["pos"], "pos", torch.int32, (C, S))
+    _need(tree["n_nodes"], "n_nodes", torch.int32, (C,))
+    p = AttnParams(C, S, Hq, Hkv, D, N, float(theta))
+    need = lib().dartree_tree_attention_workspace_bytes(ctypes.byref(p))
+    if need == 0:
+        raise DartreeError(EUNSUPPORTED, "dartree_tree_attention_workspace_bytes")
+    if ws is None:
+        ws = new_workspace(need, q.device)
+    out = torch.empty((C, S, Hq, D), dtype=torch.bfloat16, device=q.device)
+    ts = _tree_struct({k: tree[k] for k in ("mask", "pos", "n_nodes")})
+    _call("dartree_tree_attention", ctypes.byref(p), *(ctypes.c_void_p(x.data_ptr()) for x in
+                                                       (q, k_tree, v_tree, k_cache, vt_cache, n_ctx)),
+          ctypes.byref(ts), ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+          _stream(stream))
+    return out
 
 
 def verify_static(tree, target, rows: int, L: int, stream=None):

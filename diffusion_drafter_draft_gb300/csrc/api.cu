@@ -526,6 +526,32 @@ int dartree_lm_head_topk(const void* hidden, const void* W_lm, int R, int V, int
                               at<int>(ws, 0), as_stream(stream));
 }
 
+static bool attn_params_ok(const dartree_attn_params* p) {
+    return p && attn_supported(p->C, p->S, p->Hq, p->Hkv, p->D, p->N) && p->theta > 0.f && isfinite(p->theta);
+}
+
+size_t dartree_tree_attention_workspace_bytes(const dartree_attn_params* p) {
+    if (!attn_params_ok(p)) return 0;
+    return attn_plan(p->C, p->S, p->Hq, p->Hkv, p->N).total;
+}
+
+int dartree_tree_attention(const dartree_attn_params* p, const void* q, const void* k_tree, const void* v_tree,
+                           const void* k_cache, const void* vt_cache, const int32_t* n_ctx, const dartree_tree* tree,
+                           void* out, void* ws, size_t ws_bytes, void* stream) {
+    if (!p || p->C < 0) return DARTREE_EINVAL;
+    if (!attn_params_ok(p)) return DARTREE_EUNSUPPORTED;
+    if (p->C == 0) return DARTREE_OK;
+    auto al16 = [](const void* x) { return x && reinterpret_cast<uintptr_t>(x) % 16 == 0; };
+    if (!al16(q) || !al16(k_tree) || !al16(v_tree) || !al16(out) || !n_ctx || !tree || !tree->mask || !tree->pos ||
+        !tree->n_nodes || (p->N > 0 && (!al16(k_cache) || !al16(vt_cache))))
+        return DARTREE_EINVAL;
+    const AttnPlan pl = attn_plan(p->C, p->S, p->Hq, p->Hkv, p->N);
+    if (int e = check_ws(ws, ws_bytes, pl.total)) return e;
+    return launch_tree_attention(p->C, p->S, p->Hq, p->Hkv, p->N, double(p->theta), q, k_tree, v_tree, k_cache,
+                                 vt_cache, n_ctx, tree->mask, tree->pos, tree->n_nodes, out, ws, pl,
+                                 as_stream(stream));
+}
+
 int dartree_adaptive_budget(int C, int* B, int* W) {
     if (C < 1 || !B || !W) return DARTREE_EINVAL;
     const bool reduced = C >= DARTREE_REDUCED_BUDGET_FROM_C;

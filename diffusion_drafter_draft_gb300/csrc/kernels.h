@@ -30,7 +30,7 @@ std::recursive_mutex& side_mutex();
 enum KernelId {
     KID_TOPK_ROWS = 0, KID_TOPK_STREAM, KID_GEMM, KID_CONTRACT, KID_EXPAND_G, KID_GATHER, KID_SELECT,
     KID_STATE, KID_HEAP, KID_FINISH, KID_PRUNE, KID_MASK, KID_ROWMAX, KID_WALK, KID_ROWSAMPLE, KID_LMHEAD,
-    KID_LMMERGE, KID_OTHER,
+    KID_LMMERGE, KID_ATTN_PREP, KID_ATTN, KID_ATTN_COMBINE, KID_OTHER,
     KID_COUNT
 };
 // Brackets the launches of its scope with timing events when timing is enabled.
@@ -228,6 +228,19 @@ bool lmhead_supported(int R, int V, int H, int K);
 size_t lmhead_part_bytes(int R, int V, int K);
 int launch_lmhead_topk(const void* hidden, const void* W, int R, int V, int H, int K, int32_t* tok, float* val,
                        unsigned long long* part, int* status, cudaStream_t stream);
+
+// Tree attention of the verification pass (one layer, D = 128): workspace plan and launch.
+struct AttnPlan {
+    int nchunk, per, mtiles;              // key-block chunks per row tile, blocks per chunk, row tiles per group
+    size_t qr, kt, vtt, part_o, part_ml;  // workspace offsets (status word at 0)
+    size_t total;
+};
+bool attn_supported(int C, int S, int Hq, int Hkv, int D, int N);
+AttnPlan attn_plan(int C, int S, int Hq, int Hkv, int N);
+int launch_tree_attention(int C, int S, int Hq, int Hkv, int N, double theta, const void* q, const void* k_tree,
+                          const void* v_tree, const void* k_cache, const void* vt_cache, const int32_t* n_ctx,
+                          const uint8_t* mask, const int32_t* pos, const int32_t* n_nodes, void* out, void* ws,
+                          const AttnPlan& pl, cudaStream_t stream);
 
 // Bounded-wait self-test (which = 0: mbarrier, 1: grid barrier on ctr).
 int launch_selftest_wait(int which, unsigned* ctr, int* status, uint64_t limit_ns, cudaStream_t stream);

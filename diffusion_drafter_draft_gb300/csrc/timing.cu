@@ -46,7 +46,7 @@ const char* const kNames[KID_COUNT] = {
     "expand_g_kernel",   "gather_rows_kernel", "select_kernel",       "state_kernel",
     "heap_search_kernel",  "finish_kernel",    "prune_kernel",        "mask_kernel",
     "rowmax_kernel",     "walk_kernel",        "rowsample_kernel",    "lmhead_topk_kernel",
-    "lmhead_merge_kernel", "other"};
+    "lmhead_merge_kernel", "attn_prep_kernel", "attn_kernel", "attn_combine_kernel", "other"};
 }  // namespace
 
 KTimer::KTimer(int id, cudaStream_t s) : id_(id), s_(s), b_(nullptr) {

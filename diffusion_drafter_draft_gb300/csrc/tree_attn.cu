@@ -1,0 +1,558 @@
+// Tree attention of the verification pass: every drafted token of the pruned tree
+// is checked in one target forward pass with a tree-attention mask (DARTree blog
+// post, "3.2"). One attention layer over a KV cache:
+//   slot j of request c, query head h (key/value head g = h / (Hq / Hkv)) attends to
+//   the request's n_ctx cached keys and to the tree slots mask[c, j, :] marks
+//   (ancestor-or-self, from S9), with rotary embedding at position n_ctx + pos[c, j]
+//   (pos = depth, from S9); scores scaled by 1 / sqrt(D).
+//
+// Launch 1 (attn_prep_kernel, one CTA per (request, slot of a 128-slot block)):
+//   rotates the tree's queries and keys (angles in double precision), writing
+//   Qr [C, Hkv, grp*S, D] (row hg*S + j: the grp query heads of a group stacked),
+//   Kt [C, Hkv, 128, D] and the tree values transposed, Vtt [C, Hkv, D, 128];
+//   unused and padding slots are zero.
+// Launch 2 (attn_kernel, CTA = (chunk of key blocks, 128-row tile of a group's
+//   query rows, (request, group))): warp 0 loads the query tile and, per 128-key
+//   block, the keys and transposed values with TMA (128-byte swizzle) into a
+//   two-stage ring; warp 1 issues S = Q K^T into one of two TMEM score buffers and
+//   O += P V^T into a TMEM accumulator; warps 2-9 (two threads per query row, each
+//   on half of the keys and of O) mask, take the running maximum (log2 domain; O
+//   and the sums are rescaled only when the maximum grows by more than 2^8), write P
+//   in bf16 to one of two shared-memory operand buffers (so P_i V^T runs while block
+//   i+1's weights are formed), and at the end either normalise and write the output
+//   (one chunk) or write the chunk's partial (O, max, sum).
+// Launch 3 (attn_combine_kernel, several chunks only): merges the partials of a row.
+// The prefix blocks come first, the tree block (keys = the tree's slots) last.
+// Every mbarrier wait is bounded; a wait that runs out records DARTREE_ETIMEOUT.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace dartree {
+
+constexpr int AT_D = 128;        // head dimension
+constexpr int AT_BM = 128;       // query rows per tile
+constexpr int AT_BN = 128;       // keys per block
+constexpr int AT_NT = 320;       // producer, MMA, 8 softmax warps (two per TMEM lane quarter)
+constexpr int AT_SMX = 256;      // softmax threads
+constexpr int AT_MAXMT = 3;      // query-row tiles per group (grp * S <= 384)
+constexpr float AT_RESCALE = 8.0f;  // log2 growth of the maximum that forces a rescale
+
+struct AtSmem {
+    static constexpr size_t PANEL = size_t(128) * 64 * 2;  // 128 rows x 64 bf16, swizzled
+    static constexpr size_t Q_OFF = 0;                      // 2 panels
+    static constexpr size_t RING_OFF = 2 * PANEL;           // 2 stages x (K 2 panels, V^T 2 panels)
+    static constexpr size_t STAGE = 4 * PANEL;
+    static constexpr size_t P_OFF = RING_OFF + 2 * STAGE;   // 2 buffers x 2 panels
+    static constexpr size_t XCH_OFF = P_OFF + 4 * PANEL;    // float [2 halves][128 rows]
+    static constexpr size_t BAR_OFF = XCH_OFF + 2 * 128 * 4;
+    // qf, full[2], empty[2], sfull[2], sfree[2], pfull[2], odone[2]
+    static constexpr size_t SLOT_OFF = BAR_OFF + 8 * 13;
+    static constexpr size_t TOTAL = SLOT_OFF + 16 + 1024;
+};
+static_assert(AtSmem::TOTAL <= 227 * 1024, "attention tile fits in shared memory");
+
+struct AtArgs {
+    int C, S, Hq, Hkv, N, grp, rows;  // rows = grp * S
+    int nchunk, per;                  // key blocks per chunk
+    const int32_t* n_ctx;
+    const uint8_t* mask;              // [C, S, S]
+    const int32_t* n_nodes;
+    uint16_t* out;                    // [C, S, Hq, D] bf16 (one chunk)
+    float* part_o;                    // [C*Hkv, mtiles, nchunk, 128, D]
+    float* part_ml;                   // [C*Hkv, mtiles, nchunk, 128, 2]
+    int* status;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
+           (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+}
+
+// ----------------------------------------------------------------------------- prep
+
+__global__ void __launch_bounds__(128) attn_prep_kernel(const uint16_t* __restrict__ q,
+                                                        const uint16_t* __restrict__ kt,
+                                                        const uint16_t* __restrict__ vt, const int32_t* n_ctx,
+                                                        const int32_t* pos, const int32_t* n_nodes, int S, int Hq,
+                                                        int Hkv, double theta, uint16_t* __restrict__ Qr,
+                                                        uint16_t* __restrict__ Kr, uint16_t* __restrict__ Vtt) {
+    __shared__ float cs[AT_D / 2], sn[AT_D / 2];
+    const int c = blockIdx.y, j = blockIdx.x;  // j in [0, 128)
+    const int grp = Hq / Hkv;
+    const bool used = j < S && j < n_nodes[c];
+    if (used && threadIdx.x < AT_D / 2) {
+        const int i = threadIdx.x;
+        const double p = double(n_ctx[c]) + double(pos[size_t(c) * S + j]);
+        const double a = p * pow(theta, -2.0 * double(i) / double(AT_D));
+        double s_, c_;
+        sincos(a, &s_, &c_);
+        cs[i] = float(c_);
+        sn[i] = float(s_);
+    }
+    __syncthreads();
+    const int d = threadIdx.x;  // 0..127
+    const int dp = d < AT_D / 2 ? d + AT_D / 2 : d - AT_D / 2;
+    auto rot = [&](const uint16_t* x) -> uint16_t {  // x: one head's D values
+        const float v = bf16_bits_to_float(x[d]), w = bf16_bits_to_float(x[dp]);
+        const int i = d < AT_D / 2 ? d : d - AT_D / 2;
+        const float r = d < AT_D / 2 ? v * cs[i] - w * sn[i] : v * cs[i] + w * sn[i];
+        return __bfloat16_as_ushort(__float2bfloat16_rn(r));
+    };
+    if (j < S)
+        for (int h = 0; h < Hq; ++h) {
+            const int g = h / grp, hg = h - g * grp;
+            uint16_t* dst = Qr + ((size_t(c) * Hkv + g) * (size_t(grp) * S) + size_t(hg) * S + j) * AT_D;
+            dst[d] = used ? rot(q + ((size_t(c) * S + j) * Hq + h) * AT_D) : uint16_t(0);
+        }
+    for (int g = 0; g < Hkv; ++g) {
+        const size_t src = ((size_t(c) * S + j) * Hkv + g) * AT_D;
+        Kr[((size_t(c) * Hkv + g) * AT_BN + j) * AT_D + d] = used ? rot(kt + src) : uint16_t(0);
+        Vtt[((size_t(c) * Hkv + g) * AT_D + d) * AT_BN + j] = used ? vt[src + d] : uint16_t(0);
+    }
+}
+
+// ----------------------------------------------------------------------------- attention
+
+// Byte offset of (row, col) in a 128-byte-swizzled panel of 128 rows x 64 bf16.
+__device__ __forceinline__ uint32_t sw128_off(int row, int chunk16) {
+    return uint32_t(row) * 128u + uint32_t((chunk16 ^ (row & 7)) * 16);
+}
+
+__global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ CUtensorMap tmQ,
+                                                        const __grid_constant__ CUtensorMap tmK,
+                                                        const __grid_constant__ CUtensorMap tmVt,
+                                                        const __grid_constant__ CUtensorMap tmKt,
+                                                        const __grid_constant__ CUtensorMap tmVtt, AtArgs a) {
+    using L = AtSmem;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+    uint64_t* qf = bars;
+    uint64_t* full = bars + 1;
+    uint64_t* empty = bars + 3;
+    uint64_t* sfull = bars + 5;
+    uint64_t* sfree = bars + 7;
+    uint64_t* pfull = bars + 9;   // [2]: P written, by P buffer
+    uint64_t* odone = bars + 11;  // [2]: P V^T done, by P buffer
+    uint32_t* slot = reinterpret_cast<uint32_t*>(smem + L::SLOT_OFF);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int chunk = blockIdx.x, mt = blockIdx.y, cg = blockIdx.z;
+    const int c = cg / a.Hkv, g = cg - c * a.Hkv;
+    const int nctx = min(max(a.n_ctx[c], 0), a.N);
+    const int nbp = (nctx + AT_BN - 1) / AT_BN;  // prefix blocks; block nbp = the tree
+    const int b0 = chunk * a.per, b1 = min(nbp + 1, b0 + a.per);
+    const int nblk = b1 > b0 ? b1 - b0 : 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(qf, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            mbar_init(&sfull[s], 1);
+            mbar_init(&sfree[s], AT_SMX / 32);
+            mbar_init(&pfull[s], AT_SMX / 32);
+            mbar_init(&odone[s], 1);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 1) tc::tmem_alloc(slot, 512);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *slot;  // S buffers at columns 0 and 128, O at 256
+    griddep_launch_dependents();
+    griddep_wait();
+
+    if (warp == 0) {
+        if (lane == 0 && nblk > 0) {  // producer
+            const int qrow = cg * a.rows + mt * AT_BM;
+            mbar_arrive_expect_tx(qf, uint32_t(2 * L::PANEL));
+            tc::tma_load_2d(smem + L::Q_OFF, &tmQ, 0, qrow, qf);
+            tc::tma_load_2d(smem + L::Q_OFF + L::PANEL, &tmQ, 64, qrow, qf);
+            bool ok = true;
+            int i = 0;
+            for (; i < nblk && ok; ++i) {
+                const int s = i & 1, b = b0 + i;
+                if (i >= 2 && !mbar_wait_bounded(&empty[s], uint32_t((i >> 1) & 1) ^ 1u, a.status)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* st = smem + L::RING_OFF + size_t(s) * L::STAGE;
+                mbar_arrive_expect_tx(&full[s], uint32_t(L::STAGE));
+                if (b < nbp) {  // prefix block: K_cache rows, V^T_cache columns
+                    const int kr = cg * a.N + b * AT_BN;
+                    tc::tma_load_2d(st, &tmK, 0, kr, &full[s]);
+                    tc::tma_load_2d(st + L::PANEL, &tmK, 64, kr, &full[s]);
+                    tc::tma_load_2d(st + 2 * L::PANEL, &tmVt, b * AT_BN, cg * AT_D, &full[s]);
+                    tc::tma_load_2d(st + 3 * L::PANEL, &tmVt, b * AT_BN + 64, cg * AT_D, &full[s]);
+                } else {        // the tree block
+                    tc::tma_load_2d(st, &tmKt, 0, cg * AT_BN, &full[s]);
+                    tc::tma_load_2d(st + L::PANEL, &tmKt, 64, cg * AT_BN, &full[s]);
+                    tc::tma_load_2d(st + 2 * L::PANEL, &tmVtt, 0, cg * AT_D, &full[s]);
+                    tc::tma_load_2d(st + 3 * L::PANEL, &tmVtt, 64, cg * AT_D, &full[s]);
+                }
+            }
+            // copies issued and not yet seen complete land before the CTA can exit
+            mbar_wait_bounded(qf, 0, a.status);
+            for (int q = i - 1; q >= 0 && q >= i - 2; --q) mbar_wait_bounded(&full[q & 1], uint32_t(q >> 1) & 1u, a.status);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && nblk > 0) {  // MMA issuer
+            constexpr uint32_t idesc = tc::idesc_bf16_f32(AT_BM, AT_BN);
+            const uint32_t sq = smem_u32(smem + L::Q_OFF);
+            bool ok = mbar_wait_bounded(qf, 0, a.status);
+            auto pv = [&](int i) -> bool {  // O += P_i V_i^T, then release stage i
+                if (!mbar_wait_bounded(&pfull[i & 1], uint32_t(i >> 1) & 1u, a.status)) return false;
+                tc::fence_after_sync();
+                const uint32_t st = smem_u32(smem + L::RING_OFF + size_t(i & 1) * L::STAGE);
+                const uint32_t sp = smem_u32(smem + L::P_OFF + size_t(i & 1) * 2 * L::PANEL);
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const uint64_t da = tc::desc_sw128_kmajor(sp + uint32_t(p * L::PANEL));
+                    const uint64_t db = tc::desc_sw128_kmajor(st + uint32_t((2 + p) * L::PANEL));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_bf16(tmem + 256, da + 2u * kk, db + 2u * kk, idesc, i > 0 || p > 0 || kk > 0);
+                }
+                tc::mma_commit(&odone[i & 1]);
+                tc::mma_commit(&empty[i & 1]);
+                return true;
+            };
+            for (int i = 0; i < nblk && ok; ++i) {
+                const int s = i & 1;
+                if (i >= 2 && !mbar_wait_bounded(&sfree[s], uint32_t((i >> 1) - 1) & 1u, a.status)) break;
+                if (!mbar_wait_bounded(&full[s], uint32_t(i >> 1) & 1u, a.status)) break;
+                tc::fence_after_sync();
+                const uint32_t st = smem_u32(smem + L::RING_OFF + size_t(s) * L::STAGE);
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {  // S_i = Q K_i^T over the two 64-wide d panels
+                    const uint64_t da = tc::desc_sw128_kmajor(sq + uint32_t(p * L::PANEL));
+                    const uint64_t db = tc::desc_sw128_kmajor(st + uint32_t(p * L::PANEL));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_bf16(tmem + uint32_t(s * AT_BN), da + 2u * kk, db + 2u * kk, idesc, p > 0 || kk > 0);
+                }
+                tc::mma_commit(&sfull[s]);
+                if (i >= 1 && !pv(i - 1)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (ok) pv(nblk - 1);
+        }
+    } else {
+        // softmax warps 2..9: one query row per pair of threads (TMEM lane = row in the
+        // tile); `half` takes keys [64 half, 64 half + 64) of every block and the same
+        // columns of O. The halves agree on the running maximum through shared memory.
+        const int quarter = warp & 3, half = (warp - 2) >> 2;
+        const int rt = quarter * 32 + lane;                 // row in the tile
+        const int R = mt * AT_BM + rt;                      // row in the group
+        const bool real = R < a.rows;
+        const int hg = real ? R / a.S : 0, j = real ? R - hg * a.S : 0;
+        const int nn = a.n_nodes[c];
+        const bool live = real && j < nn;
+        const uint32_t trow = tmem + (uint32_t(quarter * 32) << 16);
+        const uint32_t col0 = uint32_t(half * 64);          // this thread's key / O columns
+        const float sl2 = 1.4426950408889634f / sqrtf(float(AT_D));  // log2(e) / sqrt(D)
+        float* xch = reinterpret_cast<float*>(smem + L::XCH_OFF);
+        auto ex2 = [](float x) {
+            float y;
+            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+            return y;
+        };
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int i = 0; i < nblk; ++i) {
+            const int s = i & 1, b = b0 + i;
+            ok = ok && __all_sync(0xffffffffu, mbar_wait_bounded(&sfull[s], uint32_t(i >> 1) & 1u, a.status));
+            // visibility of this thread's 64 keys as a bit mask
+            uint64_t vis = 0;
+            if (live) {
+                if (b < nbp) {
+                    const int nv = min(max(nctx - b * AT_BN - int(col0), 0), 64);
+                    vis = nv >= 64 ? ~0ull : ((1ull << nv) - 1ull);
+                } else {
+                    const uint8_t* mrow = a.mask + (size_t(c) * a.S + j) * a.S + col0;
+                    const int nv = min(max(a.S - int(col0), 0), 64);
+                    for (int q = 0; q < nv; ++q) vis |= uint64_t(mrow[q] != 0) << q;
+                }
+            }
+            // pass 1: this half's maximum of the raw scores over the visible keys
+            float mx = -INFINITY;
+            if (ok) {
+                tc::fence_after_sync();
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 32) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(trow + uint32_t(s * AT_BN) + col0 + uint32_t(c0), v);
+                    const uint32_t bits = uint32_t(vis >> c0);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, (bits >> e) & 1u ? __uint_as_float(v[e]) : -INFINITY);
+                }
+            }
+            xch[half * 128 + rt] = mx;  // (the second barrier: read before the next block writes)
+            asm volatile("bar.sync 2, %0;" :: "n"(AT_SMX) : "memory");
+            mx = fmaxf(mx, xch[(half ^ 1) * 128 + rt]);
+            asm volatile("bar.sync 2, %0;" :: "n"(AT_SMX) : "memory");
+            mx = mx > -INFINITY ? mx * sl2 : mx;
+            // a new running maximum (beyond the slack) rescales O and the sums; that
+            // needs the previous P V^T complete. TMEM accesses are warp-wide: lanes
+            // without a new maximum scale by 1.
+            const bool grow = ok && mx > m_used + AT_RESCALE;
+            const float f = grow && m_used > -INFINITY ? exp2f(m_used - mx) : 1.0f;
+            if (i >= 1 && __any_sync(0xffffffffu, grow && m_used > -INFINITY)) {
+                ok = ok && __all_sync(0xffffffffu, mbar_wait_bounded(&odone[(i - 1) & 1], uint32_t((i - 1) >> 1) & 1u,
+                                                                     a.status));
+                if (ok) {
+                    tc::fence_after_sync();
+#pragma unroll 1
+                    for (int c0 = 0; c0 < 64; c0 += 32) {
+                        uint32_t v[32];
+                        tc::tmem_ld32(trow + 256u + col0 + uint32_t(c0), v);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
+                        tc::tmem_st32(trow + 256u + col0 + uint32_t(c0), v);
+                    }
+                }
+            }
+            if (grow) {
+                l *= f;
+                m_used = mx;
+            }
+            // P buffer s was last read by P_(i-2) V^T
+            if (i >= 2)
+                ok = ok && __all_sync(0xffffffffu, mbar_wait_bounded(&odone[s], uint32_t((i - 2) >> 1) & 1u, a.status));
+            // pass 2: P = 2^(s sl2 - m) in bf16 into the operand layout (panel `half` of
+            // buffer s); the sum of the unrounded weights
+            if (ok) {
+                uint8_t* pan = smem + L::P_OFF + size_t(s) * 2 * L::PANEL + size_t(half) * L::PANEL;
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 32) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(trow + uint32_t(s * AT_BN) + col0 + uint32_t(c0), v);
+                    const uint32_t bits = uint32_t(vis >> c0);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float p0 = (bits >> e) & 1u ? ex2(fmaf(__uint_as_float(v[e]), sl2, -m_used)) : 0.f;
+                        const float p1 =
+                            (bits >> (e + 1)) & 1u ? ex2(fmaf(__uint_as_float(v[e + 1]), sl2, -m_used)) : 0.f;
+                        l += p0 + p1;
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                        pk[e / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4*>(pan + sw128_off(rt, c0 / 8 + q)) =
+                            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
+                tc::fence_before_sync();
+                fence_proxy_async_smem();  // P (generic stores) before the tensor core reads it
+            }
+            __syncwarp();
+            if (lane == 0 && ok) {
+                mbar_arrive(&sfree[s]);
+                mbar_arrive(&pfull[s]);
+            }
+        }
+        // the row's total sum: both halves
+        xch[half * 128 + rt] = l;
+        asm volatile("bar.sync 2, %0;" :: "n"(AT_SMX) : "memory");
+        l += xch[(half ^ 1) * 128 + rt];
+        // the last block's P V^T, then the row out (this half's 64 columns)
+        if (nblk > 0)
+            ok = ok && __all_sync(0xffffffffu, mbar_wait_bounded(&odone[(nblk - 1) & 1], uint32_t((nblk - 1) >> 1) & 1u,
+                                                                 a.status));
+        const bool has = ok && nblk > 0 && l > 0.f;
+        if (ok && nblk > 0) tc::fence_after_sync();
+        const int h = g * a.grp + hg;
+        if (a.nchunk == 1) {  // (TMEM loads warp-wide; padding rows load and drop)
+            uint4* dst = reinterpret_cast<uint4*>(a.out + ((size_t(c) * a.S + j) * a.Hq + h) * AT_D + col0);
+            const float inv = has ? 1.0f / l : 0.f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                uint32_t v[32];
+                if (ok && nblk > 0) tc::tmem_ld32(trow + 256u + col0 + uint32_t(c0), v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = has && live ? pack_bf16x2(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv)
+                                        : 0u;
+                if (real)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dst[c0 / 8 + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
+        } else {
+            const size_t pr = ((size_t(cg) * gridDim.y + mt) * a.nchunk + chunk) * AT_BM + rt;
+            float4* dst = reinterpret_cast<float4*>(a.part_o + pr * AT_D + col0);
+#pragma unroll 1
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                uint32_t v[32];
+                if (ok && nblk > 0) tc::tmem_ld32(trow + 256u + col0 + uint32_t(c0), v);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    dst[c0 / 4 + q] = has ? make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                        __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]))
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            if (half == 0) {
+                a.part_ml[pr * 2] = has ? m_used : -INFINITY;
+                a.part_ml[pr * 2 + 1] = has ? l : 0.f;
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) tc::tmem_dealloc(tmem, 512);
+}
+
+// ----------------------------------------------------------------------------- combine
+
+// One warp per (request, group, tile row): merge the chunks' partials and write
+// the row's output (bf16), zero for padding-free unused slots.
+__global__ void __launch_bounds__(256) attn_combine_kernel(AtArgs a, int mtiles) {
+    const int w = int(blockIdx.x) * 8 + int(threadIdx.x >> 5), lane = threadIdx.x & 31;
+    const int total = a.C * a.Hkv * mtiles * AT_BM;
+    griddep_wait();
+    if (w >= total) return;
+    const int rt = w % AT_BM, mt = (w / AT_BM) % mtiles, cg = w / (AT_BM * mtiles);
+    const int R = mt * AT_BM + rt;
+    if (R >= a.rows) return;
+    const int c = cg / a.Hkv, g = cg - c * a.Hkv;
+    const int hg = R / a.S, j = R - hg * a.S, h = g * a.grp + hg;
+    const bool live = j < a.n_nodes[c];
+    float mmax = -INFINITY;
+    for (int k = 0; k < a.nchunk; ++k) {
+        const size_t pr = ((size_t(cg) * mtiles + mt) * a.nchunk + k) * AT_BM + rt;
+        if (a.part_ml[pr * 2 + 1] > 0.f) mmax = fmaxf(mmax, a.part_ml[pr * 2]);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lsum = 0.f;
+    if (live && mmax > -INFINITY)
+        for (int k = 0; k < a.nchunk; ++k) {
+            const size_t pr = ((size_t(cg) * mtiles + mt) * a.nchunk + k) * AT_BM + rt;
+            const float lk = a.part_ml[pr * 2 + 1];
+            if (!(lk > 0.f)) continue;
+            const float f = exp2f(a.part_ml[pr * 2] - mmax);
+            const float4 o = reinterpret_cast<const float4*>(a.part_o + pr * AT_D)[lane];
+            acc.x += f * o.x;
+            acc.y += f * o.y;
+            acc.z += f * o.z;
+            acc.w += f * o.w;
+            lsum += f * lk;
+        }
+    const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+    uint2 pk = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    reinterpret_cast<uint2*>(a.out + ((size_t(c) * a.S + j) * a.Hq + h) * AT_D)[lane] = pk;
+}
+
+// ----------------------------------------------------------------------------- host
+
+bool attn_supported(int C, int S, int Hq, int Hkv, int D, int N) {
+    return C >= 0 && S >= 1 && S <= AT_BN && Hkv >= 1 && Hq >= Hkv && Hq % Hkv == 0 && D == AT_D && N >= 0 &&
+           N % 8 == 0 && (Hq / Hkv) * S <= AT_MAXMT * AT_BM;
+}
+
+static int attn_mtiles(int S, int grp) { return (grp * S + AT_BM - 1) / AT_BM; }
+
+AttnPlan attn_plan(int C, int S, int Hq, int Hkv, int N) {
+    AttnPlan p{};
+    const int grp = Hq / Hkv, mt = attn_mtiles(S, grp);
+    const int blocks = (N + AT_BN - 1) / AT_BN + 1;  // most prefix blocks + the tree block
+    const long base = long(C) * Hkv * mt;
+    int want = base > 0 ? int((2L * num_sms() + base - 1) / base) : 1;
+    if (want < 1) want = 1;
+    if (want > blocks) want = blocks;
+    p.per = (blocks + want - 1) / want;
+    p.nchunk = (blocks + p.per - 1) / p.per;
+    p.mtiles = mt;
+    size_t off = 256;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += (bytes + 255) / 256 * 256;
+        return o;
+    };
+    p.qr = take(size_t(C) * Hkv * grp * S * AT_D * 2);
+    p.kt = take(size_t(C) * Hkv * AT_BN * AT_D * 2);
+    p.vtt = take(size_t(C) * Hkv * AT_D * AT_BN * 2);
+    if (p.nchunk > 1) {
+        p.part_o = take(size_t(C) * Hkv * mt * p.nchunk * AT_BM * AT_D * 4);
+        p.part_ml = take(size_t(C) * Hkv * mt * p.nchunk * AT_BM * 2 * 4);
+    }
+    p.total = off;
+    return p;
+}
+
+int launch_tree_attention(int C, int S, int Hq, int Hkv, int N, double theta, const void* q, const void* k_tree,
+                          const void* v_tree, const void* k_cache, const void* vt_cache, const int32_t* n_ctx,
+                          const uint8_t* mask, const int32_t* pos, const int32_t* n_nodes, void* out, void* ws,
+                          const AttnPlan& pl, cudaStream_t stream) {
+    if (C == 0) return DARTREE_OK;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    int* status = reinterpret_cast<int*>(w);
+    uint16_t* Qr = reinterpret_cast<uint16_t*>(w + pl.qr);
+    uint16_t* Kt = reinterpret_cast<uint16_t*>(w + pl.kt);
+    uint16_t* Vtt = reinterpret_cast<uint16_t*>(w + pl.vtt);
+    const int grp = Hq / Hkv;
+    {
+        KTimer kt_(KID_ATTN_PREP, stream);
+        attn_prep_kernel<<<dim3(AT_BN, C), 128, 0, stream>>>(
+            static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k_tree), static_cast<const uint16_t*>(v_tree),
+            n_ctx, pos, n_nodes, S, Hq, Hkv, theta, Qr, Kt, Vtt);
+    }
+    if (cudaGetLastError() != cudaSuccess) return DARTREE_ECUDA;
+    CUtensorMap tq, tk, tvt, tkt, tvtt;
+    const int rows = grp * S;
+    // an empty cache (N = 0) still needs valid maps: point them at the tree block
+    const bool cache = N > 0;
+    if (!make_tensor_map_bf16(&tq, Qr, C * Hkv * rows, AT_D, 64, AT_BM, 128) ||
+        !make_tensor_map_bf16(&tk, cache ? k_cache : Kt, cache ? C * Hkv * N : C * Hkv * AT_BN, AT_D, 64, AT_BN,
+                              128) ||
+        !make_tensor_map_bf16(&tvt, cache ? vt_cache : Vtt, C * Hkv * AT_D, cache ? N : AT_BN, 64, AT_D, 128) ||
+        !make_tensor_map_bf16(&tkt, Kt, C * Hkv * AT_BN, AT_D, 64, AT_BN, 128) ||
+        !make_tensor_map_bf16(&tvtt, Vtt, C * Hkv * AT_D, AT_BN, 64, AT_D, 128))
+        return DARTREE_ECUDA;
+    AtArgs a{C, S, Hq, Hkv, N, grp, rows, pl.nchunk, pl.per, n_ctx, mask, n_nodes, static_cast<uint16_t*>(out),
+             pl.nchunk > 1 ? reinterpret_cast<float*>(w + pl.part_o) : nullptr,
+             pl.nchunk > 1 ? reinterpret_cast<float*>(w + pl.part_ml) : nullptr, status};
+    const size_t smem = AtSmem::TOTAL;
+    if (cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+        return DARTREE_ECUDA;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(pl.nchunk, pl.mtiles, C * Hkv);
+    cfg.blockDim = dim3(AT_NT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    {
+        KTimer kt_(KID_ATTN, stream);
+        e = cudaLaunchKernelEx(&cfg, attn_kernel, tq, tk, tvt, tkt, tvtt, a);
+    }
+    if (e != cudaSuccess) return DARTREE_ECUDA;
+    if (pl.nchunk > 1) {
+        const int warps = C * Hkv * pl.mtiles * AT_BM;
+        cudaLaunchConfig_t c2{};
+        c2.gridDim = dim3((warps + 7) / 8);
+        c2.blockDim = dim3(256);
+        c2.stream = stream;
+        c2.attrs = attr;
+        c2.numAttrs = 1;
+        {
+            KTimer kt_(KID_ATTN_COMBINE, stream);
+            e = cudaLaunchKernelEx(&c2, attn_combine_kernel, a, pl.mtiles);
+        }
+        if (e != cudaSuccess) return DARTREE_ECUDA;
+    }
+    return DARTREE_OK;
+}
+
+}  // namespace dartree

@@ -248,6 +248,46 @@ DARTREE_API int dartree_lm_head_topk(const void* hidden, const void* W_lm, int R
                                      int dtype, int32_t* tok, float* val, void* ws, size_t ws_bytes,
                                      void* stream);
 
+/* One attention layer of the target's verification pass over the pruned tree
+ * (DARTree blog post, "3.2": all drafted tokens are checked in one target pass with
+ * a tree-attention mask). Slot j of request c, query head h, attends to the c-th
+ * request's n_ctx[c] cached keys and to the tree slots tree->mask[c, j, :] marks
+ * (ancestor-or-self, S9), with rotary embedding at position n_ctx[c] + tree->pos[c, j]
+ * (pos = depth, S9) applied to the tree's queries and keys:
+ *   x'_i = x_i cos a_i - x_(i+D/2) sin a_i,  x'_(i+D/2) = x_(i+D/2) cos a_i + x_i sin a_i,
+ *   a_i = position * theta^(-2i/D), i < D/2;
+ * query head h reads key/value head h / (Hq / Hkv); scores are scaled by 1/sqrt(D).
+ * All tensors bf16, row-major, 16-byte aligned:
+ *   q         [C, S, Hq, D]    the tree's queries (unrotated)
+ *   k_tree    [C, S, Hkv, D]   the tree's keys (unrotated)
+ *   v_tree    [C, S, Hkv, D]   the tree's values
+ *   k_cache   [C, Hkv, N, D]   cached keys (already rotated), position = row
+ *   vt_cache  [C, Hkv, D, N]   cached values stored transposed (one head's keys
+ *                              contiguous per dimension: the operand layout of P V)
+ *   n_ctx     [C] int32        cached length of each request, 0..N (clamped to it);
+ *                              cache entries past it are not used but must be finite
+ *   tree      S9 output: mask [C, S, S], pos [C, S], n_nodes [C] are read
+ *   out       [C, S, Hq, D]    output rows (zero for slots j >= n_nodes[c])
+ * Scores and sums in fp32; probabilities are rounded to bf16 for the P V product.
+ * Limits (DARTREE_EUNSUPPORTED): D = 128, S <= 128, Hq a multiple of Hkv,
+ * (Hq / Hkv) * S <= 384, N a multiple of 8, theta > 0. Workspace:
+ * dartree_tree_attention_workspace_bytes (rotated tree operands and, for small
+ * batches, the partial results of the key-block chunks run in parallel). */
+typedef struct {
+    int C;        /* requests */
+    int S;        /* tree slots per request (B + 1) */
+    int Hq, Hkv;  /* query heads, key/value heads */
+    int D;        /* head dimension */
+    int N;        /* cache capacity per request and head */
+    float theta;  /* rotary base */
+} dartree_attn_params;
+
+DARTREE_API size_t dartree_tree_attention_workspace_bytes(const dartree_attn_params* p);
+DARTREE_API int dartree_tree_attention(const dartree_attn_params* p, const void* q, const void* k_tree,
+                                       const void* v_tree, const void* k_cache, const void* vt_cache,
+                                       const int32_t* n_ctx, const dartree_tree* tree, void* out, void* ws,
+                                       size_t ws_bytes, void* stream);
+
 /* Node budget and width for a batch of C concurrent requests (DARTree blog post,
  * section 4.4: at concurrency 4 the budget B shrinks from 64 to 32 and the width W
  * from 12 to 3; at concurrency 1 and 2 the defaults run). Reading: the reduced pair

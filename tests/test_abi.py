@@ -140,3 +140,29 @@ def test_lm_head_arguments_are_checked_on_the_host(L):
     small = L.dartree_lm_head_workspace_bytes(16, 1000, 128, 8)
     assert f(fake, fake, 16, 1000, 128, 8, dd.BF16, fake, fake, ws_ok, small - 8, None) == dd.EWORKSPACE
     assert f(fake, fake, 0, 1000, 128, 8, dd.BF16, fake, fake, ws_ok, 0, None) == dd.OK
+
+
+def test_tree_attention_limits_are_checked_on_the_host(L):
+    import diffusion_drafter_draft_gb300 as dd
+    P = dd.AttnParams
+    ws = L.dartree_tree_attention_workspace_bytes
+    assert ws(ctypes.byref(P(1, 65, 32, 8, 128, 2048, 1e6))) > 0
+    assert ws(ctypes.byref(P(1, 65, 32, 8, 64, 2048, 1e6))) == 0     # D != 128
+    assert ws(ctypes.byref(P(1, 129, 4, 2, 128, 2048, 1e6))) == 0    # S > 128
+    assert ws(ctypes.byref(P(1, 65, 32, 4, 128, 2048, 1e6))) == 0    # 8 heads x 65 slots > 384 rows
+    assert ws(ctypes.byref(P(1, 65, 30, 8, 128, 2048, 1e6))) == 0    # Hq not a multiple of Hkv
+    assert ws(ctypes.byref(P(1, 65, 32, 8, 128, 2047, 1e6))) == 0    # N % 8
+    assert ws(ctypes.byref(P(1, 65, 32, 8, 128, 2048, 0.0))) == 0    # theta
+    fake = ctypes.c_void_p(256)
+    tree = dd.Tree(None, None, None, None, 256, 256, 256)
+    p = P(1, 65, 32, 8, 128, 2048, 1e6)
+    need = ws(ctypes.byref(p))
+    f = L.dartree_tree_attention
+    args = [fake] * 6
+    assert f(ctypes.byref(P(1, 65, 32, 8, 64, 2048, 1e6)), *args, ctypes.byref(tree), fake, ctypes.c_void_p(1 << 20),
+             need, None) == dd.EUNSUPPORTED
+    assert f(ctypes.byref(p), ctypes.c_void_p(264), *args[1:], ctypes.byref(tree), fake, ctypes.c_void_p(1 << 20),
+             need, None) == dd.EINVAL                                  # q not 16-byte aligned
+    assert f(ctypes.byref(p), *args, ctypes.byref(tree), fake, ctypes.c_void_p(1 << 20), need - 256, None) \
+        == dd.EWORKSPACE
+    assert f(ctypes.byref(P(0, 65, 32, 8, 128, 2048, 1e6)), *args, ctypes.byref(tree), fake, None, 0, None) == dd.OK
