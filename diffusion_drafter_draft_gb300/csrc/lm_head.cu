@@ -13,10 +13,12 @@
 // (ord(logit) << 32 | ~token) above the row's current threshold. A buffer that
 // could overflow with the next tile is sorted and cut to its K best first (the
 // threshold becomes its K-th key; the cut is a radix selection in registers). At
-// the end each row's buffer is cut to its K best and written out: K keys per
-// (row, CTA), in no particular order.
-// Launch 2 (lmhead_merge_kernel, one CTA per row): radix selection of the K
-// largest keys among the row's CTA lists, sorted, written as (token, logit).
+// the end each row's buffer is cut to its K best, sorted and written out: K keys
+// per (row, CTA), largest first.
+// Launch 2 (lmhead_merge_kernel, one CTA per row): the K largest keys among the
+// row's CTA lists, sorted, written as (token, logit). Only keys at or above the
+// K-th largest list maximum can qualify; when those are few they are sorted
+// directly, else a radix selection over all the lists runs.
 // Keys are distinct (the token is in the low bits), so the result is the exact
 // top-K of the fp32 logits under (logit desc, token asc).
 // Every mbarrier wait is bounded; a wait that runs out records DARTREE_ETIMEOUT.
@@ -336,6 +338,14 @@ __global__ void __launch_bounds__(LM_NT, 1) lmhead_topk_kernel(const __grid_cons
         for (int r = ew; r < a.R; r += 4) {
             uint64_t* buf = cand + size_t(r) * LM_CAP;
             cut_row(buf, &cnt[r], &thr[r], a.K, hists + ew * 256);
+            {  // the list sorted (descending): the merge reads each list's maximum first
+                const int n = cnt[r];
+                int p = 32;
+                while (p < a.K) p <<= 1;
+                for (int q = n + lane; q < p; q += 32) buf[q] = 0ull;
+                __syncwarp();
+                warp_sort_desc(buf, p);
+            }
             unsigned long long* dst = a.part + (size_t(r) * G + b) * a.K;
             for (int k = lane; k < a.K; k += 32) dst[k] = k < cnt[r] ? buf[k] : 0ull;
         }
@@ -357,24 +367,72 @@ __global__ void __launch_bounds__(LMM_NT) lmhead_merge_kernel(const unsigned lon
     uint64_t* keys = reinterpret_cast<uint64_t*>(smem);      // [n]
     uint32_t* hist = reinterpret_cast<uint32_t*>(keys + n);  // [256]
     uint64_t* sel = reinterpret_cast<uint64_t*>(hist + 256); // [LM_CAP] (K <= LM_MAXK)
-    __shared__ uint32_t s_digit, s_need, s_nsel;
+    __shared__ uint32_t s_digit, s_need, s_inbin, s_nsel;
     const int r = blockIdx.x;
     if (threadIdx.x == 0) {
         s_digit = 0;
         s_need = 1;
+        s_inbin = 0;
     }
+    __shared__ uint64_t s_lb;
     griddep_wait();
     for (int i = threadIdx.x; i < n; i += LMM_NT) keys[i] = part[size_t(r) * n + i];
-    // radix selection of the K-th largest key, 8 bits at a time from the top;
-    // prefix/pmask: the bits fixed so far
+    __syncthreads();
+    // Every list is sorted, so its first key is its maximum; with at least K lists, the
+    // K-th largest list maximum is a lower bound of the K-th largest key (K distinct
+    // keys reach it). The keys at or above it are usually few: those are sorted directly.
+    const int G = n / K;
+    if (G >= K && G <= LM_CAP) {
+        if (threadIdx.x == 0) {
+            s_nsel = 0;
+            s_lb = 0;  // (no list maximum of rank K - 1: every key qualifies)
+        }
+        for (int b = threadIdx.x; b < G; b += LMM_NT) sel[b] = keys[b * K];
+        __syncthreads();
+        if (int(threadIdx.x) < G) {  // the list maximum of rank K - 1 (keys distinct)
+            const uint64_t m = sel[threadIdx.x];
+            int rank = 0;
+            for (int b = 0; b < G; ++b) rank += sel[b] > m ? 1 : 0;
+            if (rank == K - 1) s_lb = m;
+        }
+        __syncthreads();
+        const uint64_t lb = s_lb;
+        for (int b = threadIdx.x; b < G; b += LMM_NT)
+            for (int k = 0; k < K && keys[b * K + k] >= lb; ++k) {
+                const uint32_t at = atomicAdd(&s_nsel, 1u);
+                if (at < uint32_t(LM_CAP)) sel[at] = keys[b * K + k];
+            }
+        __syncthreads();
+        const uint32_t nsel = s_nsel;
+        if (nsel <= uint32_t(LM_CAP)) {  // each candidate's rank is its output position
+            if (threadIdx.x < nsel) {
+                const uint64_t key = sel[threadIdx.x];
+                int rank = 0;
+                for (uint32_t q = 0; q < nsel; ++q) rank += sel[q] > key ? 1 : 0;
+                if (rank < K) {
+                    tok[size_t(r) * K + rank] = int32_t(0xffffffffu - uint32_t(key));
+                    val[size_t(r) * K + rank] = f32_from_ord(uint32_t(key >> 32));
+                }
+            }
+            return;
+        }
+        __syncthreads();
+    }
+    // otherwise: radix selection of the K-th largest key, 8 bits at a time from the top;
+    // prefix/pmask: the bits fixed so far. It stops at the first digit whose bin holds
+    // exactly the keys still needed.
     uint64_t prefix = 0, pmask = 0;
     uint32_t need = uint32_t(K);
     for (int shift = 56; shift >= 0; shift -= 8) {
         for (int i = threadIdx.x; i < 256; i += LMM_NT) hist[i] = 0;
         __syncthreads();
-        for (int i = threadIdx.x; i < n; i += LMM_NT) {
-            const uint64_t k = keys[i];
-            if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 0xffu], 1u);
+        for (int i0 = 0; i0 < n; i0 += LMM_NT) {  // equal digits of a warp add once
+            const int i = i0 + int(threadIdx.x);
+            const uint64_t k = i < n ? keys[i] : 0ull;
+            const bool in = i < n && (k & pmask) == prefix;
+            const uint32_t d = in ? uint32_t(k >> shift) & 0xffu : 0x100u;
+            const uint32_t same = __match_any_sync(0xffffffffu, d);
+            if (in && (threadIdx.x & 31) == uint32_t(__ffs(same) - 1)) atomicAdd(&hist[d], uint32_t(__popc(same)));
         }
         __syncthreads();
         if (threadIdx.x < 32) {  // the digit where the count from the top reaches `need`
@@ -399,6 +457,7 @@ __global__ void __launch_bounds__(LMM_NT) lmhead_merge_kernel(const unsigned lon
                     if (run + c[j] >= need) {
                         s_digit = uint32_t(255 - 8 * lane - j);
                         s_need = need - run;
+                        s_inbin = c[j];
                         break;
                     }
                     run += c[j];
@@ -409,14 +468,16 @@ __global__ void __launch_bounds__(LMM_NT) lmhead_merge_kernel(const unsigned lon
         prefix |= uint64_t(s_digit) << shift;
         pmask |= uint64_t(0xffu) << shift;
         need = s_need;
+        const bool whole = s_inbin == s_need;  // every key of the bin is kept
         __syncthreads();
+        if (whole) break;
     }
-    // prefix is now the K-th largest key: take every key >= it (exactly K, keys distinct)
+    // keep every key at or above the prefix in the fixed bits (exactly K, keys distinct)
     if (threadIdx.x == 0) s_nsel = 0;
     __syncthreads();
     for (int i = threadIdx.x; i < n; i += LMM_NT) {
         const uint64_t k = keys[i];
-        if (k >= prefix) {
+        if ((k & pmask) >= prefix) {
             const uint32_t at = atomicAdd(&s_nsel, 1u);
             if (at < uint32_t(LM_CAP)) sel[at] = k;  // exactly K unless the lists were not written
         }

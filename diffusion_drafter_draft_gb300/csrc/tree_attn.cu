@@ -6,11 +6,12 @@
 //   (ancestor-or-self, from S9), with rotary embedding at position n_ctx + pos[c, j]
 //   (pos = depth, from S9); scores scaled by 1 / sqrt(D).
 //
-// Launch 1 (attn_prep_kernel, one CTA per (request, slot of a 128-slot block)):
-//   rotates the tree's queries and keys (angles in double precision), writing
-//   Qr [C, Hkv, grp*S, D] (row hg*S + j: the grp query heads of a group stacked),
-//   Kt [C, Hkv, 128, D] and the tree values transposed, Vtt [C, Hkv, D, 128];
-//   unused and padding slots are zero.
+// Launches 1-2 (attn_prep_kernel, one CTA per (slot of a 128-slot block, request);
+//   attn_vt_kernel, one CTA per (request, key/value head)): rotate the tree's queries
+//   and keys (angles reduced in double precision), writing Qr [C, Hkv, grp*S, D]
+//   (row hg*S + j: the grp query heads of a group stacked) and Kt [C, Hkv, 128, D],
+//   and transpose the tree's values, Vtt [C, Hkv, D, 128]; unused and padding
+//   slots are zero.
 // Launch 2 (attn_kernel, CTA = (chunk of key blocks, 128-row tile of a group's
 //   query rows, (request, group))): warp 0 loads the query tile and, per 128-key
 //   block, the keys and transposed values with TMA (128-byte swizzle) into a
@@ -75,44 +76,95 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 
 // ----------------------------------------------------------------------------- prep
 
-__global__ void __launch_bounds__(128) attn_prep_kernel(const uint16_t* __restrict__ q,
-                                                        const uint16_t* __restrict__ kt,
-                                                        const uint16_t* __restrict__ vt, const int32_t* n_ctx,
-                                                        const int32_t* pos, const int32_t* n_nodes, int S, int Hq,
-                                                        int Hkv, double theta, uint16_t* __restrict__ Qr,
-                                                        uint16_t* __restrict__ Kr, uint16_t* __restrict__ Vtt) {
+// Rotary inverse frequencies theta^(-2i/D), i < D/2, computed once on the host in double.
+struct RopeFreq {
+    double inv[AT_D / 2];
+};
+
+// One CTA per (slot of a 128-slot block, request). The slot's D/2 rotation angles
+// (position * inv_freq_i, reduced to [-pi, pi] in double; sine and cosine in float)
+// go to shared memory; then 8 threads per head unit rotate 8 pairs (i, i + D/2) each
+// with 16-byte loads and stores. Head units: the Hq query heads, then the Hkv key heads.
+constexpr int AT_PREP_NT = 256;
+
+__global__ void __launch_bounds__(AT_PREP_NT) attn_prep_kernel(
+    const uint16_t* __restrict__ q, const uint16_t* __restrict__ kt, const int32_t* n_ctx, const int32_t* pos,
+    const int32_t* n_nodes, int S, int Hq, int Hkv, const __grid_constant__ RopeFreq fr, uint16_t* __restrict__ Qr,
+    uint16_t* __restrict__ Kr) {
     __shared__ float cs[AT_D / 2], sn[AT_D / 2];
-    const int c = blockIdx.y, j = blockIdx.x;  // j in [0, 128)
-    const int grp = Hq / Hkv;
+    const int j = blockIdx.x, c = blockIdx.y;
+    const int grp = Hq / Hkv, half = AT_D / 2;
     const bool used = j < S && j < n_nodes[c];
-    if (used && threadIdx.x < AT_D / 2) {
+    if (used && threadIdx.x < half) {
         const int i = threadIdx.x;
         const double p = double(n_ctx[c]) + double(pos[size_t(c) * S + j]);
-        const double a = p * pow(theta, -2.0 * double(i) / double(AT_D));
-        double s_, c_;
-        sincos(a, &s_, &c_);
-        cs[i] = float(c_);
-        sn[i] = float(s_);
+        const double a = p * fr.inv[i];
+        const double k = rint(a * 0.15915494309189535);           // 1 / (2 pi)
+        const float r = float(fma(-k, 6.283185307179586, a));    // 2 pi
+        sincosf(r, &sn[i], &cs[i]);
     }
     __syncthreads();
-    const int d = threadIdx.x;  // 0..127
-    const int dp = d < AT_D / 2 ? d + AT_D / 2 : d - AT_D / 2;
-    auto rot = [&](const uint16_t* x) -> uint16_t {  // x: one head's D values
-        const float v = bf16_bits_to_float(x[d]), w = bf16_bits_to_float(x[dp]);
-        const int i = d < AT_D / 2 ? d : d - AT_D / 2;
-        const float r = d < AT_D / 2 ? v * cs[i] - w * sn[i] : v * cs[i] + w * sn[i];
-        return __bfloat16_as_ushort(__float2bfloat16_rn(r));
-    };
-    if (j < S)
-        for (int h = 0; h < Hq; ++h) {
-            const int g = h / grp, hg = h - g * grp;
-            uint16_t* dst = Qr + ((size_t(c) * Hkv + g) * (size_t(grp) * S) + size_t(hg) * S + j) * AT_D;
-            dst[d] = used ? rot(q + ((size_t(c) * S + j) * Hq + h) * AT_D) : uint16_t(0);
+    const int t = threadIdx.x & 7, i0 = t * 8;  // pairs i0 .. i0 + 7
+    for (int u = threadIdx.x >> 3; u < Hq + Hkv; u += AT_PREP_NT / 8) {
+        if (u < Hq && j >= S) continue;  // query rows exist for real slots only
+        const uint16_t* src;
+        uint16_t* dst;
+        if (u < Hq) {
+            const int g = u / grp, hg = u - g * grp;
+            src = q + ((size_t(c) * S + j) * Hq + u) * AT_D;
+            dst = Qr + ((size_t(c) * Hkv + g) * (size_t(grp) * S) + size_t(hg) * S + j) * AT_D;
+        } else {
+            const int g = u - Hq;
+            src = kt + ((size_t(c) * S + j) * Hkv + g) * AT_D;
+            dst = Kr + ((size_t(c) * Hkv + g) * AT_BN + j) * AT_D;
         }
-    for (int g = 0; g < Hkv; ++g) {
-        const size_t src = ((size_t(c) * S + j) * Hkv + g) * AT_D;
-        Kr[((size_t(c) * Hkv + g) * AT_BN + j) * AT_D + d] = used ? rot(kt + src) : uint16_t(0);
-        Vtt[((size_t(c) * Hkv + g) * AT_D + d) * AT_BN + j] = used ? vt[src + d] : uint16_t(0);
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+        if (used) {
+            const uint4 x4 = reinterpret_cast<const uint4*>(src + i0)[0];
+            const uint4 y4 = reinterpret_cast<const uint4*>(src + half + i0)[0];
+            const uint32_t xs[4] = {x4.x, x4.y, x4.z, x4.w}, ys[4] = {y4.x, y4.y, y4.z, y4.w};
+            uint32_t ro[4], rh[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                float a2[2], b2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int i = i0 + 2 * w + e;
+                    const float x = bf16_bits_to_float((xs[w] >> (16 * e)) & 0xffffu);
+                    const float y = bf16_bits_to_float((ys[w] >> (16 * e)) & 0xffffu);
+                    a2[e] = x * cs[i] - y * sn[i];
+                    b2[e] = y * cs[i] + x * sn[i];
+                }
+                ro[w] = pack_bf16x2(a2[0], a2[1]);
+                rh[w] = pack_bf16x2(b2[0], b2[1]);
+            }
+            lo = make_uint4(ro[0], ro[1], ro[2], ro[3]);
+            hi = make_uint4(rh[0], rh[1], rh[2], rh[3]);
+        }
+        reinterpret_cast<uint4*>(dst + i0)[0] = lo;
+        reinterpret_cast<uint4*>(dst + half + i0)[0] = hi;
+    }
+}
+
+// The tree's values transposed, Vtt[c, g, d, j] = v_tree[c, j, g, d] (zero for unused
+// and padding slots): one CTA per (request, key/value head), through a shared tile so
+// that both the reads (along d) and the writes (along j) are contiguous.
+constexpr int AT_VT_PITCH = AT_BN + 2;  // halfwords per tile row
+
+__global__ void __launch_bounds__(256) attn_vt_kernel(const uint16_t* __restrict__ vt, const int32_t* n_nodes, int S,
+                                                      int Hkv, uint16_t* __restrict__ Vtt) {
+    __shared__ uint16_t tile[AT_D][AT_VT_PITCH];  // [d][j]
+    const int cg = blockIdx.x, c = cg / Hkv, g = cg - c * Hkv;
+    const int n = min(S, n_nodes[c]);
+    for (int e = threadIdx.x; e < AT_BN * AT_D; e += 256) {
+        const int j = e / AT_D, d = e - j * AT_D;
+        tile[d][j] = j < n ? vt[((size_t(c) * S + j) * Hkv + g) * AT_D + d] : uint16_t(0);
+    }
+    __syncthreads();
+    uint16_t* dst = Vtt + size_t(cg) * AT_D * AT_BN;
+    for (int e = threadIdx.x; e < AT_D * AT_BN; e += 256) {
+        const int d = e / AT_BN, j = e - d * AT_BN;
+        dst[e] = tile[d][j];
     }
 }
 
@@ -500,11 +552,14 @@ int launch_tree_attention(int C, int S, int Hq, int Hkv, int N, double theta, co
     uint16_t* Kt = reinterpret_cast<uint16_t*>(w + pl.kt);
     uint16_t* Vtt = reinterpret_cast<uint16_t*>(w + pl.vtt);
     const int grp = Hq / Hkv;
+    RopeFreq fr;
+    for (int i = 0; i < AT_D / 2; ++i) fr.inv[i] = pow(theta, -2.0 * double(i) / double(AT_D));
     {
         KTimer kt_(KID_ATTN_PREP, stream);
-        attn_prep_kernel<<<dim3(AT_BN, C), 128, 0, stream>>>(
-            static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k_tree), static_cast<const uint16_t*>(v_tree),
-            n_ctx, pos, n_nodes, S, Hq, Hkv, theta, Qr, Kt, Vtt);
+        attn_prep_kernel<<<dim3(AT_BN, C), AT_PREP_NT, 0, stream>>>(
+            static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k_tree), n_ctx, pos, n_nodes, S, Hq, Hkv, fr,
+            Qr, Kt);
+        attn_vt_kernel<<<C * Hkv, 256, 0, stream>>>(static_cast<const uint16_t*>(v_tree), n_nodes, S, Hkv, Vtt);
     }
     if (cudaGetLastError() != cudaSuccess) return DARTREE_ECUDA;
     CUtensorMap tq, tk, tvt, tkt, tvtt;
