@@ -350,7 +350,9 @@ int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int m
     for (int bn : {256, 160, 128}) {
         if (N % bn != 0) continue;
         const long tiles = long(mt) * (N / bn), waves = (tiles + sms - 1) / sms;
-        const long cost = waves * (GT_BM + bn);
+        // mode 1 (per-depth projection) runs beside the other half's contraction:
+        // the operand bytes all its CTAs stream count, not its own span
+        const long cost = mode == 1 ? tiles * (GT_BM + bn) : waves * (GT_BM + bn);
         if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = bn; }
     }
     if (best == 256) return launch_gemm_bn<256>(A, B, M, N, K, o, status, stream, pdl);
