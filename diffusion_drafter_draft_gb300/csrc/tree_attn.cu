@@ -14,8 +14,9 @@
 //   slots are zero.
 // Launch 2 (attn_kernel, CTA = (chunk of key blocks, 128-row tile of a group's
 //   query rows, (request, group))): warp 0 loads the query tile and, per 128-key
-//   block, the keys and transposed values with TMA (128-byte swizzle) into a
-//   two-stage ring; warp 1 issues S = Q K^T into one of two TMEM score buffers and
+//   block, the keys and transposed values with TMA (128-byte swizzle) into two-stage
+//   rings, keys one block ahead of values (a key block is released as soon as its
+//   scores are formed); warp 1 issues S = Q K^T into one of two TMEM score buffers and
 //   O += P V^T into a TMEM accumulator; warps 2-9 (two threads per query row, each
 //   on half of the keys and of O) mask, take the running maximum (log2 domain; O
 //   and the sums are rescaled only when the maximum grows by more than 2^8), write P
@@ -46,13 +47,14 @@ constexpr float AT_RESCALE = 8.0f;  // log2 growth of the maximum that forces a 
 struct AtSmem {
     static constexpr size_t PANEL = size_t(128) * 64 * 2;  // 128 rows x 64 bf16, swizzled
     static constexpr size_t Q_OFF = 0;                      // 2 panels
-    static constexpr size_t RING_OFF = 2 * PANEL;           // 2 stages x (K 2 panels, V^T 2 panels)
+    static constexpr size_t RING_OFF = 2 * PANEL;           // 2 stages x (K 2 panels, V^T 2 panels), K and V
+                                                            // filled and released separately
     static constexpr size_t STAGE = 4 * PANEL;
     static constexpr size_t P_OFF = RING_OFF + 2 * STAGE;   // 2 buffers x 2 panels
     static constexpr size_t XCH_OFF = P_OFF + 4 * PANEL;    // float [2 halves][128 rows]
     static constexpr size_t BAR_OFF = XCH_OFF + 2 * 128 * 4;
-    // qf, full[2], empty[2], sfull[2], sfree[2], pfull[2], odone[2]
-    static constexpr size_t SLOT_OFF = BAR_OFF + 8 * 13;
+    // qf, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], sfree[2], pfull[2], odone[2]
+    static constexpr size_t SLOT_OFF = BAR_OFF + 8 * 17;
     static constexpr size_t TOTAL = SLOT_OFF + 16 + 1024;
 };
 static_assert(AtSmem::TOTAL <= 227 * 1024, "attention tile fits in shared memory");
@@ -185,12 +187,14 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
     uint64_t* qf = bars;
-    uint64_t* full = bars + 1;
-    uint64_t* empty = bars + 3;
-    uint64_t* sfull = bars + 5;
-    uint64_t* sfree = bars + 7;
-    uint64_t* pfull = bars + 9;   // [2]: P written, by P buffer
-    uint64_t* odone = bars + 11;  // [2]: P V^T done, by P buffer
+    uint64_t* kfull = bars + 1;    // [2]: key block landed, by stage
+    uint64_t* kempty = bars + 3;   // [2]: S = Q K^T done with it
+    uint64_t* vfull = bars + 5;    // [2]: value block landed
+    uint64_t* vempty = bars + 7;   // [2]: P V^T done with it
+    uint64_t* sfull = bars + 9;
+    uint64_t* sfree = bars + 11;
+    uint64_t* pfull = bars + 13;   // [2]: P written, by P buffer
+    uint64_t* odone = bars + 15;   // [2]: P V^T done, by P buffer
     uint32_t* slot = reinterpret_cast<uint32_t*>(smem + L::SLOT_OFF);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int chunk = blockIdx.x, mt = blockIdx.y, cg = blockIdx.z;
@@ -203,8 +207,10 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
     if (threadIdx.x == 0) {
         mbar_init(qf, 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&kfull[s], 1);
+            mbar_init(&kempty[s], 1);
+            mbar_init(&vfull[s], 1);
+            mbar_init(&vempty[s], 1);
             mbar_init(&sfull[s], 1);
             mbar_init(&sfree[s], AT_SMX / 32);
             mbar_init(&pfull[s], AT_SMX / 32);
@@ -226,32 +232,56 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
             mbar_arrive_expect_tx(qf, uint32_t(2 * L::PANEL));
             tc::tma_load_2d(smem + L::Q_OFF, &tmQ, 0, qrow, qf);
             tc::tma_load_2d(smem + L::Q_OFF + L::PANEL, &tmQ, 64, qrow, qf);
-            bool ok = true;
-            int i = 0;
-            for (; i < nblk && ok; ++i) {
+            // key blocks run one ahead of value blocks: K_i+1 needs only S_i-1 done,
+            // V_i needs P_i-2 V^T done
+            auto load_k = [&](int i) -> bool {
                 const int s = i & 1, b = b0 + i;
-                if (i >= 2 && !mbar_wait_bounded(&empty[s], uint32_t((i >> 1) & 1) ^ 1u, a.status)) {
-                    ok = false;
-                    break;
-                }
+                if (i >= 2 && !mbar_wait_bounded(&kempty[s], uint32_t((i >> 1) & 1) ^ 1u, a.status)) return false;
                 uint8_t* st = smem + L::RING_OFF + size_t(s) * L::STAGE;
-                mbar_arrive_expect_tx(&full[s], uint32_t(L::STAGE));
-                if (b < nbp) {  // prefix block: K_cache rows, V^T_cache columns
+                mbar_arrive_expect_tx(&kfull[s], uint32_t(2 * L::PANEL));
+                if (b < nbp) {  // prefix block: K_cache rows
                     const int kr = cg * a.N + b * AT_BN;
-                    tc::tma_load_2d(st, &tmK, 0, kr, &full[s]);
-                    tc::tma_load_2d(st + L::PANEL, &tmK, 64, kr, &full[s]);
-                    tc::tma_load_2d(st + 2 * L::PANEL, &tmVt, b * AT_BN, cg * AT_D, &full[s]);
-                    tc::tma_load_2d(st + 3 * L::PANEL, &tmVt, b * AT_BN + 64, cg * AT_D, &full[s]);
+                    tc::tma_load_2d(st, &tmK, 0, kr, &kfull[s]);
+                    tc::tma_load_2d(st + L::PANEL, &tmK, 64, kr, &kfull[s]);
                 } else {        // the tree block
-                    tc::tma_load_2d(st, &tmKt, 0, cg * AT_BN, &full[s]);
-                    tc::tma_load_2d(st + L::PANEL, &tmKt, 64, cg * AT_BN, &full[s]);
-                    tc::tma_load_2d(st + 2 * L::PANEL, &tmVtt, 0, cg * AT_D, &full[s]);
-                    tc::tma_load_2d(st + 3 * L::PANEL, &tmVtt, 64, cg * AT_D, &full[s]);
+                    tc::tma_load_2d(st, &tmKt, 0, cg * AT_BN, &kfull[s]);
+                    tc::tma_load_2d(st + L::PANEL, &tmKt, 64, cg * AT_BN, &kfull[s]);
+                }
+                return true;
+            };
+            auto load_v = [&](int i) -> bool {
+                const int s = i & 1, b = b0 + i;
+                if (i >= 2 && !mbar_wait_bounded(&vempty[s], uint32_t((i >> 1) & 1) ^ 1u, a.status)) return false;
+                uint8_t* st = smem + L::RING_OFF + size_t(s) * L::STAGE + 2 * L::PANEL;
+                mbar_arrive_expect_tx(&vfull[s], uint32_t(2 * L::PANEL));
+                if (b < nbp) {  // V^T_cache columns
+                    tc::tma_load_2d(st, &tmVt, b * AT_BN, cg * AT_D, &vfull[s]);
+                    tc::tma_load_2d(st + L::PANEL, &tmVt, b * AT_BN + 64, cg * AT_D, &vfull[s]);
+                } else {
+                    tc::tma_load_2d(st, &tmVtt, 0, cg * AT_D, &vfull[s]);
+                    tc::tma_load_2d(st + L::PANEL, &tmVtt, 64, cg * AT_D, &vfull[s]);
+                }
+                return true;
+            };
+            int nk = 0, nv = 0;  // blocks issued
+            bool ok = load_k(0);
+            nk = ok ? 1 : 0;
+            for (int i = 0; i < nblk && ok; ++i) {
+                if (i + 1 < nblk) {
+                    ok = load_k(i + 1);
+                    if (ok) nk = i + 2;
+                }
+                if (ok) {
+                    ok = load_v(i);
+                    if (ok) nv = i + 1;
                 }
             }
             // copies issued and not yet seen complete land before the CTA can exit
             mbar_wait_bounded(qf, 0, a.status);
-            for (int q = i - 1; q >= 0 && q >= i - 2; --q) mbar_wait_bounded(&full[q & 1], uint32_t(q >> 1) & 1u, a.status);
+            for (int q = nk - 1; q >= 0 && q >= nk - 2; --q)
+                mbar_wait_bounded(&kfull[q & 1], uint32_t(q >> 1) & 1u, a.status);
+            for (int q = nv - 1; q >= 0 && q >= nv - 2; --q)
+                mbar_wait_bounded(&vfull[q & 1], uint32_t(q >> 1) & 1u, a.status);
         }
     } else if (warp == 1) {
         if (lane == 0 && nblk > 0) {  // MMA issuer
@@ -259,7 +289,9 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
             const uint32_t sq = smem_u32(smem + L::Q_OFF);
             bool ok = mbar_wait_bounded(qf, 0, a.status);
             auto pv = [&](int i) -> bool {  // O += P_i V_i^T, then release stage i
-                if (!mbar_wait_bounded(&pfull[i & 1], uint32_t(i >> 1) & 1u, a.status)) return false;
+                if (!mbar_wait_bounded(&pfull[i & 1], uint32_t(i >> 1) & 1u, a.status) ||
+                    !mbar_wait_bounded(&vfull[i & 1], uint32_t(i >> 1) & 1u, a.status))
+                    return false;
                 tc::fence_after_sync();
                 const uint32_t st = smem_u32(smem + L::RING_OFF + size_t(i & 1) * L::STAGE);
                 const uint32_t sp = smem_u32(smem + L::P_OFF + size_t(i & 1) * 2 * L::PANEL);
@@ -272,13 +304,13 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
                         tc::mma_bf16(tmem + 256, da + 2u * kk, db + 2u * kk, idesc, i > 0 || p > 0 || kk > 0);
                 }
                 tc::mma_commit(&odone[i & 1]);
-                tc::mma_commit(&empty[i & 1]);
+                tc::mma_commit(&vempty[i & 1]);
                 return true;
             };
             for (int i = 0; i < nblk && ok; ++i) {
                 const int s = i & 1;
                 if (i >= 2 && !mbar_wait_bounded(&sfree[s], uint32_t((i >> 1) - 1) & 1u, a.status)) break;
-                if (!mbar_wait_bounded(&full[s], uint32_t(i >> 1) & 1u, a.status)) break;
+                if (!mbar_wait_bounded(&kfull[s], uint32_t(i >> 1) & 1u, a.status)) break;
                 tc::fence_after_sync();
                 const uint32_t st = smem_u32(smem + L::RING_OFF + size_t(s) * L::STAGE);
 #pragma unroll
@@ -290,6 +322,7 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
                         tc::mma_bf16(tmem + uint32_t(s * AT_BN), da + 2u * kk, db + 2u * kk, idesc, p > 0 || kk > 0);
                 }
                 tc::mma_commit(&sfull[s]);
+                tc::mma_commit(&kempty[s]);
                 if (i >= 1 && !pv(i - 1)) {
                     ok = false;
                     break;
