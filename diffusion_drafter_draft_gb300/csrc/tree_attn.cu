@@ -341,6 +341,9 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
         const int hg = real ? R / a.S : 0, j = real ? R - hg * a.S : 0;
         const int nn = a.n_nodes[c];
         const bool live = real && j < nn;
+        // a warp whose 32 rows are all padding (the last tile of a group) forms no
+        // weights: its rows of P are never read into a real output row
+        const bool warp_real = __any_sync(0xffffffffu, real);
         const uint32_t trow = tmem + (uint32_t(quarter * 32) << 16);
         const uint32_t col0 = uint32_t(half * 64);          // this thread's key / O columns
         const float sl2 = 1.4426950408889634f / sqrtf(float(AT_D));  // log2(e) / sqrt(D)
@@ -369,7 +372,7 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
             }
             // pass 1: this half's maximum of the raw scores over the visible keys
             float mx = -INFINITY;
-            if (ok) {
+            if (ok && warp_real) {
                 tc::fence_after_sync();
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 32) {
@@ -390,7 +393,7 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
             // without a new maximum scale by 1.
             const bool grow = ok && mx > m_used + AT_RESCALE;
             const float f = grow && m_used > -INFINITY ? exp2f(m_used - mx) : 1.0f;
-            if (i >= 1 && __any_sync(0xffffffffu, grow && m_used > -INFINITY)) {
+            if (i >= 1 && warp_real && __any_sync(0xffffffffu, grow && m_used > -INFINITY)) {
                 ok = ok && __all_sync(0xffffffffu, mbar_wait_bounded(&odone[(i - 1) & 1], uint32_t((i - 1) >> 1) & 1u,
                                                                      a.status));
                 if (ok) {
@@ -410,11 +413,11 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
                 m_used = mx;
             }
             // P buffer s was last read by P_(i-2) V^T
-            if (i >= 2)
+            if (i >= 2 && warp_real)
                 ok = ok && __all_sync(0xffffffffu, mbar_wait_bounded(&odone[s], uint32_t((i - 2) >> 1) & 1u, a.status));
             // pass 2: P = 2^(s sl2 - m) in bf16 into the operand layout (panel `half` of
             // buffer s); the sum of the unrounded weights
-            if (ok) {
+            if (ok && warp_real) {
                 uint8_t* pan = smem + L::P_OFF + size_t(s) * 2 * L::PANEL + size_t(half) * L::PANEL;
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 32) {
