@@ -437,7 +437,9 @@ static int launch_expand_t(const ExpandArgs& a, cudaStream_t st) {
         const bool tc_proj = sizeof(T) == 2 && gemm_tc_supported(M, a.H, a.H);
         if (tc_proj && a.uhl && contract_tc_supported(P, a.H)) {
             // tensor cores for both: U as bf16 hi/lo pairs, then the gathered contraction
-            if (int e = launch_gemm_bf16_tc(hb[cur], Wq, M, a.H, a.H, 1, nullptr, a.uhl, P, a.status, st)) return e;
+            if (int e = launch_gemm_bf16_tc(hb[cur], Wq, M, a.H, a.H, 1, nullptr, a.uhl, P, a.status, st, nullptr,
+                                            false, nullptr, a.split))
+                return e;
             if (int e = launch_contract_tc(E, a.uhl, a.cand_tok, a.cand_val, a.z, a.C, P, a.K, a.H, a.L, d,
                                            inv_sqrt_h, a.status, st))
                 return e;
@@ -497,6 +499,7 @@ int launch_expand(const ExpandArgs& a, cudaStream_t stream) {
     const size_t eb = a.dtype == DARTREE_BF16 ? 2 : 4;
     ExpandArgs h0 = a, h1 = a;
     h0.fin = h1.fin = nullptr;  // the per-depth path leaves S8-S10 to the caller
+    h0.split = h1.split = true;
     h0.C = c0;
     h1.C = a.C - c0;
     h1.hidden = static_cast<const uint8_t*>(a.hidden) + size_t(r0) * a.L * a.H * eb;

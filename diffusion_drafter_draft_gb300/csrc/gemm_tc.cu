@@ -332,7 +332,8 @@ static int launch_gemm_bn(const void* A, const void* B, int M, int N, int K, con
 }
 
 int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int mode, float* d32, uint16_t* hilo,
-                        int P, int* status, cudaStream_t stream, uint16_t* lo2, bool pdl, const GemmRowmax* rm) {
+                        int P, int* status, cudaStream_t stream, uint16_t* lo2, bool pdl, const GemmRowmax* rm,
+                        bool shared_sms) {
     if (!gemm_tc_supported(M, N, K)) return DARTREE_EUNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) % 16) return DARTREE_EINVAL;
     if (mode == 1 && (P < 1 || P > 16 || !hilo)) return DARTREE_EINVAL;
@@ -350,9 +351,10 @@ int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int m
     for (int bn : {256, 160, 128}) {
         if (N % bn != 0) continue;
         const long tiles = long(mt) * (N / bn), waves = (tiles + sms - 1) / sms;
-        // mode 1 (per-depth projection) runs beside the other half's contraction:
-        // the operand bytes all its CTAs stream count, not its own span
-        const long cost = mode == 1 ? tiles * (GT_BM + bn) : waves * (GT_BM + bn);
+        // beside other work (the per-depth projection of one half of a split batch,
+        // next to the other half's contraction) the operand bytes all its CTAs stream
+        // count, not its own span
+        const long cost = shared_sms ? tiles * (GT_BM + bn) : waves * (GT_BM + bn);
         if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = bn; }
     }
     if (best == 256) return launch_gemm_bn<256>(A, B, M, N, K, o, status, stream, pdl);

@@ -128,6 +128,7 @@ struct ExpandArgs {
     uint16_t* Ghi;            // [C*L*K, H] G = E[cand] W_q, bf16 high part
     uint16_t* Glo;            // [C*L*K, H] low part
     int g_rows;               // rows the Eg/G buffers hold (0: path unavailable)
+    bool split;               // one part of a batch split across streams (per-depth path)
     int* status;
     // Optional per-position target row maxima (bf16 rows [C*L, V]) taken inside the
     // candidate-side path's GEMM launch (keys cleared by the top-K launch)
@@ -169,9 +170,11 @@ int try_launch_expand_g(const ExpandArgs& a, cudaStream_t stream, bool* launched
 // pdl: programmatic dependent launch (A may be written by the previous kernel; B and
 // the outputs are not touched by it).
 bool gemm_tc_supported(int M, int N, int K);
+// shared_sms: the launch runs beside other work (the other half of a split batch):
+// its tile width is chosen by the operand bytes all its CTAs stream, not by its span.
 int launch_gemm_bf16_tc(const void* A, const void* B, int M, int N, int K, int mode, float* d32, uint16_t* hilo,
                         int P, int* status, cudaStream_t stream, uint16_t* lo2 = nullptr, bool pdl = false,
-                        const GemmRowmax* rm = nullptr);
+                        const GemmRowmax* rm = nullptr, bool shared_sms = false);
 
 // tcgen05 contraction of one depth: z[r,p,c] from gathered candidate rows and uhl.
 bool contract_tc_supported(int P, int H);
