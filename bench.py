@@ -371,15 +371,15 @@ def measure_attention(cfg, m, steps, warmup, torch, dd, hbm_peak, tf_peak, graph
 
 
 # DRAM bytes per launch (read + write) from one ncu capture of the current kernel on
-# this workload; the C=64 contraction and top-K were captured on fewer requests (8
-# and 20 of them) and scaled by the requests processed (their traffic is per request).
+# this workload; the C=64 contraction was captured on 8 requests and scaled by the
+# requests processed (its traffic is per request).
 # A kernel changed since its capture has no entry (traffic null).
 NCU_TRAFFIC = {
     ("cfg1_qwen3_4b_c1", "expand_g_kernel"): 15566336,      # one launch = one round, full size
     ("cfg1_qwen3_4b_c1", "gemm_bf16_tc_kernel"): 23248384,
     ("cfg1_qwen3_4b_c1", "topk_rows_kernel"): 15284736,
     ("cfg4_c64_stress", "contract_tc_kernel"): 35337472 * 8,   # one launch over all 64 requests
-    ("cfg4_c64_stress", "topk_stream_kernel"): int((100288256 + 3384576) * 64 / 20),
+    ("cfg4_c64_stress", "topk_stream_kernel"): 361796608 + 5478400,   # full size
 }
 
 
