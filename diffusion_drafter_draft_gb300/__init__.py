@@ -16,7 +16,7 @@ __all__ = [
     "DartreeError", "lib", "library_path", "F32", "BF16", "ROWS_PER_POSITION", "ROWS_PER_NODE",
     "workspace_bytes", "new_workspace", "topk", "expand", "prune", "tree_mask", "build_tree",
     "verify", "read_status", "clear_status", "Round", "EXPORTS", "heap_build", "HeapRound",
-    "verify_sample", "adaptive_budget", "lm_head_topk", "tree_attention", "AttnParams",
+    "verify_sample", "adaptive_budget", "lm_head_topk", "tree_attention", "AttnParams", "HostRounds",
 ]
 
 F32, BF16 = 0, 1
@@ -543,6 +543,55 @@ class Round:
               ctypes.c_void_p(self.out["path"].data_ptr()), ctypes.c_void_p(self.out["bonus"].data_ptr()),
               ctypes.c_void_p(self.ws.data_ptr()), self.ws.numel(), s)
         return self.out
+
+
+class HostRounds:
+    """Rounds fed from pinned host buffers, results read back into pinned host buffers.
+
+    Two device copies of the inputs: round i runs on the current stream from set
+    i % 2 while round i + 1's inputs are copied into the other set on a copy stream
+    (the copy of set b waits until the round that last read it has finished). Each
+    round's results are copied to the caller's pinned buffers on the current stream
+    right after the round, so they are complete once that stream is synchronised.
+    """
+
+    KEYS = ("base", "hidden", "anchor", "target")
+
+    def __init__(self, rnd: "Round", like: dict):
+        self.rnd = rnd
+        self.copy = torch.cuda.Stream()
+        self.bufs = [{k: torch.empty(like[k].shape, dtype=like[k].dtype, device="cuda") for k in self.KEYS}
+                     for _ in range(2)]
+        self.ready = [torch.cuda.Event() for _ in range(2)]
+        self.free = [torch.cuda.Event() for _ in range(2)]
+        self.used = [False, False]
+
+    def h2d_bytes(self) -> int:
+        return sum(b.numel() * b.element_size() for b in self.bufs[0].values())
+
+    def copy_in(self, i: int, host: dict):
+        """Enqueue the copy of round i's inputs (pinned host tensors) on the copy stream."""
+        b = i % 2
+        if self.used[b]:
+            self.copy.wait_event(self.free[b])
+        with torch.cuda.stream(self.copy):
+            for k in self.KEYS:
+                self.bufs[b][k].copy_(host[k], non_blocking=True)
+            self.ready[b].record(self.copy)
+
+    def run(self, i: int, host_out: dict):
+        """Enqueue round i on the current stream (after its inputs landed) and the copy
+        of its results into host_out (pinned tensors shaped like Round.out)."""
+        b = i % 2
+        cur = torch.cuda.current_stream()
+        cur.wait_event(self.ready[b])
+        x = self.bufs[b]
+        out = self.rnd.run(x["base"], x["hidden"], x["anchor"], x["target"])
+        self.free[b].record(cur)
+        self.used[b] = True
+        for k, v in out.items():
+            host_out[k].copy_(v, non_blocking=True)
+        return host_out
 
 
 class HeapRound:

@@ -116,3 +116,13 @@ def test_both_arms_share_the_config_object():
 
 def test_cpu_model_is_named():
     assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+
+
+def test_every_measurement_the_main_path_calls_exists():
+    import ast
+    import inspect
+    tree = ast.parse(inspect.getsource(bench.main))
+    called = {n.func.id for n in ast.walk(tree) if isinstance(n, ast.Call) and isinstance(n.func, ast.Name)}
+    missing = [n for n in called if n.startswith(("measure", "kernel_", "roofline", "cpu_", "workload_", "job_"))
+               and not hasattr(bench, n)]
+    assert not missing, missing

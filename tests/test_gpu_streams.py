@@ -72,3 +72,41 @@ def test_two_streams_run_c64_rounds_concurrently(dd):
             np.testing.assert_array_equal(r.tree[k].cpu().numpy(), ref[k], err_msg=k)
         for k in vref:
             np.testing.assert_array_equal(out[k].cpu().numpy(), vref[k], err_msg=k)
+
+
+def test_host_rounds_match_device_rounds(dd):
+    """dd.HostRounds (inputs copied from pinned host memory on a copy stream while the
+    previous round runs, results copied back) gives, round after round, the results of
+    Round.run on device inputs. Three different input sets alternate, so a round that
+    read a stale input set would show."""
+    cfg = make_config("cfg1_qwen3_4b_c1").replace(C=2)
+    sets = []
+    for seed in (11, 12, 13):
+        inp = make_inputs(cfg.replace(seed=seed))
+        sets.append(inp)
+    E, Wq = _dev(sets[0]["E"]), _dev(sets[0]["Wq"])   # the head of seed 11 for every round
+    rnd = dd.Round(E, Wq, cfg.C, cfg.L, cfg.K, cfg.W, cfg.B, cfg.beta, dd.ROWS_PER_POSITION)
+
+    def host_set(inp):
+        return dict(base=_dev(inp["base"]).cpu().pin_memory(), hidden=_dev(inp["hidden"]).cpu().pin_memory(),
+                    anchor=torch.from_numpy(inp["anchor"]).pin_memory(),
+                    target=_dev(inp["target"]).cpu().pin_memory())
+
+    hs = [host_set(inp) for inp in sets]
+    want = []
+    for h in hs:
+        o = rnd.run(*(h[k].cuda() for k in dd.HostRounds.KEYS))
+        torch.cuda.synchronize()
+        want.append({k: v.cpu().clone() for k, v in o.items()})
+    hr = dd.HostRounds(rnd, hs[0])
+    n = 7
+    outs = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in rnd.out.items()} for _ in range(n)]
+    hr.copy_in(0, hs[0])
+    for i in range(n):
+        if i + 1 < n:
+            hr.copy_in(i + 1, hs[(i + 1) % 3])
+        hr.run(i, outs[i])
+    torch.cuda.synchronize()
+    for i in range(n):
+        for k in want[i % 3]:
+            assert torch.equal(outs[i][k], want[i % 3][k]), (i, k)
