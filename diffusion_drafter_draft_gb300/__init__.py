@@ -208,7 +208,12 @@ def selftest_wait(ws: torch.Tensor, which: int, limit_us: int, stream=None) -> N
           _stream(stream))
 
 
-NUM_KERNEL_IDS = 15
+def num_kernel_ids() -> int:
+    """Kernel families the library times (ids 0 .. n-1; the last one is "other")."""
+    n = 0
+    while lib().dartree_kernel_name(n).decode() != "unknown":
+        n += 1
+    return n
 
 
 def timing(enable: bool) -> None:
@@ -219,7 +224,7 @@ def timing(enable: bool) -> None:
 def kernel_times() -> dict:
     """{kernel family: (launches, total device ms)} recorded since timing(True)."""
     out = {}
-    for k in range(NUM_KERNEL_IDS):
+    for k in range(num_kernel_ids()):
         n, ms = ctypes.c_int(0), ctypes.c_double(0.0)
         _call("dartree_timing_read", k, ctypes.byref(n), ctypes.byref(ms))
         if n.value:

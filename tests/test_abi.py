@@ -166,3 +166,13 @@ def test_tree_attention_limits_are_checked_on_the_host(L):
     assert f(ctypes.byref(p), *args, ctypes.byref(tree), fake, ctypes.c_void_p(1 << 20), need - 256, None) \
         == dd.EWORKSPACE
     assert f(ctypes.byref(P(0, 65, 32, 8, 128, 2048, 1e6)), *args, ctypes.byref(tree), fake, None, 0, None) == dd.OK
+
+
+def test_every_kernel_family_has_a_timing_name(L):
+    import diffusion_drafter_draft_gb300 as dd
+    n = dd.num_kernel_ids()
+    names = [L.dartree_kernel_name(k).decode() for k in range(n)]
+    assert names[-1] == "other" and len(set(names)) == n
+    for want in ("expand_g_kernel", "lmhead_topk_kernel", "attn_kernel", "rowsample_kernel", "heap_search_kernel"):
+        assert want in names
+    assert L.dartree_kernel_name(n).decode() == "unknown"
