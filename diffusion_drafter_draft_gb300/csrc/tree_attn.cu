@@ -13,16 +13,18 @@
 //   and transpose the tree's values, Vtt [C, Hkv, D, 128]; unused and padding
 //   slots are zero.
 // Launch 2 (attn_kernel, CTA = (chunk of key blocks, 128-row tile of a group's
-//   query rows, (request, group))): warp 0 loads the query tile and, per 128-key
-//   block, the keys and transposed values with TMA (128-byte swizzle) into two-stage
-//   rings, keys one block ahead of values (a key block is released as soon as its
-//   scores are formed); warp 1 issues S = Q K^T into one of two TMEM score buffers and
-//   O += P V^T into a TMEM accumulator; warps 2-9 (two threads per query row, each
-//   on half of the keys and of O) mask, take the running maximum (log2 domain; O
-//   and the sums are rescaled only when the maximum grows by more than 2^8), write P
-//   in bf16 to one of two shared-memory operand buffers (so P_i V^T runs while block
-//   i+1's weights are formed), and at the end either normalise and write the output
-//   (one chunk) or write the chunk's partial (O, max, sum).
+//   query rows, (request, group))): warp 0 loads, per 128-key block, the keys and
+//   transposed values with TMA (128-byte swizzle) into two-stage rings, keys one block
+//   ahead of values (a key block is released as soon as its scores are formed);
+//   warp 1 issues S = Q K^T into one of two TMEM score buffers and O += P V^T into a
+//   TMEM accumulator, both with the A operand (Q, P) in tensor memory so that shared
+//   memory serves only the key/value operands and the copies; warps 2-9 (two threads
+//   per query row, each on half of the keys and of O) first store the query tile into
+//   tensor memory, then per block mask, take the running maximum (log2 domain; O and
+//   the sums are rescaled only when the maximum grows by more than 2^8) and write P
+//   in bf16 over the block's scores (so P_i V^T runs while block i+1's weights are
+//   formed), and at the end either normalise and write the output (one chunk) or
+//   write the chunk's partial (O, max, sum).
 // Launch 3 (attn_combine_kernel, several chunks only): merges the partials of a row.
 // The prefix blocks come first, the tree block (keys = the tree's slots) last.
 // Every mbarrier wait is bounded; a wait that runs out records DARTREE_ETIMEOUT.
@@ -41,20 +43,21 @@ constexpr int AT_BM = 128;       // query rows per tile
 constexpr int AT_BN = 128;       // keys per block
 constexpr int AT_NT = 320;       // producer, MMA, 8 softmax warps (two per TMEM lane quarter)
 constexpr int AT_SMX = 256;      // softmax threads
+constexpr int AT_ST = 2;         // stages of the key and of the value ring
 constexpr int AT_MAXMT = 3;      // query-row tiles per group (grp * S <= 384)
 constexpr float AT_RESCALE = 8.0f;  // log2 growth of the maximum that forces a rescale
 
+// Shared memory holds only the key/value rings (the MMAs' B operands): the query
+// tile and the weights P are A operands read from tensor memory.
 struct AtSmem {
     static constexpr size_t PANEL = size_t(128) * 64 * 2;  // 128 rows x 64 bf16, swizzled
-    static constexpr size_t Q_OFF = 0;                      // 2 panels
-    static constexpr size_t RING_OFF = 2 * PANEL;           // 2 stages x (K 2 panels, V^T 2 panels), K and V
-                                                            // filled and released separately
+    static constexpr size_t RING_OFF = 0;                   // AT_ST stages x (K 2 panels, V^T 2 panels), K
+                                                            // and V filled and released separately
     static constexpr size_t STAGE = 4 * PANEL;
-    static constexpr size_t P_OFF = RING_OFF + 2 * STAGE;   // 2 buffers x 2 panels
-    static constexpr size_t XCH_OFF = P_OFF + 4 * PANEL;    // float [2 halves][128 rows]
+    static constexpr size_t XCH_OFF = RING_OFF + AT_ST * STAGE;  // float [2 halves][128 rows]
     static constexpr size_t BAR_OFF = XCH_OFF + 2 * 128 * 4;
-    // qf, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], sfree[2], pfull[2], odone[2]
-    static constexpr size_t SLOT_OFF = BAR_OFF + 8 * 17;
+    // qf, kfull[AT_ST], kempty[AT_ST], vfull[AT_ST], vempty[AT_ST], sfull[2], sfree[2], pfull[2], odone[2]
+    static constexpr size_t SLOT_OFF = BAR_OFF + 8 * (1 + 4 * AT_ST + 8);
     static constexpr size_t TOTAL = SLOT_OFF + 16 + 1024;
 };
 static_assert(AtSmem::TOTAL <= 227 * 1024, "attention tile fits in shared memory");
@@ -69,6 +72,7 @@ struct AtArgs {
     float* part_o;                    // [C*Hkv, mtiles, nchunk, 128, D]
     float* part_ml;                   // [C*Hkv, mtiles, nchunk, 128, 2]
     int* status;
+    const uint16_t* qr;               // [C*Hkv, rows, D] rotated queries (from attn_prep_kernel)
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -172,13 +176,7 @@ __global__ void __launch_bounds__(256) attn_vt_kernel(const uint16_t* __restrict
 
 // ----------------------------------------------------------------------------- attention
 
-// Byte offset of (row, col) in a 128-byte-swizzled panel of 128 rows x 64 bf16.
-__device__ __forceinline__ uint32_t sw128_off(int row, int chunk16) {
-    return uint32_t(row) * 128u + uint32_t((chunk16 ^ (row & 7)) * 16);
-}
-
-__global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ CUtensorMap tmQ,
-                                                        const __grid_constant__ CUtensorMap tmK,
+__global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ CUtensorMap tmK,
                                                         const __grid_constant__ CUtensorMap tmVt,
                                                         const __grid_constant__ CUtensorMap tmKt,
                                                         const __grid_constant__ CUtensorMap tmVtt, AtArgs a) {
@@ -186,15 +184,15 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
-    uint64_t* qf = bars;
-    uint64_t* kfull = bars + 1;    // [2]: key block landed, by stage
-    uint64_t* kempty = bars + 3;   // [2]: S = Q K^T done with it
-    uint64_t* vfull = bars + 5;    // [2]: value block landed
-    uint64_t* vempty = bars + 7;   // [2]: P V^T done with it
-    uint64_t* sfull = bars + 9;
-    uint64_t* sfree = bars + 11;
-    uint64_t* pfull = bars + 13;   // [2]: P written, by P buffer
-    uint64_t* odone = bars + 15;   // [2]: P V^T done, by P buffer
+    uint64_t* qf = bars;                     // the query tile is in tensor memory
+    uint64_t* kfull = bars + 1;              // [AT_ST]: key block landed, by stage
+    uint64_t* kempty = kfull + AT_ST;        // [AT_ST]: S = Q K^T done with it
+    uint64_t* vfull = kempty + AT_ST;        // [AT_ST]: value block landed
+    uint64_t* vempty = vfull + AT_ST;        // [AT_ST]: P V^T done with it
+    uint64_t* sfull = vempty + AT_ST;        // [2]: S written, by TMEM score buffer
+    uint64_t* sfree = sfull + 2;
+    uint64_t* pfull = sfree + 2;             // [2]: P written, by P buffer
+    uint64_t* odone = pfull + 2;             // [2]: P V^T done, by P buffer
     uint32_t* slot = reinterpret_cast<uint32_t*>(smem + L::SLOT_OFF);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int chunk = blockIdx.x, mt = blockIdx.y, cg = blockIdx.z;
@@ -205,12 +203,14 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
     const int nblk = b1 > b0 ? b1 - b0 : 0;
 
     if (threadIdx.x == 0) {
-        mbar_init(qf, 1);
-        for (int s = 0; s < 2; ++s) {
+        mbar_init(qf, AT_SMX / 32);
+        for (int s = 0; s < AT_ST; ++s) {
             mbar_init(&kfull[s], 1);
             mbar_init(&kempty[s], 1);
             mbar_init(&vfull[s], 1);
             mbar_init(&vempty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
             mbar_init(&sfull[s], 1);
             mbar_init(&sfree[s], AT_SMX / 32);
             mbar_init(&pfull[s], AT_SMX / 32);
@@ -222,21 +222,20 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem = *slot;  // S buffers at columns 0 and 128, O at 256
+    // TMEM columns: S buffers at 0 and 128 (P_i overwrites S_i in place: the 64 keys of
+    // half h as 32 packed bf16 pairs at 128 s + 64 h), O at 256, Q at 384 (d pairs)
+    const uint32_t tmem = *slot;
     griddep_launch_dependents();
     griddep_wait();
 
     if (warp == 0) {
         if (lane == 0 && nblk > 0) {  // producer
-            const int qrow = cg * a.rows + mt * AT_BM;
-            mbar_arrive_expect_tx(qf, uint32_t(2 * L::PANEL));
-            tc::tma_load_2d(smem + L::Q_OFF, &tmQ, 0, qrow, qf);
-            tc::tma_load_2d(smem + L::Q_OFF + L::PANEL, &tmQ, 64, qrow, qf);
-            // key blocks run one ahead of value blocks: K_i+1 needs only S_i-1 done,
-            // V_i needs P_i-2 V^T done
+            // key blocks run AT_ST - 1 ahead of value blocks: K_i+AT_ST-1 needs only S_i-1
+            // done, V_i needs P_i-AT_ST V^T done
             auto load_k = [&](int i) -> bool {
-                const int s = i & 1, b = b0 + i;
-                if (i >= 2 && !mbar_wait_bounded(&kempty[s], uint32_t((i >> 1) & 1) ^ 1u, a.status)) return false;
+                const int s = i % AT_ST, b = b0 + i;
+                if (i >= AT_ST && !mbar_wait_bounded(&kempty[s], uint32_t((i / AT_ST) & 1) ^ 1u, a.status))
+                    return false;
                 uint8_t* st = smem + L::RING_OFF + size_t(s) * L::STAGE;
                 mbar_arrive_expect_tx(&kfull[s], uint32_t(2 * L::PANEL));
                 if (b < nbp) {  // prefix block: K_cache rows
@@ -250,8 +249,9 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
                 return true;
             };
             auto load_v = [&](int i) -> bool {
-                const int s = i & 1, b = b0 + i;
-                if (i >= 2 && !mbar_wait_bounded(&vempty[s], uint32_t((i >> 1) & 1) ^ 1u, a.status)) return false;
+                const int s = i % AT_ST, b = b0 + i;
+                if (i >= AT_ST && !mbar_wait_bounded(&vempty[s], uint32_t((i / AT_ST) & 1) ^ 1u, a.status))
+                    return false;
                 uint8_t* st = smem + L::RING_OFF + size_t(s) * L::STAGE + 2 * L::PANEL;
                 mbar_arrive_expect_tx(&vfull[s], uint32_t(2 * L::PANEL));
                 if (b < nbp) {  // V^T_cache columns
@@ -263,13 +263,17 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
                 }
                 return true;
             };
+            constexpr int lead = AT_ST - 1;
             int nk = 0, nv = 0;  // blocks issued
-            bool ok = load_k(0);
-            nk = ok ? 1 : 0;
+            bool ok = true;
+            for (int i = 0; i < lead && i < nblk && ok; ++i) {
+                ok = load_k(i);
+                if (ok) nk = i + 1;
+            }
             for (int i = 0; i < nblk && ok; ++i) {
-                if (i + 1 < nblk) {
-                    ok = load_k(i + 1);
-                    if (ok) nk = i + 2;
+                if (i + lead < nblk) {
+                    ok = load_k(i + lead);
+                    if (ok) nk = i + lead + 1;
                 }
                 if (ok) {
                     ok = load_v(i);
@@ -277,52 +281,50 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
                 }
             }
             // copies issued and not yet seen complete land before the CTA can exit
-            mbar_wait_bounded(qf, 0, a.status);
-            for (int q = nk - 1; q >= 0 && q >= nk - 2; --q)
-                mbar_wait_bounded(&kfull[q & 1], uint32_t(q >> 1) & 1u, a.status);
-            for (int q = nv - 1; q >= 0 && q >= nv - 2; --q)
-                mbar_wait_bounded(&vfull[q & 1], uint32_t(q >> 1) & 1u, a.status);
+            for (int q = nk - 1; q >= 0 && q >= nk - AT_ST; --q)
+                mbar_wait_bounded(&kfull[q % AT_ST], uint32_t(q / AT_ST) & 1u, a.status);
+            for (int q = nv - 1; q >= 0 && q >= nv - AT_ST; --q)
+                mbar_wait_bounded(&vfull[q % AT_ST], uint32_t(q / AT_ST) & 1u, a.status);
         }
     } else if (warp == 1) {
         if (lane == 0 && nblk > 0) {  // MMA issuer
             constexpr uint32_t idesc = tc::idesc_bf16_f32(AT_BM, AT_BN);
-            const uint32_t sq = smem_u32(smem + L::Q_OFF);
             bool ok = mbar_wait_bounded(qf, 0, a.status);
             auto pv = [&](int i) -> bool {  // O += P_i V_i^T, then release stage i
                 if (!mbar_wait_bounded(&pfull[i & 1], uint32_t(i >> 1) & 1u, a.status) ||
-                    !mbar_wait_bounded(&vfull[i & 1], uint32_t(i >> 1) & 1u, a.status))
+                    !mbar_wait_bounded(&vfull[i % AT_ST], uint32_t(i / AT_ST) & 1u, a.status))
                     return false;
                 tc::fence_after_sync();
-                const uint32_t st = smem_u32(smem + L::RING_OFF + size_t(i & 1) * L::STAGE);
-                const uint32_t sp = smem_u32(smem + L::P_OFF + size_t(i & 1) * 2 * L::PANEL);
+                const uint32_t st = smem_u32(smem + L::RING_OFF + size_t(i % AT_ST) * L::STAGE);
+                const uint32_t ta = tmem + uint32_t((i & 1) * AT_BN);  // P_i, keys 64 p + 16 kk at 64 p + 8 kk
 #pragma unroll
                 for (int p = 0; p < 2; ++p) {
-                    const uint64_t da = tc::desc_sw128_kmajor(sp + uint32_t(p * L::PANEL));
                     const uint64_t db = tc::desc_sw128_kmajor(st + uint32_t((2 + p) * L::PANEL));
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        tc::mma_bf16(tmem + 256, da + 2u * kk, db + 2u * kk, idesc, i > 0 || p > 0 || kk > 0);
+                        tc::mma_bf16_ts(tmem + 256, ta + uint32_t(64 * p + 8 * kk), db + 2u * kk, idesc,
+                                        i > 0 || p > 0 || kk > 0);
                 }
                 tc::mma_commit(&odone[i & 1]);
-                tc::mma_commit(&vempty[i & 1]);
+                tc::mma_commit(&vempty[i % AT_ST]);
                 return true;
             };
             for (int i = 0; i < nblk && ok; ++i) {
                 const int s = i & 1;
                 if (i >= 2 && !mbar_wait_bounded(&sfree[s], uint32_t((i >> 1) - 1) & 1u, a.status)) break;
-                if (!mbar_wait_bounded(&kfull[s], uint32_t(i >> 1) & 1u, a.status)) break;
+                if (!mbar_wait_bounded(&kfull[i % AT_ST], uint32_t(i / AT_ST) & 1u, a.status)) break;
                 tc::fence_after_sync();
-                const uint32_t st = smem_u32(smem + L::RING_OFF + size_t(s) * L::STAGE);
+                const uint32_t st = smem_u32(smem + L::RING_OFF + size_t(i % AT_ST) * L::STAGE);
 #pragma unroll
                 for (int p = 0; p < 2; ++p) {  // S_i = Q K_i^T over the two 64-wide d panels
-                    const uint64_t da = tc::desc_sw128_kmajor(sq + uint32_t(p * L::PANEL));
                     const uint64_t db = tc::desc_sw128_kmajor(st + uint32_t(p * L::PANEL));
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        tc::mma_bf16(tmem + uint32_t(s * AT_BN), da + 2u * kk, db + 2u * kk, idesc, p > 0 || kk > 0);
+                        tc::mma_bf16_ts(tmem + uint32_t(s * AT_BN), tmem + 384u + uint32_t(32 * p + 8 * kk),
+                                        db + 2u * kk, idesc, p > 0 || kk > 0);
                 }
                 tc::mma_commit(&sfull[s]);
-                tc::mma_commit(&kempty[s]);
+                tc::mma_commit(&kempty[i % AT_ST]);
                 if (i >= 1 && !pv(i - 1)) {
                     ok = false;
                     break;
@@ -353,6 +355,23 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
             asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
             return y;
         };
+        // this thread's half of its query row (d in [64 half, 64 half + 64)) into TMEM
+        {
+            uint32_t v[32];
+            const uint4* src = reinterpret_cast<const uint4*>(a.qr + (size_t(cg) * a.rows + R) * AT_D + col0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint4 x = real ? src[q] : make_uint4(0, 0, 0, 0);
+                v[4 * q] = x.x;
+                v[4 * q + 1] = x.y;
+                v[4 * q + 2] = x.z;
+                v[4 * q + 3] = x.w;
+            }
+            tc::tmem_st32(trow + 384u + uint32_t(32 * half), v);
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qf);
+        }
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int i = 0; i < nblk; ++i) {
@@ -412,13 +431,10 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
                 l *= f;
                 m_used = mx;
             }
-            // P buffer s was last read by P_(i-2) V^T
-            if (i >= 2 && warp_real)
-                ok = ok && __all_sync(0xffffffffu, mbar_wait_bounded(&odone[s], uint32_t((i - 2) >> 1) & 1u, a.status));
-            // pass 2: P = 2^(s sl2 - m) in bf16 into the operand layout (panel `half` of
-            // buffer s); the sum of the unrounded weights
+            // pass 2: P = 2^(s sl2 - m) in bf16 over S_i's first 32 columns of this half
+            // (the chunk read before its packed weights are stored); the sum of the
+            // unrounded weights. P_i-2 V^T, which read this buffer, ran before S_i.
             if (ok && warp_real) {
-                uint8_t* pan = smem + L::P_OFF + size_t(s) * 2 * L::PANEL + size_t(half) * L::PANEL;
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 32) {
                     uint32_t v[32];
@@ -434,13 +450,10 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
                         const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
                         pk[e / 2] = *reinterpret_cast<const uint32_t*>(&h2);
                     }
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<uint4*>(pan + sw128_off(rt, c0 / 8 + q)) =
-                            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    tc::tmem_st16_async(trow + uint32_t(s * AT_BN) + col0 + uint32_t(c0 / 2), pk);
                 }
+                tc::tmem_wait_st();
                 tc::fence_before_sync();
-                fence_proxy_async_smem();  // P (generic stores) before the tensor core reads it
             }
             __syncwarp();
             if (lane == 0 && ok) {
@@ -598,12 +611,11 @@ int launch_tree_attention(int C, int S, int Hq, int Hkv, int N, double theta, co
         attn_vt_kernel<<<C * Hkv, 256, 0, stream>>>(static_cast<const uint16_t*>(v_tree), n_nodes, S, Hkv, Vtt);
     }
     if (cudaGetLastError() != cudaSuccess) return DARTREE_ECUDA;
-    CUtensorMap tq, tk, tvt, tkt, tvtt;
+    CUtensorMap tk, tvt, tkt, tvtt;
     const int rows = grp * S;
     // an empty cache (N = 0) still needs valid maps: point them at the tree block
     const bool cache = N > 0;
-    if (!make_tensor_map_bf16(&tq, Qr, C * Hkv * rows, AT_D, 64, AT_BM, 128) ||
-        !make_tensor_map_bf16(&tk, cache ? k_cache : Kt, cache ? C * Hkv * N : C * Hkv * AT_BN, AT_D, 64, AT_BN,
+    if (!make_tensor_map_bf16(&tk, cache ? k_cache : Kt, cache ? C * Hkv * N : C * Hkv * AT_BN, AT_D, 64, AT_BN,
                               128) ||
         !make_tensor_map_bf16(&tvt, cache ? vt_cache : Vtt, C * Hkv * AT_D, cache ? N : AT_BN, 64, AT_D, 128) ||
         !make_tensor_map_bf16(&tkt, Kt, C * Hkv * AT_BN, AT_D, 64, AT_BN, 128) ||
@@ -611,7 +623,7 @@ int launch_tree_attention(int C, int S, int Hq, int Hkv, int N, double theta, co
         return DARTREE_ECUDA;
     AtArgs a{C, S, Hq, Hkv, N, grp, rows, pl.nchunk, pl.per, n_ctx, mask, n_nodes, static_cast<uint16_t*>(out),
              pl.nchunk > 1 ? reinterpret_cast<float*>(w + pl.part_o) : nullptr,
-             pl.nchunk > 1 ? reinterpret_cast<float*>(w + pl.part_ml) : nullptr, status};
+             pl.nchunk > 1 ? reinterpret_cast<float*>(w + pl.part_ml) : nullptr, status, Qr};
     const size_t smem = AtSmem::TOTAL;
     if (cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
         return DARTREE_ECUDA;
@@ -626,7 +638,7 @@ int launch_tree_attention(int C, int S, int Hq, int Hkv, int N, double theta, co
     cudaError_t e;
     {
         KTimer kt_(KID_ATTN, stream);
-        e = cudaLaunchKernelEx(&cfg, attn_kernel, tq, tk, tvt, tkt, tvtt, a);
+        e = cudaLaunchKernelEx(&cfg, attn_kernel, tk, tvt, tkt, tvtt, a);
     }
     if (e != cudaSuccess) return DARTREE_ECUDA;
     if (pl.nchunk > 1) {
