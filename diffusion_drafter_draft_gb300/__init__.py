@@ -17,6 +17,7 @@ __all__ = [
     "workspace_bytes", "new_workspace", "topk", "expand", "prune", "tree_mask", "build_tree",
     "verify", "read_status", "clear_status", "Round", "EXPORTS", "heap_build", "HeapRound",
     "verify_sample", "adaptive_budget", "lm_head_topk", "tree_attention", "AttnParams", "HostRounds",
+    "HostInputs", "HostOutputs",
 ]
 
 F32, BF16 = 0, 1
@@ -29,7 +30,8 @@ EXPORTS = ("dartree_head_init", "dartree_workspace_bytes", "dartree_topk", "dart
            "dartree_head_prepare", "dartree_round", "dartree_selftest_wait", "dartree_timing",
            "dartree_timing_read", "dartree_kernel_name", "dartree_heap_workspace_bytes", "dartree_heap_build",
            "dartree_verify_sample", "dartree_adaptive_budget", "dartree_lm_head_workspace_bytes",
-           "dartree_lm_head_topk", "dartree_tree_attention_workspace_bytes", "dartree_tree_attention")
+           "dartree_lm_head_topk", "dartree_tree_attention_workspace_bytes", "dartree_tree_attention", "dartree_host_session_create",
+           "dartree_host_session_destroy", "dartree_host_stage", "dartree_host_round", "dartree_host_input_bytes")
 
 
 class DartreeError(RuntimeError):
@@ -116,6 +118,11 @@ def lib() -> ctypes.CDLL:
         "dartree_read_status": (i, [vp, P(ctypes.c_int32), vp]),
         "dartree_clear_status": (i, [vp, vp]),
         "dartree_status_string": (ctypes.c_char_p, [i]),
+        "dartree_host_session_create": (i, [P(Head), P(Params), i, P(vp)]),
+        "dartree_host_session_destroy": (None, [vp]),
+        "dartree_host_stage": (i, [vp, P(HostInputs)]),
+        "dartree_host_round": (i, [vp, P(HostOutputs), vp]),
+        "dartree_host_input_bytes": (sz, [vp, i]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -550,52 +557,61 @@ class Round:
         return self.out
 
 
-class HostRounds:
-    """Rounds fed from pinned host buffers, results read back into pinned host buffers.
+class HostInputs(ctypes.Structure):
+    _fields_ = [("base_logits", ctypes.c_void_p), ("block_hidden", ctypes.c_void_p), ("anchor", ctypes.c_void_p),
+                ("target", ctypes.c_void_p)]
 
-    Two device copies of the inputs: round i runs on the current stream from set
-    i % 2 while round i + 1's inputs are copied into the other set on a copy stream
-    (the copy of set b waits until the round that last read it has finished). Each
-    round's results are copied to the caller's pinned buffers on the current stream
-    right after the round, so they are complete once that stream is synchronised.
+
+class HostOutputs(ctypes.Structure):
+    _fields_ = [("accepted_len", ctypes.c_void_p), ("path", ctypes.c_void_p), ("bonus", ctypes.c_void_p)]
+
+
+class HostRounds:
+    """Rounds fed from host buffers through the library's host session
+    (dartree_host_session_create / dartree_host_stage / dartree_host_round): the
+    session holds two device sets of the inputs, and round i runs from set i % 2
+    while round i + 1's inputs are copied into the other set on the session's copy
+    stream. Each round's results are copied into the caller's host buffers on the
+    current stream right after the round, complete once that stream is synchronised.
+    Host tensors should be pinned for the copies to overlap the rounds.
     """
 
     KEYS = ("base", "hidden", "anchor", "target")
 
-    def __init__(self, rnd: "Round", like: dict):
+    def __init__(self, rnd: "Round", like: dict = None):
         self.rnd = rnd
-        self.copy = torch.cuda.Stream()
-        self.bufs = [{k: torch.empty(like[k].shape, dtype=like[k].dtype, device="cuda") for k in self.KEYS}
-                     for _ in range(2)]
-        self.ready = [torch.cuda.Event() for _ in range(2)]
-        self.free = [torch.cuda.Event() for _ in range(2)]
-        self.used = [False, False]
+        h = ctypes.c_void_p()
+        _call("dartree_host_session_create", ctypes.byref(rnd.head), ctypes.byref(rnd.p), int(rnd.rows),
+              ctypes.byref(h))
+        self._s = h
+        self._keep = []  # host tensors of the rounds in flight
+
+    def __del__(self):
+        s = getattr(self, "_s", None)
+        if s is not None and s.value and _LIB is not None:
+            _LIB.dartree_host_session_destroy(s)
+            self._s = None
 
     def h2d_bytes(self) -> int:
-        return sum(b.numel() * b.element_size() for b in self.bufs[0].values())
+        return sum(int(lib().dartree_host_input_bytes(self._s, k)) for k in range(4))
+
+    @staticmethod
+    def _host(t: torch.Tensor, name: str) -> int:
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor")
+        return t.data_ptr()
 
     def copy_in(self, i: int, host: dict):
-        """Enqueue the copy of round i's inputs (pinned host tensors) on the copy stream."""
-        b = i % 2
-        if self.used[b]:
-            self.copy.wait_event(self.free[b])
-        with torch.cuda.stream(self.copy):
-            for k in self.KEYS:
-                self.bufs[b][k].copy_(host[k], non_blocking=True)
-            self.ready[b].record(self.copy)
+        """Stage round i's inputs (host tensors, pinned for overlap): dartree_host_stage."""
+        x = HostInputs(*(self._host(host[k], k) for k in self.KEYS))
+        _call("dartree_host_stage", self._s, ctypes.byref(x))
+        self._keep = (self._keep + [host])[-2:]
 
-    def run(self, i: int, host_out: dict):
-        """Enqueue round i on the current stream (after its inputs landed) and the copy
-        of its results into host_out (pinned tensors shaped like Round.out)."""
-        b = i % 2
-        cur = torch.cuda.current_stream()
-        cur.wait_event(self.ready[b])
-        x = self.bufs[b]
-        out = self.rnd.run(x["base"], x["hidden"], x["anchor"], x["target"])
-        self.free[b].record(cur)
-        self.used[b] = True
-        for k, v in out.items():
-            host_out[k].copy_(v, non_blocking=True)
+    def run(self, i: int, host_out: dict, stream=None):
+        """Round i on the current stream from its staged inputs, results into host_out
+        (host int32 tensors shaped like Round.out): dartree_host_round."""
+        o = HostOutputs(*(self._host(host_out[k], k) for k in ("accepted_len", "path", "bonus")))
+        _call("dartree_host_round", self._s, ctypes.byref(o), _stream(stream))
         return host_out
 
 

@@ -317,6 +317,50 @@ DARTREE_API int dartree_round(const dartree_head* head, const dartree_params* p,
                               dartree_tree* tree, int32_t* accepted_len, int32_t* path, int32_t* bonus,
                               void* ws, size_t ws_bytes, void* stream);
 
+/* Rounds fed from host memory (the serving loop's view of dartree_round): a
+ * caller-owned session holds two device sets of a round's inputs, the device
+ * tree, results and workspace (one device allocation made at creation; nothing is
+ * allocated per round) and a copy stream of its own. Round i runs from input set
+ * i % 2, so the caller stages round i + 1's inputs while round i runs:
+ *   dartree_host_stage(s, in_0); for i: [dartree_host_stage(s, in_i+1);]
+ *   dartree_host_round(s, out_i, stream)
+ * dartree_host_stage enqueues the host -> device copies of one round's inputs on
+ * the session's copy stream, into the set no unfinished round reads (the copy
+ * waits on the device for the round that last read that set). At most two staged
+ * sets may be waiting: a third stage before a round returns DARTREE_EINVAL.
+ * dartree_host_round makes `stream` wait for the oldest staged set, enqueues
+ * dartree_round on it (same results and errors) and then the device -> host copies
+ * of accepted_len, path and bonus into `out`; they are valid once `stream` has been
+ * synchronised. Host buffers: pinned memory for copies that overlap the rounds
+ * (pageable memory works, with synchronous copies). A session is used by one host
+ * thread at a time; it keeps the head's pointers (E, Wq, WqT), which must stay
+ * valid. Errors: DARTREE_EINVAL (null pointers, C < 1, a shape dartree_round
+ * rejects), DARTREE_EDTYPE (dtype or row mode), DARTREE_ECUDA (allocation, stream,
+ * event or copy failures).
+ *   head, p, rows  as for dartree_round; the inputs of every round have its shapes:
+ *   base_logits [C, L, V] and block_hidden [C, L, H] in the head's dtype, anchor
+ *   [C] int32, target [C, L, V] or [C, B+1, V] (rows) in the head's dtype. */
+typedef struct dartree_host_session dartree_host_session;
+typedef struct {
+    const void* base_logits;
+    const void* block_hidden;
+    const int32_t* anchor;
+    const void* target;
+} dartree_host_inputs;
+typedef struct {
+    int32_t* accepted_len; /* [C] */
+    int32_t* path;         /* [C, L] */
+    int32_t* bonus;        /* [C] */
+} dartree_host_outputs;
+DARTREE_API int dartree_host_session_create(const dartree_head* head, const dartree_params* p, int rows,
+                                            dartree_host_session** out);
+DARTREE_API void dartree_host_session_destroy(dartree_host_session* s);
+DARTREE_API int dartree_host_stage(dartree_host_session* s, const dartree_host_inputs* in);
+DARTREE_API int dartree_host_round(dartree_host_session* s, const dartree_host_outputs* out, void* stream);
+/* Bytes of one staged input (which: 0 base_logits, 1 block_hidden, 2 anchor,
+ * 3 target); 0 for a null session or another index. */
+DARTREE_API size_t dartree_host_input_bytes(const dartree_host_session* s, int which);
+
 /* Baseline of the deferred search: node-by-node best-first drafting with one
  * correction-head evaluation per popped node ("heap pop -> correction"; DARTree
  * blog post, section 2, latency breakdown, and section 4.3, Table 2). After S1 and

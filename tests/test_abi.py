@@ -75,6 +75,38 @@ def test_argument_errors_are_reported_on_the_host(L):
                            fake, fake, ws_ok, need - 256, None) == dd.EWORKSPACE
 
 
+def test_host_session_arguments_are_checked_on_the_host(L):
+    """dartree_host_session_create rejects null pointers, an unknown row mode or
+    dtype, and shapes dartree_round would reject, before any CUDA call; stage,
+    round and input_bytes reject a null session."""
+    import diffusion_drafter_draft_gb300 as dd
+    P = dd.Params
+    fake = ctypes.c_void_p(256)  # never dereferenced: checks fail first
+    h = dd.Head()
+    assert L.dartree_head_init(ctypes.byref(h), fake, fake, 100, 64, dd.F32) == dd.OK
+    p = P(1, 4, 8, 2, 8, -0.1)
+    s = ctypes.c_void_p()
+    create = L.dartree_host_session_create
+    assert create(None, ctypes.byref(p), dd.ROWS_PER_POSITION, ctypes.byref(s)) == dd.EINVAL
+    assert create(ctypes.byref(h), None, dd.ROWS_PER_POSITION, ctypes.byref(s)) == dd.EINVAL
+    assert create(ctypes.byref(h), ctypes.byref(p), dd.ROWS_PER_POSITION, None) == dd.EINVAL
+    assert create(ctypes.byref(h), ctypes.byref(p), 5, ctypes.byref(s)) == dd.EDTYPE
+    bad = dd.Head()
+    ctypes.memmove(ctypes.byref(bad), ctypes.byref(h), ctypes.sizeof(h))
+    bad.dtype = 7
+    assert create(ctypes.byref(bad), ctypes.byref(p), dd.ROWS_PER_POSITION, ctypes.byref(s)) == dd.EDTYPE
+    assert create(ctypes.byref(h), ctypes.byref(P(0, 4, 8, 2, 8, -0.1)), dd.ROWS_PER_NODE, ctypes.byref(s)) == dd.EINVAL
+    assert create(ctypes.byref(h), ctypes.byref(P(1, 4, 8, 2, 8, 0.5)), dd.ROWS_PER_NODE, ctypes.byref(s)) == dd.EINVAL
+    assert create(ctypes.byref(h), ctypes.byref(P(1, 4, 200, 2, 8, -0.1)), dd.ROWS_PER_NODE, ctypes.byref(s)) \
+        == dd.EINVAL  # K > V
+    assert not s.value
+    hi, ho = dd.HostInputs(256, 256, 256, 256), dd.HostOutputs(256, 256, 256)
+    assert L.dartree_host_stage(None, ctypes.byref(hi)) == dd.EINVAL
+    assert L.dartree_host_round(None, ctypes.byref(ho), None) == dd.EINVAL
+    assert L.dartree_host_input_bytes(None, 0) == 0
+    L.dartree_host_session_destroy(None)  # a null session is ignored
+
+
 def test_heap_search_limits_are_checked_on_the_host(L):
     import diffusion_drafter_draft_gb300 as dd
     P = dd.Params

@@ -110,3 +110,33 @@ def test_host_rounds_match_device_rounds(dd):
     for i in range(n):
         for k in want[i % 3]:
             assert torch.equal(outs[i][k], want[i % 3][k]), (i, k)
+
+
+@pytest.mark.gpu
+def test_host_session_order_is_checked(dd):
+    """dartree_host_round with no staged inputs, and a third stage while two staged
+    sets wait for their rounds, are rejected (DARTREE_EINVAL) without enqueueing work;
+    the session carries on afterwards."""
+    cfg = make_config("cfg1_qwen3_4b_c1").replace(C=1)
+    inp = make_inputs(cfg)
+    E, Wq = _dev(inp["E"]), _dev(inp["Wq"])
+    rnd = dd.Round(E, Wq, cfg.C, cfg.L, cfg.K, cfg.W, cfg.B, cfg.beta, dd.ROWS_PER_POSITION)
+    h = dict(base=_dev(inp["base"]).cpu().pin_memory(), hidden=_dev(inp["hidden"]).cpu().pin_memory(),
+             anchor=torch.from_numpy(inp["anchor"]).pin_memory(), target=_dev(inp["target"]).cpu().pin_memory())
+    out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in rnd.out.items()}
+    hr = dd.HostRounds(rnd)
+    with pytest.raises(dd.DartreeError) as e:
+        hr.run(0, out)
+    assert e.value.code == dd.EINVAL
+    hr.copy_in(0, h)
+    hr.copy_in(1, h)
+    with pytest.raises(dd.DartreeError) as e:
+        hr.copy_in(2, h)
+    assert e.value.code == dd.EINVAL
+    for i in range(2):
+        hr.run(i, out)
+    torch.cuda.synchronize()
+    want = rnd.run(*(h[k].cuda() for k in dd.HostRounds.KEYS))
+    torch.cuda.synchronize()
+    for k, v in want.items():
+        assert torch.equal(out[k], v.cpu()), k
