@@ -25,7 +25,7 @@ struct dartree_host_session {
     void* block;  // the one device allocation holding all of the above
     cudaStream_t copy;
     cudaEvent_t ready[2];  // set b staged
-    cudaEvent_t freed[2];  // the round that read set b finished
+    cudaEvent_t freed[2];  // the round that read set b and its result copies finished
     bool used[2];
     long staged, ran;
 };
@@ -122,7 +122,11 @@ int dartree_host_session_create(const dartree_head* head, const dartree_params* 
 
 void dartree_host_session_destroy(dartree_host_session* s) {
     if (!s) return;
+    // the session's memory is freed only once no copy or round uses it
     cudaStreamSynchronize(s->copy);
+    for (int b = 0; b < 2; ++b)
+        if (s->used[b]) cudaEventSynchronize(s->freed[b]);
+    cudaGetLastError();
     release(s);
 }
 
@@ -150,15 +154,18 @@ int dartree_host_round(dartree_host_session* s, const dartree_host_outputs* out,
     if (int e = dartree_round(&s->head, &s->p, x[0], x[1], static_cast<const int32_t*>(x[2]), x[3], s->rows,
                               &s->tree, s->acc, s->path, s->bonus, s->ws, s->ws_bytes, stream))
         return e;
-    if (cudaEventRecord(s->freed[b], st) != cudaSuccess) return DARTREE_ECUDA;
-    s->used[b] = true;
     ++s->ran;
     const size_t C = size_t(s->p.C), L = size_t(s->p.L);
+    int rc = DARTREE_OK;
     if (cudaMemcpyAsync(out->accepted_len, s->acc, C * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaMemcpyAsync(out->path, s->path, C * L * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaMemcpyAsync(out->bonus, s->bonus, C * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-        return DARTREE_ECUDA;
-    return DARTREE_OK;
+        rc = DARTREE_ECUDA;
+    // set b may be refilled (and the session freed) once the round and these copies are
+    // done (recorded after whatever was enqueued, also when a copy failed)
+    if (cudaEventRecord(s->freed[b], st) != cudaSuccess) rc = DARTREE_ECUDA;
+    s->used[b] = true;
+    return rc;
 }
 
 size_t dartree_host_input_bytes(const dartree_host_session* s, int which) {

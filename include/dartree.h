@@ -334,7 +334,8 @@ DARTREE_API int dartree_round(const dartree_head* head, const dartree_params* p,
  * synchronised. Host buffers: pinned memory for copies that overlap the rounds
  * (pageable memory works, with synchronous copies). A session is used by one host
  * thread at a time; it keeps the head's pointers (E, Wq, WqT), which must stay
- * valid. Errors: DARTREE_EINVAL (null pointers, C < 1, a shape dartree_round
+ * valid. dartree_host_session_destroy waits for the session's copies and rounds
+ * (and their result copies) before freeing its memory. Errors: DARTREE_EINVAL (null pointers, C < 1, a shape dartree_round
  * rejects), DARTREE_EDTYPE (dtype or row mode), DARTREE_ECUDA (allocation, stream,
  * event or copy failures).
  *   head, p, rows  as for dartree_round; the inputs of every round have its shapes:
