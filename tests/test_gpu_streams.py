@@ -140,3 +140,37 @@ def test_host_session_order_is_checked(dd):
     torch.cuda.synchronize()
     for k, v in want.items():
         assert torch.equal(out[k], v.cpu()), k
+
+
+def test_host_session_per_node_rows_f32(dd):
+    """The host session with an fp32 head and per-node target rows ([C, B+1, V]):
+    round after round equal to Round.run on device copies of the same inputs, with
+    two input sets alternating."""
+    from dartree_inputs import breadth_first_slot_depth, make_target_per_node
+    cfg = make_config("cfg0_tiny").replace(C=3, rows="node")
+    sets = []
+    for seed in (5, 6):
+        inp = make_inputs(cfg.replace(seed=seed))
+        inp["target"] = make_target_per_node(cfg, inp, breadth_first_slot_depth(cfg))
+        sets.append(inp)
+    E = torch.from_numpy(sets[0]["E"]).cuda()
+    Wq = torch.from_numpy(sets[0]["Wq"]).cuda()
+    rnd = dd.Round(E, Wq, cfg.C, cfg.L, cfg.K, cfg.W, cfg.B, cfg.beta, dd.ROWS_PER_NODE)
+    hs = [{k: torch.from_numpy(np.ascontiguousarray(s[k])).pin_memory() for k in dd.HostRounds.KEYS} for s in sets]
+    want = []
+    for h in hs:
+        o = rnd.run(*(h[k].cuda() for k in dd.HostRounds.KEYS))
+        torch.cuda.synchronize()
+        want.append({k: v.cpu().clone() for k, v in o.items()})
+    hr = dd.HostRounds(rnd)
+    n = 5
+    outs = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in rnd.out.items()} for _ in range(n)]
+    hr.copy_in(0, hs[0])
+    for i in range(n):
+        if i + 1 < n:
+            hr.copy_in(i + 1, hs[(i + 1) % 2])
+        hr.run(i, outs[i])
+    torch.cuda.synchronize()
+    for i in range(n):
+        for k in want[i % 2]:
+            assert torch.equal(outs[i][k], want[i % 2][k]), (i, k)
