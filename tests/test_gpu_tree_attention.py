@@ -81,6 +81,9 @@ def _run(C, S, Hq, Hkv, N, seed, n_ctx=None, n_nodes=None, check=None):
     (4, 65, 32, 8, 1024, [1024, 1000, 5, 0]), # short and empty prefixes
     (3, 48, 16, 2, 512, None),                # 8 query heads per group: 384 rows = 3 full tiles
     (2, 128, 4, 2, 128, [128, 64]),           # the largest tree: 128 slots, 2 query heads per group
+    (2, 9, 4, 2, 0, None),                    # no cache at all (N = 0): the tree block alone
+    (2, 33, 8, 8, 384, [300, 384]),           # one query head per key/value head (grp = 1)
+    (3, 1, 8, 2, 256, [256, 3, 0]),           # root-only trees (S = 1)
 ])
 def test_tree_attention_matches_oracle(C, S, Hq, Hkv, N, n_ctx):
     _run(C, S, Hq, Hkv, N, seed=C * 100 + S, n_ctx=n_ctx)
