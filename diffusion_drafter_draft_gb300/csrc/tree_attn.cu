@@ -6,12 +6,11 @@
 //   (ancestor-or-self, from S9), with rotary embedding at position n_ctx + pos[c, j]
 //   (pos = depth, from S9); scores scaled by 1 / sqrt(D).
 //
-// Launches 1-2 (attn_prep_kernel, one CTA per (slot of a 128-slot block, request);
-//   attn_vt_kernel, one CTA per (request, key/value head)): rotate the tree's queries
-//   and keys (angles reduced in double precision), writing Qr [C, Hkv, grp*S, D]
-//   (row hg*S + j: the grp query heads of a group stacked) and Kt [C, Hkv, 128, D],
-//   and transpose the tree's values, Vtt [C, Hkv, D, 128]; unused and padding
-//   slots are zero.
+// Launch 1 (attn_prep_kernel: one CTA per (slot of a 128-slot block, request), then
+//   one per (request, key/value head)): rotate the tree's queries and keys (angles
+//   reduced in double precision), writing Qr [C, Hkv, grp*S, D] (row hg*S + j: the
+//   grp query heads of a group stacked) and Kt [C, Hkv, 128, D], and transpose the
+//   tree's values, Vtt [C, Hkv, D, 128]; unused and padding slots are zero.
 // Launch 2 (attn_kernel, CTA = (chunk of key blocks, 128-row tile of a group's
 //   query rows, (request, group))): warp 0 loads, per 128-key block, the keys and
 //   transposed values with TMA (128-byte swizzle) into two-stage rings, keys one block
@@ -87,18 +86,16 @@ struct RopeFreq {
     double inv[AT_D / 2];
 };
 
-// One CTA per (slot of a 128-slot block, request). The slot's D/2 rotation angles
+// The rotation, one CTA per (slot of a 128-slot block, request). The slot's D/2 rotation angles
 // (position * inv_freq_i, reduced to [-pi, pi] in double; sine and cosine in float)
 // go to shared memory; then 8 threads per head unit rotate 8 pairs (i, i + D/2) each
 // with 16-byte loads and stores. Head units: the Hq query heads, then the Hkv key heads.
 constexpr int AT_PREP_NT = 256;
 
-__global__ void __launch_bounds__(AT_PREP_NT) attn_prep_kernel(
-    const uint16_t* __restrict__ q, const uint16_t* __restrict__ kt, const int32_t* n_ctx, const int32_t* pos,
-    const int32_t* n_nodes, int S, int Hq, int Hkv, const __grid_constant__ RopeFreq fr, uint16_t* __restrict__ Qr,
-    uint16_t* __restrict__ Kr) {
-    __shared__ float cs[AT_D / 2], sn[AT_D / 2];
-    const int j = blockIdx.x, c = blockIdx.y;
+__device__ __forceinline__ void attn_rotate_slot(const uint16_t* __restrict__ q, const uint16_t* __restrict__ kt,
+                                                 const int32_t* n_ctx, const int32_t* pos, const int32_t* n_nodes,
+                                                 int S, int Hq, int Hkv, const RopeFreq& fr, uint16_t* __restrict__ Qr,
+                                                 uint16_t* __restrict__ Kr, int j, int c, float* cs, float* sn) {
     const int grp = Hq / Hkv, half = AT_D / 2;
     const bool used = j < S && j < n_nodes[c];
     if (used && threadIdx.x < half) {
@@ -153,25 +150,45 @@ __global__ void __launch_bounds__(AT_PREP_NT) attn_prep_kernel(
 }
 
 // The tree's values transposed, Vtt[c, g, d, j] = v_tree[c, j, g, d] (zero for unused
-// and padding slots): one CTA per (request, key/value head), through a shared tile so
-// that both the reads (along d) and the writes (along j) are contiguous.
-constexpr int AT_VT_PITCH = AT_BN + 2;  // halfwords per tile row
+// and padding slots): one CTA per (request, key/value head), through a shared tile;
+// 16-byte loads along d (8 values of one slot) and 16-byte stores along j (8 slots
+// of one dimension).
+constexpr int AT_VT_PITCH = AT_BN + 8;  // halfwords per tile row (rows stay 16-byte aligned)
 
-__global__ void __launch_bounds__(256) attn_vt_kernel(const uint16_t* __restrict__ vt, const int32_t* n_nodes, int S,
-                                                      int Hkv, uint16_t* __restrict__ Vtt) {
-    __shared__ uint16_t tile[AT_D][AT_VT_PITCH];  // [d][j]
-    const int cg = blockIdx.x, c = cg / Hkv, g = cg - c * Hkv;
+__device__ __forceinline__ void attn_transpose_values(const uint16_t* __restrict__ vt, const int32_t* n_nodes, int S,
+                                                      int Hkv, uint16_t* __restrict__ Vtt, int cg,
+                                                      uint16_t (*tile)[AT_VT_PITCH]) {
+    const int c = cg / Hkv, g = cg - c * Hkv;
     const int n = min(S, n_nodes[c]);
-    for (int e = threadIdx.x; e < AT_BN * AT_D; e += 256) {
-        const int j = e / AT_D, d = e - j * AT_D;
-        tile[d][j] = j < n ? vt[((size_t(c) * S + j) * Hkv + g) * AT_D + d] : uint16_t(0);
+    constexpr int DV = AT_D / 8;  // 16-byte vectors per slot
+    for (int e = threadIdx.x; e < AT_BN * DV; e += AT_PREP_NT) {  // a warp: 32 slots, one vector each
+        const int j = e % AT_BN, d0 = (e / AT_BN) * 8;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (j < n) w = *reinterpret_cast<const uint4*>(vt + ((size_t(c) * S + j) * Hkv + g) * AT_D + d0);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int q = 0; q < 8; ++q) tile[d0 + q][j] = uint16_t(ws[q >> 1] >> ((q & 1) * 16));
     }
     __syncthreads();
-    uint16_t* dst = Vtt + size_t(cg) * AT_D * AT_BN;
-    for (int e = threadIdx.x; e < AT_D * AT_BN; e += 256) {
-        const int d = e / AT_BN, j = e - d * AT_BN;
-        dst[e] = tile[d][j];
+    uint4* dst = reinterpret_cast<uint4*>(Vtt + size_t(cg) * AT_D * AT_BN);
+    constexpr int JV = AT_BN / 8;  // 16-byte vectors per transposed row
+    for (int e = threadIdx.x; e < AT_D * JV; e += AT_PREP_NT) {
+        const int d = e / JV, j0 = (e - d * JV) * 8;
+        dst[e] = *reinterpret_cast<const uint4*>(&tile[d][j0]);
     }
+}
+
+// One launch for both: CTAs [0, 128 C) rotate slot (x % 128) of request (x / 128),
+// the next C * Hkv CTAs transpose the values of one (request, key/value head).
+__global__ void __launch_bounds__(AT_PREP_NT) attn_prep_kernel(
+    const uint16_t* __restrict__ q, const uint16_t* __restrict__ kt, const uint16_t* __restrict__ v, const int32_t* n_ctx,
+    const int32_t* pos, const int32_t* n_nodes, int C, int S, int Hq, int Hkv, const __grid_constant__ RopeFreq fr,
+    uint16_t* __restrict__ Qr, uint16_t* __restrict__ Kr, uint16_t* __restrict__ Vtt) {
+    __shared__ __align__(16) uint16_t tile[AT_D][AT_VT_PITCH];  // [d][j]: the transpose's tile
+    __shared__ float cs[AT_D / 2], sn[AT_D / 2];                  // the rotation's angles
+    const int b = int(blockIdx.x), nrot = AT_BN * C;
+    if (b < nrot) attn_rotate_slot(q, kt, n_ctx, pos, n_nodes, S, Hq, Hkv, fr, Qr, Kr, b % AT_BN, b / AT_BN, cs, sn);
+    else attn_transpose_values(v, n_nodes, S, Hkv, Vtt, b - nrot, tile);
 }
 
 // ----------------------------------------------------------------------------- attention
@@ -605,10 +622,9 @@ int launch_tree_attention(int C, int S, int Hq, int Hkv, int N, double theta, co
     for (int i = 0; i < AT_D / 2; ++i) fr.inv[i] = pow(theta, -2.0 * double(i) / double(AT_D));
     {
         KTimer kt_(KID_ATTN_PREP, stream);
-        attn_prep_kernel<<<dim3(AT_BN, C), AT_PREP_NT, 0, stream>>>(
-            static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k_tree), n_ctx, pos, n_nodes, S, Hq, Hkv, fr,
-            Qr, Kt);
-        attn_vt_kernel<<<C * Hkv, 256, 0, stream>>>(static_cast<const uint16_t*>(v_tree), n_nodes, S, Hkv, Vtt);
+        attn_prep_kernel<<<AT_BN * C + C * Hkv, AT_PREP_NT, 0, stream>>>(
+            static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k_tree), static_cast<const uint16_t*>(v_tree),
+            n_ctx, pos, n_nodes, C, S, Hq, Hkv, fr, Qr, Kt, Vtt);
     }
     if (cudaGetLastError() != cudaSuccess) return DARTREE_ECUDA;
     CUtensorMap tk, tvt, tkt, tvtt;
