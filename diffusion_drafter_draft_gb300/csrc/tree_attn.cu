@@ -507,19 +507,21 @@ __global__ void __launch_bounds__(AT_NT, 1) attn_kernel(const __grid_constant__ 
                         dst[c0 / 8 + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
             }
         } else {
+            // (padding rows are never combined: nothing is written for them)
             const size_t pr = ((size_t(cg) * gridDim.y + mt) * a.nchunk + chunk) * AT_BM + rt;
             float4* dst = reinterpret_cast<float4*>(a.part_o + pr * AT_D + col0);
 #pragma unroll 1
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t v[32];
                 if (ok && nblk > 0) tc::tmem_ld32(trow + 256u + col0 + uint32_t(c0), v);
+                if (real)
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    dst[c0 / 4 + q] = has ? make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                                        __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]))
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int q = 0; q < 8; ++q)
+                        dst[c0 / 4 + q] = has ? make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]))
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            if (half == 0) {
+            if (half == 0 && real) {
                 a.part_ml[pr * 2] = has ? m_used : -INFINITY;
                 a.part_ml[pr * 2 + 1] = has ? l : 0.f;
             }
@@ -545,26 +547,51 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AtArgs a, int mtiles)
     const int c = cg / a.Hkv, g = cg - c * a.Hkv;
     const int hg = R / a.S, j = R - hg * a.S, h = g * a.grp + hg;
     const bool live = j < a.n_nodes[c];
-    float mmax = -INFINITY;
-    for (int k = 0; k < a.nchunk; ++k) {
-        const size_t pr = ((size_t(cg) * mtiles + mt) * a.nchunk + k) * AT_BM + rt;
-        if (a.part_ml[pr * 2 + 1] > 0.f) mmax = fmaxf(mmax, a.part_ml[pr * 2]);
+    const size_t pr0 = (size_t(cg) * mtiles + mt) * a.nchunk * AT_BM + rt;  // chunk k: pr0 + k * AT_BM
+    // the chunks' (max, sum) pairs, lane k taking chunks k, k + 32, ... (independent loads)
+    float mloc = -INFINITY;
+    for (int k = lane; k < a.nchunk; k += 32) {
+        const float2 ml = reinterpret_cast<const float2*>(a.part_ml)[pr0 + size_t(k) * AT_BM];
+        if (ml.y > 0.f) mloc = fmaxf(mloc, ml.x);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+    const float mmax = mloc;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float lsum = 0.f;
     if (live && mmax > -INFINITY)
-        for (int k = 0; k < a.nchunk; ++k) {
-            const size_t pr = ((size_t(cg) * mtiles + mt) * a.nchunk + k) * AT_BM + rt;
-            const float lk = a.part_ml[pr * 2 + 1];
-            if (!(lk > 0.f)) continue;
-            const float f = exp2f(a.part_ml[pr * 2] - mmax);
-            const float4 o = reinterpret_cast<const float4*>(a.part_o + pr * AT_D)[lane];
-            acc.x += f * o.x;
-            acc.y += f * o.y;
-            acc.z += f * o.z;
-            acc.w += f * o.w;
-            lsum += f * lk;
+        for (int k0 = 0; k0 < a.nchunk; k0 += 32) {
+            // lane t: chunk k0 + t's weight 2^(m - mmax) (0 for an empty chunk)
+            float fk = 0.f;
+            if (k0 + lane < a.nchunk) {
+                const float2 ml = reinterpret_cast<const float2*>(a.part_ml)[pr0 + size_t(k0 + lane) * AT_BM];
+                if (ml.y > 0.f) {
+                    fk = exp2f(ml.x - mmax);
+                    lsum += fk * ml.y;
+                }
+            }
+            const int nk = min(32, a.nchunk - k0);
+            // the chunks' rows of O, eight loads in flight
+            for (int t0 = 0; t0 < nk; t0 += 8) {
+                float4 o[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (t0 + u < nk)
+                        o[u] = reinterpret_cast<const float4*>(a.part_o + (pr0 + size_t(k0 + t0 + u) * AT_BM) * AT_D)[lane];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float f = __shfl_sync(0xffffffffu, fk, (t0 + u) & 31);
+                    if (t0 + u < nk && f > 0.f) {
+                        acc.x += f * o[u].x;
+                        acc.y += f * o[u].y;
+                        acc.z += f * o[u].z;
+                        acc.w += f * o[u].w;
+                    }
+                }
+            }
         }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
     const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
     uint2 pk = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
     reinterpret_cast<uint2*>(a.out + ((size_t(c) * a.S + j) * a.Hq + h) * AT_D)[lane] = pk;
