@@ -611,7 +611,9 @@ AttnPlan attn_plan(int C, int S, int Hq, int Hkv, int N) {
     const int grp = Hq / Hkv, mt = attn_mtiles(S, grp);
     const int blocks = (N + AT_BN - 1) / AT_BN + 1;  // most prefix blocks + the tree block
     const long base = long(C) * Hkv * mt;
-    int want = base > 0 ? int((2L * num_sms() + base - 1) / base) : 1;
+    // as many chunks of a tile's key blocks as one wave of CTAs holds (one per SM):
+    // a second, partial wave costs a CTA's fixed prologue and epilogue again
+    int want = base > 0 ? int(long(num_sms()) / base) : 1;
     if (want < 1) want = 1;
     if (want > blocks) want = blocks;
     p.per = (blocks + want - 1) / want;
