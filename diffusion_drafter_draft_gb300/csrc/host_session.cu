@@ -152,8 +152,11 @@ int dartree_host_round(dartree_host_session* s, const dartree_host_outputs* out,
     if (cudaStreamWaitEvent(st, s->ready[b], 0) != cudaSuccess) return DARTREE_ECUDA;
     void* const* x = s->in[b];
     if (int e = dartree_round(&s->head, &s->p, x[0], x[1], static_cast<const int32_t*>(x[2]), x[3], s->rows,
-                              &s->tree, s->acc, s->path, s->bonus, s->ws, s->ws_bytes, stream))
+                              &s->tree, s->acc, s->path, s->bonus, s->ws, s->ws_bytes, stream)) {
+        // (work the call enqueued before failing may still read set b)
+        if (cudaEventRecord(s->freed[b], st) == cudaSuccess) s->used[b] = true;
         return e;
+    }
     ++s->ran;
     const size_t C = size_t(s->p.C), L = size_t(s->p.L);
     int rc = DARTREE_OK;
