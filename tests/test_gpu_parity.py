@@ -166,13 +166,19 @@ def test_tiny_shapes_with_ragged_tails():
             compare_verify(o, gv, inp["target"], cfg, "position")
 
 
-@pytest.mark.parametrize("C,L,V,H,K,W,B", [(5, 5, 3001, 256, 200, 12, 30), (9, 4, 1500, 128, 33, 16, 40),
-                                           (7, 6, 2048, 384, 128, 8, 25)])
-def test_large_batch_path_shapes(C, L, V, H, K, W, B):
+@pytest.mark.parametrize("C,L,V,H,K,W,B,dtype", [(5, 5, 3001, 256, 200, 12, 30, "bf16"),
+                                                 (9, 4, 1500, 128, 33, 16, 40, "bf16"),
+                                                 (7, 6, 2048, 384, 128, 8, 25, "bf16"),
+                                                 (6, 4, 1500, 128, 40, 12, 30, "f32"),
+                                                 (32, 3, 1000, 64, 16, 4, 8, "f32")])
+def test_large_batch_path_shapes(C, L, V, H, K, W, B, dtype):
     """Batches with C*W > 48 take the per-depth path (tcgen05 projection and
-    tensor-core contraction when H is a multiple of 128)."""
+    tensor-core contraction when H is a multiple of 128 and the head is bf16; the
+    plain projection and contraction kernels for fp32 heads). From C = 32 the batch
+    expands as two halves on two streams (the last case: fp32 halves)."""
     import diffusion_drafter_draft_gb300 as dd
-    cfg = make_config("cfg1_qwen3_4b_c1").replace(C=C, L=L, V=V, H=H, K=K, W=W, B=B, seed=C * 100 + K)
+    cfg = make_config("cfg1_qwen3_4b_c1").replace(C=C, L=L, V=V, H=H, K=K, W=W, B=B, dtype=dtype,
+                                                  seed=C * 100 + K)
     inp = make_inputs(cfg)
     g, x = run_gpu_build(inp)
     o = compare_build(inp, g)
