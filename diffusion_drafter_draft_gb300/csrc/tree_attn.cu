@@ -6,7 +6,7 @@
 //   (ancestor-or-self, from S9), with rotary embedding at position n_ctx + pos[c, j]
 //   (pos = depth, from S9); scores scaled by 1 / sqrt(D).
 //
-// Launch 1 (attn_prep_kernel: one CTA per (slot of a 128-slot block, request), then
+// Launch 1 (attn_prep_kernel: one CTA per (4 slots of a 128-slot block, request), then
 //   one per (request, key/value head)): rotate the tree's queries and keys (angles
 //   reduced in double precision), writing Qr [C, Hkv, grp*S, D] (row hg*S + j: the
 //   grp query heads of a group stacked) and Kt [C, Hkv, 128, D], and transpose the
@@ -86,30 +86,38 @@ struct RopeFreq {
     double inv[AT_D / 2];
 };
 
-// The rotation, one CTA per (slot of a 128-slot block, request). The slot's D/2 rotation angles
-// (position * inv_freq_i, reduced to [-pi, pi] in double; sine and cosine in float)
-// go to shared memory; then 8 threads per head unit rotate 8 pairs (i, i + D/2) each
-// with 16-byte loads and stores. Head units: the Hq query heads, then the Hkv key heads.
+// The rotation, one CTA per (AT_RSLOTS slots of a 128-slot block, request). The slots'
+// D/2 rotation angles (position * inv_freq_i, reduced to [-pi, pi] in double; sine and
+// cosine in float) go to shared memory, one per thread; then 8 threads per (slot, head
+// unit) rotate 8 pairs (i, i + D/2) each with 16-byte loads and stores. Head units: the
+// Hq query heads, then the Hkv key heads.
 constexpr int AT_PREP_NT = 256;
+constexpr int AT_RSLOTS = AT_PREP_NT / (AT_D / 2);  // 4 slots per CTA: one angle per thread
 
-__device__ __forceinline__ void attn_rotate_slot(const uint16_t* __restrict__ q, const uint16_t* __restrict__ kt,
-                                                 const int32_t* n_ctx, const int32_t* pos, const int32_t* n_nodes,
-                                                 int S, int Hq, int Hkv, const RopeFreq& fr, uint16_t* __restrict__ Qr,
-                                                 uint16_t* __restrict__ Kr, int j, int c, float* cs, float* sn) {
+__device__ __forceinline__ void attn_rotate_slots(const uint16_t* __restrict__ q, const uint16_t* __restrict__ kt,
+                                                  const int32_t* n_ctx, const int32_t* pos, const int32_t* n_nodes,
+                                                  int S, int Hq, int Hkv, const RopeFreq& fr, uint16_t* __restrict__ Qr,
+                                                  uint16_t* __restrict__ Kr, int j0, int c, float (*cs)[AT_D / 2],
+                                                  float (*sn)[AT_D / 2]) {
     const int grp = Hq / Hkv, half = AT_D / 2;
-    const bool used = j < S && j < n_nodes[c];
-    if (used && threadIdx.x < half) {
-        const int i = threadIdx.x;
-        const double p = double(n_ctx[c]) + double(pos[size_t(c) * S + j]);
-        const double a = p * fr.inv[i];
-        const double k = rint(a * 0.15915494309189535);           // 1 / (2 pi)
-        const float r = float(fma(-k, 6.283185307179586, a));    // 2 pi
-        sincosf(r, &sn[i], &cs[i]);
+    const int nn = n_nodes[c];
+    {
+        const int sl = threadIdx.x / half, i = threadIdx.x % half, j = j0 + sl;
+        if (j < S && j < nn) {
+            const double p = double(n_ctx[c]) + double(pos[size_t(c) * S + j]);
+            const double a = p * fr.inv[i];
+            const double k = rint(a * 0.15915494309189535);           // 1 / (2 pi)
+            const float r = float(fma(-k, 6.283185307179586, a));    // 2 pi
+            sincosf(r, &sn[sl][i], &cs[sl][i]);
+        }
     }
     __syncthreads();
     const int t = threadIdx.x & 7, i0 = t * 8;  // pairs i0 .. i0 + 7
-    for (int u = threadIdx.x >> 3; u < Hq + Hkv; u += AT_PREP_NT / 8) {
+    const int units = Hq + Hkv;
+    for (int w8 = threadIdx.x >> 3; w8 < AT_RSLOTS * units; w8 += AT_PREP_NT / 8) {
+        const int sl = w8 / units, u = w8 - sl * units, j = j0 + sl;
         if (u < Hq && j >= S) continue;  // query rows exist for real slots only
+        const bool used = j < S && j < nn;
         const uint16_t* src;
         uint16_t* dst;
         if (u < Hq) {
@@ -135,8 +143,8 @@ __device__ __forceinline__ void attn_rotate_slot(const uint16_t* __restrict__ q,
                     const int i = i0 + 2 * w + e;
                     const float x = bf16_bits_to_float((xs[w] >> (16 * e)) & 0xffffu);
                     const float y = bf16_bits_to_float((ys[w] >> (16 * e)) & 0xffffu);
-                    a2[e] = x * cs[i] - y * sn[i];
-                    b2[e] = y * cs[i] + x * sn[i];
+                    a2[e] = x * cs[sl][i] - y * sn[sl][i];
+                    b2[e] = y * cs[sl][i] + x * sn[sl][i];
                 }
                 ro[w] = pack_bf16x2(a2[0], a2[1]);
                 rh[w] = pack_bf16x2(b2[0], b2[1]);
@@ -178,17 +186,20 @@ __device__ __forceinline__ void attn_transpose_values(const uint16_t* __restrict
     }
 }
 
-// One launch for both: CTAs [0, 128 C) rotate slot (x % 128) of request (x / 128),
-// the next C * Hkv CTAs transpose the values of one (request, key/value head).
+// One launch for both: the first (128 / AT_RSLOTS) C CTAs rotate AT_RSLOTS slots of a
+// request each, the next C * Hkv CTAs transpose the values of one (request, key/value head).
 __global__ void __launch_bounds__(AT_PREP_NT) attn_prep_kernel(
     const uint16_t* __restrict__ q, const uint16_t* __restrict__ kt, const uint16_t* __restrict__ v, const int32_t* n_ctx,
     const int32_t* pos, const int32_t* n_nodes, int C, int S, int Hq, int Hkv, const __grid_constant__ RopeFreq fr,
     uint16_t* __restrict__ Qr, uint16_t* __restrict__ Kr, uint16_t* __restrict__ Vtt) {
-    __shared__ __align__(16) uint16_t tile[AT_D][AT_VT_PITCH];  // [d][j]: the transpose's tile
-    __shared__ float cs[AT_D / 2], sn[AT_D / 2];                  // the rotation's angles
-    const int b = int(blockIdx.x), nrot = AT_BN * C;
-    if (b < nrot) attn_rotate_slot(q, kt, n_ctx, pos, n_nodes, S, Hq, Hkv, fr, Qr, Kr, b % AT_BN, b / AT_BN, cs, sn);
-    else attn_transpose_values(v, n_nodes, S, Hkv, Vtt, b - nrot, tile);
+    __shared__ __align__(16) uint16_t tile[AT_D][AT_VT_PITCH];       // [d][j]: the transpose's tile
+    __shared__ float cs[AT_RSLOTS][AT_D / 2], sn[AT_RSLOTS][AT_D / 2];  // the rotation's angles
+    constexpr int PER = AT_BN / AT_RSLOTS;  // rotation CTAs per request
+    const int b = int(blockIdx.x), nrot = PER * C;
+    if (b < nrot)
+        attn_rotate_slots(q, kt, n_ctx, pos, n_nodes, S, Hq, Hkv, fr, Qr, Kr, (b % PER) * AT_RSLOTS, b / PER, cs, sn);
+    else
+        attn_transpose_values(v, n_nodes, S, Hkv, Vtt, b - nrot, tile);
 }
 
 // ----------------------------------------------------------------------------- attention
@@ -651,7 +662,7 @@ int launch_tree_attention(int C, int S, int Hq, int Hkv, int N, double theta, co
     for (int i = 0; i < AT_D / 2; ++i) fr.inv[i] = pow(theta, -2.0 * double(i) / double(AT_D));
     {
         KTimer kt_(KID_ATTN_PREP, stream);
-        attn_prep_kernel<<<AT_BN * C + C * Hkv, AT_PREP_NT, 0, stream>>>(
+        attn_prep_kernel<<<(AT_BN / AT_RSLOTS) * C + C * Hkv, AT_PREP_NT, 0, stream>>>(
             static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k_tree), static_cast<const uint16_t*>(v_tree),
             n_ctx, pos, n_nodes, C, S, Hq, Hkv, fr, Qr, Kt, Vtt);
     }
