@@ -160,7 +160,8 @@ int dartree_heap_build(const dartree_head* head, const dartree_params* p, const 
     uint16_t* Eg = at<uint16_t>(ws, l.Eg);
     const int M = p->C * p->L * p->K;
     // S1 (the same launch copies the candidates' rows when it can), then G = E[cand] W_q
-    const TopkGather g{static_cast<const uint16_t*>(head->E), head->H, Eg};
+    const TopkGather g{static_cast<const uint16_t*>(head->E), head->H, Eg, head->WqT,
+                       reinterpret_cast<uintptr_t>(head->WqT) % 16 == 0 ? size_t(head->H) * head->H * 2 : 0};
     bool gathered = false;
     if (int e = launch_topk(base_logits, p->C * p->L, head->V, p->K, head->dtype, ct, cv, status, s, &g, &gathered))
         return e;
@@ -305,7 +306,9 @@ static int expand_impl(const dartree_head* head, const dartree_params* p, const 
 static int topk_for_expand(const dartree_head* head, const dartree_params* p, const void* base_logits, int32_t* ct,
                            float* cv, int* status, ExpandArgs& a, cudaStream_t s, const TopkRowmax* rm = nullptr,
                            bool* rm_done = nullptr) {
-    const TopkGather g{static_cast<const uint16_t*>(head->E), head->H, a.Eg};
+    // (the candidate-side projection GEMM that follows streams W_q^T: into L2 meanwhile)
+    const TopkGather g{static_cast<const uint16_t*>(head->E), head->H, a.Eg, a.WqT,
+                       a.WqT && reinterpret_cast<uintptr_t>(a.WqT) % 16 == 0 ? size_t(head->H) * head->H * 2 : 0};
     bool gathered = false;
     const bool want = expand_g_fits(a);
     if (int e = launch_topk(base_logits, p->C * p->L, head->V, p->K, head->dtype, ct, cv, status, s,

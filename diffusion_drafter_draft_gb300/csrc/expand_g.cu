@@ -372,10 +372,11 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
     const int f0 = int(cr) * fs;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 
-    // G (and, with_e, the E and H_d slices) of position pos; one thread
-    auto prefetch = [&](int pos, bool with_e) {
+    // G (and, with_e, the E and H_d slices) of position pos, with `extra` more bytes
+    // expected on the barrier; one thread
+    auto prefetch = [&](int pos, bool with_e, uint32_t extra) {
         const int row = (r * L + pos) * K;  // first candidate row of the position in G and E[cand]
-        mbar_arrive_expect_tx(mbar, uint32_t((2 + (with_e ? 1 : 0)) * K * fs * 2 + (with_e ? fs * 2 : 0)));
+        mbar_arrive_expect_tx(mbar, uint32_t((2 + (with_e ? 1 : 0)) * K * fs * 2 + (with_e ? fs * 2 : 0)) + extra);
         for (int b = 0; b < nb; ++b) {
             tc::tma_load_2d(gs + size_t(b) * K * 64, &tm_ghi, f0 + b * XG_GB, row, mbar);
             tc::tma_load_2d(gs + size_t(nb + b) * K * 64, &tm_glo, f0 + b * XG_GB, row, mbar);
@@ -387,23 +388,25 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
     };
 
     griddep_launch_dependents();
+    const uint32_t tbl = uint32_t(L * K * 4);  // bytes of the candidate tokens (and of their values)
     if (threadIdx.x == 0) {
         for (int i = 0; i < 5; ++i) mbar_init(&mbar[i], 1);
         fence_mbar_init();
+        // root: h = E[anchor] (this CTA's slice), on the first prefetch's barrier (the
+        // head and the anchor are not written by the kernels before this one)
+        bulk_g2s(hs, a.E + size_t(a.anchor[r]) * H + f0, uint32_t(fs * 2), mbar);
+        spar[0] = 0.f;
     }
-    // root: h = E[anchor] (this CTA's slice), s = 0
-    for (int f = threadIdx.x; f < fs; f += XG_NT) hs[f] = a.E[size_t(a.anchor[r]) * H + f0 + f];
-    if (threadIdx.x == 0) spar[0] = 0.f;
     __syncthreads();
     cluster_sync();  // every peer's exchange barriers are initialised before any store targets them
-    // the candidates, their rows and G come from the kernels before this one
+    // the candidates, their rows and G come from the kernels before this one: G of
+    // position 0 and the candidate table arrive with the root row on one barrier
     griddep_wait();
-    if (threadIdx.x == 0) prefetch(0, L > 1);
-    for (int i = threadIdx.x; i < L * K; i += XG_NT) {
-        ctok[i] = a.cand_tok[size_t(r) * L * K + i];
-        cval[i] = a.cand_val[size_t(r) * L * K + i];
+    if (threadIdx.x == 0) {
+        prefetch(0, L > 1, uint32_t(fs * 2) + 2 * tbl);
+        bulk_g2s(ctok, a.cand_tok + size_t(r) * L * K, tbl, mbar);
+        bulk_g2s(cval, a.cand_val + size_t(r) * L * K, tbl, mbar);
     }
-    __syncthreads();
     int issued = 1, waited = 0;  // prefetch phases (uniform across the CTA)
     bool pf_ok = true;           // false once a prefetch wait ran out: no further prefetches
     int cur = 0, P = 1;
@@ -516,7 +519,7 @@ __global__ void __launch_bounds__(XG_NT, 1) expand_g_kernel(XgArgs a, const __gr
                 }
             }
         } else if (threadIdx.x == 32 * RPO && pf_ok && d < L) {
-            prefetch(pos + 1, d + 1 < L);
+            prefetch(pos + 1, d + 1 < L, 0);
         }
         if (pf_ok && d < L) ++issued;
         __syncthreads();
@@ -802,6 +805,7 @@ static bool xg_fin(const ExpandArgs& a) {
 
 static int xg_plan(const ExpandArgs& a, size_t* smem) {
     if (a.dtype != DARTREE_BF16 || !a.WqT || !a.Eg || !a.Ghi || !a.Glo) return 0;
+    if (reinterpret_cast<uintptr_t>(a.E) % 16 != 0) return 0;  // the root row arrives by a bulk copy
     const int M = a.C * a.L * a.K;
     if (M > a.g_rows || a.K > XG_MAXK || a.K % 8 != 0 || a.W > XG_MAXW) return 0;
     if (!gemm_tc_supported(M, a.H, a.H) || a.H / 8 > GR_MAXV * GR_NT) return 0;

@@ -8,8 +8,10 @@
 // 128 x 64 and BN x 64 tiles with TMA (128-byte swizzle) into a ring of as many
 // stages as shared memory holds (4 for BN = 256, 6 for BN = 160 or 128);
 // warp 1's elected thread issues tcgen05.mma (4 per 64-wide k block) and
-// releases each stage with tcgen05.commit; all 4 warps then read the
-// accumulator from TMEM (one row per thread) and write the epilogue:
+// releases each stage with tcgen05.commit; all 8 warps then read the
+// accumulator from TMEM (one row per thread; warps w and w + 4 share the TMEM
+// lanes of rows 32 (w mod 4) ... and take alternate 32-column chunks) and write
+// the epilogue:
 //   mode 0: fp32 D (row-major, ld = N);
 //   mode 1: the contraction's operand, U split into a bf16 pair (hi = bf16(u),
 //           lo = bf16(u - hi)), row m = r*P + p going to rows r*32 + p and
@@ -28,7 +30,7 @@
 
 namespace dartree {
 
-constexpr int GT_BM = 128, GT_BK = 64, GT_NT = 128;
+constexpr int GT_BM = 128, GT_BK = 64, GT_NT = 256;
 
 struct GemmOut {
     int mode;          // 0: fp32 d32; 1: hi/lo bf16 pairs into hilo (row remap); 2: hi -> hilo, lo -> lo2
@@ -116,8 +118,6 @@ struct GtSmem {
     static_assert(size_t(2) * GT_BM * EPI_PITCH <= BAR, "epilogue staging fits in the operand ring");
 };
 
-__device__ __forceinline__ uint16_t bf16_rn_bits(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
-
 template <int BN>
 __global__ void __launch_bounds__(GT_NT, 1) gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                                                 const __grid_constant__ CUtensorMap tmB, int M,
@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(GT_NT, 1) gemm_bf16_tc_kernel(const __grid_con
     const uint32_t tmem = *slot;
 
     griddep_launch_dependents();
-    if (warp >= 2 && out.rm.target) gemm_rowmax_prefetch(out.rm);
+    if ((warp == 2 || warp == 3) && out.rm.target) gemm_rowmax_prefetch(out.rm);
     if (warp == 0 && lane == 0) {
         // producer: TMA ring. B is not written by the previous kernel of the stream:
         // the first stages' B tiles load before the dependency wait, A after it.
@@ -188,15 +188,17 @@ __global__ void __launch_bounds__(GT_NT, 1) gemm_bf16_tc_kernel(const __grid_con
     }
     __syncwarp();
     griddep_wait();  // (the producer's wait already covers the operands; this orders the stores)
-    if (warp >= 2 && out.rm.target) gemm_rowmax(out.rm);
+    if ((warp == 2 || warp == 3) && out.rm.target) gemm_rowmax(out.rm);
 
-    // epilogue: TMEM -> registers -> global
+    // epilogue: TMEM -> registers -> global. Warps w and w + 4 share TMEM lanes
+    // 32 (w mod 4) ... and take alternate 32-column chunks of their rows.
     const bool have = __syncthreads_and(mbar_wait_bounded(accum, 0, status) ? 1 : 0) != 0;
     tc::fence_after_sync();
-    const int m = m0 + warp * 32 + lane;
-    const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);
+    const int quarter = warp & 3, cfirst = (warp >> 2) * 32;
+    const int m = m0 + quarter * 32 + lane;
+    const uint32_t trow = tmem + (uint32_t(quarter * 32) << 16);
     if (out.mode == 0) {
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = cfirst; c0 < BN; c0 += 64) {
             uint32_t r[32];
             tc::tmem_ld32(trow + uint32_t(c0), r);
             const int n = n0 + c0;
@@ -215,19 +217,18 @@ __global__ void __launch_bounds__(GT_NT, 1) gemm_bf16_tc_kernel(const __grid_con
         constexpr int PITCH = L::EPI_PITCH;
         uint8_t* sh = smem;
         uint8_t* sl = smem + GT_BM * PITCH;
-        const int rl = warp * 32 + lane;
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        const int rl = quarter * 32 + lane;
+        for (int c0 = cfirst; c0 < BN; c0 += 64) {
             uint32_t r[32];
             tc::tmem_ld32(trow + uint32_t(c0), r);
             uint32_t hi[16], lo[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < 16; ++j) {  // two columns per conversion (each rounded to nearest even)
                 const float u0 = __uint_as_float(r[2 * j]), u1 = __uint_as_float(r[2 * j + 1]);
-                const uint16_t h0 = bf16_rn_bits(u0), h1 = bf16_rn_bits(u1);
-                const uint16_t l0 = bf16_rn_bits(u0 - bf16_bits_to_float(h0));
-                const uint16_t l1 = bf16_rn_bits(u1 - bf16_bits_to_float(h1));
-                hi[j] = uint32_t(h0) | (uint32_t(h1) << 16);
-                lo[j] = uint32_t(l0) | (uint32_t(l1) << 16);
+                const __nv_bfloat162 h = __floats2bfloat162_rn(u0, u1);
+                const __nv_bfloat162 l = __floats2bfloat162_rn(u0 - __low2float(h), u1 - __high2float(h));
+                hi[j] = *reinterpret_cast<const uint32_t*>(&h);
+                lo[j] = *reinterpret_cast<const uint32_t*>(&l);
             }
             uint4* dh = reinterpret_cast<uint4*>(sh + size_t(rl) * PITCH + size_t(c0) * 2);
             uint4* dl = reinterpret_cast<uint4*>(sl + size_t(rl) * PITCH + size_t(c0) * 2);

@@ -62,6 +62,8 @@ struct TopkGather {
     const uint16_t* E;
     int H;
     uint16_t* out;
+    const void* pre = nullptr;  // a range the launch after this one reads (16-byte aligned, a multiple of
+    size_t pre_bytes = 0;       // 16 bytes): prefetched into L2 while the rows stream, or none
 };
 
 // Maxima keys (ord(value) << 32 | ~index) of per-position target rows [rows, V],

@@ -275,7 +275,8 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
                                                           float* __restrict__ out_val, int* status,
                                                           const uint16_t* __restrict__ gE, int gH,
                                                           uint16_t* __restrict__ gout, const T* __restrict__ tgt,
-                                                          unsigned long long* __restrict__ tkeys) {
+                                                          unsigned long long* __restrict__ tkeys,
+                                                          const uint8_t* __restrict__ pre, unsigned long long pre_bytes) {
     extern __shared__ __align__(1024) uint8_t smem[];
     griddep_launch_dependents();
     constexpr int VEC = ValueKey<T>::VEC;
@@ -463,6 +464,13 @@ __global__ void __launch_bounds__(TK_NT, 4) topk_rows_kernel(const T* __restrict
     if (threadIdx.x == 0) misc[9] = uint32_t(over);
     const int excl = block_exclusive_scan<TK_NT>(cnt, wtot, reinterpret_cast<int*>(&misc[8]));
     cluster_sync();  // CTA totals visible
+    // the rows have streamed: this CTA's share of the next launch's operand into L2
+    // (HBM is idle for the rest of this launch), in 16-byte multiples
+    if (pre && threadIdx.x == 0) {
+        const unsigned long long per = (pre_bytes / gridDim.x + 15) & ~15ull, b0 = per * blockIdx.x;
+        for (unsigned long long o = b0; o < b0 + per && o < pre_bytes; o += 65536)
+            prefetch_l2_bulk(pre + o, uint32_t(min(65536ull, min(b0 + per, pre_bytes) - o)));
+    }
     if (tgt && cr == 0 && threadIdx.x == 0) {
         uint64_t m = 0;
 #pragma unroll 16
@@ -932,7 +940,8 @@ static int launch_topk_t(const void* x, int rows, int V, int K, int32_t* tok, fl
         e = cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const T*>(x), V, K, jsel, chunk, use_bulk, tok, val,
                                status, g ? g->E : nullptr, g ? g->H : 0, g ? g->out : nullptr,
                                rm && !rm->zero_only ? static_cast<const T*>(rm->target) : nullptr,
-                               rm ? rm->keys : nullptr);
+                               rm ? rm->keys : nullptr, g ? static_cast<const uint8_t*>(g->pre) : nullptr,
+                               g ? (unsigned long long)g->pre_bytes : 0ull);
     }
     return e == cudaSuccess ? DARTREE_OK : DARTREE_ECUDA;
 }
