@@ -379,9 +379,9 @@ def measure_attention(cfg, m, steps, warmup, torch, dd, hbm_peak, tf_peak, graph
 # requests processed (its traffic is per request).
 # A kernel changed since its capture has no entry (traffic null).
 NCU_TRAFFIC = {
-    ("cfg1_qwen3_4b_c1", "expand_g_kernel"): 15566336,      # one launch = one round, full size
-    ("cfg1_qwen3_4b_c1", "gemm_bf16_tc_kernel"): 23248384,
-    ("cfg1_qwen3_4b_c1", "topk_rows_kernel"): 15284736,
+    ("cfg1_qwen3_4b_c1", "expand_g_kernel"): 15566592,      # one launch = one round, full size
+    ("cfg1_qwen3_4b_c1", "gemm_bf16_tc_kernel"): 23247360,
+    ("cfg1_qwen3_4b_c1", "topk_rows_kernel"): 28392192,     # incl. the 13.1 MB L2 prefetch of W_q^T
     ("cfg4_c64_stress", "contract_tc_kernel"): 35337472 * 8,   # one launch over all 64 requests
     ("cfg4_c64_stress", "topk_stream_kernel"): 361796608 + 5478400,   # full size
 }
