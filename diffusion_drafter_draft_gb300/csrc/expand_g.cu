@@ -23,15 +23,16 @@
 //   2. the owner sums the CS partials of its rows in a fixed order, takes the
 //      log-softmax and scores, ranks the row's candidates by counting, and
 //      broadcasts the row's best min(W, K) keys, sorted, to every CTA;
-//   3. every CTA merges the P sorted lists (rank = position in its own list +
-//      binary searches in the others), so all of them take the same top-W; the
-//      kept children's state slices x = h_p + E[tok] + H_d[d-1] are formed,
+//   3. every CTA merges the P sorted lists with a bitonic merge tree (pairs of
+//      16-key lists per warp, four levels), so all of them take the same top-W;
+//      the kept children's state slices x = h_p + E[tok] + H_d[d-1] are formed,
 //      partial sums of squares exchanged, and the slices normalised into the
 //      next parent buffer.
 //
-// The candidate table of the request sits in shared memory. The G, E and H_d
-// slices of the next position arrive by TMA while the current depth runs: G as
-// 32-column tiles with 64-byte swizzle (conflict-free ldmatrix), E as one tile
+// The candidate table of the request sits in shared memory (it arrives, with the
+// root row E[anchor], by bulk copy on the first prefetch's barrier). The G, E and
+// H_d slices of the next position arrive by TMA while the current depth runs: G
+// as 32-column tiles with 64-byte swizzle (conflict-free ldmatrix), E as one tile
 // of the gathered candidate rows, H_d as one bulk copy, all completing on one
 // mbarrier. Waits are bounded; a wait that runs out records a timeout and the
 // CTA keeps taking part in every cluster barrier, so no peer is left waiting.
